@@ -1,0 +1,174 @@
+"""Pins of the oracle's number formats (MXFP4 main KV, FP8 SWA / indexer keys).
+
+Independent anchors: hand-worked vectors (tests/golden/*.txt, each citing the
+page that names the format), the E2M1 / E4M3 value tables of the OCP
+definitions, torch's own float8_e4m3fn conversion (a separate library
+routine), exhaustive round trips and scaling invariances.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# ---------------------------------------------------------------- E2M1
+def test_e2m1_value_table():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]          # OCP FP4 E2M1 grid
+    for c in range(8):
+        assert oracle.e2m1_value(c) == mags[c]
+        assert oracle.e2m1_value(c | 8) == -mags[c]
+    assert np.signbit(oracle.e2m1_value(8))
+
+
+def test_e2m1_roundtrip_all_codes():
+    for c in range(16):
+        assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
+
+
+def test_e2m1_nearest_and_ties():
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rng = np.random.default_rng(1)
+    for v in rng.uniform(0, 8, 4000):
+        c = oracle.e2m1_encode(float(v))
+        d = np.abs(grid - v)
+        assert d[c] == d.min()
+    # midpoints go to the even-mantissa neighbour
+    for mid, want in [(0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6)]:
+        assert oracle.e2m1_encode(mid) == want
+        assert oracle.e2m1_encode(-mid) == want | 8
+    assert oracle.e2m1_encode(7.99) == 7 and oracle.e2m1_encode(100.0) == 7
+
+
+# ---------------------------------------------------------------- MXFP4
+def test_mx_exponent_definition():
+    # X = floor(log2 amax) - 2 (E2M1's largest exponent is 2)
+    assert oracle.mx_exponent(1.0) == -2
+    assert oracle.mx_exponent(6.0) == 0
+    assert oracle.mx_exponent(7.99) == 0
+    assert oracle.mx_exponent(8.0) == 1
+    assert oracle.mx_exponent(0.3) == -4
+    assert oracle.mx_exponent(2.0 ** -120) == -122
+    assert oracle.mx_exponent(1e-40) == -127        # clamped at the E8M0 floor
+    assert oracle.mx_exponent(0.0) == 0
+
+
+def test_mxfp4_golden_vectors():
+    for ln in _lines("mxfp4_vectors.txt"):
+        sb, vals, codes = [p.split() for p in ln.split("|")]
+        x = np.zeros((1, 512), np.float32)
+        x[0, :32] = np.array([float(v) for v in vals], np.float32)
+        c, s = oracle.quant_mxfp4(x)
+        assert s[0, 0] == int(sb[0])
+        want = [int(h, 16) for h in codes]
+        got = [(c[0, i // 2] >> (4 * (i & 1))) & 15 for i in range(32)]
+        assert got == want
+
+
+def test_mxfp4_layout_and_roundtrip():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((64, 512)).astype(np.float32) * np.float32(3.0)
+    c, s = oracle.quant_mxfp4(x)
+    assert c.shape == (64, 256) and s.shape == (64, 16)
+    deq = oracle.dequant_mxfp4(c, s)
+    # element 2i sits in the low nibble of byte i
+    for r in range(4):
+        for d in (0, 1, 2, 3, 100, 511):
+            code = (c[r, d // 2] >> (4 * (d & 1))) & 15
+            X = int(s[r, d // 32]) - 127
+            assert deq[r, d] == oracle.e2m1_value(code) * 2.0 ** X
+    # nearest representable under the block scale, saturating beyond 6*2^X
+    for r in range(64):
+        for b in range(16):
+            X = int(s[r, b]) - 127
+            blk = x[r, b * 32:(b + 1) * 32].astype(np.float64)
+            grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6]) * 2.0 ** X
+            for v, q in zip(blk, deq[r, b * 32:(b + 1) * 32]):
+                target = min(abs(v), 6 * 2.0 ** X)
+                assert abs(abs(q) - target) == np.abs(grid - target).min()
+                assert q == 0 or np.sign(q) == np.sign(v)
+    # quantise(dequantise(q)) == q
+    c2, s2 = oracle.quant_mxfp4(deq.astype(np.float32))
+    assert np.array_equal(c, c2) and np.array_equal(s, s2)
+
+
+def test_mxfp4_power_of_two_scaling():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((16, 512)).astype(np.float32)
+    c0, s0 = oracle.quant_mxfp4(x)
+    for k in (-5, 3, 20):
+        c, s = oracle.quant_mxfp4(x * np.float32(2.0 ** k))
+        assert np.array_equal(c, c0)
+        assert np.array_equal(s.astype(int), s0.astype(int) + k)
+
+
+# ---------------------------------------------------------------- E4M3
+def test_e4m3_golden_vectors():
+    for ln in _lines("fp8_vectors.txt"):
+        v, h = ln.split()
+        assert oracle.e4m3_encode(float(v)) == int(h, 16), ln
+
+
+def test_e4m3_decode_exhaustive():
+    vals = [oracle.e4m3_value(c) for c in range(127)]
+    assert vals[0] == 0.0 and vals[126] == 448.0
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+    assert np.isnan(oracle.e4m3_value(0x7F)) and np.isnan(oracle.e4m3_value(0xFF))
+    for c in list(range(127)) + list(range(128, 255)):
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c
+    # matches torch's reading of every code
+    t = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert t[c] == oracle.e4m3_value(c)
+
+
+def test_e4m3_encode_matches_torch():
+    rng = np.random.default_rng(11)
+    # random magnitudes across the whole range, plus exact midpoints and their neighbours
+    a = np.concatenate([
+        rng.uniform(-464, 464, 20000),
+        np.exp2(rng.uniform(-14, 8.8, 20000)) * rng.choice([-1, 1], 20000),
+    ]).astype(np.float32)
+    vals = np.array([oracle.e4m3_value(c) for c in range(127)])
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)
+    near = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    a = np.concatenate([a, near, -near, [0.0, -0.0]]).astype(np.float32)
+    a = a[np.abs(a) <= 464]        # torch's cast is non-saturating above 464
+    want = torch.from_numpy(a).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(float(v)) for v in a], np.uint8)
+    bad = np.nonzero(want != got)[0]
+    assert bad.size == 0, (a[bad[:5]], want[bad[:5]], got[bad[:5]])
+
+
+def test_quant_fp8_rows():
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((32, 128)).astype(np.float32)
+    c, s = oracle.quant_fp8(x)
+    amax = np.abs(x).max(axis=1)
+    assert np.array_equal(s, (amax / np.float32(448.0)).astype(np.float32))
+    # the largest-magnitude element lands on +-448
+    j = np.abs(x).argmax(axis=1)
+    for r in range(32):
+        assert c[r, j[r]] & 0x7F == 0x7E
+    # zero row: scale 1, codes zero
+    c0, s0 = oracle.quant_fp8(np.zeros((1, 512), np.float32))
+    assert s0[0] == 1.0 and not c0.any()
+    # power-of-two rescaling leaves the codes alone and scales s exactly
+    c2, s2 = oracle.quant_fp8(x * np.float32(8.0))
+    assert np.array_equal(c, c2) and np.array_equal(s2, s * np.float32(8.0))
+    # dequantised error within half an E4M3 step of x / s: 2^-4 relative in the
+    # normal range, 2^-10 * s (half the subnormal step) below it
+    deq = oracle.dequant_fp8(c, s)
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s[:, None]) * (1 + 1e-6)
+    assert (np.abs(deq - x) <= bound).all()
