@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""CSA2 decode benchmark: query-tokens/s at 1,048,576-token context, batch 8.
+
+One step = one decode token for each of the 8 sequences through the whole
+hot path: the new token's entry is compressed (m = 1) and quantised into the
+paged cache (MXFP4 main KV, FP8 indexer key), then the 20-layer decoder
+pattern runs (Full + 3 Reuse, 4 x (Reindex + 3 Reuse)); each layer first
+quantises its own window row of the new token (FP8) and then runs
+csa2_layer.  The step is captured once as a CUDA graph and replayed.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode query-tokens/s at 1M ctx (batch 8); % of HBM roofline"
+UNIT = "query-tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--batch", type=int, default=8)
+    p.add_argument("--tokens", type=int, default=1 << 20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [x.strip() for x in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- the decode step
+class DecodeStep:
+    """Device state and the launch sequence of one decode step."""
+
+    def __init__(self, batch, tokens, seed, device):
+        import numpy as np
+        import torch
+        from compressed_sparse_attention_layer_gb300 import csa2, synth
+        from compressed_sparse_attention_layer_gb300 import workloads as W
+        from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
+
+        self.torch, self.csa2 = torch, csa2
+        self.wl = W.decode_1m(seed=seed, batch=batch, tokens=tokens)
+        self.dw = DeviceWorkload(self.wl, device=device)
+        wl, dw = self.wl, self.dw
+        B, N = wl.batch, wl.tokens[0]
+        dev = dw.dev
+        # the new token of each sequence is entry N-1 / window row (N-1) % 128
+        self.new_slots = torch.stack([dw.entry_slots(b, N - 1, N) for b in range(B)]).view(B)
+        self.C_new = torch.cat([synth.normal_bf16_torch(wl._sid(W.T_C, b), (N - 1) * 512, 512, dev)
+                                for b in range(B)]).view(B, 512)
+        self.Z_new = torch.zeros_like(self.C_new)
+        self.bias = torch.zeros((1, 512), dtype=torch.float32, device=dev)
+        self.ik_new = torch.cat([synth.normal_f32_torch(wl._sid(W.T_IK, b), (N - 1) * 128, 128, dev)
+                                 for b in range(B)]).view(B, 128)
+        self.swa_new = {l: torch.cat([synth.normal_bf16_torch(wl._sid(W.T_SWA, b, l), (N - 1) * 512, 512, dev)
+                                      for b in range(B)]).view(B, 512).float() for l in dw.layers}
+        R = wl.swa_rows
+        self.swa_rows = torch.tensor([b * R + (N - 1) % R for b in range(B)], dtype=torch.int64, device=dev)
+        self.e_new = torch.empty((B, 512), dtype=torch.float32, device=dev)
+        self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in self.scan_ev:
+            e.record()                       # materialise the CUDA events
+        self.launches = 3 + sum(1 + {"full": 5, "reindex": 3, "reuse": 1}[m] for m in wl.layers)
+        # the step's host inputs for the end-to-end leg (new token + every layer's queries)
+        self.h2d = [(self.C_new, None), (self.ik_new, None)]
+        for l in dw.layers:
+            self.h2d.append((dw.q[l], None))
+            self.h2d.append((self.swa_new[l], None))
+            if l in dw.qi:
+                self.h2d += [(dw.qi[l], None), (dw.w[l], None)]
+        self.d2h = [dw.o[l] for l in dw.layers] + [dw.lse[l] for l in dw.layers]
+
+    def enqueue(self, prof=True):
+        csa2, dw, cache = self.csa2, self.dw, self.dw.cache
+        # a1: compress the new token (m = 1), a2: MXFP4 into the cache, a3: FP8 indexer key
+        csa2.csa2_compress(self.C_new, self.Z_new, self.bias, 1, self.e_new)
+        csa2.csa2_quant_mxfp4(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
+        csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
+        for l in dw.layers:
+            # a3: this layer's window row of the new token; a4-a9: the layer
+            csa2.csa2_quant_fp8(self.swa_new[l], dw.swa_codes[l].view(-1, 512), dw.swa_scales[l].view(-1),
+                                slots=self.swa_rows)
+            full = self.wl.layers[l] == "full"
+            dw.run_layer(l, prof=self.scan_ev if (prof and full) else None)
+
+
+def run_native(args):
+    import torch
+    import torch.distributed as dist
+    from compressed_sparse_attention_layer_gb300 import build, csa2
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    build.build()
+    csa2.load()
+    dev = torch.device("cuda", local)
+    step = DecodeStep(args.batch, args.tokens, 4000 + 7919 * rank, dev)
+    B, N = step.wl.batch, step.wl.tokens[0]
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step.enqueue()                                   # eager warm-up (sets kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step.enqueue()
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region (device-resident inputs)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    scan_ms = []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(s):
+        ev0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    # dominant-kernel duration: the scan events recorded inside the graph, once per replay
+    for _ in range(min(args.steps, 10)):
+        with torch.cuda.stream(s):
+            g.replay()
+        torch.cuda.synchronize()
+        scan_ms.append(step.scan_ev[0].elapsed_time(step.scan_ev[1]))
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    value = world * B * args.steps / (ms_total / 1e3)
+
+    # ---- end to end: pinned host inputs copied in, outputs copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = [(x.cpu().pin_memory(), x) for x, _ in step.h2d]
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in step.d2h]
+        h2d_bytes = sum(h.numel() * h.element_size() for h, _ in host_in)
+        d2h_bytes = sum(h.numel() * h.element_size() for h in host_out)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            with torch.cuda.stream(s):
+                for h, d in host_in:
+                    d.copy_(h, non_blocking=True)
+                g.replay()
+                for h, d in zip(host_out, step.d2h):
+                    h.copy_(d, non_blocking=True)
+            s.synchronize()
+        el = time.perf_counter() - t0
+        te = torch.tensor([el], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * B * args.steps / float(te.item()), "unit": UNIT,
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel (the Full layer's index scan)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    E = step.wl.entries(0)
+    # algorithmic bytes per launch: 128 B codes + 4 B scale per entry read, 4 B per 8 entries
+    # of block maxima written, the 8 KB query + 128 B weights per row
+    algo_bytes = B * (E * 132 + (E // 8) * 4 + 8192 + 128)
+    scan_avg = statistics.median(scan_ms) if scan_ms else None
+    achieved = algo_bytes / (scan_avg * 1e-3) / 1e9 if scan_avg else None
+    traffic = None
+    prof_path = os.path.join(ROOT, "profiles", "traffic_index_scan.json")
+    if os.path.exists(prof_path):
+        try:
+            with open(prof_path) as f:
+                tp = json.load(f)
+            if tp.get("kernel_version") == KERNEL_VERSION:
+                traffic = tp.get("bytes_per_launch")
+        except (OSError, ValueError):
+            pass
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": (achieved / peak) if achieved else None, "traffic": traffic,
+                "kernel": "index scan (Full layer)", "kernel_ms": scan_avg,
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks else "fallback"}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(step.wl)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 accumulate over e4m3/e2m1 codes, bf16 queries",
+        "data": "synthetic (seeded counter-based generator; 64 planted blocks per sequence)",
+        "config": {"workload": f"decode_1m: batch {B} x {N} tokens, m=1, 20-layer decoder stack "
+                               "(Full+3 Reuse, 4x(Reindex+3 Reuse)), Top-512, SWA 128",
+                   "batch": B, "context_tokens": N, "layers": len(step.wl.layers),
+                   "l2": "inputs larger than L2: the Full layer scans 1.1 GB of indexer keys per step",
+                   "graph": "one CUDA graph per step"},
+        "roofline": roofline, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+KERNEL_VERSION = "simt-v1"
+
+
+# ---------------------------------------------------------------- CPU oracle
+_SAMPLES = {}
+
+
+def _prepare(wl, b):
+    """Oracle-side inputs of sequence b (its cache, window rings, queries): not timed."""
+    from tests.reference import SeqOracle
+    key = (wl.name, wl.seed, b)
+    if key not in _SAMPLES:
+        so = SeqOracle(wl, b)
+        so.ik()
+        rings = {l: so.swa_ring(l) for l in range(len(wl.layers))}
+        qs = {l: (wl.qi_bits(l, b, [0])[0], wl.w(l, b, [0])[0], wl.q_bits(l, b, [0])[0])
+              for l in range(len(wl.layers))}
+        _SAMPLES[key] = (so, rings, qs)
+    return _SAMPLES[key]
+
+
+def oracle_sample(wl, b=0, layers=None):
+    """Run the oracle through the decoder layers for sequence b's decode token.
+    Returns seconds spent in the oracle (inputs generated beforehand)."""
+    import numpy as np
+    import oracle
+
+    so, rings, qs = _prepare(wl, b)
+    t0 = time.perf_counter()
+    idx = pool = None
+    codes, scales = so.ik()
+    _, nvis = so.visible(0)
+    t = int(wl.q_pos(b)[0])
+    for l, mode in enumerate(wl.layers[:layers]):
+        qi, w, q = qs[l]
+        if mode == "full":
+            idx, pool, _ = oracle.full_select(qi, w, codes, scales, nvis)
+        elif mode == "reindex":
+            idx, _ = oracle.reindex_select(qi, w, codes, scales, pool)
+        sel = idx[idx >= 0]
+        kvc, kvs = so.kv(sel)
+        keys = oracle.attention_keys(kvc, kvs, np.arange(sel.size, dtype=np.int32), rings[l][0], rings[l][1], t)
+        oracle.attention(q, 1.0, keys)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl):
+    import oracle
+    secs = oracle_sample(wl, 0)
+    return {"value": 1.0 / secs, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"1 decode query token (sequence 0 of {wl.batch}) through all {len(wl.layers)} layers at "
+                      f"{wl.tokens[0]} tokens; {secs:.1f} s of oracle time"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from compressed_sparse_attention_layer_gb300 import workloads as W
+    oracle.build()
+    wl = W.decode_1m(seed=4000, batch=args.batch, tokens=args.tokens)
+    for _ in range(args.warmup and 1):
+        oracle_sample(wl, 0, layers=1)
+    tot = 0.0
+    for k in range(args.steps):
+        tot += oracle_sample(wl, 0)
+    value = args.steps / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"decode_1m: batch {wl.batch} x {wl.tokens[0]} tokens"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"each step: 1 decode query token of one sequence through "
+                                       f"{len(wl.layers)} layers"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_native(a)

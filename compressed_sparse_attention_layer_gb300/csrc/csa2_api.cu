@@ -1,0 +1,301 @@
+// extern "C" entry points of csa2.h: host-side validation, workspace layout,
+// kernel launches and the per-layer driver.  No entry point allocates memory.
+#include <cuda_runtime.h>
+
+#include "csa2_internal.cuh"
+
+namespace csa2 {
+
+static thread_local int g_last_cuda_error = 0;
+void set_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+// launchers defined in the kernel files
+int launch_compress(const uint16_t *, const uint16_t *, const float *, int, int64_t, float *, cudaStream_t);
+int launch_quant_mxfp4(const float *, int64_t, const int64_t *, uint8_t *, uint8_t *, int64_t, int32_t *,
+                       cudaStream_t);
+int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, float *, int64_t, int32_t *,
+                     cudaStream_t);
+int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
+                      float *, int32_t *, int64_t, cudaStream_t);
+int launch_index_pool_simt(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
+                           const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
+int launch_gather_scores(const float *, int64_t, const int32_t *, const int32_t *, int64_t, int64_t, float *,
+                         cudaStream_t);
+int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
+                cudaStream_t);
+int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
+                       cudaStream_t);
+int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
+                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t);
+size_t attn_workspace_bytes(int64_t rows);
+int topk_max_k();
+
+// ---------------------------------------------------------------- validation
+static constexpr int64_t kMaxRows = 65535;
+
+static int check_cache(const csa2_cache *c, bool need_kv, bool need_ik)
+{
+    if (!c || !c->block_table) return CSA2_ERR_NULL;
+    if (need_kv && (!c->kv_codes || !c->kv_scales)) return CSA2_ERR_NULL;
+    if (need_ik && (!c->ik_codes || !c->ik_scales)) return CSA2_ERR_NULL;
+    if (c->num_slots <= 0 || c->num_slots % CSA2_PAGE || c->max_pages <= 0) return CSA2_ERR_SHAPE;
+    if (need_kv && (!aligned(c->kv_codes, 16) || !aligned(c->kv_scales, 16))) return CSA2_ERR_ALIGN;
+    if (need_ik && (!aligned(c->ik_codes, 16) || !aligned(c->ik_scales, 16))) return CSA2_ERR_ALIGN;
+    return CSA2_OK;
+}
+
+static int check_batch(const csa2_batch *b, const csa2_cache *c)
+{
+    if (!b || !b->n_entries || !b->q_pos) return CSA2_ERR_NULL;
+    if (b->batch < 1 || b->nq < 1 || b->m < 1 || b->m > 16 || b->max_entries < 0) return CSA2_ERR_SHAPE;
+    if ((int64_t)b->batch * b->nq > kMaxRows) return CSA2_ERR_SHAPE;
+    if (c && b->max_entries > (int64_t)c->max_pages * CSA2_PAGE) return CSA2_ERR_RANGE;
+    if (b->max_entries > (int64_t)INT32_MAX) return CSA2_ERR_RANGE;
+    return CSA2_OK;
+}
+
+static int check_swa(const csa2_swa *s)
+{
+    if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
+    if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
+    if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
+    return CSA2_OK;
+}
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static inline int64_t score_ld(const csa2_batch *b)
+{
+    int64_t ld = (b->max_entries + 7) / 8 * 8;
+    return ld > 0 ? ld : 8;
+}
+
+// FULL workspace: scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
+//                 | pool scores [rows][16384] | attention workspace
+// REINDEX:        pool scores [rows][16384] | attention workspace
+struct LayerWs {
+    float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr;
+    int32_t *n_visible = nullptr;
+    void *attn = nullptr;
+    size_t attn_bytes = 0, total = 0;
+};
+
+static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
+{
+    LayerWs w;
+    const int64_t rows = (int64_t)b->batch * b->nq;
+    const int64_t ld = score_ld(b);
+    size_t off = 0;
+    char *p = static_cast<char *>(base);
+    auto take = [&](size_t bytes) {
+        void *q = p ? p + off : nullptr;
+        off += align256(bytes);
+        return q;
+    };
+    if (mode == CSA2_MODE_FULL) {
+        w.scores = (float *)take((size_t)rows * ld * 4);
+        w.block_max = (float *)take((size_t)rows * (ld / 8) * 4);
+        w.n_visible = (int32_t *)take((size_t)rows * 4);
+    }
+    if (mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX)
+        w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+    w.attn_bytes = attn_workspace_bytes(rows);
+    w.attn = take(w.attn_bytes);
+    w.total = off;
+    return w;
+}
+
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+const char *csa2_status_string(int32_t s)
+{
+    switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_NULL: return "a required pointer is NULL";
+    case CSA2_ERR_SHAPE: return "a size or count is out of range";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported argument";
+    case CSA2_ERR_RANGE: return "an index or length exceeds its buffer";
+    case CSA2_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA2_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case CSA2_ERR_CUDA: return "a CUDA call failed";
+    case CSA2_ERR_ALIGN: return "a pointer is not suitably aligned";
+    default: return "unknown status";
+    }
+}
+
+int32_t csa2_last_cuda_error(void) { return g_last_cuda_error; }
+
+int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int32_t m, int64_t n_tok,
+                  float *out, csa2_stream_t stream)
+{
+    if (m < 1 || m > 16 || n_tok < 0) return CSA2_ERR_SHAPE;
+    if (n_tok / m == 0) return CSA2_OK;
+    if (!C || !Z || !bias || !out) return CSA2_ERR_NULL;
+    return launch_compress(C, Z, bias, m, n_tok, out, (cudaStream_t)stream);
+}
+
+int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes, uint8_t *scales,
+                     int64_t num_slots, int32_t *status, csa2_stream_t stream)
+{
+    if (n < 0 || num_slots < 0) return CSA2_ERR_SHAPE;
+    if (n == 0) return CSA2_OK;
+    if (!x || !codes || !scales) return CSA2_ERR_NULL;
+    if (!slots && n > num_slots) return CSA2_ERR_RANGE;
+    if (!aligned(x, 16) || !aligned(codes, 16)) return CSA2_ERR_ALIGN;
+    return launch_quant_mxfp4(x, n, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
+}
+
+int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
+                   float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream)
+{
+    if (n < 0 || num_slots < 0 || (dim != 128 && dim != 512)) return CSA2_ERR_SHAPE;
+    if (n == 0) return CSA2_OK;
+    if (!x || !codes || !scales) return CSA2_ERR_NULL;
+    if (!slots && n > num_slots) return CSA2_ERR_RANGE;
+    if (!aligned(x, 16) || !aligned(codes, 4)) return CSA2_ERR_ALIGN;
+    return launch_quant_fp8(x, n, dim, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
+}
+
+int csa2_index_scores(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi, const float *w,
+                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, csa2_stream_t stream)
+{
+    int s = check_cache(cache, false, true);
+    if (s) return s;
+    if ((s = check_batch(batch, cache))) return s;
+    if (!qi || !w || (!scores && !block_max)) return CSA2_ERR_NULL;
+    if (ld < batch->max_entries || ld % 8 || ld <= 0) return CSA2_ERR_SHAPE;
+    return launch_index_scan(*cache, *batch, qi, w, scores, block_max, n_visible, ld, (cudaStream_t)stream);
+}
+
+int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi,
+                           const float *w, const int32_t *pool, const int32_t *pool_len, int64_t ld,
+                           float *scores, csa2_stream_t stream)
+{
+    int s = check_cache(cache, false, true);
+    if (s) return s;
+    if ((s = check_batch(batch, cache))) return s;
+    if (!qi || !w || !pool || !pool_len || !scores) return CSA2_ERR_NULL;
+    if (ld <= 0 || ld > (int64_t)1 << 24) return CSA2_ERR_SHAPE;
+    return launch_index_pool_simt(*cache, *batch, qi, w, pool, pool_len, ld, scores, (cudaStream_t)stream);
+}
+
+int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
+              int32_t k, int32_t *out, csa2_stream_t stream)
+{
+    if (rows < 0 || rows > kMaxRows * 16 || k < 1 || k > topk_max_k() || ld < 0) return CSA2_ERR_SHAPE;
+    if (rows == 0) return CSA2_OK;
+    if (!scores || !len || !out) return CSA2_ERR_NULL;
+    if (ld > (int64_t)INT32_MAX) return CSA2_ERR_RANGE;
+    return launch_topk(scores, ld, len, rows, cand, k, out, (cudaStream_t)stream);
+}
+
+int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
+                     int32_t pmax, int32_t *pool, int32_t *pool_len, csa2_stream_t stream)
+{
+    if (rows < 0 || rows > kMaxRows * 16 || pmax < 1 || pmax > CSA2_POOL_BLOCKS || ld_blocks < 0)
+        return CSA2_ERR_SHAPE;
+    if (rows == 0) return CSA2_OK;
+    if (!block_max || !n_visible || !pool || !pool_len) return CSA2_ERR_NULL;
+    if (ld_blocks > (int64_t)INT32_MAX / 8) return CSA2_ERR_RANGE;
+    return launch_topk_blocks(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len,
+                              (cudaStream_t)stream);
+}
+
+size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq)
+{
+    if (batch < 1 || nq < 1) return 0;
+    return attn_workspace_bytes((int64_t)batch * nq);
+}
+
+int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *q, float sm_scale,
+                     const int32_t *idx, int32_t k, const csa2_swa *swa, float *o, float *lse,
+                     void *workspace, size_t workspace_bytes, csa2_stream_t stream)
+{
+    int s = check_cache(cache, true, false);
+    if (s) return s;
+    if ((s = check_batch(batch, cache))) return s;
+    if ((s = check_swa(swa))) return s;
+    if (!q || !idx || !o || !lse) return CSA2_ERR_NULL;
+    if (k < 1 || k > CSA2_TOPK) return CSA2_ERR_SHAPE;
+    const size_t need = attn_workspace_bytes((int64_t)batch->batch * batch->nq);
+    if (need && (!workspace || workspace_bytes < need)) return CSA2_ERR_WORKSPACE;
+    if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
+    if (!aligned(q, 16) || !aligned(o, 16)) return CSA2_ERR_ALIGN;
+    return launch_attn(*cache, *batch, q, sm_scale, idx, k, *swa, o, lse, workspace, workspace_bytes,
+                       (cudaStream_t)stream);
+}
+
+size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
+{
+    if (!batch || batch->batch < 1 || batch->nq < 1 || mode < 0 || mode > 2) return 0;
+    return layer_ws(mode, batch, nullptr).total;
+}
+
+int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, const csa2_layer_io *io,
+               void *workspace, size_t workspace_bytes, csa2_stream_t stream)
+{
+    if (mode < CSA2_MODE_FULL || mode > CSA2_MODE_REUSE) return CSA2_ERR_UNSUPPORTED;
+    int s = check_cache(cache, true, mode != CSA2_MODE_REUSE);
+    if (s) return s;
+    if ((s = check_batch(batch, cache))) return s;
+    if (!io) return CSA2_ERR_NULL;
+    if ((s = check_swa(&io->swa))) return s;
+    if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
+    if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
+    if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
+    LayerWs ws = layer_ws(mode, batch, workspace);
+    if (ws.total && (!workspace || workspace_bytes < ws.total)) return CSA2_ERR_WORKSPACE;
+    if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
+
+    const cudaStream_t st = (cudaStream_t)stream;
+    const int32_t rows = batch->batch * batch->nq;
+    const int64_t ld = score_ld(batch);
+    auto prof = [&](void *ev) {
+        if (!ev) return CSA2_OK;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(st, &cs);
+        if (e == cudaSuccess)
+            e = cs == cudaStreamCaptureStatusActive
+                    ? cudaEventRecordWithFlags((cudaEvent_t)ev, st, cudaEventRecordExternal)
+                    : cudaEventRecord((cudaEvent_t)ev, st);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return CSA2_ERR_CUDA;
+        }
+        return CSA2_OK;
+    };
+    if (mode == CSA2_MODE_FULL) {
+        // a4: scores of every visible entry and the per-block maxima
+        if ((s = prof(io->prof_begin))) return s;
+        if ((s = launch_index_scan(*cache, *batch, io->qi, io->w, ws.scores, ws.block_max, ws.n_visible, ld, st)))
+            return s;
+        if ((s = prof(io->prof_end))) return s;
+        // a5: the best 2,048 blocks of 8 -> candidate pool
+        if ((s = launch_topk_blocks(ws.block_max, ld / 8, ws.n_visible, rows, CSA2_POOL_BLOCKS, io->pool,
+                                    io->pool_len, st)))
+            return s;
+        // a6: Top-512 of the pool
+        if ((s = launch_gather_scores(ws.scores, ld, io->pool, io->pool_len, CSA2_POOL_MAX, rows, ws.pool_scores, st)))
+            return s;
+        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st)))
+            return s;
+    } else if (mode == CSA2_MODE_REINDEX) {
+        // a7: rescore the pool with this layer's indexer query, Top-512
+        if ((s = prof(io->prof_begin))) return s;
+        if ((s = launch_index_pool_simt(*cache, *batch, io->qi, io->w, io->pool, io->pool_len, CSA2_POOL_MAX,
+                                        ws.pool_scores, st)))
+            return s;
+        if ((s = prof(io->prof_end))) return s;
+        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st)))
+            return s;
+    }
+    // a8 (REUSE) keeps io->idx as it is; a9 for every mode
+    return launch_attn(*cache, *batch, io->q, io->sm_scale, io->idx, CSA2_TOPK, io->swa, io->o, io->lse,
+                       ws.attn, ws.attn_bytes, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,137 @@
+// Internal helpers shared by the CSA2 kernels (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+// ---------------------------------------------------------------- host side
+// Last CUDA error recorded by an entry point on this thread.
+void set_cuda_error(cudaError_t e);
+
+inline int launch_status()
+{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
+    return CSA2_OK;
+}
+
+inline int ceil_div_i(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+inline bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// ---------------------------------------------------------------- device side
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ void flag(int32_t *status, int32_t bit)
+{
+    if (status) atomicOr(status, bit);
+}
+
+// Slot of logical entry e of sequence b; -1 (and a flag) if the page id is
+// outside the cache.
+__device__ __forceinline__ int64_t entry_slot(const csa2_cache &c, int b, int64_t e)
+{
+    int32_t page = __ldg(c.block_table + (int64_t)b * c.max_pages + (e >> 6));
+    int64_t slot = (int64_t)page * CSA2_PAGE + (e & 63);
+    if (page < 0 || slot >= c.num_slots) {
+        flag(c.status, CSA2_DEV_BAD_PAGE);
+        return -1;
+    }
+    return slot;
+}
+
+// Entries visible to query row r = b*Q + i ([P3] §3.3 visibility rule).
+__device__ __forceinline__ int64_t visible_entries(const csa2_batch &bt, int64_t r)
+{
+    int b = (int)(r / bt.nq);
+    int64_t t = bt.q_pos[r];
+    int64_t n = bt.n_entries[b];
+    int64_t lim = (t + 1) / bt.m;
+    if (lim < n) n = lim;
+    if (n > bt.max_entries) n = bt.max_entries;
+    if (n < 0) n = 0;
+    return n;
+}
+
+// FP8 e4m3 byte -> float (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte)
+{
+    uint32_t s = (byte & 0x80u) << 24;
+    uint32_t e = (byte >> 3) & 15u;
+    uint32_t m = byte & 7u;
+    float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+    return __uint_as_float(__float_as_uint(mag) | s);
+}
+
+// Two e4m3 bytes (low half of x) -> two halves of a __half2-packed pair via the
+// hardware conversion (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
+    return r;
+}
+
+// E2M1 magnitude code (0..7) -> float magnitude.
+__device__ __forceinline__ float e2m1_mag(uint32_t c)
+{
+    // 0, .5, 1, 1.5, 2, 3, 4, 6
+    const uint32_t e = c >> 1, mb = c & 1u;
+    return e ? __uint_as_float(((e + 126u) << 23) | (mb << 22)) : 0.5f * (float)mb;
+}
+
+__device__ __forceinline__ float e2m1_to_f32(uint32_t nib)
+{
+    float m = e2m1_mag(nib & 7u);
+    return (nib & 8u) ? -m : m;
+}
+
+// 2^k for k in [-126, 127] as a float.
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// Monotone map of a float to an unsigned key (larger float -> larger key);
+// -0.0 and +0.0 map to the same key.
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    if ((u << 1) == 0) u = 0;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        int s = lane < NT / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < NT / 32) warp_sums[lane] = s;   // inclusive
+    }
+    __syncthreads();
+    int base = wid ? warp_sums[wid - 1] : 0;
+    if (total) *total = warp_sums[NT / 32 - 1];
+    int r = base + x - v;
+    __syncthreads();
+    return r;
+}
+
+}  // namespace csa2

@@ -1,0 +1,195 @@
+// a1-a3: the CSA compressor and the MXFP4 / FP8 quantisers.
+//
+// These kernels are memory bound (a few bytes read per byte written), so the
+// design goal is coalesced 16-byte accesses and enough threads in flight:
+//  * compressor: one thread per (entry, channel) in double precision, so the
+//    single rounding to fp32 at the end matches a double-precision reference;
+//  * MXFP4: one thread per 32-element block (128 B in, 16 B codes + 1 B scale
+//    out), 16 consecutive threads covering one 512-dim entry;
+//  * FP8: one warp per row (dim 128 or 512), amax by warp shuffle.
+#include <algorithm>
+
+#include "csa2_internal.cuh"
+
+namespace csa2 {
+
+// e_j[d] = sum_i softmax_i(Z + bias) * C over the m tokens of group j.
+// "DeepSeek-V4 report explainer" §3.1; "DeepSeek-V4.1-Flash 架构详解" §2, §3.2.
+__global__ void __launch_bounds__(256) k_compress(const uint16_t *__restrict__ C,
+                                                  const uint16_t *__restrict__ Z,
+                                                  const float *__restrict__ bias, int m,
+                                                  int64_t n_ent, float *__restrict__ out)
+{
+    const int64_t total = n_ent * CSA2_HEAD_DIM;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = i / CSA2_HEAD_DIM;
+        const int d = (int)(i % CSA2_HEAD_DIM);
+        const int64_t base = j * m * CSA2_HEAD_DIM + d;
+        double zmax = -INFINITY;
+        for (int k = 0; k < m; k++) {
+            double z = (double)bf16_to_f32(Z[base + (int64_t)k * CSA2_HEAD_DIM]) +
+                       (double)bias[k * CSA2_HEAD_DIM + d];
+            zmax = z > zmax ? z : zmax;
+        }
+        double den = 0.0, num = 0.0;
+        for (int k = 0; k < m; k++) {
+            double z = (double)bf16_to_f32(Z[base + (int64_t)k * CSA2_HEAD_DIM]) +
+                       (double)bias[k * CSA2_HEAD_DIM + d];
+            double p = exp(z - zmax);
+            den += p;
+            num += p * (double)bf16_to_f32(C[base + (int64_t)k * CSA2_HEAD_DIM]);
+        }
+        out[i] = (float)(num / den);
+    }
+}
+
+// floor(log2(a)) of a finite a > 0, subnormals included.
+__device__ __forceinline__ int floor_log2(float a)
+{
+    const uint32_t u = __float_as_uint(a);
+    const int e = (int)((u >> 23) & 0xFF);
+    if (e) return e - 127;
+    return (31 - __clz(u & 0x7FFFFF)) - 149;
+}
+
+// E2M1 magnitude code of a >= 0, round to nearest with ties to the even
+// mantissa, saturating at 6: thresholds are the midpoints of the grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6}; a tie takes the even code (0, 2, 4, 6).
+__device__ __forceinline__ uint32_t e2m1_code(float a)
+{
+    return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+           (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+           (uint32_t)(a > 5.0f);
+}
+
+// One thread per 32-element block.  "DeepSeek-V4.1-Flash 架构详解" §4 (OCP MXFP4).
+__global__ void __launch_bounds__(256) k_quant_mxfp4(const float *__restrict__ x, int64_t n,
+                                                     const int64_t *__restrict__ slots,
+                                                     uint8_t *__restrict__ codes,
+                                                     uint8_t *__restrict__ scales, int64_t num_slots,
+                                                     int32_t *status)
+{
+    const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (t >= n * 16) return;
+    const int64_t r = t >> 4;
+    const int blk = (int)(t & 15);
+    const int64_t dst = slots ? slots[r] : r;
+    if (dst < 0) return;
+    if (dst >= num_slots) {
+        flag(status, CSA2_DEV_BAD_SLOT);
+        return;
+    }
+    const float4 *src = reinterpret_cast<const float4 *>(x + r * CSA2_HEAD_DIM + blk * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float4 f = __ldg(src + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(v[i]));
+    int X = 0;
+    if (amax > 0.0f) {
+        X = floor_log2(amax) - 2;
+        X = X < -127 ? -127 : (X > 127 ? 127 : X);
+    }
+    const float inv = exp2i(-X);   // -X in [-125, 127]: a normal float, exact scaling
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        const uint32_t c = e2m1_code(fabsf(v[i] * inv)) | ((__float_as_uint(v[i]) >> 31) << 3);
+        packed[i >> 3] |= c << (4 * (i & 7));
+    }
+    *reinterpret_cast<uint4 *>(codes + dst * 256 + blk * 16) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    scales[dst * 16 + blk] = (uint8_t)(X + 127);
+}
+
+// Two fp32 values -> two e4m3 bytes (lo in the low byte), round to nearest
+// even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One warp per row.  "DeepSeek-V4.1-Flash" research note §3.3 (FP8 SWA KV).
+template <int DIM>
+__global__ void __launch_bounds__(256) k_quant_fp8(const float *__restrict__ x, int64_t n,
+                                                   const int64_t *__restrict__ slots,
+                                                   uint8_t *__restrict__ codes,
+                                                   float *__restrict__ scales, int64_t num_slots,
+                                                   int32_t *status)
+{
+    constexpr int PER = DIM / 128;   // float4 chunks per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+    if (r >= n) return;
+    const int64_t dst = slots ? slots[r] : r;
+    if (dst < 0) return;
+    if (dst >= num_slots) {
+        if (lane == 0) flag(status, CSA2_DEV_BAD_SLOT);
+        return;
+    }
+    const float4 *src = reinterpret_cast<const float4 *>(x + r * DIM);
+    float4 v[PER];
+    float amax = 0.0f;
+#pragma unroll
+    for (int c = 0; c < PER; c++) {
+        v[c] = __ldg(src + c * 32 + lane);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[c].x), fabsf(v[c].y)), fmaxf(fabsf(v[c].z), fabsf(v[c].w))));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    uint32_t *dc = reinterpret_cast<uint32_t *>(codes + dst * DIM);
+#pragma unroll
+    for (int c = 0; c < PER; c++) {
+        const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(v[c].x, s), __fdiv_rn(v[c].y, s));
+        const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(v[c].z, s), __fdiv_rn(v[c].w, s));
+        dc[c * 32 + lane] = lo | (hi << 16);
+    }
+    if (lane == 0) scales[dst] = s;
+}
+
+// ---------------------------------------------------------------- launchers
+int launch_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int m, int64_t n_tok,
+                    float *out, cudaStream_t st)
+{
+    const int64_t n_ent = n_tok / m;
+    if (n_ent == 0) return CSA2_OK;
+    const int64_t total = n_ent * CSA2_HEAD_DIM;
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, 152 * 16);
+    k_compress<<<grid, 256, 0, st>>>(C, Z, bias, m, n_ent, out);
+    return launch_status();
+}
+
+int launch_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
+                       uint8_t *scales, int64_t num_slots, int32_t *status, cudaStream_t st)
+{
+    if (n == 0) return CSA2_OK;
+    const int64_t threads = n * 16;
+    k_quant_mxfp4<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(x, n, slots, codes, scales,
+                                                                     num_slots, status);
+    return launch_status();
+}
+
+int launch_quant_fp8(const float *x, int64_t n, int dim, const int64_t *slots, uint8_t *codes,
+                     float *scales, int64_t num_slots, int32_t *status, cudaStream_t st)
+{
+    if (n == 0) return CSA2_OK;
+    const unsigned grid = (unsigned)((n * 32 + 255) / 256);
+    if (dim == 128)
+        k_quant_fp8<128><<<grid, 256, 0, st>>>(x, n, slots, codes, scales, num_slots, status);
+    else
+        k_quant_fp8<512><<<grid, 256, 0, st>>>(x, n, slots, codes, scales, num_slots, status);
+    return launch_status();
+}
+
+}  // namespace csa2

@@ -30,12 +30,22 @@ _GOLD = 0x9E3779B9
 
 
 # --------------------------------------------------------------------------
-# integer hash (host: numpy uint64 holding 32-bit values)
+# integer hash (host: numpy uint32, whose multiply wraps modulo 2**32 -- the
+# same value as the masked 64-bit product of the device twin)
 # --------------------------------------------------------------------------
-def _mix_np(x: np.ndarray) -> np.ndarray:
-    x = (((x >> 16) ^ x) * _M) & MASK32
-    x = (((x >> 16) ^ x) * _M) & MASK32
-    return (x >> 16) ^ x
+_M32 = np.uint32(_M)
+_S16 = np.uint32(16)
+
+
+def _mix_np(x: np.ndarray, t: np.ndarray) -> np.ndarray:
+    """In-place 32-bit mix of x (t: scratch of the same shape)."""
+    for _ in range(2):
+        np.right_shift(x, _S16, out=t)
+        np.bitwise_xor(x, t, out=x)
+        np.multiply(x, _M32, out=x)
+    np.right_shift(x, _S16, out=t)
+    np.bitwise_xor(x, t, out=x)
+    return x
 
 
 def _mix_int(x: int) -> int:
@@ -59,23 +69,33 @@ def _keys(stream: int, hi: int):
     return k1, k2
 
 
-def hash_np(stream: int, start: int, count: int) -> np.ndarray:
-    """32-bit hashes of element indices [start, start+count) of a stream (uint64 array)."""
-    out = np.empty(count, dtype=np.uint64)
+def _generate(stream: int, start: int, count: int, out: np.ndarray, fn) -> np.ndarray:
+    """out[i] = fn(hash of element start + i), computed in cache-sized chunks."""
+    chunk = 1 << 18
+    x = np.empty(min(chunk, max(count, 1)), dtype=np.uint32)
+    t = np.empty_like(x)
     i = start
     pos = 0
-    while pos < count:                      # split where the high 32 index bits change
+    while pos < count:                      # never cross a change of the high 32 index bits
         hi = i >> 32
         lo = i & MASK32
-        n = min(count - pos, (1 << 32) - lo)
+        n = min(count - pos, (1 << 32) - lo, chunk)
         k1, k2 = _keys(stream, hi)
-        x = np.arange(lo, lo + n, dtype=np.uint64)
-        x = _mix_np(x ^ np.uint64(k1))
-        x = _mix_np(x ^ np.uint64(k2))
-        out[pos:pos + n] = x
+        xv, tv = x[:n], t[:n]
+        xv[:] = np.arange(lo, lo + n, dtype=np.uint64)
+        np.bitwise_xor(xv, np.uint32(k1), out=xv)
+        _mix_np(xv, tv)
+        np.bitwise_xor(xv, np.uint32(k2), out=xv)
+        _mix_np(xv, tv)
+        out[pos:pos + n] = fn(xv)
         pos += n
         i += n
     return out
+
+
+def hash_np(stream: int, start: int, count: int) -> np.ndarray:
+    """32-bit hashes of element indices [start, start+count) of a stream (uint32 array)."""
+    return _generate(stream, start, count, np.empty(count, np.uint32), lambda h: h)
 
 
 def hash_torch(stream: int, start: int, count: int, device):
@@ -137,20 +157,22 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 # --------------------------------------------------------------------------
 # samplers
 # --------------------------------------------------------------------------
+def _lookup(table: np.ndarray):
+    return lambda h: table.take((h >> _S16).astype(np.intp))
+
+
 def normal_bf16(stream: int, start: int, count: int, sigma: float = 1.0) -> np.ndarray:
     """bf16 bit patterns (uint16) of N(0, sigma^2) samples."""
-    h = hash_np(stream, start, count)
-    return normal_table_bf16(sigma)[(h >> 16).astype(np.int64)]
+    return _generate(stream, start, count, np.empty(count, np.uint16), _lookup(normal_table_bf16(sigma)))
 
 
 def normal_f32(stream: int, start: int, count: int, sigma: float = 1.0) -> np.ndarray:
-    h = hash_np(stream, start, count)
-    return normal_table_f32(sigma)[(h >> 16).astype(np.int64)]
+    return _generate(stream, start, count, np.empty(count, np.float32), _lookup(normal_table_f32(sigma)))
 
 
 def uniform_f32(stream: int, start: int, count: int) -> np.ndarray:
     h = hash_np(stream, start, count)
-    return (((h >> 9).astype(np.float64) + 0.5) * 2.0 ** -23).astype(np.float32)
+    return (((h >> np.uint32(9)).astype(np.float64) + 0.5) * 2.0 ** -23).astype(np.float32)
 
 
 def normal_bf16_torch(stream: int, start: int, count: int, device, sigma: float = 1.0):

@@ -1,0 +1,285 @@
+/*
+ * csa2.h -- C ABI of the CSA2 (Compressed Sparse Attention 2) attention step
+ * for one GB300 GPU (sm_103a).
+ *
+ * Sources for the operations (page title, section):
+ *   [P1] "DeepSeek-V4.1-Flash" research note (vibe-research.pages.dev)
+ *   [P2] "DeepSeek-V4.1-Flash 架构详解：CED、CSA2 与 890 字节 KV Cache" (gentlecold.top)
+ *   [P3] DeepSeek-V4 report explainer (mlqm.cn)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All data pointers are DEVICE pointers unless a comment says otherwise.
+ *   The caller owns every buffer (caches, block tables, inputs, outputs,
+ *   workspaces); the library never allocates, frees or keeps a pointer past
+ *   the call.
+ * - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *   stream).  Host pointers to descriptor structs are read during the call
+ *   only.
+ * - Every function returns CSA2_OK (0) or a negative csa2 status.  Shapes and
+ *   pointers are validated on the host before any launch; nothing is launched
+ *   when validation fails.  A launch failure returns CSA2_ERR_CUDA and
+ *   csa2_last_cuda_error() gives the cudaError_t.
+ * - Data-dependent faults found on the device (a block-table page id outside
+ *   the cache, a slot outside the cache) skip the offending access and set
+ *   a bit in the cache's optional device status word (csa2_cache.status,
+ *   CSA2_DEV_* bits), which the caller may read after synchronising.
+ * - bf16 tensors are passed as uint16_t bit patterns.
+ *
+ * Cache layout (per compressed entry "slot"; one block-table page = 64 slots)
+ * ---------------------------------------------------------------------------
+ *   kv_codes  [num_slots][256]  MXFP4 E2M1 codes of the 512-dim main KV entry:
+ *                               element 2i in the low nibble of byte i,
+ *                               element 2i+1 in the high nibble; nibble bit 3
+ *                               is the sign.  [P2] §4 (OCP MXFP4, E2M1).
+ *   kv_scales [num_slots][16]   E8M0 scale byte (2^(byte-127)) of each
+ *                               32-element block (OCP MX block size).
+ *   ik_codes  [num_slots][128]  FP8 e4m3 codes of the 128-dim indexer key.
+ *   ik_scales [num_slots]       fp32 per-entry scale of the indexer key.
+ * Logical entry e of sequence b lives in slot
+ *   block_table[b * max_pages + e / 64] * 64 + e % 64.
+ * The main KV and the indexer keys of an entry share that slot: both are
+ * produced by a Full layer and reused by the layers after it ([P2] §3 mode
+ * table).
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define CSA2_OK               0
+#define CSA2_ERR_NULL        (-1)  /* a required pointer is NULL            */
+#define CSA2_ERR_SHAPE       (-2)  /* a size or count is out of range       */
+#define CSA2_ERR_UNSUPPORTED (-3)  /* valid but not implemented (e.g. mode) */
+#define CSA2_ERR_RANGE       (-4)  /* index / length beyond a buffer        */
+#define CSA2_ERR_WORKSPACE   (-5)  /* workspace missing or too small        */
+#define CSA2_ERR_TIMEOUT     (-6)  /* a bounded device wait gave up         */
+#define CSA2_ERR_CUDA        (-7)  /* a CUDA call failed (see below)        */
+#define CSA2_ERR_ALIGN       (-8)  /* a pointer lacks the required alignment */
+
+/* bits of the device status word */
+#define CSA2_DEV_BAD_PAGE     1    /* block-table page id outside the cache */
+#define CSA2_DEV_BAD_SLOT     2    /* destination slot outside the cache    */
+#define CSA2_DEV_TIMEOUT      4    /* a bounded spin-wait ran out            */
+#define CSA2_DEV_BAD_INDEX    8    /* a selected index outside the context   */
+
+/* ---- fixed dimensions ([P2] §1 configuration table) ---------------------- */
+#define CSA2_HEADS         64     /* query heads                             */
+#define CSA2_HEAD_DIM      512    /* head dim = main KV entry width (MQA)    */
+#define CSA2_IDX_HEADS     32     /* lightning-indexer heads                  */
+#define CSA2_IDX_DIM       128    /* lightning-indexer dim                    */
+#define CSA2_TOPK          512    /* selected entries per query               */
+#define CSA2_BLOCK         8      /* positions per candidate block            */
+#define CSA2_POOL_BLOCKS   2048   /* blocks kept by a Full layer              */
+#define CSA2_POOL_MAX      16384  /* = CSA2_POOL_BLOCKS * CSA2_BLOCK          */
+#define CSA2_SWA_WINDOW    128    /* sliding-window tokens                    */
+#define CSA2_PAGE          64     /* slots per block-table page               */
+#define CSA2_MX_BLOCK      32     /* elements per MX scale                    */
+
+/* layer modes ([P2] §3 mode table) */
+#define CSA2_MODE_FULL     0
+#define CSA2_MODE_REINDEX  1
+#define CSA2_MODE_REUSE    2
+
+/* ---- descriptors -------------------------------------------------------- */
+
+/* The layer-shared global cache of compressed entries. */
+typedef struct csa2_cache {
+    uint8_t       *kv_codes;     /* [num_slots][256]                         */
+    uint8_t       *kv_scales;    /* [num_slots][16]                          */
+    uint8_t       *ik_codes;     /* [num_slots][128]                         */
+    float         *ik_scales;    /* [num_slots]                              */
+    int64_t        num_slots;    /* > 0, multiple of 64                      */
+    const int32_t *block_table;  /* [batch][max_pages] page ids              */
+    int32_t        max_pages;    /* row stride of block_table, > 0           */
+    int32_t       *status;       /* device status word (CSA2_DEV_*), or NULL */
+} csa2_cache;
+
+/* A batch of sequences, each with nq query tokens. */
+typedef struct csa2_batch {
+    int32_t        batch;        /* B >= 1                                   */
+    int32_t        nq;           /* queries per sequence Q >= 1              */
+    int32_t        m;            /* compression ratio (1 decoder, 2 encoder) */
+    int32_t        pad_;
+    int64_t        max_entries;  /* host-side bound on n_entries[b]; sizes
+                                    grids and score rows                      */
+    const int64_t *n_entries;    /* [B] entries held in the cache (device)    */
+    const int64_t *q_pos;        /* [B*Q] token position t of each query;
+                                    entry j is visible to it iff
+                                    (j+1)*m - 1 <= t and j < n_entries[b]
+                                    ([P3] §3.3: a query cannot see the rest
+                                    of its own unfinished block)              */
+} csa2_batch;
+
+/* One layer's FP8 sliding-window KV ([P1] §3.3 / [P2] §4: FP8, per layer).
+ * A ring of `rows` token rows per sequence: token t lives in row t % rows.
+ * The window of the query at token t is SWAKeys(t) = [max(s, t-127), t]
+ * ([P2] §5 bounded-replay equation), s = start[b] (0 when start is NULL).
+ * The caller guarantees that every window token of every query of the call
+ * is present in its row (rows >= 128 + spread of query positions). */
+typedef struct csa2_swa {
+    const uint8_t *codes;        /* [B][rows][512] e4m3                       */
+    const float   *scales;       /* [B][rows] fp32 per-token scale            */
+    int32_t        rows;         /* ring capacity, >= 128                     */
+    int32_t        pad_;
+    const int64_t *start;        /* [B] replay start s, or NULL               */
+} csa2_swa;
+
+/* Per-layer inputs, outputs and carried selection state for csa2_layer. */
+typedef struct csa2_layer_io {
+    const uint16_t *q;           /* bf16 [B*Q][64][512] attention queries      */
+    const uint16_t *qi;          /* bf16 [B*Q][32][128] indexer queries        */
+    const float    *w;           /* [B*Q][32] indexer head weights             */
+    csa2_swa        swa;         /* this layer's window                        */
+    float           sm_scale;    /* multiplies q.k (1 if q is pre-scaled)     */
+    int32_t         pad_;
+    int32_t        *idx;         /* [B*Q][512] selection (written by FULL and
+                                    REINDEX, read by every mode)              */
+    int32_t        *pool;        /* [B*Q][16384] candidate pool (written by
+                                    FULL, read by REINDEX)                    */
+    int32_t        *pool_len;    /* [B*Q]                                     */
+    float          *o;           /* [B*Q][64][512] attention output           */
+    float          *lse;         /* [B*Q][64] natural-log sum of exp          */
+    void           *prof_begin;  /* optional cudaEvent_t recorded on the stream
+                                    just before the layer's index kernel (the
+                                    Full scan / the Reindex pool rescoring),
+                                    as an external node when captured; NULL
+                                    for none                                   */
+    void           *prof_end;    /* optional cudaEvent_t recorded just after it */
+} csa2_layer_io;
+
+/* ---- a1: compressor ------------------------------------------------------
+ * e_j[d] = sum_{i<m} softmax_i(Z[jm+i][d] + bias[i][d]) * C[jm+i][d]
+ * [P3] §3.1 (softmax-weighted pooling of m tokens with a learned bias);
+ * [P2] §2 (C, Z projected per layer), §3.1-3.2 (m = 2 encoder, m = 1 decoder,
+ * no overlap, bias by offset within the group).
+ *   C, Z  bf16 [n_tok][512];  bias fp32 [m][512];  out fp32 [n_tok/m][512].
+ *   Trailing n_tok % m tokens are not compressed.  1 <= m <= 16.
+ *   Computed in double precision and rounded once to fp32. */
+CSA2_API int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int32_t m,
+                  int64_t n_tok, float *out, csa2_stream_t stream);
+
+/* ---- a2: MXFP4 quantisation of main-KV entries ----------------------------
+ * Per 32-element block: X = floor(log2(amax)) - 2 (0 if amax == 0), clamped
+ * to [-127, 127], stored as E8M0 byte X + 127; each element x becomes the
+ * E2M1 value nearest to x * 2^-X (ties to even mantissa, saturating at 6),
+ * its sign bit copying x's.  [P2] §4; OCP MX block 32 / E8M0.
+ *   x      fp32 [n][512] (finite values)
+ *   slots  int64 [n] destination slot of each row, or NULL for row i -> slot i;
+ *          a negative slot skips the row; a slot >= num_slots is skipped and
+ *          flagged CSA2_DEV_BAD_SLOT in *status (status may be NULL).
+ *   codes  [num_slots][256], scales [num_slots][16]  (a csa2_cache's kv_*). */
+CSA2_API int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
+                     uint8_t *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
+
+/* ---- a3: FP8 e4m3 quantisation with a per-row fp32 scale -----------------
+ * s = amax / 448 (IEEE fp32 division; s = 1 when amax == 0); each element
+ * code = e4m3(x / s) (IEEE fp32 division, round to nearest even, saturating
+ * at 448, sign kept).  Used for the SWA rows ([P1] §3.3, [P2] §4) and the
+ * indexer keys.
+ *   x fp32 [n][dim], dim in {128, 512}; slots as for csa2_quant_mxfp4;
+ *   codes [num_slots][dim], scales [num_slots]. */
+CSA2_API int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
+                   float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
+
+/* ---- a4: lightning-indexer scores over every visible entry ---------------
+ * score(p) = sum_h w[h] * ReLU(qi[h] . k_p), k_p = e4m3(code_p) * scale_p,
+ * for every entry p visible to each query; block_max[b8] = max over the
+ * visible positions of block b8 (positions 8*b8 .. 8*b8+7).
+ * [P3] §3.2 (low-dimensional query against compressed index keys);
+ * [P1] §3.2 and [P2] §3.2 (block aggregation of index scores, blocks of 8).
+ *   qi bf16 [B*Q][32][128]; w fp32 [B*Q][32]
+ *   scores     fp32 [B*Q][ld] or NULL (positions >= visible are not written)
+ *   block_max  fp32 [B*Q][ld/8] or NULL (at least one of the two non-NULL)
+ *   n_visible  int32 [B*Q] visible entries per query, or NULL
+ *   ld         row stride, multiple of 8, >= batch->max_entries. */
+CSA2_API int csa2_index_scores(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi,
+                      const float *w, float *scores, float *block_max, int32_t *n_visible,
+                      int64_t ld, csa2_stream_t stream);
+
+/* Reindex variant ([P2] §3.2: later layers rescore only the pool): scores of
+ * the entries listed in pool[r][0 .. pool_len[r]).
+ *   pool int32 [B*Q][ld] ascending positions; pool_len int32 [B*Q] (<= ld);
+ *   scores fp32 [B*Q][ld] (slot i of row r = score of pool[r][i]). */
+CSA2_API int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi,
+                           const float *w, const int32_t *pool, const int32_t *pool_len,
+                           int64_t ld, float *scores, csa2_stream_t stream);
+
+/* ---- a5/a6: Top-K selection ---------------------------------------------
+ * For each of `rows` rows: the k slots i < len[r] with the largest scores
+ * (ties -> lower slot), reported as positions (cand[r][i] when cand is
+ * non-NULL, else i) in ascending order, the rest of out[r][0..k) set to -1.
+ * With ascending cand rows, "lower slot" is "lower position".  -0.0 and +0.0
+ * compare equal.  [P2] §1 table (top-k 512), §3.2 ("its own Top-512").
+ *   scores fp32 [rows][ld]; len int32 [rows] (clamped to [0, ld]);
+ *   cand int32 [rows][ld] or NULL; out int32 [rows][k]; 1 <= k <= 4096. */
+CSA2_API int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows,
+              const int32_t *cand, int32_t k, int32_t *out, csa2_stream_t stream);
+
+/* Block level of the hierarchy ([P1] §3.2, [P2] §3.2): for each row keep the
+ * pmax blocks with the largest block_max (ties -> lower block) among the
+ * ceil(n_visible[r] / 8) blocks, and write all their visible positions in
+ * ascending order to pool[r] (pool_len[r] of them).
+ *   block_max fp32 [rows][ld_blocks]; n_visible int32 [rows];
+ *   pool int32 [rows][pmax*8]; pool_len int32 [rows]; 1 <= pmax <= 2048. */
+CSA2_API int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible,
+                     int32_t rows, int32_t pmax, int32_t *pool, int32_t *pool_len,
+                     csa2_stream_t stream);
+
+/* ---- a9: sparse MQA + SWA attention --------------------------------------
+ * For each query (b, i) at token t: key set = the selected entries
+ * idx[r][0..k) != -1 (MXFP4 main KV, dequantised exactly) followed by the
+ * window rows of tokens [max(s, t-127), t] (FP8, times the row scale); each
+ * key is also its value ([P3] §4.3).  For every head h:
+ *   l_j = sm_scale * q_h . k_j,  o_h = sum_j softmax(l)_j k_j,
+ *   lse_h = log sum_j exp(l_j);  an empty key set gives o_h = 0, lse_h = -inf.
+ * One softmax covers both branches ([P2] §1 table, §3; [P3] §3.3).
+ *   q bf16 [B*Q][64][512]; idx int32 [B*Q][k], 1 <= k <= 512 (an index at
+ *   or beyond the query's visible entries is skipped and flagged
+ *   CSA2_DEV_BAD_INDEX); o fp32 [B*Q][64][512]; lse fp32 [B*Q][64]. */
+CSA2_API int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *q,
+                     float sm_scale, const int32_t *idx, int32_t k, const csa2_swa *swa,
+                     float *o, float *lse, void *workspace, size_t workspace_bytes,
+                     csa2_stream_t stream);
+
+CSA2_API size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq);
+
+/* ---- a10: one CSA2 layer ---------------------------------------------------
+ * mode CSA2_MODE_FULL    : index every visible entry, pool of the best 2,048
+ *                          blocks of 8, Top-512 of the pool -> io->idx,
+ *                          io->pool, io->pool_len; attention.
+ *      CSA2_MODE_REINDEX : rescore io->pool with this layer's (qi, w),
+ *                          Top-512 -> io->idx; attention.
+ *      CSA2_MODE_REUSE   : attention with io->idx as it is.
+ * [P2] §3 mode table and §3.2; [P1] §3.2.  The main KV and the indexer keys
+ * are the cache's (the latest Full layer's).  workspace must hold
+ * csa2_layer_workspace_size(mode, batch) bytes, 256-byte aligned. */
+CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch,
+               const csa2_layer_io *io, void *workspace, size_t workspace_bytes,
+               csa2_stream_t stream);
+
+CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch);
+
+/* ---- errors -------------------------------------------------------------- */
+CSA2_API const char *csa2_status_string(int32_t status);   /* static string, never NULL */
+CSA2_API int32_t     csa2_last_cuda_error(void);           /* cudaError_t of the last
+                                                     CSA2_ERR_CUDA on this thread */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

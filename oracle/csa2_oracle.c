@@ -134,6 +134,7 @@ int or_mx_exponent(float amax)
  * in the low nibble of byte i, 2i+1 in the high nibble; scales: [n][16] E8M0. */
 void or_quant_mxfp4(const float *x, int64_t n, uint8_t *codes, uint8_t *scales)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; r++) {
         const float *row = x + r * 512;
         for (int b = 0; b < 16; b++) {
@@ -156,6 +157,7 @@ void or_quant_mxfp4(const float *x, int64_t n, uint8_t *codes, uint8_t *scales)
 /* Exact decode of n MXFP4 entries to doubles [n][512]. */
 void or_dequant_mxfp4(const uint8_t *codes, const uint8_t *scales, int64_t n, double *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; r++)
         for (int d = 0; d < 512; d++) {
             uint8_t byte = codes[r * 256 + d / 2];
@@ -175,6 +177,7 @@ void or_dequant_mxfp4(const uint8_t *codes, const uint8_t *scales, int64_t n, do
  * stated reading for both the SWA rows and the indexer keys. */
 void or_quant_fp8(const float *x, int64_t n, int dim, uint8_t *codes, float *scales)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n; r++) {
         const float *row = x + r * dim;
         float amax = 0.0f;
@@ -239,11 +242,14 @@ void or_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int m,
  * ReLU-weighted head sum is the stated reading. */
 double or_index_score(const uint16_t *qi, const float *w, const uint8_t *code, float scale)
 {
+    double k[128];
+    for (int d = 0; d < 128; d++)
+        k[d] = or_e4m3_value(code[d]) * (double)scale;      /* dequantised key */
     double s = 0.0;
     for (int h = 0; h < 32; h++) {
         double dot = 0.0;
         for (int d = 0; d < 128; d++)
-            dot += bf16_value(qi[h * 128 + d]) * (or_e4m3_value(code[d]) * (double)scale);
+            dot += bf16_value(qi[h * 128 + d]) * k[d];
         s += (double)w[h] * (dot > 0.0 ? dot : 0.0);
     }
     return s;

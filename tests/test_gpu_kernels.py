@@ -1,0 +1,211 @@
+"""Parity of each CUDA entry point against the CPU oracle (needs a GPU).
+
+Bit-exact: quantisers, Top-K given identical scores, pool construction.
+Tolerances (floating point): compressor rounds once from double precision on
+both sides; indexer scores rel 1e-5 (fp32 accumulation of exact products vs
+double); attention max-abs 2e-3 and rel-L2 1e-3 given identical indices.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_layer_gb300 import csa2, synth
+from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
+from compressed_sparse_attention_layer_gb300 import workloads as W
+from tests.reference import SeqOracle, attn_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from compressed_sparse_attention_layer_gb300 import build
+    build.build()
+    csa2.load()
+
+
+def _special_rows(n_rows, dim, seed):
+    """Random rows plus rows built to hit ties, signed zeros, subnormals and saturation."""
+    rng = np.random.default_rng(seed)
+    x = (rng.standard_normal((n_rows, dim)) * np.exp(rng.uniform(-6, 6, (n_rows, 1)))).astype(np.float32)
+    # MXFP4 ties: blocks whose amax is 6 contain every grid midpoint
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.9, 0.5, 3.0, 0.1], np.float32)
+    x[0, :mids.size] = mids
+    x[0, 16:16 + mids.size] = -mids
+    x[1] = 0.0
+    x[1, 3] = -0.0
+    x[2, :] = np.float32(1e-41)              # subnormal block maxima
+    x[2, 5] = np.float32(-3e-42)
+    x[3, :] = np.float32(3e38)               # huge values
+    x[3, 7] = np.float32(-1.7e38)
+    x[4, :] = -0.0
+    x[5, ::2] = np.float32(2.0 ** -130)
+    return x
+
+
+def test_quant_mxfp4_bit_exact():
+    x = _special_rows(300, 512, 1)
+    codes, scales = oracle.quant_mxfp4(x)
+    xd = torch.from_numpy(x).cuda()
+    gc = torch.zeros((320, 256), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((320, 16), dtype=torch.uint8, device="cuda")
+    csa2.csa2_quant_mxfp4(xd, gc, gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(gc[:300].cpu().numpy(), codes)
+    assert np.array_equal(gs[:300].cpu().numpy(), scales)
+    # slot mapping: scattered destinations, negative slots skipped
+    perm = np.random.default_rng(2).permutation(320)[:300].astype(np.int64)
+    perm[7] = -1
+    gc.zero_()
+    gs.zero_()
+    csa2.csa2_quant_mxfp4(xd, gc, gs, slots=torch.from_numpy(perm).cuda())
+    torch.cuda.synchronize()
+    got_c, got_s = gc.cpu().numpy(), gs.cpu().numpy()
+    keep = perm >= 0
+    assert np.array_equal(got_c[perm[keep]], codes[keep]) and np.array_equal(got_s[perm[keep]], scales[keep])
+
+
+@pytest.mark.parametrize("dim", [128, 512])
+def test_quant_fp8_bit_exact(dim):
+    x = _special_rows(257, dim, 3 + dim)
+    x[6, :] = 0.0
+    x[7, :] = np.float32(448.0)
+    x[8, :] = np.linspace(-1, 1, dim, dtype=np.float32)
+    codes, scales = oracle.quant_fp8(x)
+    gc = torch.zeros((257, dim), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((257,), dtype=torch.float32, device="cuda")
+    csa2.csa2_quant_fp8(torch.from_numpy(x).cuda(), gc, gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(gs.cpu().numpy().view(np.uint32), scales.view(np.uint32))
+    got = gc.cpu().numpy()
+    bad = np.argwhere(got != codes)
+    assert bad.size == 0, (bad[:5], x[tuple(bad[0])], got[tuple(bad[0])], codes[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("m", [1, 2, 4])
+def test_compress_matches_oracle(m):
+    n_tok = 1000 * m + (m - 1)
+    C = synth.normal_bf16(synth.stream_id(50, 1), 0, n_tok * 512).reshape(n_tok, 512)
+    Z = synth.normal_bf16(synth.stream_id(50, 2), 0, n_tok * 512).reshape(n_tok, 512)
+    bias = synth.normal_f32(synth.stream_id(50, 3), 0, m * 512, sigma=0.1).reshape(m, 512)
+    want = oracle.compress(C, Z, bias, m)
+    out = torch.empty((n_tok // m, 512), dtype=torch.float32, device="cuda")
+    t = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    csa2.csa2_compress(t(C), t(Z), torch.from_numpy(bias).cuda(), m, out)
+    got = out.cpu().numpy()
+    # both sides round once from double precision: differences need a last-bit exp tie
+    diff = got.view(np.uint32) != want.view(np.uint32)
+    assert diff.mean() <= 1e-5, diff.sum()
+    assert np.allclose(got, want, rtol=2e-7, atol=0)
+
+
+def _dw(wl, **kw):
+    return DeviceWorkload(wl, **kw)
+
+
+def test_index_scores_decode_small():
+    wl = W.decode_small()
+    dw = _dw(wl)
+    so = SeqOracle(wl, 0)
+    ld = (wl.max_entries + 7) // 8 * 8
+    scores = torch.full((1, ld), np.nan, dtype=torch.float32, device="cuda")
+    bmax = torch.full((1, ld // 8), np.nan, dtype=torch.float32, device="cuda")
+    nvis = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    csa2.csa2_index_scores(dw.cstruct, dw.batch, dw.qi[0], dw.w[0], scores, bmax, nvis, ld)
+    torch.cuda.synchronize()
+    want = so.scores(0, 0, np.arange(wl.entries(0)))
+    got = scores[0].cpu().numpy().astype(np.float64)
+    assert int(nvis[0]) == wl.entries(0)
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-5 * np.abs(want).max())
+    assert np.array_equal(bmax[0].cpu().numpy(), scores[0].cpu().numpy().reshape(-1, 8).max(axis=1))
+    assert int(dw.cache.status[0]) == 0
+
+
+def test_topk_bit_exact_given_scores():
+    rng = np.random.default_rng(9)
+    rows, ld = 6, 50000
+    s = rng.integers(0, 300, (rows, ld)).astype(np.float32) * np.float32(0.5)     # heavy ties
+    s[1] = -s[1]
+    s[2, :100] = -0.0
+    s[2, 100:] = -1.0
+    lens = np.array([50000, 49999, 40000, 600, 512, 3], np.int32)
+    cand = np.sort(rng.choice(10 ** 6, (rows, ld)), axis=1).astype(np.int32)
+    for use_cand in (False, True):
+        out = torch.empty((rows, 512), dtype=torch.int32, device="cuda")
+        csa2.csa2_topk(torch.from_numpy(s).cuda(), torch.from_numpy(lens).cuda(), 512, out,
+                       cand=torch.from_numpy(cand).cuda() if use_cand else None)
+        got = out.cpu().numpy()
+        for r in range(rows):
+            n = lens[r]
+            want = oracle.topk(s[r, :n].astype(np.float64), cand[r, :n] if use_cand else None)
+            assert np.array_equal(got[r], want), (r, use_cand)
+
+
+def test_topk_blocks_bit_exact():
+    rng = np.random.default_rng(10)
+    rows = 4
+    nvis = np.array([1 << 20, 1000003, 16384 * 8 + 5, 9], np.int32)
+    ld_b = (int(nvis.max()) + 7) // 8
+    bm = rng.integers(0, 5000, (rows, ld_b)).astype(np.float32)
+    pool = torch.full((rows, 16384), -7, dtype=torch.int32, device="cuda")
+    plen = torch.zeros((rows,), dtype=torch.int32, device="cuda")
+    csa2.csa2_topk_blocks(torch.from_numpy(bm).cuda(), torch.from_numpy(nvis).cuda(), 2048, pool, plen)
+    got, gl = pool.cpu().numpy(), plen.cpu().numpy()
+    for r in range(rows):
+        n = int(nvis[r])
+        scores = np.repeat(bm[r, :(n + 7) // 8].astype(np.float64), 8)[:n]   # block max = that value
+        want = oracle.block_pool(scores, n)
+        assert gl[r] == want.size and np.array_equal(got[r, :gl[r]], want), r
+
+
+def test_sparse_attn_given_oracle_indices():
+    wl = W.decode_small()
+    dw = _dw(wl)
+    so = SeqOracle(wl, 0)
+    idx, pool, _ = so.full(0, 0)
+    o_ref, lse_ref = so.attention(0, 0, idx)
+    o = torch.empty((1, 64, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((1, 64), dtype=torch.float32, device="cuda")
+    ws_n = csa2.csa2_sparse_attn_workspace_size(1, 1)
+    ws = torch.empty((max(ws_n, 256),), dtype=torch.uint8, device="cuda")
+    csa2.csa2_sparse_attn(dw.cstruct, dw.batch, dw.q[0], 1.0, torch.from_numpy(idx[None]).cuda(), dw.swa(0),
+                          o, lse, workspace=ws)
+    ok, info = attn_close(o[0].cpu().numpy(), lse[0].cpu().numpy(), o_ref, lse_ref)
+    assert ok, info
+    # a shorter, padded selection (-1 slots) and the window alone
+    idx2 = idx.copy()
+    idx2[100:] = -1
+    o_ref2, lse_ref2 = so.attention(0, 0, idx2)
+    csa2.csa2_sparse_attn(dw.cstruct, dw.batch, dw.q[0], 1.0, torch.from_numpy(idx2[None]).cuda(), dw.swa(0),
+                          o, lse, workspace=ws)
+    ok, info = attn_close(o[0].cpu().numpy(), lse[0].cpu().numpy(), o_ref2, lse_ref2)
+    assert ok, info
+    idx3 = np.full_like(idx, -1)
+    o_ref3, lse_ref3 = so.attention(0, 0, idx3)
+    csa2.csa2_sparse_attn(dw.cstruct, dw.batch, dw.q[0], 1.0, torch.from_numpy(idx3[None]).cuda(), dw.swa(0),
+                          o, lse, workspace=ws)
+    ok, info = attn_close(o[0].cpu().numpy(), lse[0].cpu().numpy(), o_ref3, lse_ref3)
+    assert ok, info
+
+
+def test_device_generator_matches_host():
+    s = synth.stream_id(3, 4, 5)
+    for start, count in [(0, 100000), ((1 << 32) - 500, 1000)]:
+        a = synth.normal_bf16(s, start, count)
+        b = synth.normal_bf16_torch(s, start, count, "cuda").view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(a, b)
+        assert np.array_equal(synth.uniform_f32(s, start, count),
+                              synth.uniform_f32_torch(s, start, count, "cuda").cpu().numpy())
+
+
+def test_bad_page_ids_are_flagged_not_read():
+    wl = W.decode_small()
+    dw = _dw(wl)
+    dw.cache.block_table[0, 3] = 10 ** 6          # outside the cache
+    dw.cache.block_table[0, 5] = -4
+    dw.cstruct = dw.cache.struct()
+    dw.run_layer(0)
+    torch.cuda.synchronize()
+    assert int(dw.cache.status[0]) & csa2.DEV_BAD_PAGE
+    assert torch.isfinite(dw.o[0]).all()
