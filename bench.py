@@ -193,12 +193,14 @@ def run_native(args):
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
+    torch.cuda.nvtx.range_push("csa2_timed")
     with torch.cuda.stream(s):
         ev0.record(s)
         for _ in range(args.steps):
             g.replay()
         ev1.record(s)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
