@@ -61,6 +61,8 @@ EXPORTS = {
     "csa2_layer": (ctypes.c_int, [_i32, ctypes.POINTER(Cache), ctypes.POINTER(Batch), ctypes.POINTER(LayerIO),
                                   _vp, _sz, _vp]),
     "csa2_layer_workspace_size": (_sz, [_i32, ctypes.POINTER(Batch)]),
+    "csa2_layer_noalloc": (ctypes.c_int, [_i32, ctypes.POINTER(Cache), ctypes.POINTER(Batch),
+                                          ctypes.POINTER(LayerIO), _vp]),
     "csa2_status_string": (ctypes.c_char_p, [_i32]),
     "csa2_last_cuda_error": (_i32, []),
 }
@@ -237,3 +239,9 @@ def csa2_layer(mode: int, cache: Cache, batch: Batch, io: LayerIO, workspace, st
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("csa2_layer", load().csa2_layer(int(mode), ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(io),
                                            _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def csa2_layer_noalloc(mode: int, cache: Cache, batch: Batch, io: LayerIO, stream=None):
+    """csa2_layer with the library's static scratch instead of a caller workspace."""
+    _check("csa2_layer_noalloc", load().csa2_layer_noalloc(int(mode), ctypes.byref(cache), ctypes.byref(batch),
+                                                           ctypes.byref(io), _stream(stream)))

@@ -274,6 +274,28 @@ CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch 
 
 CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch);
 
+/* ---- allocation-free layer call --------------------------------------------
+ * No counterpart in the source pages: a library convenience for callers that
+ * cannot allocate device memory per call (a plugin whose host program owns
+ * every device allocation, a serving loop that allocates nothing after
+ * start-up).  Same computation and arguments as csa2_layer without the
+ * workspace: the scratch is one static device array of
+ * CSA2_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library, held on
+ * every GPU that loads the library until the process exits.
+ * - Returns CSA2_ERR_WORKSPACE, before any device work, when
+ *   csa2_layer_workspace_size(mode, batch) exceeds CSA2_NOALLOC_SCRATCH_BYTES
+ *   (for example a Full layer over 8 x 1M entries); use csa2_layer there.
+ * - The first call on a device looks up the array's device address with that
+ *   device current (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.  `stream` must belong to the current device.
+ * - Every call on a device shares the one array, which keeps the previous
+ *   call's contents (nothing in it needs to start at zero).  Calls whose
+ *   work overlaps on the GPU (other streams, other host threads) race on it
+ *   and corrupt each other's results: serialise them. */
+#define CSA2_NOALLOC_SCRATCH_BYTES (16u << 20)
+CSA2_API int csa2_layer_noalloc(int32_t mode, const csa2_cache *cache, const csa2_batch *batch,
+                                const csa2_layer_io *io, csa2_stream_t stream);
+
 /* ---- errors -------------------------------------------------------------- */
 CSA2_API const char *csa2_status_string(int32_t status);   /* static string, never NULL */
 CSA2_API int32_t     csa2_last_cuda_error(void);           /* cudaError_t of the last

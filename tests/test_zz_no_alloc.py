@@ -1,0 +1,80 @@
+"""csa2_layer_noalloc: the layer call for callers that cannot allocate.
+
+A caller that cannot hand the library a workspace buffer (a plugin whose host
+program owns all device memory, a serving loop that allocates nothing after
+start-up) uses this entry point; its scratch is a static device array of
+CSA2_NOALLOC_SCRATCH_BYTES inside the library.  These checks compare it with
+csa2_layer given a caller workspace, on the same inputs, for two calls in a
+row (the array keeps the previous call's contents), and check that work too
+large for the array is refused before anything runs.
+
+Collected last on purpose (file name), so a run that stops at the first
+failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from compressed_sparse_attention_layer_gb300 import csa2
+from compressed_sparse_attention_layer_gb300 import workloads as W
+from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
+from tests.reference import attn_close
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 16 << 20
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from compressed_sparse_attention_layer_gb300 import build
+    build.build()
+    csa2.load()
+
+
+def _run(dw, use_noalloc):
+    dw.idx.fill_(-1)
+    dw.pool.fill_(-1)
+    dw.pool_len.zero_()
+    out = {}
+    for l in dw.layers:
+        dw.o[l].fill_(np.nan)
+        dw.lse[l].fill_(np.nan)
+        mode = csa2.MODES[dw.wl.layers[l]]
+        if use_noalloc:
+            csa2.csa2_layer_noalloc(mode, dw.cstruct, dw.batch, dw.io(l))
+        else:
+            dw.run_layer(l)
+        torch.cuda.synchronize()
+        out[l] = (dw.idx.cpu().numpy().copy(), dw.pool_len.cpu().numpy().copy(),
+                  dw.o[l].cpu().numpy().copy(), dw.lse[l].cpu().numpy().copy())
+    return out
+
+
+def test_noalloc_layer_matches_layer_twice():
+    wl = W.Workload("noalloc", 4242, 3, [4096, 2500, 20000], 1,
+                    ["full", "reuse", "reindex", "reuse"], planted_blocks=4)
+    dw = DeviceWorkload(wl)
+    for mode in (0, 1, 2):
+        assert csa2.csa2_layer_workspace_size(mode, dw.batch) <= SCRATCH_BYTES
+    want = _run(dw, use_noalloc=False)
+    for call in range(2):
+        got = _run(dw, use_noalloc=True)
+        for l in dw.layers:
+            assert np.array_equal(got[l][0], want[l][0]), (call, l, "indices")
+            assert np.array_equal(got[l][1], want[l][1]), (call, l, "pool sizes")
+            for r in range(dw.rows):
+                ok, info = attn_close(got[l][2][r], got[l][3][r], want[l][2][r], want[l][3][r])
+                assert ok, (call, l, r, info)
+    assert int(dw.cache.status[0]) == 0
+
+
+def test_noalloc_refuses_work_beyond_its_scratch():
+    lib = csa2.load()
+    big = csa2.Batch(8, 1, 1, 0, 1 << 20, None, None)           # a Full layer over 8 x 1M entries
+    assert lib.csa2_layer_workspace_size(0, ctypes.byref(big)) > SCRATCH_BYTES
+    cache, io = csa2.Cache(), csa2.LayerIO()
+    st = lib.csa2_layer_noalloc(0, ctypes.byref(cache), ctypes.byref(big), ctypes.byref(io), None)
+    assert st == -5                                              # CSA2_ERR_WORKSPACE, nothing launched
