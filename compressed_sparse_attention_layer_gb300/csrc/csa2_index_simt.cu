@@ -139,12 +139,3 @@ int launch_gather_scores(const float *scores, int64_t ld, const int32_t *pool, c
 }
 
 }  // namespace csa2
-
-namespace csa2 {
-// The full scan of a Full layer.
-int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
-{
-    return launch_index_simt(c, bt, qi, w, scores, block_max, n_visible, ld, st);
-}
-}  // namespace csa2

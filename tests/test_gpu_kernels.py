@@ -209,3 +209,55 @@ def test_bad_page_ids_are_flagged_not_read():
     torch.cuda.synchronize()
     assert int(dw.cache.status[0]) & csa2.DEV_BAD_PAGE
     assert torch.isfinite(dw.o[0]).all()
+
+
+def _index_rows(dw, ld):
+    rows = dw.rows
+    scores = torch.full((rows, ld), np.nan, dtype=torch.float32, device="cuda")
+    bmax = torch.full((rows, ld // 8), np.nan, dtype=torch.float32, device="cuda")
+    nvis = torch.zeros((rows,), dtype=torch.int32, device="cuda")
+    l = dw.wl.layers.index("full")
+    csa2.csa2_index_scores(dw.cstruct, dw.batch, dw.qi[l], dw.w[l], scores, bmax, nvis, ld)
+    torch.cuda.synchronize()
+    return scores.cpu().numpy(), bmax.cpu().numpy(), nvis.cpu().numpy()
+
+
+def test_index_scores_ragged_and_extreme_heads():
+    """Ragged rows (persistent work list) and indexer-query heads spanning
+    2^-60 .. 2^60 in magnitude (the per-head power-of-two scaling)."""
+    wl = W.Workload("ragged_ix", 61, 4, [1000, 70001, 130, 9], 1, ["full"])
+    dw = _dw(wl)
+    mult = np.exp2(np.linspace(-60, 60, 32)).astype(np.float32)
+    for b in range(wl.batch):
+        qi = synth.bf16_bits_to_f32(wl.qi_bits(0, b)[0]) * mult[:, None]
+        bits = torch.from_numpy(qi).to(torch.bfloat16)
+        dw.qi[0][b].copy_(bits.cuda())
+    ld = (wl.max_entries + 7) // 8 * 8
+    s, bm, nv = _index_rows(dw, ld)
+    for b in range(wl.batch):
+        so = SeqOracle(wl, b)
+        E = wl.entries(b)
+        assert nv[b] == E
+        qib = dw.qi[0][b].cpu().view(torch.int16).numpy().view(np.uint16)
+        codes, scales = so.ik()
+        want = oracle.index_scores(qib, wl.w(0, b)[0], codes, scales)
+        got = s[b, :E].astype(np.float64)
+        assert np.allclose(got, want, rtol=1e-5, atol=1e-6 * np.abs(want).max()), b
+        nb = (E + 7) // 8
+        pad = np.full(nb * 8, -np.inf, np.float32)
+        pad[:E] = s[b, :E]
+        assert np.array_equal(bm[b, :nb], pad.reshape(nb, 8).max(axis=1)), b
+
+
+def test_index_scores_many_query_rows_causal():
+    """More than 256 query rows (one grid row per query) with causal visibility."""
+    wl = W.Workload("causal_ix", 62, 1, [6000], 1, ["full"], nq=300, prefill_new=300, swa_rows=300 + 128)
+    dw = _dw(wl)
+    ld = (wl.max_entries + 7) // 8 * 8
+    s, bm, nv = _index_rows(dw, ld)
+    so = SeqOracle(wl, 0)
+    for i in (0, 1, 137, 299):
+        t, nvis = so.visible(i)
+        assert nv[i] == nvis == t + 1
+        want = so.scores(0, i, np.arange(nvis))
+        assert np.allclose(s[i, :nvis], want, rtol=1e-5, atol=1e-6 * np.abs(want).max()), i
