@@ -95,16 +95,6 @@ __global__ void __launch_bounds__(IX_THREADS) k_index_simt(
     }
 }
 
-int launch_index_simt(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
-{
-    const int64_t rows = (int64_t)bt.batch * bt.nq;
-    dim3 grid((unsigned)ceil_div_i(bt.max_entries > 0 ? bt.max_entries : 1, IX_THREADS), (unsigned)rows);
-    k_index_simt<false><<<grid, IX_THREADS, 0, st>>>(c, bt, qi, w, nullptr, nullptr, scores, block_max,
-                                                     n_visible, ld);
-    return launch_status();
-}
-
 int launch_index_pool_simt(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi,
                            const float *w, const int32_t *pool, const int32_t *pool_len, int64_t ld,
                            float *scores, cudaStream_t st)
