@@ -17,7 +17,7 @@ int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, fl
                      cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
                       float *, int32_t *, int64_t, cudaStream_t);
-int launch_index_pool_simt(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
+int launch_index_pool(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
                            const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
 int launch_gather_scores(const float *, int64_t, const int32_t *, const int32_t *, int64_t, int64_t, float *,
                          cudaStream_t);
@@ -180,7 +180,7 @@ int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *batch, con
     if ((s = check_batch(batch, cache))) return s;
     if (!qi || !w || !pool || !pool_len || !scores) return CSA2_ERR_NULL;
     if (ld <= 0 || ld > (int64_t)1 << 24) return CSA2_ERR_SHAPE;
-    return launch_index_pool_simt(*cache, *batch, qi, w, pool, pool_len, ld, scores, (cudaStream_t)stream);
+    return launch_index_pool(*cache, *batch, qi, w, pool, pool_len, ld, scores, (cudaStream_t)stream);
 }
 
 int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
@@ -286,7 +286,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     } else if (mode == CSA2_MODE_REINDEX) {
         // a7: rescore the pool with this layer's indexer query, Top-512
         if ((s = prof(io->prof_begin))) return s;
-        if ((s = launch_index_pool_simt(*cache, *batch, io->qi, io->w, io->pool, io->pool_len, CSA2_POOL_MAX,
+        if ((s = launch_index_pool(*cache, *batch, io->qi, io->w, io->pool, io->pool_len, CSA2_POOL_MAX,
                                         ws.pool_scores, st)))
             return s;
         if ((s = prof(io->prof_end))) return s;

@@ -26,7 +26,7 @@
 
 namespace csa2 {
 
-constexpr int AC_THREADS = 128;
+constexpr int AC_THREADS = 256;                   // two threads per key
 constexpr int AC_KEYS = 128;                       // keys per chunk (MMA M of the first product)
 constexpr int AC_MAX_CHUNKS = CSA2_TOPK / AC_KEYS + 1;
 constexpr uint32_t AC_IDESC_S = tc::idesc_f16(128, 64, 1, 1, 0, 0);   // K-major A and B
@@ -53,18 +53,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// MXFP4 entry -> bf16 row of the key tile (exact).
+// Half (`half` = 0: dims 0..255, 1: dims 256..511) of an MXFP4 entry -> bf16
+// row of the key tile (exact).
 __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint8_t *codes,
-                                               const uint8_t *scales)
+                                               const uint8_t *scales, int half)
 {
-    const uint4 sc = __ldg(reinterpret_cast<const uint4 *>(scales));
+    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(scales) + half);
     const uint8_t *scb = reinterpret_cast<const uint8_t *>(&sc);
-    const uint4 *src = reinterpret_cast<const uint4 *>(codes);
+    const uint4 *src = reinterpret_cast<const uint4 *>(codes) + 8 * half;
 #pragma unroll 4
-    for (int i = 0; i < 16; i++) {                 // 16 bytes = 32 elements = one MX block
-        const uint4 u = __ldg(src + i);
-        const float f = exp2i((int)scb[i] - 127 < -126 ? -126 : (int)scb[i] - 127);
-        const float f2 = (int)scb[i] - 127 < -126 ? 0.5f : 1.0f;      // X = -127
+    for (int ii = 0; ii < 8; ii++) {               // 16 bytes = 32 elements = one MX block
+        const int i = ii + 8 * half;
+        const uint4 u = __ldg(src + ii);
+        const int X = (int)scb[ii] - 127;
+        const float f = exp2i(X < -126 ? -126 : X);
+        const float f2 = X < -126 ? 0.5f : 1.0f;      // X = -127
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int j = 0; j < 4; j++) {              // 8 elements -> one 16-byte chunk
@@ -80,13 +83,14 @@ __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, con
     }
 }
 
-// FP8 window row -> bf16 row of the key tile (codes only; exact).
-__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint8_t *codes)
+// Half of an FP8 window row -> bf16 row of the key tile (codes only; exact).
+__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint8_t *codes, int half)
 {
-    const uint4 *src = reinterpret_cast<const uint4 *>(codes);
+    const uint4 *src = reinterpret_cast<const uint4 *>(codes) + 16 * half;
 #pragma unroll 4
-    for (int i = 0; i < 32; i++) {                 // 16 codes per load
-        const uint4 u = __ldg(src + i);
+    for (int ii = 0; ii < 16; ii++) {              // 16 codes per load
+        const int i = ii + 16 * half;
+        const uint4 u = __ldg(src + ii);
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
         uint4 o0, o1;
         uint32_t *a = reinterpret_cast<uint32_t *>(&o0);
@@ -109,10 +113,10 @@ __device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, c
     }
 }
 
-__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row)
+__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int half)
 {
 #pragma unroll 8
-    for (int i = 0; i < 64; i++)
+    for (int i = 32 * half; i < 32 * half + 32; i++)
         *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 8 * i, AC_KEYS)) = make_uint4(0, 0, 0, 0);
 }
 
@@ -125,6 +129,8 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     extern __shared__ uint8_t smem_raw[];
     AcSmem &S = *reinterpret_cast<AcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int key = tid & (AC_KEYS - 1), half = tid >> 7;   // key row; half of the dims / heads
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quarter of this warp
     const int64_t r = blockIdx.x;
     const int chunk = blockIdx.y;
     const int b = (int)(r / bt.nq);
@@ -140,27 +146,27 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM);
 #pragma unroll 4
-        for (int i = 0; i < 32; i++) {
+        for (int i = 0; i < 16; i++) {
             const int e = 8 * (tid + AC_THREADS * i);
             const uint4 v = __ldg(src + tid + AC_THREADS * i);
             *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 9, e & 511, CSA2_HEADS)) = v;
         }
     }
 
-    // ---- this thread's key: dequantise into row tid of the key tile
+    // ---- this thread's key: dequantise its half into row `key` of the key tile
     float kscale = 1.0f;          // multiplies the logit and the probability (window rows)
     bool valid = false;
     if (!window) {
-        const int j = chunk * AC_KEYS + tid;
+        const int j = chunk * AC_KEYS + key;
         if (j < k) {
             const int32_t p = idx[r * k + j];
             if (p >= 0) {
                 if (p >= visible_entries(bt, r)) {
-                    flag(c.status, CSA2_DEV_BAD_INDEX);
+                    if (half == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
                 } else {
                     const int64_t slot = entry_slot(c, b, p);
                     if (slot >= 0) {
-                        store_main_key(S.k, tid, c.kv_codes + slot * 256, c.kv_scales + slot * 16);
+                        store_main_key(S.k, key, c.kv_codes + slot * 256, c.kv_scales + slot * 16, half);
                         valid = true;
                     }
                 }
@@ -172,15 +178,15 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
         int64_t lo = t - (CSA2_SWA_WINDOW - 1);
         lo = lo < s0 ? s0 : lo;
         lo = lo < 0 ? 0 : lo;
-        if (lo + tid <= t) {
-            const int64_t row = (lo + tid) % swa.rows;
+        if (lo + key <= t) {
+            const int64_t row = (lo + key) % swa.rows;
             const int64_t off = (int64_t)b * swa.rows + row;
-            store_window_key(S.k, tid, swa.codes + off * CSA2_HEAD_DIM);
+            store_window_key(S.k, key, swa.codes + off * CSA2_HEAD_DIM, half);
             kscale = swa.scales[off];
             valid = true;
         }
     }
-    if (!valid) zero_key(S.k, tid);
+    if (!valid) zero_key(S.k, key, half);
 
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -207,28 +213,29 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     }
     tc::tc_fence_after();
     {
-        // ---- logits of this thread's key for the 64 heads, transposed into smem
+        // ---- logits of this key for this half's 32 heads, transposed into smem
         const float lscale = sm_scale * kscale;
-#pragma unroll
-        for (int half = 0; half < 2; half++) {
+        {
             uint32_t acc[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)half * 32u, acc);
+            tc::tmem_ld32(tmem + lane_base + (uint32_t)half * 32u, acc);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int h = 0; h < 32; h++)
-                S.u.s.red[half * 32 + h][tid] = valid ? __uint_as_float(acc[h]) * lscale : -INFINITY;
+                S.u.s.red[half * 32 + h][key] = valid ? __uint_as_float(acc[h]) * lscale : -INFINITY;
         }
         __syncthreads();
-        // ---- per-head max and sum over the chunk: two threads per head
+        // ---- per-head max and sum over the chunk: four threads per head
         {
-            const int h = tid >> 1, part = tid & 1;
+            const int h = tid >> 2, part = tid & 3;
             float mx = -INFINITY;
-            for (int j = part; j < AC_KEYS; j += 2) mx = fmaxf(mx, S.u.s.red[h][j]);
+            for (int j = part; j < AC_KEYS; j += 4) mx = fmaxf(mx, S.u.s.red[h][j]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
             float sum = 0.0f;
             if (mx != -INFINITY)
-                for (int j = part; j < AC_KEYS; j += 2) sum += expf(S.u.s.red[h][j] - mx);
+                for (int j = part; j < AC_KEYS; j += 4) sum += expf(S.u.s.red[h][j] - mx);
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if (part == 0) {
                 S.m[h] = mx;
                 S.l[h] = sum;
@@ -237,12 +244,13 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
         __syncthreads();
         // ---- P^T (times the window scale) as bf16 hi + lo, K-major rows = heads
 #pragma unroll 4
-        for (int h = 0; h < CSA2_HEADS; h++) {
+        for (int hh = 0; hh < 32; hh++) {
+            const int h = half * 32 + hh;
             const float mx = S.m[h];
-            const float p = (valid && mx != -INFINITY) ? expf(S.u.s.red[h][tid] - mx) * kscale : 0.0f;
+            const float p = (valid && mx != -INFINITY) ? expf(S.u.s.red[h][key] - mx) * kscale : 0.0f;
             const __nv_bfloat16 hi = __float2bfloat16_rn(p);
             const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-            const uint32_t off = tc::sw128_offset(h, tid, CSA2_HEADS);
+            const uint32_t off = tc::sw128_offset(h, key, CSA2_HEADS);
             *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p_hi + off) = hi;
             *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p_lo + off) = lo;
         }
@@ -277,21 +285,17 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     }
     tc::tc_fence_after();
     {
-        // ---- partial output: thread = dim within the M-tile, 64 heads per tile
+        // ---- partial output: lane = dim within the M-tile, this half's 32 heads
         const int64_t base = (r * AC_MAX_CHUNKS + chunk) * (int64_t)CSA2_HEADS;
         float *po = part_o + base * CSA2_HEAD_DIM;
 #pragma unroll 1
         for (int mt = 0; mt < 4; mt++) {
-            const int d = 128 * mt + warp * 32 + (tid & 31);
+            const int d = 128 * mt + (warp & 3) * 32 + (tid & 31);
+            uint32_t acc[32];
+            tc::tmem_ld32(tmem + lane_base + 64u + 64u * (uint32_t)mt + 32u * (uint32_t)half, acc);
+            tc::tmem_ld_wait();
 #pragma unroll
-            for (int half = 0; half < 2; half++) {
-                uint32_t acc[32];
-                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + 64u + 64u * (uint32_t)mt + 32u * (uint32_t)half,
-                              acc);
-                tc::tmem_ld_wait();
-#pragma unroll
-                for (int h = 0; h < 32; h++) po[(int64_t)(half * 32 + h) * CSA2_HEAD_DIM + d] = __uint_as_float(acc[h]);
-            }
+            for (int h = 0; h < 32; h++) po[(int64_t)(half * 32 + h) * CSA2_HEAD_DIM + d] = __uint_as_float(acc[h]);
         }
         if (tid < CSA2_HEADS) {
             part_ml[(base + tid) * 2] = S.m[tid];
@@ -306,37 +310,51 @@ teardown:
 }
 
 // o = sum_c e^(m_c - M) O_c / sum_c e^(m_c - M) l_c, lse = M + log L; one CTA per
-// (row, 8 heads), thread = 2 dims.
-__global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ part_o,
+// (row, 4 heads), thread = 4 consecutive dims (float4), all chunk loads in flight.
+__global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml, int nchunks,
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
     const int64_t r = blockIdx.x;
-    const int h0 = blockIdx.y * 8;
     const int tid = threadIdx.x;
-#pragma unroll 1
-    for (int hh = 0; hh < 8; hh++) {
-        const int h = h0 + hh;
+#pragma unroll
+    for (int hh = 0; hh < 4; hh++) {
+        const int h = blockIdx.y * 4 + hh;
+        float mc[AC_MAX_CHUNKS], lc[AC_MAX_CHUNKS];
+        float4 v[AC_MAX_CHUNKS];
         float M = -INFINITY;
-        for (int ch = 0; ch < nchunks; ch++)
-            M = fmaxf(M, part_ml[((r * AC_MAX_CHUNKS + ch) * CSA2_HEADS + h) * 2]);
-        float L = 0.0f;
-        float2 acc = make_float2(0.0f, 0.0f);
-        if (M != -INFINITY) {
-            for (int ch = 0; ch < nchunks; ch++) {
+#pragma unroll
+        for (int ch = 0; ch < AC_MAX_CHUNKS; ch++) {
+            if (ch < nchunks) {
                 const int64_t base = (r * AC_MAX_CHUNKS + ch) * CSA2_HEADS + h;
-                const float mc = part_ml[base * 2];
-                if (mc == -INFINITY) continue;
-                const float wgt = expf(mc - M);
-                L += wgt * part_ml[base * 2 + 1];
-                const float2 v = *reinterpret_cast<const float2 *>(part_o + base * CSA2_HEAD_DIM + 2 * tid);
-                acc.x = fmaf(wgt, v.x, acc.x);
-                acc.y = fmaf(wgt, v.y, acc.y);
+                const float2 ml = *reinterpret_cast<const float2 *>(part_ml + base * 2);
+                mc[ch] = ml.x;
+                lc[ch] = ml.y;
+                v[ch] = *reinterpret_cast<const float4 *>(part_o + base * CSA2_HEAD_DIM + 4 * tid);
+                M = fmaxf(M, ml.x);
+            } else {
+                mc[ch] = -INFINITY;
+                lc[ch] = 0.0f;
+                v[ch] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float L = 0.0f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int ch = 0; ch < AC_MAX_CHUNKS; ch++) {
+                if (mc[ch] == -INFINITY) continue;
+                const float wgt = expf(mc[ch] - M);
+                L = fmaf(wgt, lc[ch], L);
+                acc.x = fmaf(wgt, v[ch].x, acc.x);
+                acc.y = fmaf(wgt, v[ch].y, acc.y);
+                acc.z = fmaf(wgt, v[ch].z, acc.z);
+                acc.w = fmaf(wgt, v[ch].w, acc.w);
             }
         }
         const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        *reinterpret_cast<float2 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 2 * tid) =
-            make_float2(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<float4 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 4 * tid) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (tid == 0) lse[r * CSA2_HEADS + h] = L > 0.0f ? M + logf(L) : -INFINITY;
     }
 }
@@ -368,7 +386,7 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
                                                                        part_ml, nchunks);
     int s = launch_status();
     if (s) return s;
-    k_attn_combine<<<dim3((unsigned)rows, CSA2_HEADS / 8), 256, 0, st>>>(part_o, part_ml, nchunks, o, lse);
+    k_attn_combine<<<dim3((unsigned)rows, CSA2_HEADS / 4), 128, 0, st>>>(part_o, part_ml, nchunks, o, lse);
     return launch_status();
 }
 

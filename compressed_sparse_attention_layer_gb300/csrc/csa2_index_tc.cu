@@ -149,10 +149,22 @@ __device__ __forceinline__ void issue_tile_mma(const TsSmem &S, int stage, uint3
     }
 }
 
-template <bool PERSIST>
+// Entries scored by row r: every visible entry (the Full layer's scan) or the
+// first pool_len[r] positions of its candidate pool (a Reindex layer).
+template <bool POOL>
+__device__ __forceinline__ int64_t row_entries(const csa2_batch &bt, const int32_t *pool_len, int64_t ld, int r)
+{
+    if (!POOL) return visible_entries(bt, r);
+    int64_t n = pool_len[r];
+    return n < 0 ? 0 : (n > ld ? ld : n);
+}
+
+template <bool PERSIST, bool POOL>
 __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batch bt,
                                                          const uint16_t *__restrict__ qi,
                                                          const float *__restrict__ w,
+                                                         const int32_t *__restrict__ pool,
+                                                         const int32_t *__restrict__ pool_len,
                                                          float *__restrict__ scores,
                                                          float *__restrict__ block_max,
                                                          int32_t *__restrict__ n_visible, int64_t ld)
@@ -173,9 +185,9 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
     int64_t g0, g1;
     if (PERSIST) {
         for (int r = tid; r < rows; r += TS_THREADS) {
-            const int64_t nv = visible_entries(bt, r);
+            const int64_t nv = row_entries<POOL>(bt, pool_len, ld, r);
             S.prefix[r + 1] = (int32_t)((nv + TS_TILE - 1) / TS_TILE);
-            if (blockIdx.x == 0 && n_visible) n_visible[r] = (int32_t)nv;
+            if (!POOL && blockIdx.x == 0 && n_visible) n_visible[r] = (int32_t)nv;
         }
         __syncthreads();
         if (tid == 0) {
@@ -188,9 +200,9 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
         g1 = total * (blockIdx.x + 1) / gridDim.x;
     } else {
         const int r = blockIdx.y;
-        const int64_t nv = visible_entries(bt, r);
+        const int64_t nv = row_entries<POOL>(bt, pool_len, ld, r);
         const int64_t T = (nv + TS_TILE - 1) / TS_TILE;
-        if (blockIdx.x == 0 && tid == 0 && n_visible) n_visible[r] = (int32_t)nv;
+        if (!POOL && blockIdx.x == 0 && tid == 0 && n_visible) n_visible[r] = (int32_t)nv;
         g0 = T * blockIdx.x / gridDim.x;
         g1 = T * (blockIdx.x + 1) / gridDim.x;
     }
@@ -217,16 +229,32 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
         g += nt;
         const int b = r / bt.nq;
         const int64_t nvis = visible_entries(bt, r);
+        const int64_t n = row_entries<POOL>(bt, pool_len, ld, r);
+        const int32_t *prow = POOL ? pool + (int64_t)r * ld : nullptr;
+        // slot i of the row -> entry position (pool rows list positions)
+        auto load_slot = [&](int64_t i, KeyRegs &kr) {
+            if (!POOL) {
+                key_load(c, b, i, nvis, kr);
+                return;
+            }
+            int64_t p = i < n ? (int64_t)prow[i] : nvis;
+            if (i < n && (p < 0 || p >= nvis)) {
+                flag(c.status, CSA2_DEV_BAD_INDEX);
+                p = nvis;
+            }
+            key_load(c, b, p, nvis, kr);
+            if (i < n && kr.state == 0) kr.state = 2;
+        };
         load_query(S, qi + (int64_t)r * 4096, w + (int64_t)r * 32);
 
         KeyRegs ka, kb;                             // tiles of even / odd index
-        key_load(c, b, j0 * TS_TILE + tid, nvis, ka);
+        load_slot(j0 * TS_TILE + tid, ka);
         key_store(S.a[0], tid, ka);
         float scale_even = ka.scale;
         int state_even = ka.state;
         float scale_odd = 0.0f;
         int state_odd = 0;
-        if (nt > 1) key_load(c, b, (j0 + 1) * TS_TILE + tid, nvis, kb);
+        if (nt > 1) load_slot((j0 + 1) * TS_TILE + tid, kb);
         tc::fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -248,7 +276,7 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
                     scale_odd = kb.scale;
                     state_odd = kb.state;
                 }
-                if (i + 2 < nt) key_load(c, b, (j0 + i + 2) * TS_TILE + tid, nvis, ka);
+                if (i + 2 < nt) load_slot((j0 + i + 2) * TS_TILE + tid, ka);
             } else {
                 scale_cur = scale_odd;
                 state_cur = state_odd;
@@ -257,7 +285,7 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
                     scale_even = ka.scale;
                     state_even = ka.state;
                 }
-                if (i + 2 < nt) key_load(c, b, (j0 + i + 2) * TS_TILE + tid, nvis, kb);
+                if (i + 2 < nt) load_slot((j0 + i + 2) * TS_TILE + tid, kb);
             }
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
@@ -285,9 +313,9 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
             sc *= scale_cur;
             if (state_cur != 1) sc = -INFINITY;
             const int64_t p = (j0 + i) * TS_TILE + tid;
-            const bool valid = p < nvis;
+            const bool valid = p < n;
             if (valid && scores) scores[(int64_t)r * ld + p] = sc;
-            if (block_max) {
+            if (!POOL && block_max) {
                 float m = valid ? sc : -INFINITY;
 #pragma unroll
                 for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -313,31 +341,50 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
 
 static int g_num_sms = 0;
 
-int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
+template <bool POOL>
+static int launch_index(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                        const int32_t *pool, const int32_t *pool_len, float *scores, float *block_max,
+                        int32_t *n_visible, int64_t ld, cudaStream_t st)
 {
     const int rows = bt.batch * bt.nq;
     const size_t smem = sizeof(TsSmem) + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_index_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_index_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(k_index_tc<true, POOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_index_tc<false, POOL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (!g_num_sms) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        }
         attr = true;
     }
     const int per_sm = 3;
-    const int64_t tiles_bound = (int64_t)rows * ((bt.max_entries + TS_TILE - 1) / TS_TILE);
+    const int64_t per_row = POOL ? ld : bt.max_entries;
+    const int64_t tiles_row = std::max<int64_t>(1, (per_row + TS_TILE - 1) / TS_TILE);
     if (rows <= TS_PERSIST_ROWS) {
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_bound, (int64_t)g_num_sms * per_sm));
-        k_index_tc<true><<<grid, TS_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(rows * tiles_row, (int64_t)g_num_sms * per_sm));
+        k_index_tc<true, POOL><<<grid, TS_THREADS, smem, st>>>(c, bt, qi, w, pool, pool_len, scores, block_max,
+                                                               n_visible, ld);
     } else {
-        const int64_t tiles_row = std::max<int64_t>(1, (bt.max_entries + TS_TILE - 1) / TS_TILE);
         const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_num_sms * per_sm + rows - 1) / rows));
-        k_index_tc<false><<<dim3(x, rows), TS_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
+        k_index_tc<false, POOL><<<dim3(x, rows), TS_THREADS, smem, st>>>(c, bt, qi, w, pool, pool_len, scores,
+                                                                        block_max, n_visible, ld);
     }
     return launch_status();
+}
+
+int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
+{
+    return launch_index<false>(c, bt, qi, w, nullptr, nullptr, scores, block_max, n_visible, ld, st);
+}
+
+// a7: a Reindex layer rescoring its candidate pool ("DeepSeek-V4.1-Flash 架构详解" §3.2).
+int launch_index_pool(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                      const int32_t *pool, const int32_t *pool_len, int64_t ld, float *scores, cudaStream_t st)
+{
+    return launch_index<true>(c, bt, qi, w, pool, pool_len, scores, nullptr, nullptr, ld, st);
 }
 
 }  // namespace csa2

@@ -51,9 +51,23 @@ __device__ void find_threshold(const Src &src, int64_t n, int k, TkShared &sh, u
         const uint32_t dmask = (1u << widths[pass]) - 1u;
         for (int b = tid; b < 2048; b += TK_THREADS) sh.hist[b] = 0;
         __syncthreads();
-        for (int64_t i = tid; i < n; i += TK_THREADS) {
-            const uint32_t u = src(i);
-            if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & dmask], 1u);
+        // every lane of a warp runs the same trip count; lanes with the same digit
+        // combine their counts before one shared-memory atomic
+        const int lane = tid & 31;
+        for (int64_t base = tid - lane; base < n; base += TK_THREADS) {
+            const int64_t i = base + lane;
+            uint32_t u = 0;
+            bool on = false;
+            if (i < n) {
+                u = src(i);
+                on = (u & mask) == prefix;
+            }
+            const uint32_t act = __ballot_sync(0xffffffffu, on);
+            if (on) {
+                const uint32_t bin = (u >> shift) & dmask;
+                const uint32_t peers = __match_any_sync(act, bin);
+                if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
+            }
         }
         __syncthreads();
         // bins in descending order: thread t owns bins 2047-2t and 2046-2t

@@ -261,3 +261,32 @@ def test_index_scores_many_query_rows_causal():
         assert nv[i] == nvis == t + 1
         want = so.scores(0, i, np.arange(nvis))
         assert np.allclose(s[i, :nvis], want, rtol=1e-5, atol=1e-6 * np.abs(want).max()), i
+
+
+def test_index_scores_pool_gathered():
+    """Reindex rescoring of a scattered candidate pool (incl. a ragged tail and an
+    out-of-range position, which is flagged and scored -inf)."""
+    wl = W.Workload("pool_ix", 63, 3, [50000, 9000, 70000], 1, ["full"])
+    dw = _dw(wl)
+    rng = np.random.default_rng(63)
+    ld = 16384
+    pool = np.full((3, ld), -1, np.int32)
+    lens = np.array([16384, 1000, 7], np.int32)
+    for b in range(3):
+        blocks = np.sort(rng.choice(wl.entries(b) // 8, lens[b] // 8 + 1, replace=False))
+        pos = (blocks[:, None] * 8 + np.arange(8)).reshape(-1)[:lens[b]]
+        pool[b, :lens[b]] = pos
+    pool[2, 3] = wl.entries(2) + 5            # beyond the context
+    scores = torch.full((3, ld), np.nan, dtype=torch.float32, device="cuda")
+    csa2.csa2_index_scores_pool(dw.cstruct, dw.batch, dw.qi[0], dw.w[0], torch.from_numpy(pool).cuda(),
+                                torch.from_numpy(lens).cuda(), scores)
+    torch.cuda.synchronize()
+    got = scores.cpu().numpy()
+    for b in range(3):
+        so = SeqOracle(wl, b)
+        ok = (pool[b, :lens[b]] >= 0) & (pool[b, :lens[b]] < wl.entries(b))
+        want = so.scores(0, 0, pool[b, :lens[b]][ok])
+        assert np.allclose(got[b, :lens[b]][ok], want, rtol=1e-5, atol=1e-6 * np.abs(want).max()), b
+        assert np.all(np.isneginf(got[b, :lens[b]][~ok]))
+        assert np.all(np.isnan(got[b, lens[b]:]))
+    assert int(dw.cache.status[0]) & csa2.DEV_BAD_INDEX
