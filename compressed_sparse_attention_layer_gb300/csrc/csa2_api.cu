@@ -29,6 +29,7 @@ int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float,
                 const csa2_swa &, float *, float *, void *, size_t, cudaStream_t);
 size_t attn_workspace_bytes(int64_t rows);
 int topk_max_k();
+int64_t topk_max_len();
 
 // ---------------------------------------------------------------- validation
 static constexpr int64_t kMaxRows = 65535;
@@ -189,7 +190,7 @@ int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows,
     if (rows < 0 || rows > kMaxRows * 16 || k < 1 || k > topk_max_k() || ld < 0) return CSA2_ERR_SHAPE;
     if (rows == 0) return CSA2_OK;
     if (!scores || !len || !out) return CSA2_ERR_NULL;
-    if (ld > (int64_t)INT32_MAX) return CSA2_ERR_RANGE;
+    if (ld > topk_max_len()) return CSA2_ERR_SHAPE;
     return launch_topk(scores, ld, len, rows, cand, k, out, (cudaStream_t)stream);
 }
 
@@ -200,7 +201,7 @@ int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n
         return CSA2_ERR_SHAPE;
     if (rows == 0) return CSA2_OK;
     if (!block_max || !n_visible || !pool || !pool_len) return CSA2_ERR_NULL;
-    if (ld_blocks > (int64_t)INT32_MAX / 8) return CSA2_ERR_RANGE;
+    if (ld_blocks > topk_max_len()) return CSA2_ERR_SHAPE;
     return launch_topk_blocks(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len,
                               (cudaStream_t)stream);
 }
@@ -246,6 +247,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if ((s = check_swa(&io->swa))) return s;
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
+    if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
     LayerWs ws = layer_ws(mode, batch, workspace);
     if (ws.total && (!workspace || workspace_bytes < ws.total)) return CSA2_ERR_WORKSPACE;

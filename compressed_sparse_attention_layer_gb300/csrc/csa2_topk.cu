@@ -1,46 +1,80 @@
 // a5/a6: Top-K selection with ties broken toward the lower slot.
 //
-// One 1024-thread CTA per row.  Radix select on order-preserving 32-bit keys
-// (11 + 11 + 10 bit digits, shared-memory histograms) finds the k-th largest
-// key T and how many keys equal to T must be taken; an ordered compaction
-// (block-wide prefix sums over contiguous per-thread chunks) then writes the
-// chosen positions in ascending slot order, taking the lowest-slot ties.
-// Rows of up to TK_STAGE elements are staged in shared memory once; longer
-// rows are re-read from global memory (L2) on each pass.
-// "DeepSeek-V4.1-Flash 架构详解" §1 table (top-k 512), §3.2 (block pool of
-// 2,048 blocks of 8, then its own Top-512); the research note §3.2.
+// One thread-block cluster per row ("DeepSeek-V4.1-Flash 架构详解" §1 table:
+// top-k 512; §3.2: the best 2,048 blocks of 8 form the candidate pool, then
+// the pool's own Top-512; the research note §3.2).  The CL CTAs of a cluster
+// each stage one contiguous 1/CL of the row in shared memory as
+// order-preserving 32-bit keys, read once from global memory.  A radix select
+// over 11 + 11 + 10-bit digits finds the k-th largest key T: each CTA counts
+// its slice, the histograms are summed through distributed shared memory, and
+// every CTA takes the same decision.  An ordered compaction then writes every
+// key > T and the lowest-slot keys == T: each CTA learns how many selected
+// slots lie in the slices before its own from the cluster's counts, so the
+// output comes out in ascending slot order without atomics deciding order.
+#include <cooperative_groups.h>
+
 #include "csa2_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace csa2 {
 
-constexpr int TK_THREADS = 1024;
-constexpr int TK_STAGE = 40960;            // staged keys (160 KB of shared memory)
+constexpr int TK_THREADS = 512;
+constexpr int TK_SLICE = 16384;            // keys staged per CTA (64 KB)
 constexpr int TK_MAX_K = 4096;
-
-struct SmemKeys {
-    const uint32_t *k;
-    __device__ __forceinline__ uint32_t operator()(int64_t i) const { return k[i]; }
-};
-struct GmemKeys {
-    const float *s;
-    __device__ __forceinline__ uint32_t operator()(int64_t i) const { return order_key(__ldg(s + i)); }
-};
 
 struct TkShared {
     uint32_t hist[2048];
     int warp_sums[32];
-    int total;
+    int cnt[2];                            // this CTA's (count > T, count == T)
     uint32_t digit;
     int above;
 };
 
-// k-th largest key T among n keys (n > k) and the number of keys equal to T
-// that belong to the top k.
-template <class Src>
-__device__ void find_threshold(const Src &src, int64_t n, int k, TkShared &sh, uint32_t &T,
-                               int &need_eq)
+// Sum the cluster's histograms; find the bin holding the kk-th largest key
+// among those matching the prefix so far, and the count above that bin.
+template <int CL>
+__device__ void cluster_digit(cg::cluster_group &cluster, TkShared &sh, int kk, uint32_t &digit, int &above)
 {
     const int tid = threadIdx.x;
+    int c[4] = {0, 0, 0, 0};                         // bins 2047-4t .. 2044-4t, descending
+#pragma unroll
+    for (int q = 0; q < CL; q++) {
+        const uint32_t *h = cluster.map_shared_rank(sh.hist, q);
+#pragma unroll
+        for (int j = 0; j < 4; j++) c[j] += (int)h[2047 - 4 * tid - j];
+    }
+    const int tot = c[0] + c[1] + c[2] + c[3];
+    const int excl = block_exclusive_scan<TK_THREADS>(tot, sh.warp_sums, nullptr);
+    if (excl < kk && excl + tot >= kk) {
+        int acc = excl;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            if (acc + c[j] >= kk) {
+                sh.digit = 2047 - 4 * tid - j;
+                sh.above = acc;
+                break;
+            }
+            acc += c[j];
+        }
+    }
+    __syncthreads();
+    digit = sh.digit;
+    above = sh.above;
+}
+
+// Top k of a row of n keys; this CTA holds keys[0 .. m) = slots [lo, lo + m).
+// emit(rank, slot) for every selected slot of this slice, rank ascending with
+// the slot across the whole row.
+template <int CL, class Emit>
+__device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys, int64_t lo, int m, int64_t n,
+                               int k, TkShared &sh, Emit emit)
+{
+    const int tid = threadIdx.x;
+    if (n <= k) {                                    // everything is selected: rank = slot
+        for (int i = tid; i < m; i += TK_THREADS) emit((int)(lo + i), lo + i);
+        return;
+    }
     uint32_t prefix = 0, mask = 0;
     int kk = k;
     const int shifts[3] = {21, 10, 0};
@@ -51,190 +85,214 @@ __device__ void find_threshold(const Src &src, int64_t n, int k, TkShared &sh, u
         const uint32_t dmask = (1u << widths[pass]) - 1u;
         for (int b = tid; b < 2048; b += TK_THREADS) sh.hist[b] = 0;
         __syncthreads();
-        // every lane of a warp runs the same trip count; lanes with the same digit
-        // combine their counts before one shared-memory atomic
-        const int lane = tid & 31;
-        for (int64_t base = tid - lane; base < n; base += TK_THREADS) {
-            const int64_t i = base + lane;
-            uint32_t u = 0;
-            bool on = false;
-            if (i < n) {
-                u = src(i);
-                on = (u & mask) == prefix;
-            }
-            const uint32_t act = __ballot_sync(0xffffffffu, on);
-            if (on) {
-                const uint32_t bin = (u >> shift) & dmask;
-                const uint32_t peers = __match_any_sync(act, bin);
-                if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[bin], (uint32_t)__popc(peers));
-            }
+        for (int i = tid; i < m; i += TK_THREADS) {
+            const uint32_t u = keys[i];
+            if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & dmask], 1u);
         }
-        __syncthreads();
-        // bins in descending order: thread t owns bins 2047-2t and 2046-2t
-        const int c0 = (int)sh.hist[2047 - 2 * tid], c1 = (int)sh.hist[2046 - 2 * tid];
-        const int excl = block_exclusive_scan<TK_THREADS>(c0 + c1, sh.warp_sums, nullptr);
-        if (excl < kk && excl + c0 + c1 >= kk) {
-            if (excl + c0 >= kk) {
-                sh.digit = 2047 - 2 * tid;
-                sh.above = excl;
-            } else {
-                sh.digit = 2046 - 2 * tid;
-                sh.above = excl + c0;
-            }
-        }
-        __syncthreads();
-        prefix |= sh.digit << shift;
+        cluster.sync();                              // every slice counted
+        uint32_t d;
+        int above;
+        cluster_digit<CL>(cluster, sh, kk, d, above);
+        prefix |= d << shift;
         mask |= dmask << shift;
-        kk -= sh.above;
-        __syncthreads();
+        kk -= above;
+        cluster.sync();                              // every CTA done reading before the reset
     }
-    T = prefix;
-    need_eq = kk;
-}
+    const uint32_t T = prefix;
+    const int need_eq = kk;                          // ties with T that are selected, lowest slots first
 
-// Emit, in ascending slot order, every slot with key > T and the first
-// need_eq slots with key == T: emit(j, i) for output rank j and slot i.
-template <class Src, class Emit>
-__device__ void ordered_compact(const Src &src, int64_t n, uint32_t T, int need_eq, TkShared &sh,
-                                Emit emit)
-{
-    const int tid = threadIdx.x;
-    const int64_t chunk = ((n + TK_THREADS - 1) / TK_THREADS) | 1;   // odd: no bank conflicts
-    const int64_t lo = tid * chunk < n ? tid * chunk : n;
-    const int64_t hi = lo + chunk < n ? lo + chunk : n;
+    // ---- counts of this thread's chunk, of this slice, and of the slices before it
+    const int chunk = ((m + TK_THREADS - 1) / TK_THREADS) | 1;    // odd: no bank conflicts
+    const int a = tid * chunk < m ? tid * chunk : m;
+    const int e = a + chunk < m ? a + chunk : m;
     int gt = 0, eq = 0;
-    for (int64_t i = lo; i < hi; i++) {
-        const uint32_t u = src(i);
+    for (int i = a; i < e; i++) {
+        const uint32_t u = keys[i];
         gt += u > T;
         eq += u == T;
     }
-    const int eq_before = block_exclusive_scan<TK_THREADS>(eq, sh.warp_sums, nullptr);
-    int take = need_eq - eq_before;
+    int tot_gt = 0, tot_eq = 0;
+    const int gt_local = block_exclusive_scan<TK_THREADS>(gt, sh.warp_sums, &tot_gt);
+    const int eq_local = block_exclusive_scan<TK_THREADS>(eq, sh.warp_sums, &tot_eq);
+    if (tid == 0) {
+        sh.cnt[0] = tot_gt;
+        sh.cnt[1] = tot_eq;
+    }
+    cluster.sync();
+    int gt_slices = 0, eq_slices = 0;
+    const int me = (int)cluster.block_rank();
+    for (int q = 0; q < me; q++) {
+        const int *cq = cluster.map_shared_rank(sh.cnt, q);
+        gt_slices += cq[0];
+        eq_slices += cq[1];
+    }
+    cluster.sync();                                  // counts read before any CTA exits
+    const int eq_prior = eq_slices + eq_local;       // ties in slots before this chunk
+    int take = need_eq - eq_prior;
     take = take < 0 ? 0 : (take > eq ? eq : take);
-    int off = block_exclusive_scan<TK_THREADS>(gt + take, sh.warp_sums, nullptr);
+    int off = gt_slices + gt_local + (eq_prior < need_eq ? eq_prior : need_eq);
     int seen = 0;
-    for (int64_t i = lo; i < hi; i++) {
-        const uint32_t u = src(i);
+    for (int i = a; i < e; i++) {
+        const uint32_t u = keys[i];
         if (u > T) {
-            emit(off++, i);
+            emit(off++, lo + i);
         } else if (u == T && seen < take) {
-            emit(off++, i);
+            emit(off++, lo + i);
             seen++;
         }
     }
 }
 
-// Select the top k of row (src, n); emit(j, slot) for j < min(n, k).
-template <class Emit>
-__device__ void select_row(const float *row, int64_t n, int k, uint32_t *stage, TkShared &sh,
-                           Emit emit)
-{
-    if (n <= k) {
-        for (int64_t i = threadIdx.x; i < n; i += TK_THREADS) emit((int)i, i);
-        return;
-    }
-    uint32_t T;
-    int need_eq;
-    if (n <= TK_STAGE) {
-        for (int64_t i = threadIdx.x; i < n; i += TK_THREADS) stage[i] = order_key(__ldg(row + i));
-        __syncthreads();
-        SmemKeys src{stage};
-        find_threshold(src, n, k, sh, T, need_eq);
-        ordered_compact(src, n, T, need_eq, sh, emit);
-    } else {
-        GmemKeys src{row};
-        find_threshold(src, n, k, sh, T, need_eq);
-        ordered_compact(src, n, T, need_eq, sh, emit);
-    }
-}
-
+// ---------------------------------------------------------------- kernels
+// Top-k slots of each row of scores (reported as cand positions when given).
+template <int CL>
 __global__ void __launch_bounds__(TK_THREADS) k_topk(const float *__restrict__ scores, int64_t ld,
                                                      const int32_t *__restrict__ len,
                                                      const int32_t *__restrict__ cand, int k,
                                                      int32_t *__restrict__ out)
 {
-    extern __shared__ uint32_t stage[];
+    extern __shared__ uint32_t keys[];
     __shared__ TkShared sh;
-    const int64_t r = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int64_t r = blockIdx.x / CL;
+    const int q = (int)cluster.block_rank();
     int64_t n = len[r];
     n = n < 0 ? 0 : (n > ld ? ld : n);
+    const int64_t slice = (n + CL - 1) / CL;
+    const int64_t lo = q * slice < n ? q * slice : n;
+    const int m = (int)((lo + slice < n ? lo + slice : n) - lo);
+    const float *row = scores + r * ld + lo;
+    for (int i = threadIdx.x; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
+    __syncthreads();
     int32_t *o = out + r * k;
     const int32_t *cr = cand ? cand + r * ld : nullptr;
-    select_row(scores + r * ld, n, k, stage, sh, [&](int j, int64_t i) {
+    cluster_select<CL>(cluster, keys, lo, m, n, k, sh, [&](int j, int64_t i) {
         if (j < k) o[j] = cr ? cr[i] : (int32_t)i;
     });
     const int64_t nsel = n < k ? n : k;
-    for (int64_t j = nsel + threadIdx.x; j < k; j += TK_THREADS) o[j] = -1;
+    if (q == CL - 1)
+        for (int64_t j = nsel + threadIdx.x; j < k; j += TK_THREADS) o[j] = -1;
 }
 
-__global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restrict__ block_max,
-                                                            int64_t ld_blocks,
-                                                            const int32_t *__restrict__ n_visible,
-                                                            int pmax, int32_t *__restrict__ pool,
+// Block level of the hierarchy: the pmax best blocks -> their visible positions.
+template <int CL>
+__global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restrict__ block_max, int64_t ld_blocks,
+                                                            const int32_t *__restrict__ n_visible, int pmax,
+                                                            int32_t *__restrict__ pool,
                                                             int32_t *__restrict__ pool_len)
 {
-    extern __shared__ uint32_t stage[];
+    extern __shared__ uint32_t keys[];
     __shared__ TkShared sh;
-    __shared__ int32_t sel[CSA2_POOL_BLOCKS];
-    const int64_t r = blockIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int64_t r = blockIdx.x / CL;
+    const int q = (int)cluster.block_rank();
     int64_t nv = n_visible[r];
     nv = nv < 0 ? 0 : (nv > ld_blocks * 8 ? ld_blocks * 8 : nv);
     const int64_t nb = (nv + 7) / 8;
-    select_row(block_max + r * ld_blocks, nb, pmax, stage, sh, [&](int j, int64_t i) {
-        if (j < pmax) sel[j] = (int32_t)i;
-    });
+    const int64_t slice = (nb + CL - 1) / CL;
+    const int64_t lo = q * slice < nb ? q * slice : nb;
+    const int m = (int)((lo + slice < nb ? lo + slice : nb) - lo);
+    const float *row = block_max + r * ld_blocks + lo;
+    for (int i = threadIdx.x; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
     __syncthreads();
-    const int nsel = (int)(nb < pmax ? nb : pmax);
     int32_t *pr = pool + r * (int64_t)pmax * 8;
-    for (int j = threadIdx.x; j < nsel * 8; j += TK_THREADS) {
-        const int64_t p = (int64_t)sel[j >> 3] * 8 + (j & 7);
-        if (p < nv) pr[j] = (int32_t)p;
-    }
-    if (threadIdx.x == 0) {
-        int total = 0;
-        if (nsel > 0) {
-            const int64_t last = (int64_t)sel[nsel - 1] * 8;
-            const int64_t tail = nv - last < 8 ? nv - last : 8;
-            total = (nsel - 1) * 8 + (int)tail;
+    const int nsel = (int)(nb < pmax ? nb : pmax);
+    cluster_select<CL>(cluster, keys, lo, m, nb, pmax, sh, [&](int j, int64_t blk) {
+        if (j >= pmax) return;
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const int64_t p = blk * 8 + t;
+            if (p < nv) pr[(int64_t)j * 8 + t] = (int32_t)p;
         }
-        pool_len[r] = total;
-    }
+        if (j == nsel - 1) {                         // the last selected block sets the pool size
+            const int64_t tail = nv - blk * 8 < 8 ? nv - blk * 8 : 8;
+            pool_len[r] = (nsel - 1) * 8 + (int)tail;
+        }
+    });
+    if (nsel == 0 && q == 0 && threadIdx.x == 0) pool_len[r] = 0;
 }
 
-static int topk_smem_bytes(int64_t n_max)
+// Cluster size for rows of up to n keys: slices of at most TK_SLICE keys.
+static int topk_cluster_for(int64_t n)
 {
-    const int64_t n = n_max < TK_STAGE ? n_max : TK_STAGE;
-    return (int)(n * 4);
+    return n > 4 * (int64_t)TK_SLICE ? 8 : (n > 2 * (int64_t)TK_SLICE ? 4 : (n > TK_SLICE ? 2 : 1));
+}
+
+template <class K, class... Args>
+static int launch_cluster(K kernel, int cl, int64_t ld, int32_t rows, cudaStream_t st, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows * (unsigned)cl);
+    cfg.blockDim = dim3(TK_THREADS);
+    cfg.dynamicSmemBytes = (size_t)(((ld + cl - 1) / cl) * 4);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cl;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+template <int CL>
+static int topk_cl(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
+                   int32_t k, int32_t *out, cudaStream_t st)
+{
+    static bool attr = false;                        // raise the limit once, before any graph capture
+    if (!attr) {
+        cudaFuncSetAttribute(k_topk<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SLICE * 4);
+        attr = true;
+    }
+    return launch_cluster(k_topk<CL>, CL, ld, rows, st, scores, ld, len, cand, (int)k, out);
+}
+
+template <int CL>
+static int blocks_cl(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
+                     int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
+{
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_topk_blocks<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SLICE * 4);
+        attr = true;
+    }
+    return launch_cluster(k_topk_blocks<CL>, CL, ld_blocks, rows, st, block_max, ld_blocks, n_visible, (int)pmax,
+                          pool, pool_len);
 }
 
 int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
                 int32_t k, int32_t *out, cudaStream_t st)
 {
     if (rows == 0) return CSA2_OK;
-    const int smem = topk_smem_bytes(ld);
-    static bool attr = false;                   // raise the limit once, before any graph capture
-    if (!attr) {
-        cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_STAGE * 4);
-        attr = true;
+    switch (topk_cluster_for(ld)) {
+    case 1: return topk_cl<1>(scores, ld, len, rows, cand, k, out, st);
+    case 2: return topk_cl<2>(scores, ld, len, rows, cand, k, out, st);
+    case 4: return topk_cl<4>(scores, ld, len, rows, cand, k, out, st);
+    default: return topk_cl<8>(scores, ld, len, rows, cand, k, out, st);
     }
-    k_topk<<<rows, TK_THREADS, smem, st>>>(scores, ld, len, cand, k, out);
-    return launch_status();
 }
 
-int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible,
-                       int32_t rows, int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
+int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
+                       int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
 {
     if (rows == 0) return CSA2_OK;
-    const int smem = topk_smem_bytes(ld_blocks);
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_topk_blocks, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_STAGE * 4);
-        attr = true;
+    switch (topk_cluster_for(ld_blocks)) {
+    case 1: return blocks_cl<1>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
+    case 2: return blocks_cl<2>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
+    case 4: return blocks_cl<4>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
+    default: return blocks_cl<8>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
     }
-    k_topk_blocks<<<rows, TK_THREADS, smem, st>>>(block_max, ld_blocks, n_visible, pmax, pool, pool_len);
-    return launch_status();
 }
 
 int topk_max_k() { return TK_MAX_K; }
+
+// Longest row a Top-K call accepts: 8 slices of TK_SLICE keys.
+int64_t topk_max_len() { return 8 * (int64_t)TK_SLICE; }
 
 }  // namespace csa2

@@ -226,7 +226,8 @@ CSA2_API int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *b
  * With ascending cand rows, "lower slot" is "lower position".  -0.0 and +0.0
  * compare equal.  [P2] §1 table (top-k 512), §3.2 ("its own Top-512").
  *   scores fp32 [rows][ld]; len int32 [rows] (clamped to [0, ld]);
- *   cand int32 [rows][ld] or NULL; out int32 [rows][k]; 1 <= k <= 4096. */
+ *   cand int32 [rows][ld] or NULL; out int32 [rows][k]; 1 <= k <= 4096;
+ *   ld <= 131072 (CSA2_ERR_SHAPE otherwise). */
 CSA2_API int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows,
               const int32_t *cand, int32_t k, int32_t *out, csa2_stream_t stream);
 
@@ -235,7 +236,9 @@ CSA2_API int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int3
  * ceil(n_visible[r] / 8) blocks, and write all their visible positions in
  * ascending order to pool[r] (pool_len[r] of them).
  *   block_max fp32 [rows][ld_blocks]; n_visible int32 [rows];
- *   pool int32 [rows][pmax*8]; pool_len int32 [rows]; 1 <= pmax <= 2048. */
+ *   pool int32 [rows][pmax*8]; pool_len int32 [rows]; 1 <= pmax <= 2048;
+ *   ld_blocks <= 131072, i.e. at most 1,048,576 visible entries (the pages'
+ *   maximum context; CSA2_ERR_SHAPE otherwise). */
 CSA2_API int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible,
                      int32_t rows, int32_t pmax, int32_t *pool, int32_t *pool_len,
                      csa2_stream_t stream);
@@ -266,7 +269,8 @@ CSA2_API size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq);
  *                          Top-512 -> io->idx; attention.
  *      CSA2_MODE_REUSE   : attention with io->idx as it is.
  * [P2] §3 mode table and §3.2; [P1] §3.2.  The main KV and the indexer keys
- * are the cache's (the latest Full layer's).  workspace must hold
+ * are the cache's (the latest Full layer's).  A Full layer takes at most
+ * 1,048,576 entries (batch->max_entries).  workspace must hold
  * csa2_layer_workspace_size(mode, batch) bytes, 256-byte aligned. */
 CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch,
                const csa2_layer_io *io, void *workspace, size_t workspace_bytes,
