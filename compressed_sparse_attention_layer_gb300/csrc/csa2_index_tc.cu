@@ -1,9 +1,11 @@
-// a4: the Full layer's lightning-indexer scan on the tcgen05 tensor cores.
+// a7: lightning-indexer scores of a gathered list of entries on the tcgen05
+// tensor cores -- a Reindex layer rescoring its candidate pool
+// ("DeepSeek-V4.1-Flash 架构详解" §3 mode table, §3.2).  The same kernel
+// also scores every visible entry (template flag POOL = false); the Full
+// layer's scan itself runs on the TMA-fed e4m3 kernel.
 //
-// score(p) = s_p * sum_h w_h ReLU(qi_h . code_p) for every visible entry p,
-// and the maximum of each aligned block of 8 positions
-// ("DeepSeek-V4 report explainer" §3.2; "DeepSeek-V4.1-Flash" research note
-// §3.2; "DeepSeek-V4.1-Flash 架构详解" §3.2).
+// score(p) = s_p * sum_h w_h ReLU(qi_h . code_p)
+// ("DeepSeek-V4 report explainer" §3.2).
 //
 // Per 128-entry tile: D[128 entries x 32 heads] = A[128 x 128] * B[32 x 128]^T
 // with A = the e4m3 key codes widened to f16 (exact) and B = the indexer query
@@ -372,12 +374,6 @@ static int launch_index(const csa2_cache &c, const csa2_batch &bt, const uint16_
                                                                         block_max, n_visible, ld);
     }
     return launch_status();
-}
-
-int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
-{
-    return launch_index<false>(c, bt, qi, w, nullptr, nullptr, scores, block_max, n_visible, ld, st);
 }
 
 // a7: a Reindex layer rescoring its candidate pool ("DeepSeek-V4.1-Flash 架构详解" §3.2).
