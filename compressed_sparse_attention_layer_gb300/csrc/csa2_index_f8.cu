@@ -199,40 +199,50 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
         const int64_t nvis = visible_entries(bt, r);
 
         if (warp == 0) {
-            // ---------------- TMA producer
-            if (lane == 0) {
-                for (int64_t i = 0; i < nt; i++) {
+            // ---------------- TMA producer: page ids of 32 tiles at a time, one lane per tile
+            int32_t my_pg[2] = {-1, -1};
+            for (int64_t i = 0; i < nt; i++) {
+                if ((i & 31) == 0) {
+                    const int64_t pt = (j0 + i + lane) * F8_TILE;     // tile i + lane
+#pragma unroll
+                    for (int h = 0; h < 2; h++) {
+                        const int64_t e0 = pt + 64 * h;
+                        my_pg[h] = -2;                                // -2: beyond the visible entries
+                        if (i + lane < nt && e0 < nvis)
+                            my_pg[h] = __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
+                    }
+                }
+                const int32_t pg0 = __shfl_sync(0xffffffffu, my_pg[0], (int)(i & 31));
+                const int32_t pg1 = __shfl_sync(0xffffffffu, my_pg[1], (int)(i & 31));
+                if (lane == 0) {
                     const int64_t ti = it + i;
                     const int stage = (int)(ti % F8_STAGES);
                     const int k = (int)(ti / F8_STAGES);
+                    bool ok = true;
                     if (k > 0 && !tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort)) {
                         *abort = 1;
                         flag(c.status, CSA2_DEV_TIMEOUT);
-                        break;
+                        ok = false;
                     }
-                    const int64_t p0 = (j0 + i) * F8_TILE;
-                    int32_t page[2] = {-1, -1};
-                    uint32_t bytes = 0;
+                    if (ok) {
+                        const int32_t pgs[2] = {pg0, pg1};
+                        uint32_t bytes = 0;
 #pragma unroll
-                    for (int h = 0; h < 2; h++) {
-                        const int64_t e0 = p0 + 64 * h;
-                        if (e0 < nvis) {
-                            const int32_t pg = __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
-                            if (pg >= 0 && ((int64_t)pg + 1) * CSA2_PAGE <= c.num_slots) {
-                                page[h] = pg;
-                                bytes += 64 * 128;
-                            } else {
-                                flag(c.status, CSA2_DEV_BAD_PAGE);
-                            }
+                        for (int h = 0; h < 2; h++) {
+                            if (pgs[h] == -2) continue;
+                            if (pgs[h] >= 0 && ((int64_t)pgs[h] + 1) * CSA2_PAGE <= c.num_slots) bytes += 64 * 128;
+                            else flag(c.status, CSA2_DEV_BAD_PAGE);
                         }
-                    }
-                    tc::mbar_arrive_expect_tx(&S.full[stage], bytes);
+                        tc::mbar_arrive_expect_tx(&S.full[stage], bytes);
 #pragma unroll
-                    for (int h = 0; h < 2; h++)
-                        if (page[h] >= 0)
-                            tc::tma_load_2d(S.a[stage] + h * 64 * 128, &tmap, 0, page[h] * CSA2_PAGE, &S.full[stage]);
-                    last_full_k[stage] = k;
+                        for (int h = 0; h < 2; h++)
+                            if (pgs[h] >= 0 && ((int64_t)pgs[h] + 1) * CSA2_PAGE <= c.num_slots)
+                                tc::tma_load_2d(S.a[stage] + h * 64 * 128, &tmap, 0, pgs[h] * CSA2_PAGE,
+                                                &S.full[stage]);
+                        last_full_k[stage] = k;
+                    }
                 }
+                if (__shfl_sync(0xffffffffu, *abort, 0)) break;
             }
         } else if (warp == 1) {
             // ---------------- query operand + MMA issue
@@ -298,7 +308,26 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
             float wv[32];
 #pragma unroll
             for (int h = 0; h < 32; h++) wv[h] = S.wq[seg & 1][h];
+            // the scale of this lane's entry, two tiles ahead: page id for tile i+2,
+            // scale for tile i+1, use for tile i
+            const int64_t rowp = (int64_t)qd * 32 + lane;
+            auto page_of = [&](int64_t i) -> int32_t {
+                const int64_t p = (j0 + i) * F8_TILE + rowp;
+                if (i >= nt || p >= nvis) return -2;
+                return __ldg(c.block_table + (int64_t)b * c.max_pages + (p >> 6));
+            };
+            auto scale_of = [&](int64_t i, int32_t pg) -> float {
+                const int64_t p = (j0 + i) * F8_TILE + rowp;
+                if (pg == -2) return 0.0f;
+                const int64_t slot = (int64_t)pg * CSA2_PAGE + (p & 63);
+                if (pg < 0 || slot >= c.num_slots) return -INFINITY;            // bad page: score -inf
+                return __ldg(c.ik_scales + slot);
+            };
+            int32_t pg_next = page_of(1);
+            float sc_cur = scale_of(0, page_of(0));
             for (int64_t i = 0; i < nt; i++) {
+                const int32_t pg_next2 = page_of(i + 2);
+                const float sc_next = scale_of(i + 1, pg_next);
                 const int64_t ti = it + i;
                 const int acc = (int)(ti % F8_ACC);
                 bool ok = tc::mbar_wait_or_abort(&S.tfull[acc], (uint32_t)((ti / F8_ACC) & 1), abort);
@@ -318,18 +347,16 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&S.tempty[acc]);
-                const int64_t p = (j0 + i) * F8_TILE + qd * 32 + lane;
+                const int64_t p = (j0 + i) * F8_TILE + rowp;
                 const bool valid = p < nvis;
                 float sc = -INFINITY;
                 if (valid) {
-                    const int32_t pg = __ldg(c.block_table + (int64_t)b * c.max_pages + (p >> 6));
-                    const int64_t slot = (int64_t)pg * CSA2_PAGE + (p & 63);
-                    if (pg >= 0 && slot < c.num_slots) {
+                    if (sc_cur != -INFINITY) {
                         float acc_s = 0.0f;
 #pragma unroll
                         for (int h = 0; h < 32; h++)
                             acc_s = fmaf(wv[h], fmaxf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.0f), acc_s);
-                        sc = acc_s * __ldg(c.ik_scales + slot);
+                        sc = acc_s * sc_cur;
                     }
                     if (scores) scores[(int64_t)r * ld + p] = sc;
                 }
@@ -339,6 +366,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                     for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                     if ((lane & 7) == 0 && valid) block_max[(int64_t)r * (ld / 8) + (p >> 3)] = m;
                 }
+                sc_cur = sc_next;
+                pg_next = pg_next2;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&S.wfree[seg & 1]);   // this warp is done with seg's weights
