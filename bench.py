@@ -300,7 +300,7 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-KERNEL_VERSION = "f8-tma-scan-v1"
+KERNEL_VERSION = "f8-tma-scan-v2"
 
 
 # ---------------------------------------------------------------- CPU oracle

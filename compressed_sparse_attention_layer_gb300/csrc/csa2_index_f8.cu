@@ -10,11 +10,12 @@
 // (8 KB) into a 128-byte-swizzled shared-memory tile, which is directly the
 // K-major A operand (M = 128 entries, K = 128 codes).  The indexer query is
 // the B operand split into two e4m3 parts per head, hi = e4m3(q'), lo =
-// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256): N = 64 rows
-// (32 heads x {hi, lo}).  D[128 x 64] fp32 in tensor memory; the epilogue
-// adds hi + lo per head, applies ReLU, w_h * 2^e_h and the entry's scale.
+// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  Per K step two
+// N = 32 products (A x hi, then A x lo) accumulate into the same fp32
+// D[128 entries x 32 heads] in tensor memory; the epilogue applies ReLU,
+// w_h * 2^e_h and the entry's scale.
 //
-// Warp roles (192 threads): warp 0 issues TMA into an 8-stage ring, warp 1
+// Warp roles (192 threads): warp 0 issues TMA into a 12-stage ring, warp 1
 // writes the query operand of each row and issues the MMAs (one thread),
 // warps 2-5 drain four tensor-memory accumulators.  A persistent grid walks
 // one global list of (row, tile) items so ragged batches stay balanced.
@@ -29,12 +30,12 @@
 
 namespace csa2 {
 
-constexpr int F8_STAGES = 8;
-constexpr int F8_ACC = 4;
+constexpr int F8_STAGES = 12;
+constexpr int F8_ACC = 8;                  // tensor-memory accumulators of 32 columns
 constexpr int F8_THREADS = 192;
 constexpr int F8_TILE = 128;
 constexpr int F8_PERSIST_ROWS = 256;
-constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 64);
+constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 32);
 
 struct F8Smem {
     uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (TMA)
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
         S.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 1) tc::tmem_alloc(&S.tmem, F8_ACC * 64);
+    if (warp == 1) tc::tmem_alloc(&S.tmem, F8_ACC * 32);
 
     int64_t g0, g1;
     if (PERSIST) {
@@ -282,10 +283,14 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                         tc::tc_fence_after();
                         const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++)       // K = 128 codes in steps of 32
-                            tc::mma_f8(tmem + (uint32_t)acc * 64u,
-                                       tc::smem_desc(as + kk * 32, 16, 1024, tc::kSwizzle128B),
+                        for (int kk = 0; kk < 4; kk++) {     // K = 128 codes in steps of 32
+                            const uint64_t ad = tc::smem_desc(as + kk * 32, 16, 1024, tc::kSwizzle128B);
+                            tc::mma_f8(tmem + (uint32_t)acc * 32u, ad,
                                        tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC, kk > 0);
+                            tc::mma_f8(tmem + (uint32_t)acc * 32u, ad,
+                                       tc::smem_desc(b0 + 32 * 128 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC,
+                                       1);
+                        }
                         tc::mma_commit(&S.empty[stage]);
                         tc::mma_commit(&S.tfull[acc]);
                         last_tile = ti;
@@ -339,10 +344,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                     break;
                 }
                 tc::tc_fence_after();
-                uint32_t hi[32], lo[32];
-                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 64u;
-                tc::tmem_ld32(ta, hi);
-                tc::tmem_ld32(ta + 32u, lo);
+                uint32_t d[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 32u, d);
                 tc::tmem_ld_wait();
                 tc::tc_fence_before();
                 __syncwarp();
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                         float acc_s = 0.0f;
 #pragma unroll
                         for (int h = 0; h < 32; h++)
-                            acc_s = fmaf(wv[h], fmaxf(__uint_as_float(hi[h]) + __uint_as_float(lo[h]), 0.0f), acc_s);
+                            acc_s = fmaf(wv[h], fmaxf(__uint_as_float(d[h]), 0.0f), acc_s);
                         sc = acc_s * sc_cur;
                     }
                     if (scores) scores[(int64_t)r * ld + p] = sc;
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 1) tc::tmem_dealloc(tmem, F8_ACC * 64);
+    if (warp == 1) tc::tmem_dealloc(tmem, F8_ACC * 32);
 }
 
 // ---------------------------------------------------------------- host side

@@ -42,7 +42,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
 {
     for (uint32_t i = 0; i < limit; i++) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(32);
+        if (i > 4096) __nanosleep(64);
     }
     return false;
 }
@@ -66,7 +66,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     for (uint32_t i = 0; i < limit; i++) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
-        if (i > 64) __nanosleep(32);
+        if (i > 4096) __nanosleep(64);
     }
     return false;
 }
