@@ -7,16 +7,22 @@
 // Split over keys: CTA (row, chunk) takes 128 keys -- chunks 0..3 the selected
 // entries idx[128c .. 128c+127], the last chunk the window rows -- and all 64
 // heads:
-//   1. dequantise its keys into a 128 x 512 bf16 tile (MXFP4 e2m1 * 2^X is
-//      exact in bf16; window codes e4m3 are exact, their fp32 row scale is
-//      applied to the logit and to the probability instead);
+//   1. dequantise its keys into a 128 x 512 bf16 tile: MXFP4 bytes through a
+//      256-entry table (byte -> two bf16 magnitudes with signs) and one bf16x2
+//      multiply by 2^X per block; window codes e4m3 by placing their bits in a
+//      bf16 and one multiply by 2^120 -- both exact; the window's fp32 row scale
+//      is applied to the logit and to the probability instead;
 //   2. S^T[128 keys x 64 heads] = K Q^T   (M = keys, N = heads, K = 512 dims);
 //   3. per-head max m_c and sum l_c over the chunk, P = exp(S - m_c) split into
-//      bf16 hi + lo (P = hi + lo to 2^-17);
-//   4. O^T[512 dims x 64 heads] = V^T P^T with the same key tile read as an
-//      MN-major operand (4 M-tiles of 128 dims, K = 128 keys, hi and lo);
+//      bf16 hi + lo (P = hi + lo to 2^-17), stacked as one 128-row operand;
+//   4. [O_hi | O_lo]^T[512 dims x 128] = V^T [P_hi | P_lo]^T with the same key
+//      tile read as an MN-major operand (4 M-tiles of 128 dims, K = 128 keys,
+//      N = 128); the epilogue adds the two halves;
 //   5. the unnormalised partial O_c and (m_c, l_c) go to the workspace.
 // A second kernel merges the chunks of each row: O = sum_c e^(m_c-M) O_c / L.
+// 512 threads: four per key (128 dims each) for the loads and dequantisation,
+// eight per head for the softmax statistics, one M-tile row each for the
+// epilogue.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -26,11 +32,11 @@
 
 namespace csa2 {
 
-constexpr int AC_THREADS = 256;                   // two threads per key
+constexpr int AC_THREADS = 512;
 constexpr int AC_KEYS = 128;                       // keys per chunk (MMA M of the first product)
 constexpr int AC_MAX_CHUNKS = CSA2_TOPK / AC_KEYS + 1;
 constexpr uint32_t AC_IDESC_S = tc::idesc_f16(128, 64, 1, 1, 0, 0);   // K-major A and B
-constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 64, 1, 1, 1, 0);   // MN-major A (V^T)
+constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 128, 1, 1, 1, 0);  // MN-major A (V^T), N = hi|lo
 
 struct AcSmem {
     uint8_t k[8 * AC_KEYS * 128];                  // [slab of 64 dims][128 keys][128 B]   128 KB
@@ -38,11 +44,13 @@ struct AcSmem {
         uint8_t q[8 * CSA2_HEADS * 128];           // [slab][64 heads][128 B]              64 KB
         struct {
             float red[CSA2_HEADS][AC_KEYS];        // logits, transposed                  32 KB
-            uint8_t p_hi[2 * CSA2_HEADS * 128];    // [slab of 64 keys][64 heads][128 B]  16 KB
-            uint8_t p_lo[2 * CSA2_HEADS * 128];    //                                     16 KB
+            uint8_t p[2 * 2 * CSA2_HEADS * 128];   // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB
         } s;
     } u;
+    uint32_t e2m1_pair[256];                       // byte -> bf16x2 of its two E2M1 codes
     float m[CSA2_HEADS], l[CSA2_HEADS];
+    float kscale[AC_KEYS];
+    int valid[AC_KEYS];
     uint64_t mbar;
     uint32_t tmem;
 };
@@ -53,84 +61,101 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Half (`half` = 0: dims 0..255, 1: dims 256..511) of an MXFP4 entry -> bf16
-// row of the key tile (exact).
-__device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint8_t *codes,
-                                               const uint8_t *scales, int half)
+// a (bf16x2) * b (bf16x2), exact when the products are representable.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
 {
-    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(scales) + half);
-    const uint8_t *scb = reinterpret_cast<const uint8_t *>(&sc);
-    const uint4 *src = reinterpret_cast<const uint4 *>(codes) + 8 * half;
-#pragma unroll 4
-    for (int ii = 0; ii < 8; ii++) {               // 16 bytes = 32 elements = one MX block
-        const int i = ii + 8 * half;
-        const uint4 u = __ldg(src + ii);
-        const int X = (int)scb[ii] - 127;
-        const float f = exp2i(X < -126 ? -126 : X);
-        const float f2 = X < -126 ? 0.5f : 1.0f;      // X = -127
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+    uint32_t r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(0x80008000u));
+    return r;
+}
+
+// 2^X (X in [-127, 127]) as a bf16, in both halves.
+__device__ __forceinline__ uint32_t pow2_bf16x2(int X)
+{
+    const uint32_t h = X >= -126 ? (uint32_t)(X + 127) << 7 : 0x0040u;   // 2^-127 is subnormal
+    return h | (h << 16);
+}
+
+// Quarter `qt` (dims 128 qt .. 128 qt + 127) of an MXFP4 entry -> bf16 row of
+// the key tile (exact): the table gives the two E2M1 magnitudes of a byte with
+// their signs, one bf16x2 multiply applies the block's 2^X.
+__device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[4], uint32_t sc,
+                                               int qt, const uint32_t *pair)
+{
 #pragma unroll
-        for (int j = 0; j < 4; j++) {              // 8 elements -> one 16-byte chunk
+    for (int blk = 0; blk < 4; blk++) {            // 16 bytes = 32 elements = one MX block
+        const uint32_t f = pow2_bf16x2((int)((sc >> (8 * blk)) & 0xFFu) - 127);
+        const uint32_t w[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {              // 4 bytes = 8 elements -> one 16-byte chunk
             uint4 o;
-            uint32_t *ow = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const uint32_t b = (wd[j] >> (8 * e)) & 0xFFu;
-                ow[e] = pack_bf16x2(e2m1_to_f32(b & 15u) * f * f2, e2m1_to_f32(b >> 4) * f * f2);
-            }
-            *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 32 * i + 8 * j, AC_KEYS)) = o;
+            o.x = bf16x2_mul(pair[w[j] & 0xFFu], f);
+            o.y = bf16x2_mul(pair[(w[j] >> 8) & 0xFFu], f);
+            o.z = bf16x2_mul(pair[(w[j] >> 16) & 0xFFu], f);
+            o.w = bf16x2_mul(pair[w[j] >> 24], f);
+            *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 32 * blk + 8 * j, AC_KEYS)) = o;
         }
     }
 }
 
-// Half of an FP8 window row -> bf16 row of the key tile (codes only; exact).
-__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint8_t *codes, int half)
+// Two e4m3 codes (low bytes of the halves of v) -> bf16x2 of their values:
+// sign and the 7 exponent/mantissa bits moved into bf16 position give the
+// value times 2^-120, which one exact multiply by 2^120 restores (subnormal
+// codes included).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v)
 {
-    const uint4 *src = reinterpret_cast<const uint4 *>(codes) + 16 * half;
-#pragma unroll 4
-    for (int ii = 0; ii < 16; ii++) {              // 16 codes per load
-        const int i = ii + 16 * half;
-        const uint4 u = __ldg(src + ii);
-        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t bits = ((v & 0x007F007Fu) << 4) | ((v & 0x00800080u) << 8);
+    return bf16x2_mul(bits, 0x7B807B80u);          // 2^120 in both halves
+}
+
+// Quarter `qt` of an FP8 window row -> bf16 row of the key tile (codes only; exact).
+__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[8], int qt)
+{
+#pragma unroll
+    for (int i = 0; i < 8; i++) {                  // 16 codes per load -> two 16-byte chunks
+        const uint32_t w[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
         uint4 o0, o1;
-        uint32_t *a = reinterpret_cast<uint32_t *>(&o0);
-        uint32_t *b = reinterpret_cast<uint32_t *>(&o1);
-#pragma unroll
-        for (int e = 0; e < 4; e++) {
-            const uint32_t w = wd[e];
-            const uint32_t v = pack_bf16x2(e4m3_to_f32(w & 0xFFu), e4m3_to_f32((w >> 8) & 0xFFu));
-            const uint32_t v2 = pack_bf16x2(e4m3_to_f32((w >> 16) & 0xFFu), e4m3_to_f32(w >> 24));
-            if (e < 2) {
-                a[2 * e] = v;
-                a[2 * e + 1] = v2;
-            } else {
-                b[2 * (e - 2)] = v;
-                b[2 * (e - 2) + 1] = v2;
-            }
-        }
-        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 16 * i, AC_KEYS)) = o0;
-        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 16 * i + 8, AC_KEYS)) = o1;
+        o0.x = e4m3x2_to_bf16x2(__byte_perm(w[0], 0, 0x4140));
+        o0.y = e4m3x2_to_bf16x2(__byte_perm(w[0], 0, 0x4342));
+        o0.z = e4m3x2_to_bf16x2(__byte_perm(w[1], 0, 0x4140));
+        o0.w = e4m3x2_to_bf16x2(__byte_perm(w[1], 0, 0x4342));
+        o1.x = e4m3x2_to_bf16x2(__byte_perm(w[2], 0, 0x4140));
+        o1.y = e4m3x2_to_bf16x2(__byte_perm(w[2], 0, 0x4342));
+        o1.z = e4m3x2_to_bf16x2(__byte_perm(w[3], 0, 0x4140));
+        o1.w = e4m3x2_to_bf16x2(__byte_perm(w[3], 0, 0x4342));
+        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 16 * i, AC_KEYS)) = o0;
+        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 16 * i + 8, AC_KEYS)) = o1;
     }
 }
 
-__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int half)
+__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int qt)
 {
-#pragma unroll 8
-    for (int i = 32 * half; i < 32 * half + 32; i++)
+#pragma unroll 4
+    for (int i = 16 * qt; i < 16 * qt + 16; i++)
         *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 8 * i, AC_KEYS)) = make_uint4(0, 0, 0, 0);
 }
 
-__global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch bt,
-                                                        const uint16_t *__restrict__ q, float sm_scale,
-                                                        const int32_t *__restrict__ idx, int k, csa2_swa swa,
-                                                        float *__restrict__ part_o, float *__restrict__ part_ml,
-                                                        int nchunks)
+// 16 consecutive 32-bit TMEM columns of this warp's lane quarter.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_batch bt,
+                                                           const uint16_t *__restrict__ q, float sm_scale,
+                                                           const int32_t *__restrict__ idx, int k, csa2_swa swa,
+                                                           float *__restrict__ part_o, float *__restrict__ part_ml,
+                                                           int nchunks)
 {
     extern __shared__ uint8_t smem_raw[];
     AcSmem &S = *reinterpret_cast<AcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int key = tid & (AC_KEYS - 1), half = tid >> 7;   // key row; half of the dims / heads
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // TMEM lane quarter of this warp
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int key = tid & (AC_KEYS - 1), qt = tid >> 7;          // key row; quarter of the dims / heads
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16; // TMEM lane quarter of this warp
     const int64_t r = blockIdx.x;
     const int chunk = blockIdx.y;
     const int b = (int)(r / bt.nq);
@@ -141,32 +166,30 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
         tc::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&S.tmem, 512);
-
-    // ---- queries: 64 x 512 bf16, coalesced 16-byte loads into the swizzled B tile
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM);
-#pragma unroll 4
-        for (int i = 0; i < 16; i++) {
-            const int e = 8 * (tid + AC_THREADS * i);
-            const uint4 v = __ldg(src + tid + AC_THREADS * i);
-            *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 9, e & 511, CSA2_HEADS)) = v;
-        }
+    if (tid < 256) {                               // E2M1 pair table
+        const uint32_t lo = tid & 15u, hi = tid >> 4;
+        S.e2m1_pair[tid] = pack_bf16x2(e2m1_to_f32(lo), e2m1_to_f32(hi));
     }
 
-    // ---- this thread's key: dequantise its half into row `key` of the key tile
+    // ---- this thread's key: locate it and start loading its quarter
     float kscale = 1.0f;          // multiplies the logit and the probability (window rows)
     bool valid = false;
+    uint4 kc[8];
+    uint32_t ksc = 0;
     if (!window) {
         const int j = chunk * AC_KEYS + key;
         if (j < k) {
             const int32_t p = idx[r * k + j];
             if (p >= 0) {
                 if (p >= visible_entries(bt, r)) {
-                    if (half == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
+                    if (qt == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
                 } else {
                     const int64_t slot = entry_slot(c, b, p);
                     if (slot >= 0) {
-                        store_main_key(S.k, key, c.kv_codes + slot * 256, c.kv_scales + slot * 16, half);
+                        const uint4 *src = reinterpret_cast<const uint4 *>(c.kv_codes + slot * 256) + 4 * qt;
+#pragma unroll
+                        for (int i = 0; i < 4; i++) kc[i] = __ldg(src + i);
+                        ksc = __ldg(reinterpret_cast<const uint32_t *>(c.kv_scales + slot * 16) + qt);
                         valid = true;
                     }
                 }
@@ -181,12 +204,43 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
         if (lo + key <= t) {
             const int64_t row = (lo + key) % swa.rows;
             const int64_t off = (int64_t)b * swa.rows + row;
-            store_window_key(S.k, key, swa.codes + off * CSA2_HEAD_DIM, half);
+            const uint4 *src = reinterpret_cast<const uint4 *>(swa.codes + off * CSA2_HEAD_DIM) + 8 * qt;
+#pragma unroll
+            for (int i = 0; i < 8; i++) kc[i] = __ldg(src + i);
             kscale = swa.scales[off];
             valid = true;
         }
     }
-    if (!valid) zero_key(S.k, key, half);
+
+    // ---- queries: 64 x 512 bf16, coalesced 16-byte loads into the swizzled B tile
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM);
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) v[i] = __ldg(src + tid + AC_THREADS * i);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const int e = 8 * (tid + AC_THREADS * i);
+            *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 9, e & 511, CSA2_HEADS)) = v[i];
+        }
+    }
+    if (qt == 0) {
+        S.kscale[key] = kscale;
+        S.valid[key] = valid;
+    }
+    __syncthreads();                               // the pair table is ready
+
+    // ---- dequantise the key quarter into row `key` of the key tile
+    if (valid) {
+        if (window) {
+            store_window_key(S.k, key, kc, qt);
+        } else {
+            const uint4 (&kc4)[4] = *reinterpret_cast<const uint4 (*)[4]>(kc);
+            store_main_key(S.k, key, kc4, ksc, qt, S.e2m1_pair);
+        }
+    } else {
+        zero_key(S.k, key, qt);
+    }
 
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -197,7 +251,7 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     // ---- S^T = K Q^T
     if (tid == 0) {
         const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.u.q);
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 32; kk++) {          // 512 dims in steps of 16
             const uint32_t off = (uint32_t)(kk >> 2) * (AC_KEYS * 128) + (uint32_t)(kk & 3) * 32u;
             const uint32_t offq = (uint32_t)(kk >> 2) * (CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
@@ -213,29 +267,35 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     }
     tc::tc_fence_after();
     {
-        // ---- logits of this key for this half's 32 heads, transposed into smem
-        const float lscale = sm_scale * kscale;
+        // ---- logits of this key for this quarter's 16 heads, transposed into smem
+        const bool kv = S.valid[key];
+        const float lscale = sm_scale * S.kscale[key];
         {
-            uint32_t acc[32];
-            tc::tmem_ld32(tmem + lane_base + (uint32_t)half * 32u, acc);
+            uint32_t acc[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)qt * 16u, acc);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 32; h++)
-                S.u.s.red[half * 32 + h][key] = valid ? __uint_as_float(acc[h]) * lscale : -INFINITY;
+            for (int h = 0; h < 16; h++)
+                S.u.s.red[qt * 16 + h][key] = kv ? __uint_as_float(acc[h]) * lscale : -INFINITY;
         }
         __syncthreads();
-        // ---- per-head max and sum over the chunk: four threads per head
+        // ---- per-head max and sum over the chunk: eight threads per head
         {
-            const int h = tid >> 2, part = tid & 3;
+            const int h = tid >> 3, part = tid & 7;
             float mx = -INFINITY;
-            for (int j = part; j < AC_KEYS; j += 4) mx = fmaxf(mx, S.u.s.red[h][j]);
+#pragma unroll 4
+            for (int j = part; j < AC_KEYS; j += 8) mx = fmaxf(mx, S.u.s.red[h][j]);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             float sum = 0.0f;
-            if (mx != -INFINITY)
-                for (int j = part; j < AC_KEYS; j += 4) sum += expf(S.u.s.red[h][j] - mx);
+            if (mx != -INFINITY) {
+#pragma unroll 4
+                for (int j = part; j < AC_KEYS; j += 8) sum += expf(S.u.s.red[h][j] - mx);
+            }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             if (part == 0) {
                 S.m[h] = mx;
                 S.l[h] = sum;
@@ -243,16 +303,16 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
         }
         __syncthreads();
         // ---- P^T (times the window scale) as bf16 hi + lo, K-major rows = heads
+        const float vscale = S.kscale[key];
 #pragma unroll 4
-        for (int hh = 0; hh < 32; hh++) {
-            const int h = half * 32 + hh;
+        for (int hh = 0; hh < 16; hh++) {
+            const int h = qt * 16 + hh;
             const float mx = S.m[h];
-            const float p = (valid && mx != -INFINITY) ? expf(S.u.s.red[h][key] - mx) * kscale : 0.0f;
+            const float p = (kv && mx != -INFINITY) ? expf(S.u.s.red[h][key] - mx) * vscale : 0.0f;
             const __nv_bfloat16 hi = __float2bfloat16_rn(p);
             const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-            const uint32_t off = tc::sw128_offset(h, key, CSA2_HEADS);
-            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p_hi + off) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p_lo + off) = lo;
+            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p + tc::sw128_offset(h, key, 2 * CSA2_HEADS)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p + tc::sw128_offset(CSA2_HEADS + h, key, 2 * CSA2_HEADS)) = lo;
         }
     }
     tc::fence_proxy_async_smem();
@@ -260,20 +320,21 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     __syncthreads();
     tc::tc_fence_after();
 
-    // ---- O^T = V^T P^T: 4 tiles of 128 dims, K = 128 keys, hi then lo
+    // ---- [O_hi | O_lo]^T = V^T [P_hi | P_lo]^T: 4 tiles of 128 dims, K = 128 keys,
+    //      N = 128; the tile of dims 128 mt .. +127 lands in columns 128 mt .. +127
+    //      (S has been read out, its columns are reused)
     if (tid == 0) {
         const uint32_t k0 = tc::smem_u32(S.k);
-        const uint32_t ph = tc::smem_u32(S.u.s.p_hi), pl = tc::smem_u32(S.u.s.p_lo);
-#pragma unroll
+        const uint32_t p0 = tc::smem_u32(S.u.s.p);
+#pragma unroll 1
         for (int mt = 0; mt < 4; mt++) {
-            const uint32_t d = tmem + 64u + 64u * (uint32_t)mt;
-#pragma unroll
+            const uint32_t d = tmem + 128u * (uint32_t)mt;
+#pragma unroll 1
             for (int kk = 0; kk < 8; kk++) {       // 16 keys per step
                 const uint64_t ad = tc::smem_desc(k0 + (uint32_t)(2 * mt) * (AC_KEYS * 128) + (uint32_t)kk * 2048u,
                                                   AC_KEYS * 128, 1024, tc::kSwizzle128B);
-                const uint32_t boff = (uint32_t)(kk >> 2) * (CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
-                tc::mma_f16(d, ad, tc::smem_desc(ph + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, kk > 0);
-                tc::mma_f16(d, ad, tc::smem_desc(pl + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, 1);
+                const uint32_t boff = (uint32_t)(kk >> 2) * (2 * CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
+                tc::mma_f16(d, ad, tc::smem_desc(p0 + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, kk > 0);
             }
         }
         tc::mma_commit(&S.mbar);
@@ -285,17 +346,21 @@ __global__ void __launch_bounds__(AC_THREADS) k_attn_tc(csa2_cache c, csa2_batch
     }
     tc::tc_fence_after();
     {
-        // ---- partial output: lane = dim within the M-tile, this half's 32 heads
+        // ---- partial output: warp group g takes M-tile g, lane = dim, 64 heads
         const int64_t base = (r * AC_MAX_CHUNKS + chunk) * (int64_t)CSA2_HEADS;
         float *po = part_o + base * CSA2_HEAD_DIM;
+        const int mt = warp >> 2;
+        const int d = 128 * mt + (warp & 3) * 32 + lane;
 #pragma unroll 1
-        for (int mt = 0; mt < 4; mt++) {
-            const int d = 128 * mt + (warp & 3) * 32 + (tid & 31);
-            uint32_t acc[32];
-            tc::tmem_ld32(tmem + lane_base + 64u + 64u * (uint32_t)mt + 32u * (uint32_t)half, acc);
+        for (int half = 0; half < 2; half++) {
+            uint32_t ahi[32], alo[32];
+            const uint32_t col = 128u * (uint32_t)mt + 32u * (uint32_t)half;
+            tc::tmem_ld32(tmem + lane_base + col, ahi);
+            tc::tmem_ld32(tmem + lane_base + col + 64u, alo);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int h = 0; h < 32; h++) po[(int64_t)(half * 32 + h) * CSA2_HEAD_DIM + d] = __uint_as_float(acc[h]);
+            for (int h = 0; h < 32; h++)
+                po[(int64_t)(half * 32 + h) * CSA2_HEAD_DIM + d] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
         }
         if (tid < CSA2_HEADS) {
             part_ml[(base + tid) * 2] = S.m[tid];
