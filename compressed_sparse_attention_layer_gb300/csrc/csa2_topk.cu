@@ -5,10 +5,12 @@
 // the pool's own Top-512; the research note §3.2).  The CL CTAs of a cluster
 // each stage one contiguous 1/CL of the row in shared memory as
 // order-preserving 32-bit keys, read once from global memory.  A radix select
-// over 11 + 11 + 10-bit digits finds the k-th largest key T: each CTA counts
-// its slice, the histograms are summed through distributed shared memory, and
-// every CTA takes the same decision.  An ordered compaction then writes every
-// key > T and the lowest-slot keys == T: each CTA learns how many selected
+// finds the k-th largest key T: the digits are 11-bit fields of (key - kmin)
+// from the top bit of the row's actual range (kmax - kmin), so that scores
+// crowded into a few exponents still spread over all 2,048 bins; each CTA
+// counts its slice, the histograms are summed through distributed shared
+// memory, and every CTA takes the same decision.  An ordered compaction then
+// writes every key > T and the lowest-slot keys == T: each CTA learns how many selected
 // slots lie in the slices before its own from the cluster's counts, so the
 // output comes out in ascending slot order without atomics deciding order.
 #include <cooperative_groups.h>
@@ -24,34 +26,87 @@ constexpr int TK_SLICE = 16384;            // keys staged per CTA (64 KB)
 constexpr int TK_MAX_K = 4096;
 
 struct TkShared {
-    uint32_t hist[2048];
+    uint32_t hist[2048];                   // this CTA's slice counts
+    uint32_t own[2048];                    // cluster totals of the bins this rank owns
+    int own_total;                         // their sum
     int warp_sums[32];
     int cnt[2];                            // this CTA's (count > T, count == T)
     uint32_t digit;
     int above;
+    uint32_t kmin, kmax;                   // this CTA's key range
 };
 
-// Sum the cluster's histograms; find the bin holding the kk-th largest key
-// among those matching the prefix so far, and the count above that bin.
+// 32-bit load from the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_ld(const void *p, int rank)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p)), ra, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+// Find the bin holding the kk-th largest key among those counted, and the
+// count above that bin, from the CL slice histograms of the cluster.  Each CTA
+// first totals its own 256 bins across the cluster (8 remote loads for 256
+// threads); every CTA then reads the CL slice totals, finds the slice with
+// the crossing, fetches that slice's 256 totals and scans them: the same
+// decision everywhere.  Ends with the cluster synchronised.
 template <int CL>
 __device__ void cluster_digit(cg::cluster_group &cluster, TkShared &sh, int kk, uint32_t &digit, int &above)
 {
     const int tid = threadIdx.x;
-    int c[4] = {0, 0, 0, 0};                         // bins 2047-4t .. 2044-4t, descending
+    const int me = (int)cluster.block_rank();
+    constexpr int BPR = 2048 / CL;                   // bins owned per rank
+    constexpr int PER = BPR > TK_THREADS ? BPR / TK_THREADS : 1;   // bins per thread
+    constexpr int ACTIVE = BPR / PER;                // threads holding bins
+    // ---- 1. own bins, cluster totals
+    int v = 0;
+    if (tid < ACTIVE) {
 #pragma unroll
-    for (int q = 0; q < CL; q++) {
-        const uint32_t *h = cluster.map_shared_rank(sh.hist, q);
+        for (int j = 0; j < PER; j++) {
+            const int bin = tid * PER + j;
+            uint32_t acc = 0;
 #pragma unroll
-        for (int j = 0; j < 4; j++) c[j] += (int)h[2047 - 4 * tid - j];
+            for (int q = 0; q < CL; q++) acc += dsmem_ld(&sh.hist[BPR * me + bin], q);
+            sh.own[bin] = acc;
+            v += (int)acc;
+        }
     }
-    const int tot = c[0] + c[1] + c[2] + c[3];
-    const int excl = block_exclusive_scan<TK_THREADS>(tot, sh.warp_sums, nullptr);
-    if (excl < kk && excl + tot >= kk) {
-        int acc = excl;
+    int tot = 0;
+    (void)block_exclusive_scan<TK_THREADS>(v, sh.warp_sums, &tot);
+    if (tid == 0) sh.own_total = tot;
+    cluster.sync();
+    // ---- 2. the slice holding the crossing (ranks from the top bins down)
+    if (tid == 0) {
+        int acc = 0, slice = 0, slice_above = 0;
+        for (int q = CL - 1; q >= 0; q--) {
+            const int t = (int)dsmem_ld(&sh.own_total, q);
+            if (acc < kk && acc + t >= kk) {
+                slice = q;
+                slice_above = acc;
+            }
+            acc += t;
+        }
+        sh.digit = (uint32_t)slice;
+        sh.above = slice_above;
+    }
+    __syncthreads();
+    const int slice = (int)sh.digit, slice_above = sh.above;
+    // ---- 3. the crossing bin inside that slice, bins in descending order
+    int c[PER];
+    int csum = 0;
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
+    for (int j = 0; j < PER; j++) {
+        c[j] = tid < ACTIVE ? (int)dsmem_ld(&sh.own[BPR - 1 - (tid * PER + j)], slice) : 0;
+        csum += c[j];
+    }
+    const int excl = block_exclusive_scan<TK_THREADS>(csum, sh.warp_sums, nullptr);
+    if (tid < ACTIVE && slice_above + excl < kk && slice_above + excl + csum >= kk) {
+        int acc = slice_above + excl;
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
             if (acc + c[j] >= kk) {
-                sh.digit = 2047 - 4 * tid - j;
+                sh.digit = (uint32_t)(BPR * slice + BPR - 1 - (tid * PER + j));
                 sh.above = acc;
                 break;
             }
@@ -75,19 +130,50 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         for (int i = tid; i < m; i += TK_THREADS) emit((int)(lo + i), lo + i);
         return;
     }
-    uint32_t prefix = 0, mask = 0;
+    // ---- the row's key range (cluster-wide), digits relative to its minimum
+    {
+        uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+        for (int i = tid; i < m; i += TK_THREADS) {
+            mn = min(mn, keys[i]);
+            mx = max(mx, keys[i]);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        if (tid == 0) {
+            sh.kmin = 0xFFFFFFFFu;
+            sh.kmax = 0u;
+        }
+        __syncthreads();
+        if ((tid & 31) == 0) {
+            atomicMin(&sh.kmin, mn);
+            atomicMax(&sh.kmax, mx);
+        }
+    }
+    cluster.sync();
+    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+    for (int q = 0; q < CL; q++) {
+        const TkShared *o = cluster.map_shared_rank(&sh, q);
+        kmin = min(kmin, o->kmin);
+        kmax = max(kmax, o->kmax);
+    }
+    const uint32_t range = kmax - kmin;
+    const int nbits = range ? 32 - __clz(range) : 1;
+    uint32_t prefix = 0, mask = 0;                   // over rel = key - kmin
     int kk = k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
 #pragma unroll 1
-    for (int pass = 0; pass < 3; pass++) {
-        const int shift = shifts[pass];
-        const uint32_t dmask = (1u << widths[pass]) - 1u;
+    for (int top = nbits; top > 0; top -= 11) {
+        const int width = top < 11 ? top : 11;
+        const int shift = top - width;
+        const uint32_t dmask = (1u << width) - 1u;
         for (int b = tid; b < 2048; b += TK_THREADS) sh.hist[b] = 0;
         __syncthreads();
         for (int i = tid; i < m; i += TK_THREADS) {
-            const uint32_t u = keys[i];
-            if ((u & mask) == prefix) atomicAdd(&sh.hist[(u >> shift) & dmask], 1u);
+            const uint32_t rel = keys[i] - kmin;
+            if ((rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
         }
         cluster.sync();                              // every slice counted
         uint32_t d;
@@ -98,7 +184,7 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         kk -= above;
         cluster.sync();                              // every CTA done reading before the reset
     }
-    const uint32_t T = prefix;
+    const uint32_t T = prefix + kmin;
     const int need_eq = kk;                          // ties with T that are selected, lowest slots first
 
     // ---- counts of this thread's chunk, of this slice, and of the slices before it
@@ -143,6 +229,35 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
     }
 }
 
+// Stage row[0 .. m) as order keys: 16-byte loads, many in flight.
+__device__ __forceinline__ void stage_keys(uint32_t *keys, const float *row, int m)
+{
+    const int tid = threadIdx.x;
+    if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+        const int m4 = m >> 2;
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll 4
+        for (int i = tid; i < m4; i += TK_THREADS) {
+            const float4 v = __ldg(r4 + i);
+            *reinterpret_cast<uint4 *>(keys + 4 * i) =
+                make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+        }
+        for (int i = 4 * m4 + tid; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
+    } else {
+#pragma unroll 8
+        for (int i = tid; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
+    }
+}
+
+// Slice of a row of n keys held by cluster rank q: a multiple of 4 keys so
+// that slices of 16-byte aligned rows stay aligned.
+__device__ __forceinline__ void slice_of(int64_t n, int cl, int q, int64_t &lo, int &m)
+{
+    const int64_t slice = ((n + cl - 1) / cl + 3) & ~(int64_t)3;
+    lo = q * slice < n ? q * slice : n;
+    m = (int)((lo + slice < n ? lo + slice : n) - lo);
+}
+
 // ---------------------------------------------------------------- kernels
 // Top-k slots of each row of scores (reported as cand positions when given).
 template <int CL>
@@ -158,11 +273,10 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(const float *__restrict__ s
     const int q = (int)cluster.block_rank();
     int64_t n = len[r];
     n = n < 0 ? 0 : (n > ld ? ld : n);
-    const int64_t slice = (n + CL - 1) / CL;
-    const int64_t lo = q * slice < n ? q * slice : n;
-    const int m = (int)((lo + slice < n ? lo + slice : n) - lo);
-    const float *row = scores + r * ld + lo;
-    for (int i = threadIdx.x; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
+    int64_t lo;
+    int m;
+    slice_of(n, CL, q, lo, m);
+    stage_keys(keys, scores + r * ld + lo, m);
     __syncthreads();
     int32_t *o = out + r * k;
     const int32_t *cr = cand ? cand + r * ld : nullptr;
@@ -189,11 +303,10 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
     int64_t nv = n_visible[r];
     nv = nv < 0 ? 0 : (nv > ld_blocks * 8 ? ld_blocks * 8 : nv);
     const int64_t nb = (nv + 7) / 8;
-    const int64_t slice = (nb + CL - 1) / CL;
-    const int64_t lo = q * slice < nb ? q * slice : nb;
-    const int m = (int)((lo + slice < nb ? lo + slice : nb) - lo);
-    const float *row = block_max + r * ld_blocks + lo;
-    for (int i = threadIdx.x; i < m; i += TK_THREADS) keys[i] = order_key(__ldg(row + i));
+    int64_t lo;
+    int m;
+    slice_of(nb, CL, q, lo, m);
+    stage_keys(keys, block_max + r * ld_blocks + lo, m);
     __syncthreads();
     int32_t *pr = pool + r * (int64_t)pmax * 8;
     const int nsel = (int)(nb < pmax ? nb : pmax);
@@ -212,10 +325,11 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
     if (nsel == 0 && q == 0 && threadIdx.x == 0) pool_len[r] = 0;
 }
 
-// Cluster size for rows of up to n keys: slices of at most TK_SLICE keys.
+// Cluster size for rows of up to n keys: small rows on one or two CTAs, the
+// 16,384-entry pools on four, longer rows on eight (slices <= TK_SLICE keys).
 static int topk_cluster_for(int64_t n)
 {
-    return n > 4 * (int64_t)TK_SLICE ? 8 : (n > 2 * (int64_t)TK_SLICE ? 4 : (n > TK_SLICE ? 2 : 1));
+    return n > 32768 ? 8 : (n > 8192 ? 4 : (n > 2048 ? 2 : 1));
 }
 
 template <class K, class... Args>
@@ -224,7 +338,7 @@ static int launch_cluster(K kernel, int cl, int64_t ld, int32_t rows, cudaStream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows * (unsigned)cl);
     cfg.blockDim = dim3(TK_THREADS);
-    cfg.dynamicSmemBytes = (size_t)(((ld + cl - 1) / cl) * 4);
+    cfg.dynamicSmemBytes = (size_t)((((ld + cl - 1) / cl + 3) & ~(int64_t)3) * 4);
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
