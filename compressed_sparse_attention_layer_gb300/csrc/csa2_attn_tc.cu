@@ -4,25 +4,30 @@
 // softmax covers the selected entries and the window ("DeepSeek-V4.1-Flash
 // 架构详解" §1 table, §3; explainer §3.3).
 //
-// Split over keys: CTA (row, chunk) takes 128 keys -- chunks 0..3 the selected
-// entries idx[128c .. 128c+127], the last chunk the window rows -- and all 64
-// heads:
-//   1. dequantise its keys into a 128 x 512 bf16 tile: MXFP4 bytes through a
-//      256-entry table (byte -> two bf16 magnitudes with signs) and one bf16x2
-//      multiply by 2^X per block; window codes e4m3 by placing their bits in a
-//      bf16 and one multiply by 2^120 -- both exact; the window's fp32 row scale
-//      is applied to the logit and to the probability instead;
-//   2. S^T[128 keys x 64 heads] = K Q^T   (M = keys, N = heads, K = 512 dims);
-//   3. per-head max m_c and sum l_c over the chunk, P = exp(S - m_c) split into
-//      bf16 hi + lo (P = hi + lo to 2^-17), stacked as one 128-row operand;
-//   4. [O_hi | O_lo]^T[512 dims x 128] = V^T [P_hi | P_lo]^T with the same key
-//      tile read as an MN-major operand (4 M-tiles of 128 dims, K = 128 keys,
-//      N = 128); the epilogue adds the two halves;
-//   5. the unnormalised partial O_c and (m_c, l_c) go to the workspace.
+// Work unit (row, chunk): 128 keys -- chunks 0..3 the selected entries
+// idx[128c .. 128c+127], the last chunk the window rows -- and all 64 heads.
+// A cluster of four CTAs takes one unit, CTA d the dims 128 d .. 128 d + 127:
+//   1. dequantise its slice of the keys into a 128 x 128 bf16 tile: MXFP4
+//      bytes through a 256-entry table (byte -> two bf16 magnitudes with
+//      signs) and one bf16x2 multiply by 2^X per block; window codes e4m3 by
+//      placing their bits in a bf16 and one multiply by 2^120 -- both exact;
+//      the window's fp32 row scale is applied to the logit and to the
+//      probability instead;
+//   2. partial S^T[128 keys x 64 heads] = K_d Q_d^T over its 128 dims
+//      (M = keys, N = heads); each 16-head slice of it is stored straight
+//      into the shared memory of the CTA that owns those heads;
+//   3. after a cluster barrier CTA d sums the four partials of heads
+//      16 d .. 16 d + 15 (in rank order, so every run gives the same logits),
+//      takes their max m_c and sum l_c over the chunk, and writes
+//      P = exp(S - m_c) as bf16 hi + lo (P = hi + lo to 2^-17) into the
+//      probability operand of all four CTAs;
+//   4. O_d^T[128 dims x 64 heads] = V_d^T P_hi^T + V_d^T P_lo^T, reading the
+//      same key tile as an MN-major operand (V = K);
+//   5. the unnormalised partial O_c (this CTA's dims) and (m_c, l_c) go to the
+//      workspace.
 // A second kernel merges the chunks of each row: O = sum_c e^(m_c-M) O_c / L.
-// 512 threads: four per key (128 dims each) for the loads and dequantisation,
-// eight per head for the softmax statistics, one M-tile row each for the
-// epilogue.
+// 256 threads: two per key (64 dims each) for the loads and dequantisation,
+// sixteen per owned head for the softmax, one TMEM lane each in the epilogues.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -32,28 +37,69 @@
 
 namespace csa2 {
 
-constexpr int AC_THREADS = 512;
+constexpr int AC_THREADS = 256;
 constexpr int AC_KEYS = 128;                       // keys per chunk (MMA M of the first product)
+constexpr int AC_CL = 4;                           // CTAs per cluster, one per 128-dim slice
+constexpr int AC_DIMS = CSA2_HEAD_DIM / AC_CL;     // 128
+constexpr int AC_OWN = CSA2_HEADS / AC_CL;         // heads reduced by each CTA: 16
 constexpr int AC_MAX_CHUNKS = CSA2_TOPK / AC_KEYS + 1;
 constexpr uint32_t AC_IDESC_S = tc::idesc_f16(128, 64, 1, 1, 0, 0);   // K-major A and B
-constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 128, 1, 1, 1, 0);  // MN-major A (V^T), N = hi|lo
+constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 64, 1, 1, 1, 0);   // MN-major A (V^T)
 
 struct AcSmem {
-    uint8_t k[8 * AC_KEYS * 128];                  // [slab of 64 dims][128 keys][128 B]   128 KB
+    uint8_t k[2 * AC_KEYS * 128];                  // [slab of 64 dims][128 keys][128 B]   32 KB
     union {
-        uint8_t q[8 * CSA2_HEADS * 128];           // [slab][64 heads][128 B]              64 KB
-        struct {
-            float red[CSA2_HEADS][AC_KEYS];        // logits, transposed                  32 KB
-            uint8_t p[2 * 2 * CSA2_HEADS * 128];   // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB
-        } s;
-    } u;
+        uint8_t q[2 * CSA2_HEADS * 128];           // [slab][64 heads][128 B]              16 KB
+        uint8_t p[2 * 2 * CSA2_HEADS * 128];       // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB
+    } u;                                           // P arrives after the first cluster barrier,
+                                                   // when this CTA's first product is done with Q
+    float ps[AC_CL][AC_OWN][AC_KEYS];              // [source CTA][owned head][key] partial logits 32 KB
     uint32_t e2m1_pair[256];                       // byte -> bf16x2 of its two E2M1 codes
-    float m[CSA2_HEADS], l[CSA2_HEADS];
     float kscale[AC_KEYS];
     int valid[AC_KEYS];
     uint64_t mbar;
     uint32_t tmem;
 };
+
+// ---------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; release/acquire at cluster scope.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u4(uint32_t addr, const uint4 &v)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Order this thread's generic writes to shared memory anywhere in the cluster
+// before later tensor-core (async proxy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_cluster()
+{
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -76,14 +122,15 @@ __device__ __forceinline__ uint32_t pow2_bf16x2(int X)
     return h | (h << 16);
 }
 
-// Quarter `qt` (dims 128 qt .. 128 qt + 127) of an MXFP4 entry -> bf16 row of
-// the key tile (exact): the table gives the two E2M1 magnitudes of a byte with
-// their signs, one bf16x2 multiply applies the block's 2^X.
+// Half `hf` (local dims 64 hf .. 64 hf + 63, two MX blocks) of this CTA's
+// slice of an MXFP4 entry -> bf16 row of the key tile (exact): the table gives
+// the two E2M1 magnitudes of a byte with their signs, one bf16x2 multiply
+// applies the block's 2^X.
 __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[4], uint32_t sc,
-                                               int qt, const uint32_t *pair)
+                                               int hf, const uint32_t *pair)
 {
 #pragma unroll
-    for (int blk = 0; blk < 4; blk++) {            // 16 bytes = 32 elements = one MX block
+    for (int blk = 0; blk < 2; blk++) {            // 16 bytes = 32 elements = one MX block
         const uint32_t f = pow2_bf16x2((int)((sc >> (8 * blk)) & 0xFFu) - 127);
         const uint32_t w[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
 #pragma unroll
@@ -93,7 +140,7 @@ __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, con
             o.y = bf16x2_mul(pair[(w[j] >> 8) & 0xFFu], f);
             o.z = bf16x2_mul(pair[(w[j] >> 16) & 0xFFu], f);
             o.w = bf16x2_mul(pair[w[j] >> 24], f);
-            *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 32 * blk + 8 * j, AC_KEYS)) = o;
+            *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 32 * blk + 8 * j, AC_KEYS)) = o;
         }
     }
 }
@@ -108,11 +155,12 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v)
     return bf16x2_mul(bits, 0x7B807B80u);          // 2^120 in both halves
 }
 
-// Quarter `qt` of an FP8 window row -> bf16 row of the key tile (codes only; exact).
-__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[8], int qt)
+// Half `hf` of this CTA's slice of an FP8 window row -> bf16 row of the key
+// tile (codes only; exact).
+__device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[4], int hf)
 {
 #pragma unroll
-    for (int i = 0; i < 8; i++) {                  // 16 codes per load -> two 16-byte chunks
+    for (int i = 0; i < 4; i++) {                  // 16 codes per load -> two 16-byte chunks
         const uint32_t w[4] = {c[i].x, c[i].y, c[i].z, c[i].w};
         uint4 o0, o1;
         o0.x = e4m3x2_to_bf16x2(__byte_perm(w[0], 0, 0x4140));
@@ -123,16 +171,16 @@ __device__ __forceinline__ void store_window_key(uint8_t *ktile, uint32_t row, c
         o1.y = e4m3x2_to_bf16x2(__byte_perm(w[2], 0, 0x4342));
         o1.z = e4m3x2_to_bf16x2(__byte_perm(w[3], 0, 0x4140));
         o1.w = e4m3x2_to_bf16x2(__byte_perm(w[3], 0, 0x4342));
-        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 16 * i, AC_KEYS)) = o0;
-        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 128 * qt + 16 * i + 8, AC_KEYS)) = o1;
+        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 16 * i, AC_KEYS)) = o0;
+        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 16 * i + 8, AC_KEYS)) = o1;
     }
 }
 
-__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int qt)
+__device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int hf)
 {
-#pragma unroll 4
-    for (int i = 16 * qt; i < 16 * qt + 16; i++)
-        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 8 * i, AC_KEYS)) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 8 * i, AC_KEYS)) = make_uint4(0, 0, 0, 0);
 }
 
 // 16 consecutive 32-bit TMEM columns of this warp's lane quarter.
@@ -145,36 +193,49 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
-__global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_batch bt,
-                                                           const uint16_t *__restrict__ q, float sm_scale,
-                                                           const int32_t *__restrict__ idx, int k, csa2_swa swa,
-                                                           float *__restrict__ part_o, float *__restrict__ part_ml,
-                                                           int nchunks)
+__global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
+    k_attn_tc(csa2_cache c, csa2_batch bt, const uint16_t *__restrict__ q, float sm_scale,
+              const int32_t *__restrict__ idx, int k, csa2_swa swa, float *__restrict__ part_o,
+              float *__restrict__ part_ml, int nchunks)
 {
     extern __shared__ uint8_t smem_raw[];
     AcSmem &S = *reinterpret_cast<AcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int key = tid & (AC_KEYS - 1), qt = tid >> 7;          // key row; quarter of the dims / heads
+    const int key = tid & (AC_KEYS - 1), hf = tid >> 7;          // key row; half of this CTA's dims
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16; // TMEM lane quarter of this warp
-    const int64_t r = blockIdx.x;
-    const int chunk = blockIdx.y;
+    const uint32_t col_half = 32u * (uint32_t)(warp >> 2);        // TMEM column half of this warp
+    const uint32_t dq = cluster_rank();                           // dims 128 dq .. 128 dq + 127
+    const int chunk = blockIdx.x / AC_CL;
+    const int64_t r = blockIdx.y;
     const int b = (int)(r / bt.nq);
     const bool window = chunk == nchunks - 1;
+    const int64_t base = (r * AC_MAX_CHUNKS + chunk) * (int64_t)CSA2_HEADS;
 
     if (tid == 0) {
         tc::mbar_init(&S.mbar, 1);
         tc::fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(&S.tmem, 512);
-    if (tid < 256) {                               // E2M1 pair table
+    if (warp == 0) tc::tmem_alloc(&S.tmem, 128);  // columns 0-63: S^T, 64-127: O^T
+    {                                              // E2M1 pair table
         const uint32_t lo = tid & 15u, hi = tid >> 4;
         S.e2m1_pair[tid] = pack_bf16x2(e2m1_to_f32(lo), e2m1_to_f32(hi));
     }
 
-    // ---- this thread's key: locate it and start loading its quarter
+    // ---- this CTA's 128 dims of the 64 queries (coalesced 16-byte loads)
+    uint4 qv[4];
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM + AC_DIMS * dq);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int e = tid + AC_THREADS * i;
+            qv[i] = __ldg(src + (e >> 4) * (CSA2_HEAD_DIM / 8) + (e & 15));
+        }
+    }
+
+    // ---- this thread's key: locate it and start loading its 64 dims
     float kscale = 1.0f;          // multiplies the logit and the probability (window rows)
     bool valid = false;
-    uint4 kc[8];
+    uint4 kc[4];
     uint32_t ksc = 0;
     if (!window) {
         const int j = chunk * AC_KEYS + key;
@@ -182,14 +243,15 @@ __global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_ba
             const int32_t p = idx[r * k + j];
             if (p >= 0) {
                 if (p >= visible_entries(bt, r)) {
-                    if (qt == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
+                    if (hf == 0 && dq == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
                 } else {
                     const int64_t slot = entry_slot(c, b, p);
                     if (slot >= 0) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(c.kv_codes + slot * 256) + 4 * qt;
-#pragma unroll
-                        for (int i = 0; i < 4; i++) kc[i] = __ldg(src + i);
-                        ksc = __ldg(reinterpret_cast<const uint32_t *>(c.kv_scales + slot * 16) + qt);
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(c.kv_codes + slot * 256 + AC_DIMS / 2 * dq) + 2 * hf;
+                        kc[0] = __ldg(src);
+                        kc[1] = __ldg(src + 1);
+                        ksc = __ldg(reinterpret_cast<const uint16_t *>(c.kv_scales + slot * 16 + 4 * dq) + hf);
                         valid = true;
                     }
                 }
@@ -204,42 +266,33 @@ __global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_ba
         if (lo + key <= t) {
             const int64_t row = (lo + key) % swa.rows;
             const int64_t off = (int64_t)b * swa.rows + row;
-            const uint4 *src = reinterpret_cast<const uint4 *>(swa.codes + off * CSA2_HEAD_DIM) + 8 * qt;
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(swa.codes + off * CSA2_HEAD_DIM + AC_DIMS * dq) + 4 * hf;
 #pragma unroll
-            for (int i = 0; i < 8; i++) kc[i] = __ldg(src + i);
+            for (int i = 0; i < 4; i++) kc[i] = __ldg(src + i);
             kscale = swa.scales[off];
             valid = true;
         }
     }
 
-    // ---- queries: 64 x 512 bf16, coalesced 16-byte loads into the swizzled B tile
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM);
-        uint4 v[8];
+    // ---- the queries' slice arrives while the key lookups run
 #pragma unroll
-        for (int i = 0; i < 8; i++) v[i] = __ldg(src + tid + AC_THREADS * i);
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            const int e = 8 * (tid + AC_THREADS * i);
-            *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 9, e & 511, CSA2_HEADS)) = v[i];
-        }
+    for (int i = 0; i < 4; i++) {
+        const int e = tid + AC_THREADS * i;        // head e / 16, 16-byte chunk e % 16
+        *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 4, 8 * (e & 15), CSA2_HEADS)) = qv[i];
     }
-    if (qt == 0) {
+    if (hf == 0) {
         S.kscale[key] = kscale;
         S.valid[key] = valid;
     }
     __syncthreads();                               // the pair table is ready
 
-    // ---- dequantise the key quarter into row `key` of the key tile
+    // ---- dequantise into row `key` of the key tile
     if (valid) {
-        if (window) {
-            store_window_key(S.k, key, kc, qt);
-        } else {
-            const uint4 (&kc4)[4] = *reinterpret_cast<const uint4 (*)[4]>(kc);
-            store_main_key(S.k, key, kc4, ksc, qt, S.e2m1_pair);
-        }
+        if (window) store_window_key(S.k, key, kc, hf);
+        else store_main_key(S.k, key, kc, ksc, hf, S.e2m1_pair);
     } else {
-        zero_key(S.k, key, qt);
+        zero_key(S.k, key, hf);
     }
 
     tc::fence_proxy_async_smem();
@@ -248,11 +301,11 @@ __global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_ba
     tc::tc_fence_after();
     const uint32_t tmem = S.tmem;
 
-    // ---- S^T = K Q^T
+    // ---- partial S^T = K_d Q_d^T over this CTA's 128 dims
     if (tid == 0) {
         const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.u.q);
-#pragma unroll 1
-        for (int kk = 0; kk < 32; kk++) {          // 512 dims in steps of 16
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {           // 16 dims per step
             const uint32_t off = (uint32_t)(kk >> 2) * (AC_KEYS * 128) + (uint32_t)(kk & 3) * 32u;
             const uint32_t offq = (uint32_t)(kk >> 2) * (CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
             tc::mma_f16(tmem, tc::smem_desc(k0 + off, 16, 1024, tc::kSwizzle128B),
@@ -260,168 +313,178 @@ __global__ void __launch_bounds__(AC_THREADS, 1) k_attn_tc(csa2_cache c, csa2_ba
         }
         tc::mma_commit(&S.mbar);
     }
-    bool ok = tc::mbar_wait(&S.mbar, 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
-        goto teardown;
-    }
+    // A CTA whose product timed out still passes both cluster barriers (the
+    // other three wait there) but writes no output; the status word says why.
+    const bool fail = __syncthreads_or(!tc::mbar_wait(&S.mbar, 0));
     tc::tc_fence_after();
-    {
-        // ---- logits of this key for this quarter's 16 heads, transposed into smem
-        const bool kv = S.valid[key];
-        const float lscale = sm_scale * S.kscale[key];
-        {
-            uint32_t acc[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)qt * 16u, acc);
-            tc::tmem_ld_wait();
+    if (!fail) {
+        // heads col_half .. +15 belong to CTA col_half / 16, the next 16 to the one after
+        uint32_t acc[32];
+        tc::tmem_ld32(tmem + lane_base + col_half, acc);
+        tc::tmem_ld_wait();
+        const int kr = (warp & 3) * 32 + lane;
+        const uint32_t la = tc::smem_u32(&S.ps[dq][0][kr]);
+        const uint32_t ra0 = cluster_map(la, col_half / AC_OWN), ra1 = cluster_map(la, col_half / AC_OWN + 1);
 #pragma unroll
-            for (int h = 0; h < 16; h++)
-                S.u.s.red[qt * 16 + h][key] = kv ? __uint_as_float(acc[h]) * lscale : -INFINITY;
+        for (int j = 0; j < 16; j++) {
+            st_cluster_f32(ra0 + (uint32_t)j * (AC_KEYS * 4), acc[j]);
+            st_cluster_f32(ra1 + (uint32_t)j * (AC_KEYS * 4), acc[16 + j]);
         }
-        __syncthreads();
-        // ---- per-head max and sum over the chunk: eight threads per head
-        {
-            const int h = tid >> 3, part = tid & 7;
-            float mx = -INFINITY;
-#pragma unroll 4
-            for (int j = part; j < AC_KEYS; j += 8) mx = fmaxf(mx, S.u.s.red[h][j]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    } else if (tid == 0) {
+        flag(c.status, CSA2_DEV_TIMEOUT);
+    }
+    cluster_sync();                                // the four partials of the owned heads are here
+
+    // ---- owned heads 16 dq .. 16 dq + 15: sixteen threads per head, eight
+    //      consecutive keys per thread
+    {
+        const int hl = tid >> 4, h = AC_OWN * (int)dq + hl, part = tid & 15;
+        float4 v[AC_CL][2];
+#pragma unroll
+        for (int src = 0; src < AC_CL; src++) {
+            v[src][0] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part]);
+            v[src][1] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part + 4]);
+        }
+        float lg[8];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
             float sum = 0.0f;
-            if (mx != -INFINITY) {
-#pragma unroll 4
-                for (int j = part; j < AC_KEYS; j += 8) sum += expf(S.u.s.red[h][j] - mx);
+#pragma unroll
+            for (int src = 0; src < AC_CL; src++) {
+                const float4 &w = v[src][j >> 2];
+                sum += (j & 3) == 0 ? w.x : (j & 3) == 1 ? w.y : (j & 3) == 2 ? w.z : w.w;
             }
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (part == 0) {
-                S.m[h] = mx;
-                S.l[h] = sum;
-            }
+            const int kj = 8 * part + j;
+            lg[j] = S.valid[kj] ? sum * (sm_scale * S.kscale[kj]) : -INFINITY;
+            mx = fmaxf(mx, lg[j]);
         }
-        __syncthreads();
-        // ---- P^T (times the window scale) as bf16 hi + lo, K-major rows = heads
-        const float vscale = S.kscale[key];
-#pragma unroll 4
-        for (int hh = 0; hh < 16; hh++) {
-            const int h = qt * 16 + hh;
-            const float mx = S.m[h];
-            const float p = (kv && mx != -INFINITY) ? expf(S.u.s.red[h][key] - mx) * vscale : 0.0f;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p + tc::sw128_offset(h, key, 2 * CSA2_HEADS)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(S.u.s.p + tc::sw128_offset(CSA2_HEADS + h, key, 2 * CSA2_HEADS)) = lo;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float e[8], l = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            e[j] = mx != -INFINITY && lg[j] != -INFINITY ? __expf(lg[j] - mx) : 0.0f;
+            l += e[j];
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        uint32_t hi2[4], lo2[4];
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            const float p0 = e[j] * S.kscale[8 * part + j], p1 = e[j + 1] * S.kscale[8 * part + j + 1];
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
+            const float2 hf2 = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf2.x, p1 - hf2.y);
+            hi2[j >> 1] = *reinterpret_cast<const uint32_t *>(&hi);
+            lo2[j >> 1] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
+        // row h (hi) and 64 + h (lo) of the probability operand, keys 8 part .. +7
+        const uint32_t chunk16 = (uint32_t)((part & 7) ^ (h & 7)) << 4;
+        const uint32_t off_hi = (uint32_t)(part >> 3) * (2 * CSA2_HEADS * 128) + (uint32_t)h * 128u + chunk16;
+        const uint32_t off_lo = off_hi + CSA2_HEADS * 128;
+        const uint32_t p0 = tc::smem_u32(S.u.p);
+        const uint4 vhi = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+        const uint4 vlo = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
+#pragma unroll
+        for (int dst = 0; dst < AC_CL; dst++) {
+            st_cluster_u4(cluster_map(p0 + off_hi, (uint32_t)dst), vhi);
+            st_cluster_u4(cluster_map(p0 + off_lo, (uint32_t)dst), vlo);
+        }
+        if (part == 0 && !fail) {
+            part_ml[(base + h) * 2] = mx;
+            part_ml[(base + h) * 2 + 1] = l;
         }
     }
-    tc::fence_proxy_async_smem();
+    fence_proxy_async_cluster();
     tc::tc_fence_before();
-    __syncthreads();
+    cluster_sync();                                // P complete everywhere; partials no longer read
     tc::tc_fence_after();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // let the merge kernel be scheduled
 
-    // ---- [O_hi | O_lo]^T = V^T [P_hi | P_lo]^T: 4 tiles of 128 dims, K = 128 keys,
-    //      N = 128; the tile of dims 128 mt .. +127 lands in columns 128 mt .. +127
-    //      (S has been read out, its columns are reused)
-    if (tid == 0) {
-        const uint32_t k0 = tc::smem_u32(S.k);
-        const uint32_t p0 = tc::smem_u32(S.u.s.p);
-#pragma unroll 1
-        for (int mt = 0; mt < 4; mt++) {
-            const uint32_t d = tmem + 128u * (uint32_t)mt;
-#pragma unroll 1
-            for (int kk = 0; kk < 8; kk++) {       // 16 keys per step
-                const uint64_t ad = tc::smem_desc(k0 + (uint32_t)(2 * mt) * (AC_KEYS * 128) + (uint32_t)kk * 2048u,
-                                                  AC_KEYS * 128, 1024, tc::kSwizzle128B);
-                const uint32_t boff = (uint32_t)(kk >> 2) * (2 * CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
-                tc::mma_f16(d, ad, tc::smem_desc(p0 + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, kk > 0);
-            }
+    // ---- O_d^T = V_d^T P_hi^T + V_d^T P_lo^T: M = 128 dims, K = 128 keys, N = 64 heads
+    if (tid == 0 && !fail) {
+        tc::fence_proxy_async_smem();
+        const uint32_t k0 = tc::smem_u32(S.k), p0 = tc::smem_u32(S.u.p);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) {           // 16 keys per step
+            const uint64_t ad = tc::smem_desc(k0 + (uint32_t)kk * 2048u, AC_KEYS * 128, 1024, tc::kSwizzle128B);
+            const uint32_t boff = (uint32_t)(kk >> 2) * (2 * CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
+            tc::mma_f16(tmem + 64u, ad, tc::smem_desc(p0 + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, kk > 0);
+            tc::mma_f16(tmem + 64u, ad, tc::smem_desc(p0 + boff + CSA2_HEADS * 128, 16, 1024, tc::kSwizzle128B),
+                        AC_IDESC_O, 1);
         }
         tc::mma_commit(&S.mbar);
     }
-    ok = tc::mbar_wait(&S.mbar, 1);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
-        goto teardown;
-    }
-    tc::tc_fence_after();
-    {
-        // ---- partial output: warp group g takes M-tile g, lane = dim, 64 heads
-        const int64_t base = (r * AC_MAX_CHUNKS + chunk) * (int64_t)CSA2_HEADS;
-        float *po = part_o + base * CSA2_HEAD_DIM;
-        const int mt = warp >> 2;
-        const int d = 128 * mt + (warp & 3) * 32 + lane;
-#pragma unroll 1
-        for (int half = 0; half < 2; half++) {
-            uint32_t ahi[32], alo[32];
-            const uint32_t col = 128u * (uint32_t)mt + 32u * (uint32_t)half;
-            tc::tmem_ld32(tmem + lane_base + col, ahi);
-            tc::tmem_ld32(tmem + lane_base + col + 64u, alo);
+    if (!fail) {
+        const bool fail2 = __syncthreads_or(!tc::mbar_wait(&S.mbar, 1));
+        tc::tc_fence_after();
+        if (!fail2) {
+            // ---- partial output: lane = dim of this CTA's slice, 32 heads per warp
+            uint32_t acc[32];
+            tc::tmem_ld32(tmem + lane_base + 64u + col_half, acc);
             tc::tmem_ld_wait();
+            float *po = part_o + base * CSA2_HEAD_DIM + AC_DIMS * dq + (warp & 3) * 32 + lane;
 #pragma unroll
-            for (int h = 0; h < 32; h++)
-                po[(int64_t)(half * 32 + h) * CSA2_HEAD_DIM + d] = __uint_as_float(ahi[h]) + __uint_as_float(alo[h]);
-        }
-        if (tid < CSA2_HEADS) {
-            part_ml[(base + tid) * 2] = S.m[tid];
-            part_ml[(base + tid) * 2 + 1] = S.l[tid];
+            for (int j = 0; j < 32; j++) po[(int64_t)(col_half + j) * CSA2_HEAD_DIM] = __uint_as_float(acc[j]);
+        } else if (tid == 0) {
+            flag(c.status, CSA2_DEV_TIMEOUT);
         }
     }
-teardown:
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, 512);
+    if (warp == 0) tc::tmem_dealloc(tmem, 128);
 }
 
 // o = sum_c e^(m_c - M) O_c / sum_c e^(m_c - M) l_c, lse = M + log L; one CTA per
-// (row, 4 heads), thread = 4 consecutive dims (float4), all chunk loads in flight.
-__global__ void __launch_bounds__(128) k_attn_combine(const float *__restrict__ part_o,
+// (row, 2 heads), thread = 4 consecutive dims (float4) of one head, all chunk
+// loads in flight.  Launched as a programmatic dependent of the attention
+// kernel: it is scheduled early and waits for that grid's results here.
+__global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml, int nchunks,
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t r = blockIdx.x;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x & 127;
+    const int h = blockIdx.y * 2 + (threadIdx.x >> 7);
+    float mc[AC_MAX_CHUNKS], lc[AC_MAX_CHUNKS];
+    float4 v[AC_MAX_CHUNKS];
+    float M = -INFINITY;
 #pragma unroll
-    for (int hh = 0; hh < 4; hh++) {
-        const int h = blockIdx.y * 4 + hh;
-        float mc[AC_MAX_CHUNKS], lc[AC_MAX_CHUNKS];
-        float4 v[AC_MAX_CHUNKS];
-        float M = -INFINITY;
+    for (int ch = 0; ch < AC_MAX_CHUNKS; ch++) {
+        if (ch < nchunks) {
+            const int64_t base = (r * AC_MAX_CHUNKS + ch) * CSA2_HEADS + h;
+            const float2 ml = *reinterpret_cast<const float2 *>(part_ml + base * 2);
+            mc[ch] = ml.x;
+            lc[ch] = ml.y;
+            v[ch] = *reinterpret_cast<const float4 *>(part_o + base * CSA2_HEAD_DIM + 4 * tid);
+            M = fmaxf(M, ml.x);
+        } else {
+            mc[ch] = -INFINITY;
+            lc[ch] = 0.0f;
+            v[ch] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    float L = 0.0f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
 #pragma unroll
         for (int ch = 0; ch < AC_MAX_CHUNKS; ch++) {
-            if (ch < nchunks) {
-                const int64_t base = (r * AC_MAX_CHUNKS + ch) * CSA2_HEADS + h;
-                const float2 ml = *reinterpret_cast<const float2 *>(part_ml + base * 2);
-                mc[ch] = ml.x;
-                lc[ch] = ml.y;
-                v[ch] = *reinterpret_cast<const float4 *>(part_o + base * CSA2_HEAD_DIM + 4 * tid);
-                M = fmaxf(M, ml.x);
-            } else {
-                mc[ch] = -INFINITY;
-                lc[ch] = 0.0f;
-                v[ch] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            if (mc[ch] == -INFINITY) continue;
+            const float wgt = expf(mc[ch] - M);
+            L = fmaf(wgt, lc[ch], L);
+            acc.x = fmaf(wgt, v[ch].x, acc.x);
+            acc.y = fmaf(wgt, v[ch].y, acc.y);
+            acc.z = fmaf(wgt, v[ch].z, acc.z);
+            acc.w = fmaf(wgt, v[ch].w, acc.w);
         }
-        float L = 0.0f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int ch = 0; ch < AC_MAX_CHUNKS; ch++) {
-                if (mc[ch] == -INFINITY) continue;
-                const float wgt = expf(mc[ch] - M);
-                L = fmaf(wgt, lc[ch], L);
-                acc.x = fmaf(wgt, v[ch].x, acc.x);
-                acc.y = fmaf(wgt, v[ch].y, acc.y);
-                acc.z = fmaf(wgt, v[ch].z, acc.z);
-                acc.w = fmaf(wgt, v[ch].w, acc.w);
-            }
-        }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        *reinterpret_cast<float4 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 4 * tid) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        if (tid == 0) lse[r * CSA2_HEADS + h] = L > 0.0f ? M + logf(L) : -INFINITY;
     }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    *reinterpret_cast<float4 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 4 * tid) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (tid == 0) lse[r * CSA2_HEADS + h] = L > 0.0f ? M + logf(L) : -INFINITY;
 }
 
 size_t attn_workspace_bytes(int64_t rows)
@@ -442,16 +505,32 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
     float *part_ml = reinterpret_cast<float *>(static_cast<char *>(ws) + po_bytes);
     const int nchunks = (k + AC_KEYS - 1) / AC_KEYS + 1;
     const size_t smem = sizeof(AcSmem) + 1024;
+    if (rows > 65535) return CSA2_ERR_SHAPE;       // rows run along the grid's y dimension
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         attr = true;
     }
-    k_attn_tc<<<dim3((unsigned)rows, nchunks), AC_THREADS, smem, st>>>(c, bt, q, sm_scale, idx, k, swa, part_o,
-                                                                       part_ml, nchunks);
+    k_attn_tc<<<dim3((unsigned)(AC_CL * nchunks), (unsigned)rows), AC_THREADS, smem, st>>>(
+        c, bt, q, sm_scale, idx, k, swa, part_o, part_ml, nchunks);
     int s = launch_status();
     if (s) return s;
-    k_attn_combine<<<dim3((unsigned)rows, CSA2_HEADS / 4), 128, 0, st>>>(part_o, part_ml, nchunks, o, lse);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, CSA2_HEADS / 2);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_combine, (const float *)part_o, (const float *)part_ml,
+                                             nchunks, o, lse);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
     return launch_status();
 }
 
