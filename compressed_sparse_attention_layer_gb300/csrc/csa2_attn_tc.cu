@@ -6,27 +6,30 @@
 //
 // Work unit (row, chunk): 128 keys -- chunks 0..3 the selected entries
 // idx[128c .. 128c+127], the last chunk the window rows -- and all 64 heads.
-// A cluster of four CTAs takes one unit, CTA d the dims 128 d .. 128 d + 127:
-//   1. dequantise its slice of the keys into a 128 x 128 bf16 tile: MXFP4
+// A cluster of two CTAs takes one unit, CTA d the dims 256 d .. 256 d + 255
+// (the cluster size is a compile-time constant; four CTAs of 128 dims also
+// work but leave some SMs with two CTAs of one launch on an 8-row decode):
+//   1. dequantise its slice of the keys into a 128 x 256 bf16 tile: MXFP4
 //      bytes through a 256-entry table (byte -> two bf16 magnitudes with
 //      signs) and one bf16x2 multiply by 2^X per block; window codes e4m3 by
 //      placing their bits in a bf16 and one multiply by 2^120 -- both exact;
 //      the window's fp32 row scale is applied to the logit and to the
 //      probability instead;
-//   2. partial S^T[128 keys x 64 heads] = K_d Q_d^T over its 128 dims
-//      (M = keys, N = heads); each 16-head slice of it is stored straight
-//      into the shared memory of the CTA that owns those heads;
-//   3. after a cluster barrier CTA d sums the four partials of heads
-//      16 d .. 16 d + 15 (in rank order, so every run gives the same logits),
+//   2. partial S^T[128 keys x 64 heads] = K_d Q_d^T over its dims (M = keys,
+//      N = heads); each 32-head slice of it is stored straight into the
+//      shared memory of the CTA that owns those heads;
+//   3. after a cluster barrier CTA d sums the partials of heads
+//      32 d .. 32 d + 31 (in rank order, so every run gives the same logits),
 //      takes their max m_c and sum l_c over the chunk, and writes
 //      P = exp(S - m_c) as bf16 hi + lo (P = hi + lo to 2^-17) into the
-//      probability operand of all four CTAs;
-//   4. O_d^T[128 dims x 64 heads] = V_d^T P_hi^T + V_d^T P_lo^T, reading the
-//      same key tile as an MN-major operand (V = K);
+//      probability operand of every CTA of the cluster;
+//   4. [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T, reading the same key tile
+//      as an MN-major operand (V = K; M-tiles of 128 dims, K = 128 keys,
+//      N = 128); the epilogue adds the two halves;
 //   5. the unnormalised partial O_c (this CTA's dims) and (m_c, l_c) go to the
 //      workspace.
 // A second kernel merges the chunks of each row: O = sum_c e^(m_c-M) O_c / L.
-// 256 threads: two per key (64 dims each) for the loads and dequantisation,
+// 512 threads: four per key (64 dims each) for the loads and dequantisation,
 // sixteen per owned head for the softmax, one TMEM lane each in the epilogues.
 #include <cuda_bf16.h>
 
@@ -37,19 +40,27 @@
 
 namespace csa2 {
 
-constexpr int AC_THREADS = 256;
+#ifndef CSA2_ATTN_CLUSTER
+#define CSA2_ATTN_CLUSTER 2
+#endif
 constexpr int AC_KEYS = 128;                       // keys per chunk (MMA M of the first product)
-constexpr int AC_CL = 4;                           // CTAs per cluster, one per 128-dim slice
-constexpr int AC_DIMS = CSA2_HEAD_DIM / AC_CL;     // 128
-constexpr int AC_OWN = CSA2_HEADS / AC_CL;         // heads reduced by each CTA: 16
+constexpr int AC_CL = CSA2_ATTN_CLUSTER;           // CTAs per cluster, one per slice of the dims
+constexpr int AC_DIMS = CSA2_HEAD_DIM / AC_CL;     // dims per CTA
+constexpr int AC_SLABS = AC_DIMS / 64;             // 64-dim slabs per CTA = threads per key
+constexpr int AC_THREADS = AC_KEYS * AC_SLABS;
+constexpr int AC_OWN = CSA2_HEADS / AC_CL;         // heads reduced by each CTA
+constexpr int AC_MT = AC_DIMS / 128;               // M-tiles of the value product
+constexpr uint32_t AC_TMEM_COLS = AC_MT * 128;     // S^T in columns 0-63, then O^T tile mt at 128 mt
 constexpr int AC_MAX_CHUNKS = CSA2_TOPK / AC_KEYS + 1;
-constexpr uint32_t AC_IDESC_S = tc::idesc_f16(128, 64, 1, 1, 0, 0);   // K-major A and B
-constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 64, 1, 1, 1, 0);   // MN-major A (V^T)
+constexpr uint32_t AC_IDESC_S = tc::idesc_f16(128, 64, 1, 1, 0, 0);    // K-major A and B
+constexpr uint32_t AC_IDESC_O = tc::idesc_f16(128, 128, 1, 1, 1, 0);   // MN-major A (V^T), N = hi|lo
+static_assert(AC_CL == 2 || AC_CL == 4, "two or four CTAs per cluster");
+static_assert(AC_THREADS / 16 == AC_OWN, "sixteen threads per owned head");
 
 struct AcSmem {
-    uint8_t k[2 * AC_KEYS * 128];                  // [slab of 64 dims][128 keys][128 B]   32 KB
+    uint8_t k[AC_SLABS * AC_KEYS * 128];           // [slab of 64 dims][128 keys][128 B]
     union {
-        uint8_t q[2 * CSA2_HEADS * 128];           // [slab][64 heads][128 B]              16 KB
+        uint8_t q[AC_SLABS * CSA2_HEADS * 128];    // [slab][64 heads][128 B]
         uint8_t p[2 * 2 * CSA2_HEADS * 128];       // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB
     } u;                                           // P arrives after the first cluster barrier,
                                                    // when this CTA's first product is done with Q
@@ -193,7 +204,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
-__global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
+__global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_CL == 4 ? 2 : 1)
     k_attn_tc(csa2_cache c, csa2_batch bt, const uint16_t *__restrict__ q, float sm_scale,
               const int32_t *__restrict__ idx, int k, csa2_swa swa, float *__restrict__ part_o,
               float *__restrict__ part_ml, int nchunks)
@@ -201,10 +212,9 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     extern __shared__ uint8_t smem_raw[];
     AcSmem &S = *reinterpret_cast<AcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int key = tid & (AC_KEYS - 1), hf = tid >> 7;          // key row; half of this CTA's dims
+    const int key = tid & (AC_KEYS - 1), hf = tid >> 7;          // key row; 64-dim slab of this CTA
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16; // TMEM lane quarter of this warp
-    const uint32_t col_half = 32u * (uint32_t)(warp >> 2);        // TMEM column half of this warp
-    const uint32_t dq = cluster_rank();                           // dims 128 dq .. 128 dq + 127
+    const uint32_t dq = cluster_rank();                           // dims AC_DIMS dq .. + AC_DIMS - 1
     const int chunk = blockIdx.x / AC_CL;
     const int64_t r = blockIdx.y;
     const int b = (int)(r / bt.nq);
@@ -215,20 +225,21 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
         tc::mbar_init(&S.mbar, 1);
         tc::fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(&S.tmem, 128);  // columns 0-63: S^T, 64-127: O^T
-    {                                              // E2M1 pair table
+    if (warp == 0) tc::tmem_alloc(&S.tmem, AC_TMEM_COLS);
+    if (tid < 256) {                               // E2M1 pair table
         const uint32_t lo = tid & 15u, hi = tid >> 4;
         S.e2m1_pair[tid] = pack_bf16x2(e2m1_to_f32(lo), e2m1_to_f32(hi));
     }
 
-    // ---- this CTA's 128 dims of the 64 queries (coalesced 16-byte loads)
+    // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
+    constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
     uint4 qv[4];
     {
         const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM + AC_DIMS * dq);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int e = tid + AC_THREADS * i;
-            qv[i] = __ldg(src + (e >> 4) * (CSA2_HEAD_DIM / 8) + (e & 15));
+            qv[i] = __ldg(src + (e / QCH) * (CSA2_HEAD_DIM / 8) + (e % QCH));
         }
     }
 
@@ -238,11 +249,12 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     uint4 kc[4];
     uint32_t ksc = 0;
     if (!window) {
+        const int64_t vis = visible_entries(bt, r);   // issued alongside the index load
         const int j = chunk * AC_KEYS + key;
         if (j < k) {
             const int32_t p = idx[r * k + j];
             if (p >= 0) {
-                if (p >= visible_entries(bt, r)) {
+                if (p >= vis) {
                     if (hf == 0 && dq == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
                 } else {
                     const int64_t slot = entry_slot(c, b, p);
@@ -251,7 +263,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
                             reinterpret_cast<const uint4 *>(c.kv_codes + slot * 256 + AC_DIMS / 2 * dq) + 2 * hf;
                         kc[0] = __ldg(src);
                         kc[1] = __ldg(src + 1);
-                        ksc = __ldg(reinterpret_cast<const uint16_t *>(c.kv_scales + slot * 16 + 4 * dq) + hf);
+                        ksc = __ldg(reinterpret_cast<const uint16_t *>(c.kv_scales + slot * 16 + AC_DIMS / 32 * dq) +
+                                    hf);
                         valid = true;
                     }
                 }
@@ -278,8 +291,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     // ---- the queries' slice arrives while the key lookups run
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const int e = tid + AC_THREADS * i;        // head e / 16, 16-byte chunk e % 16
-        *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e >> 4, 8 * (e & 15), CSA2_HEADS)) = qv[i];
+        const int e = tid + AC_THREADS * i;
+        *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
     }
     if (hf == 0) {
         S.kscale[key] = kscale;
@@ -301,11 +314,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     tc::tc_fence_after();
     const uint32_t tmem = S.tmem;
 
-    // ---- partial S^T = K_d Q_d^T over this CTA's 128 dims
+    // ---- partial S^T = K_d Q_d^T over this CTA's dims
     if (tid == 0) {
         const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.u.q);
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) {           // 16 dims per step
+        for (int kk = 0; kk < AC_DIMS / 16; kk++) {   // 16 dims per step
             const uint32_t off = (uint32_t)(kk >> 2) * (AC_KEYS * 128) + (uint32_t)(kk & 3) * 32u;
             const uint32_t offq = (uint32_t)(kk >> 2) * (CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
             tc::mma_f16(tmem, tc::smem_desc(k0 + off, 16, 1024, tc::kSwizzle128B),
@@ -314,28 +327,32 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
         tc::mma_commit(&S.mbar);
     }
     // A CTA whose product timed out still passes both cluster barriers (the
-    // other three wait there) but writes no output; the status word says why.
+    // others wait there) but writes no output; the status word says why.
     const bool fail = __syncthreads_or(!tc::mbar_wait(&S.mbar, 0));
     tc::tc_fence_after();
     if (!fail) {
-        // heads col_half .. +15 belong to CTA col_half / 16, the next 16 to the one after
-        uint32_t acc[32];
-        tc::tmem_ld32(tmem + lane_base + col_half, acc);
+        // this warp: keys of its lane quarter, heads col .. col + 64 / AC_SLABS - 1,
+        // each group of 16 heads stored into the shared memory of its owner
+        constexpr int NG = 4 / AC_SLABS;           // groups of 16 heads per warp
+        const uint32_t col = 64u / AC_SLABS * (uint32_t)(warp >> 2);
+        uint32_t acc[NG][16];
+#pragma unroll
+        for (int g = 0; g < NG; g++) tmem_ld16(tmem + lane_base + col + 16u * g, acc[g]);
         tc::tmem_ld_wait();
         const int kr = (warp & 3) * 32 + lane;
-        const uint32_t la = tc::smem_u32(&S.ps[dq][0][kr]);
-        const uint32_t ra0 = cluster_map(la, col_half / AC_OWN), ra1 = cluster_map(la, col_half / AC_OWN + 1);
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            st_cluster_f32(ra0 + (uint32_t)j * (AC_KEYS * 4), acc[j]);
-            st_cluster_f32(ra1 + (uint32_t)j * (AC_KEYS * 4), acc[16 + j]);
+        for (int g = 0; g < NG; g++) {
+            const uint32_t h0 = col + 16u * g;
+            const uint32_t ra = cluster_map(tc::smem_u32(&S.ps[dq][h0 % AC_OWN][kr]), h0 / AC_OWN);
+#pragma unroll
+            for (int j = 0; j < 16; j++) st_cluster_f32(ra + (uint32_t)j * (AC_KEYS * 4), acc[g][j]);
         }
     } else if (tid == 0) {
         flag(c.status, CSA2_DEV_TIMEOUT);
     }
-    cluster_sync();                                // the four partials of the owned heads are here
+    cluster_sync();                                // the partials of the owned heads are here
 
-    // ---- owned heads 16 dq .. 16 dq + 15: sixteen threads per head, eight
+    // ---- owned heads AC_OWN dq .. : sixteen threads per head, eight
     //      consecutive keys per thread
     {
         const int hl = tid >> 4, h = AC_OWN * (int)dq + hl, part = tid & 15;
@@ -402,17 +419,21 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     tc::tc_fence_after();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // let the merge kernel be scheduled
 
-    // ---- O_d^T = V_d^T P_hi^T + V_d^T P_lo^T: M = 128 dims, K = 128 keys, N = 64 heads
+    // ---- [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T: M-tiles of 128 dims, K = 128 keys,
+    //      N = 128; tile mt in columns 128 mt .. +127 (S has been read out)
     if (tid == 0 && !fail) {
         tc::fence_proxy_async_smem();
         const uint32_t k0 = tc::smem_u32(S.k), p0 = tc::smem_u32(S.u.p);
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) {           // 16 keys per step
-            const uint64_t ad = tc::smem_desc(k0 + (uint32_t)kk * 2048u, AC_KEYS * 128, 1024, tc::kSwizzle128B);
-            const uint32_t boff = (uint32_t)(kk >> 2) * (2 * CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
-            tc::mma_f16(tmem + 64u, ad, tc::smem_desc(p0 + boff, 16, 1024, tc::kSwizzle128B), AC_IDESC_O, kk > 0);
-            tc::mma_f16(tmem + 64u, ad, tc::smem_desc(p0 + boff + CSA2_HEADS * 128, 16, 1024, tc::kSwizzle128B),
-                        AC_IDESC_O, 1);
+        for (int mt = 0; mt < AC_MT; mt++) {
+#pragma unroll
+            for (int kk = 0; kk < 8; kk++) {       // 16 keys per step
+                const uint64_t ad = tc::smem_desc(k0 + (uint32_t)(2 * mt) * (AC_KEYS * 128) + (uint32_t)kk * 2048u,
+                                                  AC_KEYS * 128, 1024, tc::kSwizzle128B);
+                const uint32_t boff = (uint32_t)(kk >> 2) * (2 * CSA2_HEADS * 128) + (uint32_t)(kk & 3) * 32u;
+                tc::mma_f16(tmem + 128u * (uint32_t)mt, ad, tc::smem_desc(p0 + boff, 16, 1024, tc::kSwizzle128B),
+                            AC_IDESC_O, kk > 0);
+            }
         }
         tc::mma_commit(&S.mbar);
     }
@@ -420,13 +441,17 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
         const bool fail2 = __syncthreads_or(!tc::mbar_wait(&S.mbar, 1));
         tc::tc_fence_after();
         if (!fail2) {
-            // ---- partial output: lane = dim of this CTA's slice, 32 heads per warp
-            uint32_t acc[32];
-            tc::tmem_ld32(tmem + lane_base + 64u + col_half, acc);
+            // ---- partial output: M-tile mt, 32 heads per warp, lane = dim; hi + lo
+            const int u = warp >> 2, mt = u >> 1, hh = u & 1;
+            uint32_t ahi[32], alo[32];
+            const uint32_t colo = 128u * (uint32_t)mt + 32u * (uint32_t)hh;
+            tc::tmem_ld32(tmem + lane_base + colo, ahi);
+            tc::tmem_ld32(tmem + lane_base + colo + 64u, alo);
             tc::tmem_ld_wait();
-            float *po = part_o + base * CSA2_HEAD_DIM + AC_DIMS * dq + (warp & 3) * 32 + lane;
+            float *po = part_o + (base + 32 * hh) * CSA2_HEAD_DIM + AC_DIMS * dq + 128 * mt + (warp & 3) * 32 + lane;
 #pragma unroll
-            for (int j = 0; j < 32; j++) po[(int64_t)(col_half + j) * CSA2_HEAD_DIM] = __uint_as_float(acc[j]);
+            for (int j = 0; j < 32; j++)
+                po[(int64_t)j * CSA2_HEAD_DIM] = __uint_as_float(ahi[j]) + __uint_as_float(alo[j]);
         } else if (tid == 0) {
             flag(c.status, CSA2_DEV_TIMEOUT);
         }
@@ -434,7 +459,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 2)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 0) tc::tmem_dealloc(tmem, 128);
+    if (warp == 0) tc::tmem_dealloc(tmem, AC_TMEM_COLS);
 }
 
 // o = sum_c e^(m_c - M) O_c / sum_c e^(m_c - M) l_c, lse = M + log L; one CTA per
