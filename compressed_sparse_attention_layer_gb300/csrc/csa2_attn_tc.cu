@@ -65,9 +65,9 @@ struct AcSmem {
     } u;                                           // P arrives after the first cluster barrier,
                                                    // when this CTA's first product is done with Q
     float ps[AC_CL][AC_OWN][AC_KEYS];              // [source CTA][owned head][key] partial logits 32 KB
-    uint32_t e2m1_pair[256];                       // byte -> bf16x2 of its two E2M1 codes
-    float kscale[AC_KEYS];
-    int valid[AC_KEYS];
+    uint32_t e2m1_pair[256][32];                   // byte -> bf16x2 of its two E2M1 codes, one
+                                                   // copy per lane (bank = lane: no conflicts)  32 KB
+    float kscale[AC_KEYS];                         // window row scale (1 for entries), -1: no key
     uint64_t mbar;
     uint32_t tmem;
 };
@@ -112,12 +112,6 @@ __device__ __forceinline__ void fence_proxy_async_cluster()
     asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-
 // a (bf16x2) * b (bf16x2), exact when the products are representable.
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
 {
@@ -133,12 +127,12 @@ __device__ __forceinline__ uint32_t pow2_bf16x2(int X)
     return h | (h << 16);
 }
 
-// Half `hf` (local dims 64 hf .. 64 hf + 63, two MX blocks) of this CTA's
+// Slab `hf` (local dims 64 hf .. 64 hf + 63, two MX blocks) of this CTA's
 // slice of an MXFP4 entry -> bf16 row of the key tile (exact): the table gives
-// the two E2M1 magnitudes of a byte with their signs, one bf16x2 multiply
-// applies the block's 2^X.
+// the two E2M1 values of a byte with their signs (this lane's copy), one
+// bf16x2 multiply applies the block's 2^X.
 __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[4], uint32_t sc,
-                                               int hf, const uint32_t *pair)
+                                               int hf, const uint32_t (*pair)[32], uint32_t lane)
 {
 #pragma unroll
     for (int blk = 0; blk < 2; blk++) {            // 16 bytes = 32 elements = one MX block
@@ -147,13 +141,24 @@ __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, con
 #pragma unroll
         for (int j = 0; j < 4; j++) {              // 4 bytes = 8 elements -> one 16-byte chunk
             uint4 o;
-            o.x = bf16x2_mul(pair[w[j] & 0xFFu], f);
-            o.y = bf16x2_mul(pair[(w[j] >> 8) & 0xFFu], f);
-            o.z = bf16x2_mul(pair[(w[j] >> 16) & 0xFFu], f);
-            o.w = bf16x2_mul(pair[w[j] >> 24], f);
+            o.x = bf16x2_mul(pair[w[j] & 0xFFu][lane], f);
+            o.y = bf16x2_mul(pair[(w[j] >> 8) & 0xFFu][lane], f);
+            o.z = bf16x2_mul(pair[(w[j] >> 16) & 0xFFu][lane], f);
+            o.w = bf16x2_mul(pair[w[j] >> 24][lane], f);
             *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 32 * blk + 8 * j, AC_KEYS)) = o;
         }
     }
+}
+
+// The two E2M1 codes of a byte (low nibble first) -> bf16x2 of their values:
+// sign to bit 15, the three exponent/mantissa bits to bits 6-8 give the value
+// times 2^-126 (0.5 as a bf16 subnormal), which one exact multiply by 2^126
+// restores.
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t byte)
+{
+    const uint32_t lo = byte & 15u, hi = (byte >> 4) & 15u;
+    const uint32_t bits = ((lo & 7u) << 6) | ((lo & 8u) << 12) | ((hi & 7u) << 22) | ((hi & 8u) << 28);
+    return bf16x2_mul(bits, 0x7E807E80u);          // 2^126 in both halves
 }
 
 // Two e4m3 codes (low bytes of the halves of v) -> bf16x2 of their values:
@@ -226,9 +231,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         tc::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&S.tmem, AC_TMEM_COLS);
-    if (tid < 256) {                               // E2M1 pair table
-        const uint32_t lo = tid & 15u, hi = tid >> 4;
-        S.e2m1_pair[tid] = pack_bf16x2(e2m1_to_f32(lo), e2m1_to_f32(hi));
+    // E2M1 pair table: 2048 16-byte chunks of four copies each, consecutive per lane
+#pragma unroll
+    for (int ch = tid; ch < 256 * 32 / 4; ch += AC_THREADS) {
+        const uint32_t v = e2m1x2_to_bf16x2((uint32_t)ch >> 3);
+        reinterpret_cast<uint4 *>(&S.e2m1_pair[0][0])[ch] = make_uint4(v, v, v, v);
     }
 
     // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
@@ -295,15 +302,14 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
     }
     if (hf == 0) {
-        S.kscale[key] = kscale;
-        S.valid[key] = valid;
+        S.kscale[key] = valid ? kscale : -1.0f;
     }
     __syncthreads();                               // the pair table is ready
 
     // ---- dequantise into row `key` of the key tile
     if (valid) {
         if (window) store_window_key(S.k, key, kc, hf);
-        else store_main_key(S.k, key, kc, ksc, hf, S.e2m1_pair);
+        else store_main_key(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
     } else {
         zero_key(S.k, key, hf);
     }
@@ -362,6 +368,9 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
             v[src][0] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part]);
             v[src][1] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part + 4]);
         }
+        float ks[8];                               // scales of keys 8 part .. +7 (-1: none)
+        *reinterpret_cast<float4 *>(ks) = *reinterpret_cast<const float4 *>(&S.kscale[8 * part]);
+        *reinterpret_cast<float4 *>(ks + 4) = *reinterpret_cast<const float4 *>(&S.kscale[8 * part + 4]);
         float lg[8];
         float mx = -INFINITY;
 #pragma unroll
@@ -372,8 +381,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
                 const float4 &w = v[src][j >> 2];
                 sum += (j & 3) == 0 ? w.x : (j & 3) == 1 ? w.y : (j & 3) == 2 ? w.z : w.w;
             }
-            const int kj = 8 * part + j;
-            lg[j] = S.valid[kj] ? sum * (sm_scale * S.kscale[kj]) : -INFINITY;
+            lg[j] = ks[j] >= 0.0f ? sum * (sm_scale * ks[j]) : -INFINITY;
             mx = fmaxf(mx, lg[j]);
         }
 #pragma unroll
@@ -389,7 +397,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         uint32_t hi2[4], lo2[4];
 #pragma unroll
         for (int j = 0; j < 8; j += 2) {
-            const float p0 = e[j] * S.kscale[8 * part + j], p1 = e[j + 1] * S.kscale[8 * part + j + 1];
+            const float p0 = e[j] * fmaxf(ks[j], 0.0f), p1 = e[j + 1] * fmaxf(ks[j + 1], 0.0f);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
             const float2 hf2 = __bfloat1622float2(hi);
             const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf2.x, p1 - hf2.y);
