@@ -1,10 +1,9 @@
 """Whole layers through csa2_layer against the oracle (needs a GPU).
 
-Rules (from the task's correctness bar): Reuse propagation bit-exact; Top-K
+Parity bar: Reuse propagation bit-exact; Top-K
 valid (every selected index scores >= the oracle's k-th score - 1e-3|score|)
-with >= 99.5% overlap; attention within max-abs 2e-3 / rel-L2 1e-3 given the
-same indices (checked whenever the GPU and oracle sets agree, which the
-planted workloads make the common case).
+with >= 99.5% overlap; attention within max-abs 2e-3 / rel-L2 1e-3 against the
+oracle's attention over the indices the layer selected, in every layer.
 """
 import numpy as np
 import pytest
@@ -18,7 +17,7 @@ from tests.reference import SeqOracle, attn_close, topk_valid
 pytestmark = pytest.mark.gpu
 
 
-def _check_sequence(dw, b, i=0, check_attn_when_equal=True):
+def _check_sequence(dw, b, i=0):
     wl = dw.wl
     so = SeqOracle(wl, b)
     r = b * wl.nq + i
@@ -41,11 +40,11 @@ def _check_sequence(dw, b, i=0, check_attn_when_equal=True):
             assert ok, (l, mode, info)
         else:
             assert np.array_equal(got_idx, dw.hist_idx[l - 1][r]), (l, "reuse must copy bit-exactly")
-        sel = got_idx if check_attn_when_equal else idx_ref
-        if np.array_equal(np.sort(got_idx), np.sort(idx_ref)):
-            o_ref, lse_ref = so.attention(l, i, idx_ref)
-            ok, info = attn_close(dw.o[l][r].cpu().numpy(), dw.lse[l][r].cpu().numpy(), o_ref, lse_ref)
-            assert ok, (l, mode, info)
+        # attention given the indices the layer actually selected (the oracle's
+        # attention over the GPU's set; the set itself was checked above)
+        o_ref, lse_ref = so.attention(l, i, got_idx)
+        ok, info = attn_close(dw.o[l][r].cpu().numpy(), dw.lse[l][r].cpu().numpy(), o_ref, lse_ref)
+        assert ok, (l, mode, info)
 
 
 def _run_recording(dw):
@@ -99,3 +98,50 @@ def test_layer_decode_group_full_size():
         _check_sequence(dw, b)
     for b in range(wl.batch):
         assert np.isin(wl.planted_positions(b), dw.hist_idx[0][b]).all()
+
+
+def test_layer_prefill_sampled_rows():
+    """Prefill at full size: 65,536-token prefix + 8,192 new tokens, m = 2
+    (36,864 entries), 8,192 causal query rows, Full + 5 Reuse.  Rows with
+    different visible counts (even and odd positions, first and last) are
+    checked end to end against the oracle."""
+    wl = W.prefill()
+    dw = DeviceWorkload(wl)
+    _run_recording(dw)
+    for i in (0, 1, 2047, 8191):
+        _check_sequence(dw, 0, i)
+    del dw
+    torch.cuda.empty_cache()
+
+
+def test_layer_decode_ragged_sampled():
+    """128 sequences with log-uniform lengths in [4,096, 1,048,576], the 20-layer
+    decoder pattern; the shortest, the median and the longest sequence checked
+    end to end."""
+    wl = W.decode_ragged()
+    dw = DeviceWorkload(wl)
+    _run_recording(dw)
+    lens = np.array([wl.entries(b) for b in range(wl.batch)])
+    order = np.argsort(lens, kind="stable")
+    for b in (int(order[0]), int(order[len(order) // 2]), int(order[-1])):
+        _check_sequence(dw, b)
+    del dw
+    torch.cuda.empty_cache()
+
+
+def test_layer_decode_1m_sampled():
+    """The benchmark's workload at full size (8 x 1,048,576 tokens, 64 planted
+    blocks each, 20 layers), through the same csa2_layer calls; sequences 0 and
+    7 checked end to end, and on all 8 the planted positions are in the Full
+    layer's candidate pool (the stack's only Full layer is layer 0)."""
+    wl = W.decode_1m()
+    dw = DeviceWorkload(wl)
+    _run_recording(dw)
+    for b in (0, 7):
+        _check_sequence(dw, b)
+    pool = dw.pool.cpu().numpy()
+    pool_len = dw.pool_len.cpu().numpy()
+    for b in range(wl.batch):
+        assert np.isin(wl.planted_positions(b), pool[b][: pool_len[b]]).all()
+    del dw
+    torch.cuda.empty_cache()
