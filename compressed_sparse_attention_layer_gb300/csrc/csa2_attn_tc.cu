@@ -199,16 +199,6 @@ __device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int hf)
         *reinterpret_cast<uint4 *>(ktile + tc::sw128_offset(row, 64 * hf + 8 * i, AC_KEYS)) = make_uint4(0, 0, 0, 0);
 }
 
-// 16 consecutive 32-bit TMEM columns of this warp's lane quarter.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-
 __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_CL == 4 ? 2 : 1)
     k_attn_tc(csa2_cache c, csa2_batch bt, const uint16_t *__restrict__ q, float sm_scale,
               const int32_t *__restrict__ idx, int k, csa2_swa swa, float *__restrict__ part_o,
@@ -343,7 +333,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const uint32_t col = 64u / AC_SLABS * (uint32_t)(warp >> 2);
         uint32_t acc[NG][16];
 #pragma unroll
-        for (int g = 0; g < NG; g++) tmem_ld16(tmem + lane_base + col + 16u * g, acc[g]);
+        for (int g = 0; g < NG; g++) tc::tmem_ld16(tmem + lane_base + col + 16u * g, acc[g]);
         tc::tmem_ld_wait();
         const int kr = (warp & 3) * 32 + lane;
 #pragma unroll

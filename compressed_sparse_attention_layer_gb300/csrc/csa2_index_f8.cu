@@ -1,27 +1,34 @@
-// a4: the Full layer's lightning-indexer scan, TMA-fed e4m3 keys on the
-// kind::f8f6f4 tensor cores.
+// a4: the Full layer's lightning-indexer scan, e4m3 keys streamed into shared
+// memory by cp.async and multiplied on the kind::f8f6f4 tensor cores.
 //
 // score(p) = s_p * sum_h w_h ReLU(qi_h . code_p) and the maximum of each
 // aligned block of 8 positions ("DeepSeek-V4 report explainer" §3.2;
 // "DeepSeek-V4.1-Flash" research note §3.2; "DeepSeek-V4.1-Flash 架构详解"
 // §3.2).
 //
-// The keys stay e4m3 end to end: TMA copies each 64-entry page of codes
-// (8 KB) into a 128-byte-swizzled shared-memory tile, which is directly the
-// K-major A operand (M = 128 entries, K = 128 codes).  The indexer query is
+// The keys stay e4m3 end to end: the 16-byte chunks of each 64-entry page of
+// codes (8 KB) are copied by cp.async into a 128-byte-swizzled shared-memory
+// tile, which is directly the K-major A operand (M = 128 entries, K = 128
+// codes).  cp.async rather than the tensor-map TMA: on this gather of random
+// 8 KB pages the TMA stream saturates near 5.3 TB/s while the load-store
+// path sustains above 6 TB/s with fewer bytes in flight.  The indexer query is
 // the B operand split into two e4m3 parts per head, hi = e4m3(q'), lo =
-// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  Per K step two
-// N = 32 products (A x hi, then A x lo) accumulate into the same fp32
-// D[128 entries x 32 heads] in tensor memory; the epilogue applies ReLU,
-// w_h * 2^e_h and the entry's scale.
+// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  hi and lo are
+// stacked as one N = 64 operand (rows 0-31 hi, 32-63 lo), so each K step is
+// one MMA that reads the key tile once; the fp32 D[128 entries x 64] in
+// tensor memory holds A.hi in columns 0-31 and A.lo in 32-63, and the
+// epilogue adds them, applies ReLU, w_h * 2^e_h and the entry's scale.
 //
-// Warp roles (192 threads): warp 0 issues TMA into a 12-stage ring, warp 1
-// writes the query operand of each row and issues the MMAs (one thread),
-// warps 2-5 drain four tensor-memory accumulators.  A persistent grid walks
-// one global list of (row, tile) items so ragged batches stay balanced.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
+// Warp roles (320 threads): warps 0-3 copy key tiles into a 12-stage ring
+// (eight 16-byte chunks per thread per tile), warp 0 also the entries' fp32
+// scales into the same stage, so that no role waits on a dependent global
+// load per tile; warps 4-7 drain eight tensor-memory accumulators (TMEM lane
+// quarter = warp % 4) and free a stage once they have read its scales (its
+// MMAs are complete by then); warp 8 writes the query operand of each row,
+// and lane 0 of warps 8 and 9 issue the MMAs of the even and odd tiles (two
+// issuing threads: one alone, waiting on barriers between tiles, leaves the
+// tensor pipe idle half the time).  A persistent grid walks one
+// global list of (row, tile) items so ragged batches stay balanced.
 #include <algorithm>
 #include <mutex>
 
@@ -31,15 +38,18 @@
 namespace csa2 {
 
 constexpr int F8_STAGES = 12;
-constexpr int F8_ACC = 8;                  // tensor-memory accumulators of 32 columns
-constexpr int F8_THREADS = 192;
+constexpr int F8_ACC = 8;                  // tensor-memory accumulators of 64 columns (hi | lo)
+constexpr int F8_THREADS = 320;
+constexpr int F8_PROD = 128;               // producer threads (warps 0-3)
+constexpr int F8_MMA_WARP = 8;
 constexpr int F8_TILE = 128;
 constexpr int F8_PERSIST_ROWS = 256;
-constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 32);
+constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 64);
 
 struct F8Smem {
-    uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (TMA)
+    uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (cp.async)
     uint8_t b[2][64 * 128];                // query hi (rows 0-31) and lo (rows 32-63), per segment parity
+    float sc[F8_STAGES][F8_TILE];          // fp32 scales of the stage's entries (cp.async)
     float wq[2][32];                       // w_h * 2^e_h, per segment parity
     uint64_t full[F8_STAGES], empty[F8_STAGES], tfull[F8_ACC], tempty[F8_ACC];
     uint64_t bfree[2], wready[2], wfree[2];
@@ -47,6 +57,31 @@ struct F8Smem {
     int abort;
     int32_t prefix[F8_PERSIST_ROWS + 1];
 };
+
+// Scales copied for the entries of a page whose id lies outside the cache:
+// they score -inf.
+__device__ __align__(16) float g_neg_inf_scales[64] = {
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
+    -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
+
+// 16-byte global -> shared copy through the load-store path (L1 bypassed).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
 
 // e_h with max|q_h| * 2^-e_h in [128, 256).
 __device__ __forceinline__ int head_exponent(float amax)
@@ -117,8 +152,8 @@ __device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const
 }
 
 template <bool PERSIST>
-__global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constant__ CUtensorMap tmap, csa2_cache c,
-                                                            csa2_batch bt, const uint16_t *__restrict__ qi,
+__global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_batch bt,
+                                                            const uint16_t *__restrict__ qi,
                                                             const float *__restrict__ w, float *__restrict__ scores,
                                                             float *__restrict__ block_max,
                                                             int32_t *__restrict__ n_visible, int64_t ld)
@@ -130,22 +165,22 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
 
     if (tid == 0) {
         for (int i = 0; i < F8_STAGES; i++) {
-            tc::mbar_init(&S.full[i], 1);
-            tc::mbar_init(&S.empty[i], 1);
+            tc::mbar_init(&S.full[i], F8_PROD);
+            tc::mbar_init(&S.empty[i], 4);           // the epilogue warps, after the tile's MMAs and scale reads
         }
         for (int i = 0; i < F8_ACC; i++) {
             tc::mbar_init(&S.tfull[i], 1);
             tc::mbar_init(&S.tempty[i], 4);
         }
         for (int i = 0; i < 2; i++) {
-            tc::mbar_init(&S.bfree[i], 1);
+            tc::mbar_init(&S.bfree[i], 2);           // both MMA issuers
             tc::mbar_init(&S.wready[i], 32);
             tc::mbar_init(&S.wfree[i], 4);
         }
         S.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 1) tc::tmem_alloc(&S.tmem, F8_ACC * 32);
+    if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_ACC * 64);
 
     int64_t g0, g1;
     if (PERSIST) {
@@ -181,9 +216,6 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
     int r = PERSIST ? 0 : (int)blockIdx.y;
     int64_t g = g0, it = 0;
     int seg = 0;
-    int last_full_k[F8_STAGES];
-#pragma unroll
-    for (int i = 0; i < F8_STAGES; i++) last_full_k[i] = -1;
     int64_t last_tile = -1;
 
     while (g < g1 && !*abort) {
@@ -199,77 +231,91 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
         const int b = r / bt.nq;
         const int64_t nvis = visible_entries(bt, r);
 
-        if (warp == 0) {
-            // ---------------- TMA producer: page ids of 32 tiles at a time, one lane per tile
+        if (warp < 4) {
+            // ---------------- producers: page ids of 32 tiles at a time (one lane per
+            // tile), then per tile eight 16-byte chunks of codes per thread (thread t:
+            // chunk t % 8 of rows t / 8 + 16 j); warp 0 also the tile's 128 scales
+            const uint32_t a0 = tc::smem_u32(S.a[0]);
+            const int pt = warp * 32 + lane;
             int32_t my_pg[2] = {-1, -1};
             for (int64_t i = 0; i < nt; i++) {
                 if ((i & 31) == 0) {
-                    const int64_t pt = (j0 + i + lane) * F8_TILE;     // tile i + lane
+                    const int64_t e = (j0 + i + lane) * F8_TILE;     // tile i + lane
 #pragma unroll
                     for (int h = 0; h < 2; h++) {
-                        const int64_t e0 = pt + 64 * h;
+                        const int64_t e0 = e + 64 * h;
                         my_pg[h] = -2;                                // -2: beyond the visible entries
-                        if (i + lane < nt && e0 < nvis)
-                            my_pg[h] = __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
+                        if (i + lane < nt && e0 < nvis) {
+                            const int32_t pg = __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
+                            my_pg[h] = pg >= 0 && ((int64_t)pg + 1) * CSA2_PAGE <= c.num_slots ? pg : -1;
+                        }
                     }
                 }
-                const int32_t pg0 = __shfl_sync(0xffffffffu, my_pg[0], (int)(i & 31));
-                const int32_t pg1 = __shfl_sync(0xffffffffu, my_pg[1], (int)(i & 31));
-                if (lane == 0) {
-                    const int64_t ti = it + i;
-                    const int stage = (int)(ti % F8_STAGES);
-                    const int k = (int)(ti / F8_STAGES);
-                    bool ok = true;
-                    if (k > 0 && !tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort)) {
+                const int32_t pgs[2] = {__shfl_sync(0xffffffffu, my_pg[0], (int)(i & 31)),
+                                        __shfl_sync(0xffffffffu, my_pg[1], (int)(i & 31))};
+                const int64_t ti = it + i;
+                const int stage = (int)(ti % F8_STAGES);
+                const int k = (int)(ti / F8_STAGES);
+                const bool ok = k == 0 || tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) {
                         *abort = 1;
                         flag(c.status, CSA2_DEV_TIMEOUT);
-                        ok = false;
                     }
-                    if (ok) {
-                        const int32_t pgs[2] = {pg0, pg1};
-                        uint32_t bytes = 0;
-#pragma unroll
-                        for (int h = 0; h < 2; h++) {
-                            if (pgs[h] == -2) continue;
-                            if (pgs[h] >= 0 && ((int64_t)pgs[h] + 1) * CSA2_PAGE <= c.num_slots) bytes += 64 * 128;
-                            else flag(c.status, CSA2_DEV_BAD_PAGE);
-                        }
-                        tc::mbar_arrive_expect_tx(&S.full[stage], bytes);
-#pragma unroll
-                        for (int h = 0; h < 2; h++)
-                            if (pgs[h] >= 0 && ((int64_t)pgs[h] + 1) * CSA2_PAGE <= c.num_slots)
-                                tc::tma_load_2d(S.a[stage] + h * 64 * 128, &tmap, 0, pgs[h] * CSA2_PAGE,
-                                                &S.full[stage]);
-                        last_full_k[stage] = k;
-                    }
+                    break;
                 }
-                if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+                const uint32_t dst = a0 + (uint32_t)stage * (F8_TILE * 128);
+#pragma unroll
+                for (int jj = 0; jj < 8; jj++) {
+                    const int e = pt + F8_PROD * jj;                  // 16-byte chunk of the tile
+                    const int row = e >> 3, ch = e & 7, h = jj >> 2;  // rows 0-63: page 0, 64-127: page 1
+                    if (pgs[h] >= 0)
+                        cp_async16(dst + (uint32_t)row * 128u + ((uint32_t)(ch ^ (row & 7)) << 4),
+                                   c.ik_codes + ((int64_t)pgs[h] * CSA2_PAGE + (row & 63)) * 128 + ch * 16);
+                }
+                if (warp == 0) {
+                    const int h = lane >> 4;                          // entries 4 lane .. 4 lane + 3
+                    const float *src = pgs[h] >= 0 ? c.ik_scales + (int64_t)pgs[h] * CSA2_PAGE + 4 * (lane & 15)
+                                                   : g_neg_inf_scales + 4 * (lane & 15);
+                    if (pgs[h] != -2) cp_async16(tc::smem_u32(&S.sc[stage][4 * lane]), src);
+                    if (pgs[h] == -1 && (lane & 15) == 0) flag(c.status, CSA2_DEV_BAD_PAGE);
+                }
+                cp_async_arrive(&S.full[stage]);
             }
-        } else if (warp == 1) {
-            // ---------------- query operand + MMA issue
-            // the operand and weights of segment seg-2 must be done with: its MMAs
-            // completed (bfree) and the epilogue finished its tiles (wfree)
+        } else if (warp >= F8_MMA_WARP) {
+            // ---------------- query operand (warp 8) + MMA issue: lane 0 of warp 8 takes the
+            // even tiles, lane 0 of warp 9 the odd ones (one issuing thread cannot keep
+            // the tensor pipe busy while it also waits on barriers)
+            const int is = warp - F8_MMA_WARP;
             bool ok = true;
-            if (seg >= 2 && lane == 0) {
-                const uint32_t par = (uint32_t)(((seg >> 1) - 1) & 1);
-                ok = tc::mbar_wait_or_abort(&S.bfree[seg & 1], par, abort) &&
-                     tc::mbar_wait_or_abort(&S.wfree[seg & 1], par, abort);
+            if (is == 0) {
+                // the operand and weights of segment seg-2 must be done with: its MMAs
+                // completed (bfree, both issuers) and the epilogue finished its tiles (wfree)
+                if (seg >= 2 && lane == 0) {
+                    const uint32_t par = (uint32_t)(((seg >> 1) - 1) & 1);
+                    ok = tc::mbar_wait_or_abort(&S.bfree[seg & 1], par, abort) &&
+                         tc::mbar_wait_or_abort(&S.wfree[seg & 1], par, abort);
+                }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (ok) {
+                    write_query_operand(S.b[seg & 1], S.wq[seg & 1], qi + (int64_t)r * 4096, w + (int64_t)r * 32);
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(&S.wready[seg & 1]);
+                }
+            } else if (lane == 0) {
+                ok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) {
                 if (lane == 0) {
                     *abort = 1;
                     flag(c.status, CSA2_DEV_TIMEOUT);
                 }
             } else {
-                write_query_operand(S.b[seg & 1], S.wq[seg & 1], qi + (int64_t)r * 4096, w + (int64_t)r * 32);
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&S.wready[seg & 1]);
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t a0 = tc::smem_u32(S.a[0]);
                     const uint32_t b0 = tc::smem_u32(S.b[seg & 1]);
-                    for (int64_t i = 0; i < nt; i++) {
+                    for (int64_t i = (is - it) & 1; i < nt; i += 2) {   // tiles ti = it + i with ti % 2 == is
                         const int64_t ti = it + i;
                         const int stage = (int)(ti % F8_STAGES);
                         const int acc = (int)(ti % F8_ACC);
@@ -280,18 +326,18 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                             flag(c.status, CSA2_DEV_TIMEOUT);
                             break;
                         }
+                        // the producers' cp.async writes, acquired through the barrier, made
+                        // visible to the tensor core's (async-proxy) operand reads
+                        tc::fence_proxy_async_smem();
                         tc::tc_fence_after();
                         const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++) {     // K = 128 codes in steps of 32
-                            const uint64_t ad = tc::smem_desc(as + kk * 32, 16, 1024, tc::kSwizzle128B);
-                            tc::mma_f8(tmem + (uint32_t)acc * 32u, ad,
+                        for (int kk = 0; kk < 4; kk++)       // K = 128 codes in steps of 32; N = hi | lo
+                            tc::mma_f8(tmem + (uint32_t)acc * 64u,
+                                       tc::smem_desc(as + kk * 32, 16, 1024, tc::kSwizzle128B),
                                        tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC, kk > 0);
-                            tc::mma_f8(tmem + (uint32_t)acc * 32u, ad,
-                                       tc::smem_desc(b0 + 32 * 128 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC,
-                                       1);
-                        }
-                        tc::mma_commit(&S.empty[stage]);
+                        // the stage is released by the epilogue, which reads its scales only
+                        // after this commit: the MMAs are done with the codes by then
                         tc::mma_commit(&S.tfull[acc]);
                         last_tile = ti;
                     }
@@ -300,7 +346,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                 __syncwarp();
             }
         } else {
-            // ---------------- epilogue: warps 2-5, TMEM lanes by warp % 4
+            // ---------------- epilogue: warps 4-7, TMEM lanes by warp % 4
             const int qd = warp & 3;
             const bool wok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
             if (!__all_sync(0xffffffffu, wok)) {
@@ -310,32 +356,17 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                 }
                 break;
             }
-            float wv[32];
-#pragma unroll
-            for (int h = 0; h < 32; h++) wv[h] = S.wq[seg & 1][h];
-            // the scale of this lane's entry, two tiles ahead: page id for tile i+2,
-            // scale for tile i+1, use for tile i
+            const float *wv = S.wq[seg & 1];              // broadcast shared-memory reads
             const int64_t rowp = (int64_t)qd * 32 + lane;
-            auto page_of = [&](int64_t i) -> int32_t {
-                const int64_t p = (j0 + i) * F8_TILE + rowp;
-                if (i >= nt || p >= nvis) return -2;
-                return __ldg(c.block_table + (int64_t)b * c.max_pages + (p >> 6));
-            };
-            auto scale_of = [&](int64_t i, int32_t pg) -> float {
-                const int64_t p = (j0 + i) * F8_TILE + rowp;
-                if (pg == -2) return 0.0f;
-                const int64_t slot = (int64_t)pg * CSA2_PAGE + (p & 63);
-                if (pg < 0 || slot >= c.num_slots) return -INFINITY;            // bad page: score -inf
-                return __ldg(c.ik_scales + slot);
-            };
-            int32_t pg_next = page_of(1);
-            float sc_cur = scale_of(0, page_of(0));
             for (int64_t i = 0; i < nt; i++) {
-                const int32_t pg_next2 = page_of(i + 2);
-                const float sc_next = scale_of(i + 1, pg_next);
                 const int64_t ti = it + i;
                 const int acc = (int)(ti % F8_ACC);
-                bool ok = tc::mbar_wait_or_abort(&S.tfull[acc], (uint32_t)((ti / F8_ACC) & 1), abort);
+                const int stage = (int)(ti % F8_STAGES);
+                // the MMAs of tile ti are done, so its stage's data has landed: the wait on
+                // full[stage] returns at once and acquires the producers' scale copies (the
+                // stage cannot refill before this warp's arrival on empty[stage] below)
+                bool ok = tc::mbar_wait_or_abort(&S.tfull[acc], (uint32_t)((ti / F8_ACC) & 1), abort) &&
+                          tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / F8_STAGES) & 1), abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) {
                         *abort = 1;
@@ -344,22 +375,30 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                     break;
                 }
                 tc::tc_fence_after();
-                uint32_t d[32];
-                tc::tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 32u, d);
+                uint32_t dh[32], dl[32];
+                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 64u;
+                tc::tmem_ld32(ta, dh);
+                tc::tmem_ld32(ta + 32u, dl);
+                const float sc_cur = S.sc[stage][rowp];
                 tc::tmem_ld_wait();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&S.tempty[acc]);
+                if (lane == 0) {
+                    tc::mbar_arrive(&S.tempty[acc]);
+                    tc::mbar_arrive(&S.empty[stage]);
+                }
                 const int64_t p = (j0 + i) * F8_TILE + rowp;
                 const bool valid = p < nvis;
                 float sc = -INFINITY;
                 if (valid) {
                     if (sc_cur != -INFINITY) {
-                        float acc_s = 0.0f;
+                        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four independent chains
 #pragma unroll
-                        for (int h = 0; h < 32; h++)
-                            acc_s = fmaf(wv[h], fmaxf(__uint_as_float(d[h]), 0.0f), acc_s);
-                        sc = acc_s * sc_cur;
+                        for (int h = 0; h < 32; h++) {
+                            const float x = __uint_as_float(dh[h]) + __uint_as_float(dl[h]);
+                            part[h & 3] = fmaf(wv[h], fmaxf(x, 0.0f), part[h & 3]);
+                        }
+                        sc = ((part[0] + part[1]) + (part[2] + part[3])) * sc_cur;
                     }
                     if (scores) scores[(int64_t)r * ld + p] = sc;
                 }
@@ -369,8 +408,6 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
                     for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                     if ((lane & 7) == 0 && valid) block_max[(int64_t)r * (ld / 8) + (p >> 3)] = m;
                 }
-                sc_cur = sc_next;
-                pg_next = pg_next2;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&S.wfree[seg & 1]);   // this warp is done with seg's weights
@@ -381,55 +418,29 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(const __grid_constan
     }
 
     // ---- teardown: nothing in flight may outlive the CTA's shared and tensor memory
+    if (warp < 4) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (*abort) {
-        if (tid == 0)
-            for (int s = 0; s < F8_STAGES; s++)
-                if (last_full_k[s] >= 0) tc::mbar_wait(&S.full[s], (uint32_t)(last_full_k[s] & 1), 1u << 20);
-        if (tid == 32 && last_tile >= 0)
-            tc::mbar_wait(&S.tfull[last_tile % F8_ACC], (uint32_t)((last_tile / F8_ACC) & 1), 1u << 20);
-    }
+    if (*abort && (tid == F8_MMA_WARP * 32 || tid == (F8_MMA_WARP + 1) * 32) && last_tile >= 0)
+        tc::mbar_wait(&S.tfull[last_tile % F8_ACC], (uint32_t)((last_tile / F8_ACC) & 1), 1u << 20);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 1) tc::tmem_dealloc(tmem, F8_ACC * 32);
+    if (warp == F8_MMA_WARP) tc::tmem_dealloc(tmem, F8_ACC * 64);
 }
 
 // ---------------------------------------------------------------- host side
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static std::once_flag g_encode_once;
 static int g_sms = 0;
-
-static int make_key_map(const csa2_cache &c, CUtensorMap *map)
-{
-    std::call_once(g_encode_once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void *fn = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    });
-    if (!g_encode) return CSA2_ERR_CUDA;
-    const cuuint64_t dims[2] = {128, (cuuint64_t)c.num_slots};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {128, 64};
-    const cuuint32_t es[2] = {1, 1};
-    const CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, c.ik_codes, dims, strides, box, es,
-                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return res == CUDA_SUCCESS ? CSA2_OK : CSA2_ERR_CUDA;
-}
+static std::once_flag g_sms_once;
 
 int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                       float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
 {
-    CUtensorMap map;
-    int s = make_key_map(c, &map);
-    if (s) return s;
+    std::call_once(g_sms_once, [] {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (g_sms <= 0) return CSA2_ERR_CUDA;
     const int rows = bt.batch * bt.nq;
     const size_t smem = sizeof(F8Smem) + 1024;
     static bool attr = false;
@@ -441,11 +452,10 @@ int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t 
     const int64_t tiles_row = std::max<int64_t>(1, (bt.max_entries + F8_TILE - 1) / F8_TILE);
     if (rows <= F8_PERSIST_ROWS) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)rows * tiles_row, g_sms));
-        k_index_f8<true><<<grid, F8_THREADS, smem, st>>>(map, c, bt, qi, w, scores, block_max, n_visible, ld);
+        k_index_f8<true><<<grid, F8_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
     } else {
         const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + rows - 1) / rows));
-        k_index_f8<false><<<dim3(x, rows), F8_THREADS, smem, st>>>(map, c, bt, qi, w, scores, block_max, n_visible,
-                                                                   ld);
+        k_index_f8<false><<<dim3(x, rows), F8_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
     }
     return launch_status();
 }
