@@ -315,7 +315,7 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-KERNEL_VERSION = "f8-cpasync-scan-v3"
+KERNEL_VERSION = "f8-cpasync-scan-v4"
 
 
 # ---------------------------------------------------------------- CPU oracle

@@ -19,16 +19,17 @@
 // tensor memory holds A.hi in columns 0-31 and A.lo in 32-63, and the
 // epilogue adds them, applies ReLU, w_h * 2^e_h and the entry's scale.
 //
-// Warp roles (320 threads): warps 0-3 copy key tiles into a 12-stage ring
-// (eight 16-byte chunks per thread per tile), warp 0 also the entries' fp32
+// A tile is 256 entries (four pages): two M = 128 halves per K step.  Warp
+// roles (448 threads): warps 0-3 copy key tiles into a 6-stage ring (sixteen
+// 16-byte chunks per thread per tile), warps 0-1 also the entries' fp32
 // scales into the same stage, so that no role waits on a dependent global
-// load per tile; warps 4-7 drain eight tensor-memory accumulators (TMEM lane
-// quarter = warp % 4) and free a stage once they have read its scales (its
-// MMAs are complete by then); warp 8 writes the query operand of each row,
-// and lane 0 of warps 8 and 9 issue the MMAs of the even and odd tiles (two
-// issuing threads: one alone, waiting on barriers between tiles, leaves the
-// tensor pipe idle half the time).  A persistent grid walks one
-// global list of (row, tile) items so ragged batches stay balanced.
+// load per tile; warps 4-11 drain four tensor-memory accumulators (warp w:
+// half (w - 4) / 4, TMEM lane quarter w % 4) and free a stage once they have
+// read its scales (its MMAs are complete by then); warp 12 writes the query
+// operand of each row, and lane 0 of warps 12 and 13 issue the MMAs of the
+// even and odd tiles (one issuing thread that also waits on barriers between
+// tiles leaves the tensor pipe idle half the time).  A persistent grid walks
+// one global list of (row, tile) items so ragged batches stay balanced.
 #include <algorithm>
 #include <mutex>
 
@@ -37,17 +38,19 @@
 
 namespace csa2 {
 
-constexpr int F8_STAGES = 12;
-constexpr int F8_ACC = 8;                  // tensor-memory accumulators of 64 columns (hi | lo)
-constexpr int F8_THREADS = 320;
+constexpr int F8_TILE = 256;               // entries per tile: 4 pages, two MMA halves of M = 128
+constexpr int F8_STAGES = 6;               // 32 KB of codes per stage
+constexpr int F8_ACC = 4;                  // tensor-memory accumulators of 128 columns (2 halves x hi | lo)
 constexpr int F8_PROD = 128;               // producer threads (warps 0-3)
-constexpr int F8_MMA_WARP = 8;
-constexpr int F8_TILE = 128;
+constexpr int F8_EPI_WARP = 4;             // epilogue warps 4-11: half (w - 4) / 4, lane quarter w % 4
+constexpr int F8_EPI = 8;
+constexpr int F8_MMA_WARP = 12;            // MMA issuers: warps 12 and 13
+constexpr int F8_THREADS = 448;
 constexpr int F8_PERSIST_ROWS = 256;
 constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 64);
 
 struct F8Smem {
-    uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (cp.async)
+    uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (cp.async); rows 128 h .. of half h
     uint8_t b[2][64 * 128];                // query hi (rows 0-31) and lo (rows 32-63), per segment parity
     float sc[F8_STAGES][F8_TILE];          // fp32 scales of the stage's entries (cp.async)
     float wq[2][32];                       // w_h * 2^e_h, per segment parity
@@ -108,17 +111,18 @@ __device__ __forceinline__ uint32_t sw128_b8(uint32_t row, uint32_t k)
     return row * 128u + ((((k >> 4) ^ (row & 7u)) << 4) | (k & 15u));
 }
 
-// Warp 1: the two-part e4m3 query operand of row r and w_h * 2^e_h; lane h = head h.
+// The two-part e4m3 query operand of row r and w_h * 2^e_h, written by one
+// warp; lane h = head h.  Two passes over the head's 128 dims (the maximum,
+// then the conversion) keep half of it in registers at a time.
 __device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const uint16_t *qr, const float *wr)
 {
     const int h = threadIdx.x & 31;
     const uint4 *src = reinterpret_cast<const uint4 *>(qr + h * 128);
-    uint4 raw[16];
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; i++) {
-        raw[i] = __ldg(src + i);
-        const uint32_t w4[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+        const uint4 raw = __ldg(src + i);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int j = 0; j < 4; j++) {
             amax = fmaxf(amax, fabsf(__uint_as_float(w4[j] << 16)));
@@ -128,12 +132,13 @@ __device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const
     const int e = head_exponent(amax);
     const float f = exp2i(-e);
     wq[h] = wr[h] * exp2i(e);
-#pragma unroll
+#pragma unroll 2
     for (int i = 0; i < 16; i += 2) {               // 16 dims per 16-byte chunk of the operand
         uint32_t hiw[4], low[4];
 #pragma unroll
         for (int half = 0; half < 2; half++) {
-            const uint32_t w4[4] = {raw[i + half].x, raw[i + half].y, raw[i + half].z, raw[i + half].w};
+            const uint4 raw = __ldg(src + i + half);
+            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
             for (int j = 0; j < 4; j += 2) {
                 float v[4] = {__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f,
@@ -166,21 +171,21 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
     if (tid == 0) {
         for (int i = 0; i < F8_STAGES; i++) {
             tc::mbar_init(&S.full[i], F8_PROD);
-            tc::mbar_init(&S.empty[i], 4);           // the epilogue warps, after the tile's MMAs and scale reads
+            tc::mbar_init(&S.empty[i], F8_EPI);      // the epilogue warps, after the tile's MMAs and scale reads
         }
         for (int i = 0; i < F8_ACC; i++) {
             tc::mbar_init(&S.tfull[i], 1);
-            tc::mbar_init(&S.tempty[i], 4);
+            tc::mbar_init(&S.tempty[i], F8_EPI);
         }
         for (int i = 0; i < 2; i++) {
             tc::mbar_init(&S.bfree[i], 2);           // both MMA issuers
             tc::mbar_init(&S.wready[i], 32);
-            tc::mbar_init(&S.wfree[i], 4);
+            tc::mbar_init(&S.wfree[i], F8_EPI);
         }
         S.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_ACC * 64);
+    if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_ACC * 128);
 
     int64_t g0, g1;
     if (PERSIST) {
@@ -233,16 +238,16 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 
         if (warp < 4) {
             // ---------------- producers: page ids of 32 tiles at a time (one lane per
-            // tile), then per tile eight 16-byte chunks of codes per thread (thread t:
-            // chunk t % 8 of rows t / 8 + 16 j); warp 0 also the tile's 128 scales
+            // tile), then per tile sixteen 16-byte chunks of codes per thread (thread t:
+            // chunk t % 8 of rows t / 8 + 16 j); warps 0-1 also the tile's 256 scales
             const uint32_t a0 = tc::smem_u32(S.a[0]);
             const int pt = warp * 32 + lane;
-            int32_t my_pg[2] = {-1, -1};
+            int32_t my_pg[4] = {-1, -1, -1, -1};
             for (int64_t i = 0; i < nt; i++) {
                 if ((i & 31) == 0) {
                     const int64_t e = (j0 + i + lane) * F8_TILE;     // tile i + lane
 #pragma unroll
-                    for (int h = 0; h < 2; h++) {
+                    for (int h = 0; h < 4; h++) {
                         const int64_t e0 = e + 64 * h;
                         my_pg[h] = -2;                                // -2: beyond the visible entries
                         if (i + lane < nt && e0 < nvis) {
@@ -251,8 +256,9 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         }
                     }
                 }
-                const int32_t pgs[2] = {__shfl_sync(0xffffffffu, my_pg[0], (int)(i & 31)),
-                                        __shfl_sync(0xffffffffu, my_pg[1], (int)(i & 31))};
+                int32_t pgs[4];
+#pragma unroll
+                for (int h = 0; h < 4; h++) pgs[h] = __shfl_sync(0xffffffffu, my_pg[h], (int)(i & 31));
                 const int64_t ti = it + i;
                 const int stage = (int)(ti % F8_STAGES);
                 const int k = (int)(ti / F8_STAGES);
@@ -266,19 +272,20 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
                 const uint32_t dst = a0 + (uint32_t)stage * (F8_TILE * 128);
 #pragma unroll
-                for (int jj = 0; jj < 8; jj++) {
+                for (int jj = 0; jj < 16; jj++) {
                     const int e = pt + F8_PROD * jj;                  // 16-byte chunk of the tile
-                    const int row = e >> 3, ch = e & 7, h = jj >> 2;  // rows 0-63: page 0, 64-127: page 1
+                    const int row = e >> 3, ch = e & 7, h = jj >> 2;  // rows 64 h .. 64 h + 63: page h
                     if (pgs[h] >= 0)
                         cp_async16(dst + (uint32_t)row * 128u + ((uint32_t)(ch ^ (row & 7)) << 4),
                                    c.ik_codes + ((int64_t)pgs[h] * CSA2_PAGE + (row & 63)) * 128 + ch * 16);
                 }
-                if (warp == 0) {
-                    const int h = lane >> 4;                          // entries 4 lane .. 4 lane + 3
-                    const float *src = pgs[h] >= 0 ? c.ik_scales + (int64_t)pgs[h] * CSA2_PAGE + 4 * (lane & 15)
-                                                   : g_neg_inf_scales + 4 * (lane & 15);
-                    if (pgs[h] != -2) cp_async16(tc::smem_u32(&S.sc[stage][4 * lane]), src);
-                    if (pgs[h] == -1 && (lane & 15) == 0) flag(c.status, CSA2_DEV_BAD_PAGE);
+                if (warp < 2) {
+                    const int q = pt;                                 // entries 4 q .. 4 q + 3
+                    const int h = q >> 4;
+                    const float *src = pgs[h] >= 0 ? c.ik_scales + (int64_t)pgs[h] * CSA2_PAGE + 4 * (q & 15)
+                                                   : g_neg_inf_scales + 4 * (q & 15);
+                    if (pgs[h] != -2) cp_async16(tc::smem_u32(&S.sc[stage][4 * q]), src);
+                    if (pgs[h] == -1 && (q & 15) == 0) flag(c.status, CSA2_DEV_BAD_PAGE);
                 }
                 cp_async_arrive(&S.full[stage]);
             }
@@ -332,10 +339,13 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         tc::tc_fence_after();
                         const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
 #pragma unroll
-                        for (int kk = 0; kk < 4; kk++)       // K = 128 codes in steps of 32; N = hi | lo
-                            tc::mma_f8(tmem + (uint32_t)acc * 64u,
-                                       tc::smem_desc(as + kk * 32, 16, 1024, tc::kSwizzle128B),
-                                       tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC, kk > 0);
+                        for (int hf = 0; hf < 2; hf++)       // two halves of 128 entries
+#pragma unroll
+                            for (int kk = 0; kk < 4; kk++)   // K = 128 codes in steps of 32; N = hi | lo
+                                tc::mma_f8(tmem + (uint32_t)acc * 128u + 64u * hf,
+                                           tc::smem_desc(as + hf * (128 * 128) + kk * 32, 16, 1024, tc::kSwizzle128B),
+                                           tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC,
+                                           kk > 0);
                         // the stage is released by the epilogue, which reads its scales only
                         // after this commit: the MMAs are done with the codes by then
                         tc::mma_commit(&S.tfull[acc]);
@@ -346,8 +356,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 __syncwarp();
             }
         } else {
-            // ---------------- epilogue: warps 4-7, TMEM lanes by warp % 4
-            const int qd = warp & 3;
+            // ---------------- epilogue: warps 4-11, half (warp - 4) / 4, TMEM lanes by warp % 4
+            const int qd = warp & 3, hf = (warp - F8_EPI_WARP) >> 2;
             const bool wok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
             if (!__all_sync(0xffffffffu, wok)) {
                 if (lane == 0) {
@@ -357,7 +367,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 break;
             }
             const float *wv = S.wq[seg & 1];              // broadcast shared-memory reads
-            const int64_t rowp = (int64_t)qd * 32 + lane;
+            const int64_t rowp = (int64_t)hf * 128 + qd * 32 + lane;
             for (int64_t i = 0; i < nt; i++) {
                 const int64_t ti = it + i;
                 const int acc = (int)(ti % F8_ACC);
@@ -375,31 +385,32 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                     break;
                 }
                 tc::tc_fence_after();
-                uint32_t dh[32], dl[32];
-                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 64u;
-                tc::tmem_ld32(ta, dh);
-                tc::tmem_ld32(ta + 32u, dl);
+                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 128u + 64u * (uint32_t)hf;
                 const float sc_cur = S.sc[stage][rowp];
-                tc::tmem_ld_wait();
+                const int64_t p = (j0 + i) * F8_TILE + rowp;
+                const bool valid = p < nvis;
+                float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};             // four independent chains
+#pragma unroll
+                for (int c16 = 0; c16 < 2; c16++) {                    // heads 16 c16 .. 16 c16 + 15
+                    uint32_t dh[16], dl[16];
+                    tc::tmem_ld16(ta + 16u * c16, dh);
+                    tc::tmem_ld16(ta + 32u + 16u * c16, dl);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; j++) {
+                        const float x = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
+                        part[j & 3] = fmaf(wv[16 * c16 + j], fmaxf(x, 0.0f), part[j & 3]);
+                    }
+                }
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     tc::mbar_arrive(&S.tempty[acc]);
                     tc::mbar_arrive(&S.empty[stage]);
                 }
-                const int64_t p = (j0 + i) * F8_TILE + rowp;
-                const bool valid = p < nvis;
                 float sc = -INFINITY;
                 if (valid) {
-                    if (sc_cur != -INFINITY) {
-                        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four independent chains
-#pragma unroll
-                        for (int h = 0; h < 32; h++) {
-                            const float x = __uint_as_float(dh[h]) + __uint_as_float(dl[h]);
-                            part[h & 3] = fmaf(wv[h], fmaxf(x, 0.0f), part[h & 3]);
-                        }
-                        sc = ((part[0] + part[1]) + (part[2] + part[3])) * sc_cur;
-                    }
+                    if (sc_cur != -INFINITY) sc = ((part[0] + part[1]) + (part[2] + part[3])) * sc_cur;
                     if (scores) scores[(int64_t)r * ld + p] = sc;
                 }
                 if (block_max) {
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == F8_MMA_WARP) tc::tmem_dealloc(tmem, F8_ACC * 64);
+    if (warp == F8_MMA_WARP) tc::tmem_dealloc(tmem, F8_ACC * 128);
 }
 
 // ---------------------------------------------------------------- host side
