@@ -19,10 +19,10 @@ int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, 
                       float *, int32_t *, int64_t, cudaStream_t);
 int launch_index_pool(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
                            const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
-int launch_gather_scores(const float *, int64_t, const int32_t *, const int32_t *, int64_t, int64_t, float *,
-                         cudaStream_t);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
                 cudaStream_t);
+int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int32_t *, int32_t, int32_t,
+                     int32_t *, cudaStream_t);
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
@@ -72,7 +72,7 @@ static inline int64_t score_ld(const csa2_batch *b)
 }
 
 // FULL workspace: scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
-//                 | pool scores [rows][16384] | attention workspace
+//                 | attention workspace
 // REINDEX:        pool scores [rows][16384] | attention workspace
 struct LayerWs {
     float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr;
@@ -98,8 +98,7 @@ static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
         w.block_max = (float *)take((size_t)rows * (ld / 8) * 4);
         w.n_visible = (int32_t *)take((size_t)rows * 4);
     }
-    if (mode == CSA2_MODE_FULL || mode == CSA2_MODE_REINDEX)
-        w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+    if (mode == CSA2_MODE_REINDEX) w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
     w.attn_bytes = attn_workspace_bytes(rows);
     w.attn = take(w.attn_bytes);
     w.total = off;
@@ -280,10 +279,8 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
         if ((s = launch_topk_blocks(ws.block_max, ld / 8, ws.n_visible, rows, CSA2_POOL_BLOCKS, io->pool,
                                     io->pool_len, st)))
             return s;
-        // a6: Top-512 of the pool
-        if ((s = launch_gather_scores(ws.scores, ld, io->pool, io->pool_len, CSA2_POOL_MAX, rows, ws.pool_scores, st)))
-            return s;
-        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st)))
+        // a6: Top-512 of the pool, its scores read from the scan's score rows
+        if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st)))
             return s;
     } else if (mode == CSA2_MODE_REINDEX) {
         // a7: rescore the pool with this layer's indexer query, Top-512

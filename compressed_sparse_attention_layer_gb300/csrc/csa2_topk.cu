@@ -1,10 +1,14 @@
-// a5/a6: Top-K selection with ties broken toward the lower slot.
+// a5/a6: Top-K selection with ties broken toward the lower slot
+// ("DeepSeek-V4.1-Flash 架构详解" §1 table: top-k 512; §3.2: the best 2,048
+// blocks of 8 form the candidate pool, then the pool's own Top-512; the
+// research note §3.2).
 //
-// One thread-block cluster per row ("DeepSeek-V4.1-Flash 架构详解" §1 table:
-// top-k 512; §3.2: the best 2,048 blocks of 8 form the candidate pool, then
-// the pool's own Top-512; the research note §3.2).  The CL CTAs of a cluster
-// each stage one contiguous 1/CL of the row in shared memory as
-// order-preserving 32-bit keys, read once from global memory.  A radix select
+// Rows of up to 16,384 keys (the pool Top-512) run on one CTA per row with the
+// keys in registers (k_topk_rows; description below).  The block level and
+// generic rows longer than 16,384 keys use one thread-block cluster per row:
+// the CL CTAs each stage one contiguous 1/CL of
+// the row in shared memory as order-preserving 32-bit keys, read once from
+// global memory.  A radix select
 // finds the k-th largest key T: the digits are 11-bit fields of (key - kmin)
 // from the top bit of the row's actual range (kmax - kmin), so that scores
 // crowded into a few exponents still spread over all 2,048 bins; each CTA
@@ -325,8 +329,255 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
     if (nsel == 0 && q == 0 && threadIdx.x == 0) pool_len[r] = 0;
 }
 
-// Cluster size for rows of up to n keys: small rows on one or two CTAs, the
-// 16,384-entry pools on four, longer rows on eight (slices <= TK_SLICE keys).
+// ---------------------------------------------------------------- one CTA per row, keys in registers
+// Rows of up to RS_MAX = 16,384 keys: 1,024 threads hold 16 consecutive slots
+// each (thread t: slots 16 t .. 16 t + 15) as order keys in registers.  The
+// k-th largest key T is found by a radix select on (key - kmin) over the
+// row's actual range, 8 bits per round from the top, each round counted in
+// per-warp shared-memory histograms (no atomics across warps) and summed per
+// bin; one packed block scan of (count > T, count == T) then places every
+// selected slot: rank = slots above T before it + the ties before it, ties
+// taken lowest slot first -- so the output is in ascending slot order and
+// identical on every run.
+constexpr int RS_THREADS = 1024;
+constexpr int RS_PER = 16;
+constexpr int RS_MAX = RS_THREADS * RS_PER;
+
+struct __align__(16) RsShared {                // 16-byte vector accesses to hist and tot
+    uint32_t hist[RS_THREADS / 32][256];   // per-warp digit counts
+    uint32_t tot[256];                     // digit counts of the block
+    uint32_t warp_u[RS_THREADS / 32];
+    uint32_t kmin, kmax;
+    uint32_t digit;
+    int above;
+};
+
+// Block-wide exclusive scan of one 32-bit value per thread (1,024 threads).
+__device__ __forceinline__ uint32_t rs_exclusive_scan(uint32_t v, RsShared &sh)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh.warp_u[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+        uint32_t s2 = sh.warp_u[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, s2, o);
+            if (lane >= o) s2 += y;
+        }
+        sh.warp_u[lane] = s2;                          // inclusive
+    }
+    __syncthreads();
+    const uint32_t base = wid ? sh.warp_u[wid - 1] : 0u;
+    __syncthreads();                                   // warp_u free for the next use
+    return base + x - v;
+}
+
+// Top k (k >= 1) of the n valid keys key[] of this row (bit j of `valid`
+// marks slot 16 t + j as valid); calls emit(rank, j) for every selected slot
+// 16 t + j, ranks ascending with the slot.  Returns the number selected,
+// min(n, k).
+template <class Emit>
+__device__ int rs_select(const uint32_t (&key)[RS_PER], uint32_t valid, int n, int k, RsShared &sh, Emit emit)
+{
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (n <= k) {                                      // everything valid is selected, in slot order
+        uint32_t off = rs_exclusive_scan(__popc(valid), sh);
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++)
+            if (valid >> j & 1u) emit((int)off++, j);
+        return n;
+    }
+    // ---- the valid keys' range
+    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++)
+        if (valid >> j & 1u) {
+            mn = min(mn, key[j]);
+            mx = max(mx, key[j]);
+        }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (tid == 0) {
+        sh.kmin = 0xFFFFFFFFu;
+        sh.kmax = 0u;
+    }
+    __syncthreads();
+    if (lane == 0) {
+        atomicMin(&sh.kmin, mn);
+        atomicMax(&sh.kmax, mx);
+    }
+    __syncthreads();
+    const uint32_t kmin = sh.kmin, range = sh.kmax - kmin;
+    const int nbits = range ? 32 - __clz(range) : 0;
+    uint32_t prefix = 0, mask = 0;                     // over rel = key - kmin
+    int kk = k;
+#pragma unroll 1
+    for (int top = nbits; top > 0; top -= 8) {
+        const int width = top < 8 ? top : 8;
+        const int shift = top - width;
+        const uint32_t dmask = (1u << width) - 1u;
+        *reinterpret_cast<uint4 *>(&sh.hist[wid][4 * lane]) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(&sh.hist[wid][128 + 4 * lane]) = make_uint4(0u, 0u, 0u, 0u);
+        if (tid < 256) sh.tot[tid] = 0u;
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++) {
+            const uint32_t rel = key[j] - kmin;
+            if ((valid >> j & 1u) && (rel & mask) == prefix) atomicAdd(&sh.hist[wid][(rel >> shift) & dmask], 1u);
+        }
+        __syncthreads();
+        {
+            // every thread sums one bin over 8 warps' counts, four groups per bin
+            const int bin = tid & 255, grp = tid >> 8;
+            uint32_t t = 0;
+#pragma unroll
+            for (int w2 = 0; w2 < 8; w2++) t += sh.hist[8 * grp + w2][bin];
+            if (t) atomicAdd(&sh.tot[bin], t);
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // lane L holds bins 8 L .. 8 L + 7; keys above a bin = the bins of the higher lanes
+            // (a suffix sum) + this lane's higher bins
+            const uint4 t0 = *reinterpret_cast<const uint4 *>(&sh.tot[8 * lane]);   // RsShared is 16-aligned
+            const uint4 t1 = *reinterpret_cast<const uint4 *>(&sh.tot[8 * lane + 4]);
+            const uint32_t c[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+            uint32_t csum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; q++) csum += c[q];
+            uint32_t incl = csum;                      // sum over lanes >= this one
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += y;
+            }
+            uint32_t acc = incl - csum;                // keys in the bins of the higher lanes
+            if (acc < (uint32_t)kk && incl >= (uint32_t)kk) {
+#pragma unroll
+                for (int q = 7; q >= 0; q--) {
+                    if (acc + c[q] >= (uint32_t)kk) {
+                        sh.digit = (uint32_t)(8 * lane + q);
+                        sh.above = (int)acc;
+                        break;
+                    }
+                    acc += c[q];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= sh.digit << shift;
+        mask |= dmask << shift;
+        kk -= sh.above;
+        // digit, above and tot are rewritten only after another block barrier
+    }
+    const uint32_t T = prefix + kmin;
+    const int need_eq = kk;                            // ties with T that are selected, lowest slots first
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++)
+        if (valid >> j & 1u) {
+            gt += key[j] > T;
+            eq += key[j] == T;
+        }
+    const uint32_t pre = rs_exclusive_scan((gt << 16) | eq, sh);   // both sums <= 16,384
+    const int gt_prior = (int)(pre >> 16), eq_prior = (int)(pre & 0xFFFFu);
+    int take = need_eq - eq_prior;
+    take = take < 0 ? 0 : (take > (int)eq ? (int)eq : take);
+    int off = gt_prior + (eq_prior < need_eq ? eq_prior : need_eq);
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++) {
+        if (!(valid >> j & 1u)) continue;
+        if (key[j] > T) {
+            emit(off++, j);
+        } else if (key[j] == T && take > 0) {
+            emit(off++, j);
+            take--;
+        }
+    }
+    return k;
+}
+
+// Slots 16 t .. 16 t + 15 of a row of n keys as order keys: direct
+// (row[i]) when ind is NULL, else gathered (src[ind[i]]; an index outside
+// [0, src_len) reads as -inf).  Returns the valid mask (slots < n).
+__device__ __forceinline__ uint32_t rs_load(const float *__restrict__ row, const int32_t *__restrict__ ind,
+                                            int64_t src_len, int n, uint32_t (&key)[RS_PER])
+{
+    const int s0 = RS_PER * threadIdx.x;
+    uint32_t valid = 0;
+    if (!ind) {
+        if (s0 + RS_PER <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+            for (int q = 0; q < RS_PER / 4; q++) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(row + s0) + q);
+                key[4 * q] = order_key(v.x);
+                key[4 * q + 1] = order_key(v.y);
+                key[4 * q + 2] = order_key(v.z);
+                key[4 * q + 3] = order_key(v.w);
+            }
+            return 0xFFFFu;
+        }
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++) {
+            key[j] = 0u;
+            if (s0 + j < n) {
+                key[j] = order_key(__ldg(row + s0 + j));
+                valid |= 1u << j;
+            }
+        }
+        return valid;
+    }
+    int32_t p[RS_PER];
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++) p[j] = s0 + j < n ? __ldg(ind + s0 + j) : -1;
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++) {
+        key[j] = 0u;
+        if (s0 + j < n) {
+            key[j] = order_key(p[j] >= 0 && p[j] < src_len ? __ldg(row + p[j]) : -INFINITY);
+            valid |= 1u << j;
+        }
+    }
+    return valid;
+}
+
+// Top k of each row (one CTA per row, len[r] <= RS_MAX slots): keys direct
+// (scores[r][i]) or gathered through ind (scores[r][ind[r][i]], scores rows of
+// src_len), reported as cand[r][i] (or i) ascending, -1 after.
+__global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__restrict__ scores, int64_t src_len,
+                                                              const int32_t *__restrict__ ind, int64_t ld,
+                                                              const int32_t *__restrict__ len,
+                                                              const int32_t *__restrict__ cand, int k,
+                                                              int32_t *__restrict__ out)
+{
+    __shared__ RsShared sh;
+    const int64_t r = blockIdx.x;
+    int64_t n64 = len[r];
+    n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
+    const int n = (int)n64;
+    uint32_t key[RS_PER];
+    const uint32_t valid = ind ? rs_load(scores + r * src_len, ind + r * ld, src_len, n, key)
+                               : rs_load(scores + r * ld, nullptr, 0, n, key);
+    int32_t *o = out + r * k;
+    const int32_t *cr = cand ? cand + r * ld : nullptr;
+    const int s0 = RS_PER * threadIdx.x;
+    const int nsel = rs_select(key, valid, n, k, sh, [&](int j, int jj) {
+        o[j] = cr ? __ldg(cr + s0 + jj) : s0 + jj;
+    });
+    for (int j = nsel + (int)threadIdx.x; j < k; j += RS_THREADS) o[j] = -1;
+}
+
+// Cluster size for rows of up to n keys (slices <= TK_SLICE keys): the block
+// level of long rows and generic rows longer than RS_MAX keys.
 static int topk_cluster_for(int64_t n)
 {
     return n > 32768 ? 8 : (n > 8192 ? 4 : (n > 2048 ? 2 : 1));
@@ -384,12 +635,28 @@ int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t row
                 int32_t k, int32_t *out, cudaStream_t st)
 {
     if (rows == 0) return CSA2_OK;
+    if (ld <= RS_MAX) {
+        k_topk_rows<<<(unsigned)rows, RS_THREADS, 0, st>>>(scores, 0, nullptr, ld, len, cand, k, out);
+        return launch_status();
+    }
     switch (topk_cluster_for(ld)) {
     case 1: return topk_cl<1>(scores, ld, len, rows, cand, k, out, st);
     case 2: return topk_cl<2>(scores, ld, len, rows, cand, k, out, st);
     case 4: return topk_cl<4>(scores, ld, len, rows, cand, k, out, st);
     default: return topk_cl<8>(scores, ld, len, rows, cand, k, out, st);
     }
+}
+
+// Top-k of the pool positions pool[r][0 .. pool_len[r]) by their scores in a
+// full score row (scores[r][pool[r][i]], rows of ld_scores), reported as
+// positions, ascending.
+int launch_topk_pool(const float *scores, int64_t ld_scores, const int32_t *pool, int64_t ld_pool,
+                     const int32_t *pool_len, int32_t rows, int32_t k, int32_t *out, cudaStream_t st)
+{
+    if (rows == 0) return CSA2_OK;
+    if (ld_pool > RS_MAX) return CSA2_ERR_SHAPE;
+    k_topk_rows<<<(unsigned)rows, RS_THREADS, 0, st>>>(scores, ld_scores, pool, ld_pool, pool_len, pool, k, out);
+    return launch_status();
 }
 
 int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,

@@ -142,6 +142,31 @@ def test_topk_bit_exact_given_scores():
             assert np.array_equal(got[r], want), (r, use_cand)
 
 
+def test_topk_rows_of_at_most_16384_bit_exact():
+    """Rows that fit one CTA (the pool Top-512 path): heavy ties, -0.0 / +0.0,
+    -inf, fewer valid slots than k, exactly k, one, none; with and without cand."""
+    rng = np.random.default_rng(19)
+    rows, ld = 9, 16384
+    s = rng.integers(0, 200, (rows, ld)).astype(np.float32) * np.float32(0.25)
+    s[1] = -s[1]
+    s[2, ::2] = -0.0
+    s[2, 1::2] = 0.0
+    s[3, :] = 7.0                                              # all equal: lowest slots win
+    s[4, 5000:] = -np.inf
+    s[5] = rng.standard_normal(ld).astype(np.float32)          # distinct values
+    lens = np.array([16384, 16383, 16384, 16384, 9000, 513, 512, 1, 0], np.int32)
+    cand = np.sort(rng.choice(10 ** 6, (rows, ld)), axis=1).astype(np.int32)
+    for use_cand in (False, True):
+        out = torch.full((rows, 512), -7, dtype=torch.int32, device="cuda")
+        csa2.csa2_topk(torch.from_numpy(s).cuda(), torch.from_numpy(lens).cuda(), 512, out,
+                       cand=torch.from_numpy(cand).cuda() if use_cand else None)
+        got = out.cpu().numpy()
+        for r in range(rows):
+            n = lens[r]
+            want = oracle.topk(s[r, :n].astype(np.float64), cand[r, :n] if use_cand else None)
+            assert np.array_equal(got[r], want), (r, use_cand)
+
+
 def test_topk_blocks_bit_exact():
     rng = np.random.default_rng(10)
     rows = 4
@@ -155,6 +180,25 @@ def test_topk_blocks_bit_exact():
     for r in range(rows):
         n = int(nvis[r])
         scores = np.repeat(bm[r, :(n + 7) // 8].astype(np.float64), 8)[:n]   # block max = that value
+        want = oracle.block_pool(scores, n)
+        assert gl[r] == want.size and np.array_equal(got[r, :gl[r]], want), r
+
+
+def test_topk_blocks_single_stage_bit_exact():
+    """Rows of at most 16,384 blocks (one select per row): ties, fewer blocks
+    than the pool holds, a partial last block."""
+    rng = np.random.default_rng(11)
+    nvis = np.array([131072, 131067, 70000, 16384, 100, 0], np.int32)
+    rows = nvis.size
+    ld_b = 16384
+    bm = rng.integers(0, 300, (rows, ld_b)).astype(np.float32)
+    pool = torch.full((rows, 16384), -7, dtype=torch.int32, device="cuda")
+    plen = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
+    csa2.csa2_topk_blocks(torch.from_numpy(bm).cuda(), torch.from_numpy(nvis).cuda(), 2048, pool, plen)
+    got, gl = pool.cpu().numpy(), plen.cpu().numpy()
+    for r in range(rows):
+        n = int(nvis[r])
+        scores = np.repeat(bm[r, :(n + 7) // 8].astype(np.float64), 8)[:n]
         want = oracle.block_pool(scores, n)
         assert gl[r] == want.size and np.array_equal(got[r, :gl[r]], want), r
 
