@@ -4,9 +4,9 @@
 One step = one decode token for each of the 8 sequences through the whole
 hot path: the new token's entry is compressed (m = 1) and quantised into the
 paged cache (MXFP4 main KV, FP8 indexer key), then the 20-layer decoder
-pattern runs (Full + 3 Reuse, 4 x (Reindex + 3 Reuse)); each layer first
-quantises its own window row of the new token (FP8) and then runs
-csa2_layer.  The step is captured once as a CUDA graph and replayed.
+pattern runs (Full + 3 Reuse, 4 x (Reindex + 3 Reuse)) through csa2_layer,
+whose attention call also quantises the layer's FP8 window row of the new
+token into its ring.  The step is captured once as a CUDA graph and replayed.
 
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -148,13 +148,11 @@ class DecodeStep:
                                  for b in range(B)]).view(B, 128)
         self.swa_new = {l: torch.cat([synth.normal_bf16_torch(wl._sid(W.T_SWA, b, l), (N - 1) * 512, 512, dev)
                                       for b in range(B)]).view(B, 512).float() for l in dw.layers}
-        R = wl.swa_rows
-        self.swa_rows = torch.tensor([b * R + (N - 1) % R for b in range(B)], dtype=torch.int64, device=dev)
         self.e_new = torch.empty((B, 512), dtype=torch.float32, device=dev)
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 3 + sum(1 + {"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers)
+        self.launches = 3 + sum({"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers)
         # the step's host inputs for the end-to-end leg (new token + every layer's queries)
         self.h2d = [(self.C_new, None), (self.ik_new, None)]
         for l in dw.layers:
@@ -171,11 +169,10 @@ class DecodeStep:
         csa2.csa2_quant_mxfp4(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
         csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
         for l in dw.layers:
-            # a3: this layer's window row of the new token; a4-a9: the layer
-            csa2.csa2_quant_fp8(self.swa_new[l], dw.swa_codes[l].view(-1, 512), dw.swa_scales[l].view(-1),
-                                slots=self.swa_rows)
+            # a3-a9: the layer; its attention call also quantises this layer's window
+            # row of the new token into the ring (csa2_swa.new_rows)
             full = self.wl.layers[l] == "full"
-            dw.run_layer(l, prof=self.scan_ev if (prof and full) else None)
+            dw.run_layer(l, prof=self.scan_ev if (prof and full) else None, new_rows=self.swa_new[l])
 
 
 def run_native(args):

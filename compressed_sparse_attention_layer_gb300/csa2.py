@@ -36,7 +36,7 @@ class Batch(ctypes.Structure):
 
 
 class Swa(ctypes.Structure):
-    _fields_ = [("codes", _vp), ("scales", _vp), ("rows", _i32), ("pad_", _i32), ("start", _vp)]
+    _fields_ = [("codes", _vp), ("scales", _vp), ("rows", _i32), ("pad_", _i32), ("start", _vp), ("new_rows", _vp)]
 
 
 class LayerIO(ctypes.Structure):
@@ -155,9 +155,11 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
                  _ptr(q_pos, torch.int64, "q_pos"))
 
 
-def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None) -> Swa:
+def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None) -> Swa:
+    """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
+    into the ring by the attention call itself."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
-               0, _ptr(start, torch.int64, "swa start"))
+               0, _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"))
 
 
 # ---------------------------------------------------------------- entry points

@@ -55,11 +55,17 @@ static int check_batch(const csa2_batch *b, const csa2_cache *c)
     return CSA2_OK;
 }
 
-static int check_swa(const csa2_swa *s)
+static int check_swa(const csa2_swa *s, const csa2_batch *b)
 {
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
+    if (s->new_rows) {
+        // the window of a query in a multi-token chunk holds other new tokens, which
+        // must be in the ring before any query attends: quantise them first instead
+        if (b->nq != 1) return CSA2_ERR_UNSUPPORTED;
+        if (!aligned(s->new_rows, 16)) return CSA2_ERR_ALIGN;
+    }
     return CSA2_OK;
 }
 
@@ -218,7 +224,7 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
     int s = check_cache(cache, true, false);
     if (s) return s;
     if ((s = check_batch(batch, cache))) return s;
-    if ((s = check_swa(swa))) return s;
+    if ((s = check_swa(swa, batch))) return s;
     if (!q || !idx || !o || !lse) return CSA2_ERR_NULL;
     if (k < 1 || k > CSA2_TOPK) return CSA2_ERR_SHAPE;
     const size_t need = attn_workspace_bytes((int64_t)batch->batch * batch->nq);
@@ -243,7 +249,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (s) return s;
     if ((s = check_batch(batch, cache))) return s;
     if (!io) return CSA2_ERR_NULL;
-    if ((s = check_swa(&io->swa))) return s;
+    if ((s = check_swa(&io->swa, batch))) return s;
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;

@@ -273,7 +273,44 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         int64_t lo = t - (CSA2_SWA_WINDOW - 1);
         lo = lo < s0 ? s0 : lo;
         lo = lo < 0 ? 0 : lo;
-        if (lo + key <= t) {
+        const int kn = (int)(t - lo);                 // the query's own token (when it is in the window)
+        if (swa.new_rows && kn >= 0 && kn < AC_KEYS && (warp & 3) == (kn >> 5)) {
+            // this warp holds the new token's key in lane kn % 32: the whole warp takes
+            // the row's largest magnitude; the 16 lanes that loaded this thread-slab's
+            // dims (float4 chunks base .. base + 15 of the row) each quantise four of
+            // them exactly as the FP8 quantiser would and store them to the ring; the
+            // key's lane collects the 16 words
+            const float4 *nr = reinterpret_cast<const float4 *>(swa.new_rows + r * CSA2_HEAD_DIM);
+            float4 v[4];
+            float amax = 0.0f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; c4++) {
+                v[c4] = __ldg(nr + c4 * 32 + lane);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[c4].x), fabsf(v[c4].y)), fmaxf(fabsf(v[c4].z), fabsf(v[c4].w))));
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float sc = fp8_row_scale(amax);
+            const int base = (AC_DIMS * (int)dq + 64 * hf) / 4;          // first float4 of the slab
+            const int cb = base >> 5, lb = base & 31;                     // its register and lane
+            const float4 x = cb == 0 ? v[0] : cb == 1 ? v[1] : cb == 2 ? v[2] : v[3];
+            const uint32_t wd = f32x2_to_e4m3x2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc)) |
+                                (f32x2_to_e4m3x2(__fdiv_rn(x.z, sc), __fdiv_rn(x.w, sc)) << 16);
+            const int64_t off = (int64_t)b * swa.rows + t % swa.rows;
+            if (lane >= lb && lane < lb + 16)
+                reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(swa.codes) + off * CSA2_HEAD_DIM)[base + (lane - lb)] = wd;
+            uint32_t got[16];
+#pragma unroll
+            for (int q2 = 0; q2 < 16; q2++) got[q2] = __shfl_sync(0xffffffffu, wd, lb + q2);
+            if (key == kn) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) kc[i] = make_uint4(got[4 * i], got[4 * i + 1], got[4 * i + 2], got[4 * i + 3]);
+                if (dq == 0 && hf == 0) const_cast<float *>(swa.scales)[off] = sc;
+                kscale = sc;
+                valid = true;
+            }
+        }
+        if (lo + key <= t && !(swa.new_rows && key == kn)) {
             const int64_t row = (lo + key) % swa.rows;
             const int64_t off = (int64_t)b * swa.rows + row;
             const uint4 *src =

@@ -79,6 +79,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x)
     return r;
 }
 
+// Two fp32 values -> two e4m3 bytes (lo in the low byte), round to nearest
+// even, saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Per-row FP8 scale from the row's largest magnitude: amax / 448 (fp32 IEEE
+// division), 1 for an all-zero row.
+__device__ __forceinline__ float fp8_row_scale(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f); }
+
 // E2M1 magnitude code (0..7) -> float magnitude.
 __device__ __forceinline__ float e2m1_mag(uint32_t c)
 {

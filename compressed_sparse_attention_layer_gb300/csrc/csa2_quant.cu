@@ -110,15 +110,6 @@ __global__ void __launch_bounds__(256) k_quant_mxfp4(const float *__restrict__ x
     scales[dst * 16 + blk] = (uint8_t)(X + 127);
 }
 
-// Two fp32 values -> two e4m3 bytes (lo in the low byte), round to nearest
-// even, saturating to +-448.
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 // One warp per row.  "DeepSeek-V4.1-Flash" research note §3.3 (FP8 SWA KV).
 template <int DIM>
 __global__ void __launch_bounds__(256) k_quant_fp8(const float *__restrict__ x, int64_t n,
@@ -147,7 +138,7 @@ __global__ void __launch_bounds__(256) k_quant_fp8(const float *__restrict__ x, 
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const float s = fp8_row_scale(amax);
     uint32_t *dc = reinterpret_cast<uint32_t *>(codes + dst * DIM);
 #pragma unroll
     for (int c = 0; c < PER; c++) {

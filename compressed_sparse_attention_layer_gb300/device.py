@@ -130,18 +130,27 @@ class DeviceWorkload:
         self.swa_codes[l] = codes
         self.swa_scales[l] = scales
 
-    def swa(self, l) -> csa2.Swa:
-        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l])
+    def swa(self, l, new_rows=None) -> csa2.Swa:
+        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows)
 
-    def io(self, l, prof=None) -> csa2.LayerIO:
+    def swa_new_rows(self, l) -> torch.Tensor:
+        """fp32 [B][512]: the window row of each sequence's decode token (nq = 1)."""
+        wl, dev = self.wl, self.dev
+        assert wl.nq == 1
+        return torch.cat([_dev_normal_bf16(wl._sid(T_SWA, b, l), int(wl.q_pos(b)[0]) * 512, 512, dev).float()
+                          for b in range(wl.batch)]).view(wl.batch, 512)
+
+    def io(self, l, prof=None, new_rows=None) -> csa2.LayerIO:
         qi = self.qi.get(l, self.dummy_qi)
         w = self.w.get(l, self.dummy_w)
-        return csa2.layer_io(self.q[l], qi, w, self.swa(l), 1.0, self.idx, self.pool, self.pool_len,
+        return csa2.layer_io(self.q[l], qi, w, self.swa(l, new_rows), 1.0, self.idx, self.pool, self.pool_len,
                              self.o[l], self.lse[l], prof=prof)
 
-    def run_layer(self, l, stream=None, prof=None):
+    def run_layer(self, l, stream=None, prof=None, new_rows=None):
+        """new_rows: optional window rows of the decode tokens, quantised into the
+        ring by the layer call itself (see csa2_swa.new_rows)."""
         mode = csa2.MODES[self.wl.layers[l]]
-        csa2.csa2_layer(mode, self.cstruct, self.batch, self.io(l, prof), self.workspace, stream=stream)
+        csa2.csa2_layer(mode, self.cstruct, self.batch, self.io(l, prof, new_rows), self.workspace, stream=stream)
 
     def run(self, stream=None, on_layer=None):
         for l in self.layers:

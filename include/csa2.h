@@ -137,6 +137,12 @@ typedef struct csa2_swa {
     int32_t        rows;         /* ring capacity, >= 128                     */
     int32_t        pad_;
     const int64_t *start;        /* [B] replay start s, or NULL               */
+    const float   *new_rows;     /* NULL, or fp32 [B][512] (decode, Q = 1):   */
+                                 /* the window row of each query's own token, */
+                                 /* quantised by the attention call itself    */
+                                 /* into ring row q_pos % rows (codes and     */
+                                 /* scale written, as csa2_quant_fp8 would)   */
+                                 /* before it is attended; 16-byte aligned    */
 } csa2_swa;
 
 /* Per-layer inputs, outputs and carried selection state for csa2_layer. */

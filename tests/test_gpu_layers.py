@@ -145,3 +145,26 @@ def test_layer_decode_1m_sampled():
         assert np.isin(wl.planted_positions(b), pool[b][: pool_len[b]]).all()
     del dw
     torch.cuda.empty_cache()
+
+
+def test_window_row_quantised_inside_the_attention_call():
+    """csa2_swa.new_rows: the decode token's window row quantised by the layer
+    call itself gives the same ring bytes and the same o / lse, bit for bit, as
+    csa2_quant_fp8 followed by the layer."""
+    wl = W.Workload("fused_swa", 71, 3, [5000, 300, 77], 1, ["full", "reuse"])
+    ref = DeviceWorkload(wl)                      # its rings already hold the decode tokens' rows
+    ref.run()
+    fused = DeviceWorkload(wl)
+    R = wl.swa_rows
+    for l in fused.layers:
+        for b in range(wl.batch):
+            t = int(wl.q_pos(b)[0])
+            fused.swa_codes[l][b, t % R] = 0x77       # stale bytes the call must overwrite
+            fused.swa_scales[l][b, t % R] = 3.0
+        fused.run_layer(l, new_rows=fused.swa_new_rows(l))
+    torch.cuda.synchronize()
+    for l in fused.layers:
+        assert torch.equal(fused.swa_codes[l], ref.swa_codes[l]), l
+        assert torch.equal(fused.swa_scales[l].view(torch.int32), ref.swa_scales[l].view(torch.int32)), l
+        assert torch.equal(fused.o[l].view(torch.int32), ref.o[l].view(torch.int32)), l
+        assert torch.equal(fused.lse[l].view(torch.int32), ref.lse[l].view(torch.int32)), l
