@@ -227,6 +227,10 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const uint32_t v = e2m1x2_to_bf16x2((uint32_t)ch >> 3);
         reinterpret_cast<uint4 *>(&S.e2m1_pair[0][0])[ch] = make_uint4(v, v, v, v);
     }
+    // Launched as a programmatic dependent of the previous kernel on the stream:
+    // everything above touches only this CTA's own state; inputs are read below,
+    // after that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
     constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
@@ -505,6 +509,8 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ 
                                                       const float *__restrict__ part_ml, int nchunks,
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
+    // the next kernel on the stream may be scheduled now; it waits for this grid
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t r = blockIdx.x;
     const int tid = threadIdx.x & 127;
@@ -572,8 +578,24 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
         cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         attr = true;
     }
-    k_attn_tc<<<dim3((unsigned)(AC_CL * nchunks), (unsigned)rows), AC_THREADS, smem, st>>>(
-        c, bt, q, sm_scale, idx, k, swa, part_o, part_ml, nchunks);
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t ac = {};
+        ac.gridDim = dim3((unsigned)(AC_CL * nchunks), (unsigned)rows);
+        ac.blockDim = dim3(AC_THREADS);
+        ac.dynamicSmemBytes = smem;
+        ac.stream = st;
+        ac.attrs = pdl;
+        ac.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&ac, k_attn_tc, c, bt, q, sm_scale, idx, k, swa, part_o, part_ml,
+                                                 nchunks);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return CSA2_ERR_CUDA;
+        }
+    }
     int s = launch_status();
     if (s) return s;
     cudaLaunchConfig_t cfg = {};

@@ -560,6 +560,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__rest
                                                               int32_t *__restrict__ out)
 {
     __shared__ RsShared sh;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // a dependent waits for this grid
     const int64_t r = blockIdx.x;
     int64_t n64 = len[r];
     n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
