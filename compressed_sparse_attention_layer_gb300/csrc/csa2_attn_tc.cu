@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     // Launched as a programmatic dependent of the previous kernel on the stream:
     // everything above touches only this CTA's own state; inputs are read below,
     // after that kernel has completed.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
 
     // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
     constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
@@ -456,7 +456,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     tc::tc_fence_before();
     cluster_sync();                                // P complete everywhere; partials no longer read
     tc::tc_fence_after();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // let the merge kernel be scheduled
+    pdl_launch_dependents();                       // let the merge kernel be scheduled
 
     // ---- [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T: M-tiles of 128 dims, K = 128 keys,
     //      N = 128; tile mt in columns 128 mt .. +127 (S has been read out)
@@ -510,8 +510,8 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ 
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
     // the next kernel on the stream may be scheduled now; it waits for this grid
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     const int tid = threadIdx.x & 127;
     const int h = blockIdx.y * 2 + (threadIdx.x >> 7);

@@ -186,6 +186,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
         tc::fence_mbar_init();
     }
     if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_ACC * 128);
+    // launched as a programmatic dependent: the set-up above is local; the
+    // batch, cache and queries are read below, once the previous kernel is done
+    pdl_launch_dependents();
+    pdl_wait();
 
     int64_t g0, g1;
     if (PERSIST) {
@@ -463,12 +467,12 @@ int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t 
     const int64_t tiles_row = std::max<int64_t>(1, (bt.max_entries + F8_TILE - 1) / F8_TILE);
     if (rows <= F8_PERSIST_ROWS) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)rows * tiles_row, g_sms));
-        k_index_f8<true><<<grid, F8_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
-    } else {
-        const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + rows - 1) / rows));
-        k_index_f8<false><<<dim3(x, rows), F8_THREADS, smem, st>>>(c, bt, qi, w, scores, block_max, n_visible, ld);
+        return launch_pdl(k_index_f8<true>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, scores, block_max,
+                          n_visible, ld);
     }
-    return launch_status();
+    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + rows - 1) / rows));
+    return launch_pdl(k_index_f8<false>, dim3(x, rows), dim3(F8_THREADS), smem, st, c, bt, qi, w, scores, block_max,
+                      n_visible, ld);
 }
 
 }  // namespace csa2

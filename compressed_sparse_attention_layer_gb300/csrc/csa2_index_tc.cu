@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(TS_THREADS) k_index_tc(csa2_cache c, csa2_batc
         tc::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&S.tmem, 64);
+    pdl_launch_dependents();                      // programmatic dependent launch: inputs are read
+    pdl_wait();                                   // below, once the previous kernel is done
 
     // ---- this CTA's range of global tiles
     int64_t g0, g1;
@@ -366,14 +368,12 @@ static int launch_index(const csa2_cache &c, const csa2_batch &bt, const uint16_
     const int64_t tiles_row = std::max<int64_t>(1, (per_row + TS_TILE - 1) / TS_TILE);
     if (rows <= TS_PERSIST_ROWS) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(rows * tiles_row, (int64_t)g_num_sms * per_sm));
-        k_index_tc<true, POOL><<<grid, TS_THREADS, smem, st>>>(c, bt, qi, w, pool, pool_len, scores, block_max,
-                                                               n_visible, ld);
-    } else {
-        const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_num_sms * per_sm + rows - 1) / rows));
-        k_index_tc<false, POOL><<<dim3(x, rows), TS_THREADS, smem, st>>>(c, bt, qi, w, pool, pool_len, scores,
-                                                                        block_max, n_visible, ld);
+        return launch_pdl(k_index_tc<true, POOL>, dim3(grid), dim3(TS_THREADS), smem, st, c, bt, qi, w, pool,
+                          pool_len, scores, block_max, n_visible, ld);
     }
-    return launch_status();
+    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_num_sms * per_sm + rows - 1) / rows));
+    return launch_pdl(k_index_tc<false, POOL>, dim3(x, rows), dim3(TS_THREADS), smem, st, c, bt, qi, w, pool, pool_len,
+                      scores, block_max, n_visible, ld);
 }
 
 // a7: a Reindex layer rescoring its candidate pool ("DeepSeek-V4.1-Flash 架构详解" §3.2).

@@ -22,11 +22,41 @@ inline int launch_status()
     return CSA2_OK;
 }
 
+// Launch `kernel` as a programmatic dependent of the previous kernel on the
+// stream: its CTAs may start while that kernel drains and must execute
+// pdl_wait() before reading anything it wrote.
+template <class K, class... Args>
+inline int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args)
+{
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 inline int ceil_div_i(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 inline bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 // ---------------------------------------------------------------- device side
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now (it still waits for this grid before reading its results) /
+// wait until the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __device__ __forceinline__ void flag(int32_t *status, int32_t bit)

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) k_compress(const uint16_t *__restrict__ C
                                                   const float *__restrict__ bias, int m,
                                                   int64_t n_ent, float *__restrict__ out)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t total = n_ent * CSA2_HEAD_DIM;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -70,6 +72,8 @@ __global__ void __launch_bounds__(256) k_quant_mxfp4(const float *__restrict__ x
                                                      uint8_t *__restrict__ scales, int64_t num_slots,
                                                      int32_t *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     if (t >= n * 16) return;
     const int64_t r = t >> 4;
@@ -118,6 +122,8 @@ __global__ void __launch_bounds__(256) k_quant_fp8(const float *__restrict__ x, 
                                                    float *__restrict__ scales, int64_t num_slots,
                                                    int32_t *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int PER = DIM / 128;   // float4 chunks per lane
     const int lane = threadIdx.x & 31;
     const int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -157,8 +163,7 @@ int launch_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int
     if (n_ent == 0) return CSA2_OK;
     const int64_t total = n_ent * CSA2_HEAD_DIM;
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 152 * 16);
-    k_compress<<<grid, 256, 0, st>>>(C, Z, bias, m, n_ent, out);
-    return launch_status();
+    return launch_pdl(k_compress, dim3(grid), dim3(256), 0, st, C, Z, bias, m, n_ent, out);
 }
 
 int launch_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
@@ -166,9 +171,8 @@ int launch_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t 
 {
     if (n == 0) return CSA2_OK;
     const int64_t threads = n * 16;
-    k_quant_mxfp4<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(x, n, slots, codes, scales,
-                                                                     num_slots, status);
-    return launch_status();
+    return launch_pdl(k_quant_mxfp4, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, x, n, slots, codes,
+                      scales, num_slots, status);
 }
 
 int launch_quant_fp8(const float *x, int64_t n, int dim, const int64_t *slots, uint8_t *codes,
@@ -177,10 +181,9 @@ int launch_quant_fp8(const float *x, int64_t n, int dim, const int64_t *slots, u
     if (n == 0) return CSA2_OK;
     const unsigned grid = (unsigned)((n * 32 + 255) / 256);
     if (dim == 128)
-        k_quant_fp8<128><<<grid, 256, 0, st>>>(x, n, slots, codes, scales, num_slots, status);
-    else
-        k_quant_fp8<512><<<grid, 256, 0, st>>>(x, n, slots, codes, scales, num_slots, status);
-    return launch_status();
+        return launch_pdl(k_quant_fp8<128>, dim3(grid), dim3(256), 0, st, x, n, slots, codes, scales, num_slots,
+                          status);
+    return launch_pdl(k_quant_fp8<512>, dim3(grid), dim3(256), 0, st, x, n, slots, codes, scales, num_slots, status);
 }
 
 }  // namespace csa2

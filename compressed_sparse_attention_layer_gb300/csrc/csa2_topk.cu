@@ -272,6 +272,8 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(const float *__restrict__ s
 {
     extern __shared__ uint32_t keys[];
     __shared__ TkShared sh;
+    pdl_launch_dependents();
+    pdl_wait();
     cg::cluster_group cluster = cg::this_cluster();
     const int64_t r = blockIdx.x / CL;
     const int q = (int)cluster.block_rank();
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
 {
     extern __shared__ uint32_t keys[];
     __shared__ TkShared sh;
+    pdl_launch_dependents();
+    pdl_wait();
     cg::cluster_group cluster = cg::this_cluster();
     const int64_t r = blockIdx.x / CL;
     const int q = (int)cluster.block_rank();
@@ -560,7 +564,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__rest
                                                               int32_t *__restrict__ out)
 {
     __shared__ RsShared sh;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // a dependent waits for this grid
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t r = blockIdx.x;
     int64_t n64 = len[r];
     n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
@@ -592,13 +597,15 @@ static int launch_cluster(K kernel, int cl, int64_t ld, int32_t rows, cudaStream
     cfg.blockDim = dim3(TK_THREADS);
     cfg.dynamicSmemBytes = (size_t)((((ld + cl - 1) / cl + 3) & ~(int64_t)3) * 4);
     cfg.stream = st;
-    cudaLaunchAttribute at[1];
+    cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)cl;
     at[0].val.clusterDim.y = 1;
     at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // a programmatic dependent
+    at[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     if (e != cudaSuccess) {
         set_cuda_error(e);
@@ -637,8 +644,8 @@ int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t row
 {
     if (rows == 0) return CSA2_OK;
     if (ld <= RS_MAX) {
-        k_topk_rows<<<(unsigned)rows, RS_THREADS, 0, st>>>(scores, 0, nullptr, ld, len, cand, k, out);
-        return launch_status();
+        return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, (int64_t)0,
+                          (const int32_t *)nullptr, ld, len, cand, (int)k, out);
     }
     switch (topk_cluster_for(ld)) {
     case 1: return topk_cl<1>(scores, ld, len, rows, cand, k, out, st);
@@ -656,8 +663,8 @@ int launch_topk_pool(const float *scores, int64_t ld_scores, const int32_t *pool
 {
     if (rows == 0) return CSA2_OK;
     if (ld_pool > RS_MAX) return CSA2_ERR_SHAPE;
-    k_topk_rows<<<(unsigned)rows, RS_THREADS, 0, st>>>(scores, ld_scores, pool, ld_pool, pool_len, pool, k, out);
-    return launch_status();
+    return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, ld_scores, pool, ld_pool,
+                      pool_len, pool, (int)k, out);
 }
 
 int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
