@@ -152,7 +152,7 @@ class DecodeStep:
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 3 + sum({"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers)
+        self.launches = 3 + sum({"full": 6, "reindex": 4, "reuse": 2}[m] for m in wl.layers)
         # the step's host inputs for the end-to-end leg (new token + every layer's queries)
         self.h2d = [(self.C_new, None), (self.ik_new, None)]
         for l in dw.layers:

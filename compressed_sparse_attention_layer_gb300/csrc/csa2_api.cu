@@ -17,6 +17,10 @@ int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, fl
                      cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
                       float *, int32_t *, int64_t, cudaStream_t);
+int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, const int32_t *, int64_t, uint8_t *,
+                       float *, cudaStream_t);
+int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const uint16_t *, const float *,
+                       const int32_t *, int64_t, float *, cudaStream_t);
 int launch_index_pool(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
                            const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
@@ -79,9 +83,11 @@ static inline int64_t score_ld(const csa2_batch *b)
 
 // FULL workspace: scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
 //                 | attention workspace
-// REINDEX:        pool scores [rows][16384] | attention workspace
+// REINDEX:        pool scores [rows][16384] | pool key codes [rows][16384][128]
+//                 | pool key scales [rows][16384] | attention workspace
 struct LayerWs {
-    float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr;
+    float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr, *pool_kscales = nullptr;
+    uint8_t *pool_kcodes = nullptr;
     int32_t *n_visible = nullptr;
     void *attn = nullptr;
     size_t attn_bytes = 0, total = 0;
@@ -104,7 +110,13 @@ static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
         w.block_max = (float *)take((size_t)rows * (ld / 8) * 4);
         w.n_visible = (int32_t *)take((size_t)rows * 4);
     }
-    if (mode == CSA2_MODE_REINDEX) w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+    if (mode == CSA2_MODE_REINDEX) {
+        w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+        // the pool's keys, when the caller carries no copy of them (the size
+        // query counts them: the layer may be called either way)
+        w.pool_kcodes = (uint8_t *)take((size_t)rows * CSA2_POOL_MAX * 128);
+        w.pool_kscales = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+    }
     w.attn_bytes = attn_workspace_bytes(rows);
     w.attn = take(w.attn_bytes);
     w.total = off;
@@ -252,6 +264,8 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if ((s = check_swa(&io->swa, batch))) return s;
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
+    if (!io->pool_codes != !io->pool_scales) return CSA2_ERR_NULL;
+    if (io->pool_codes && (!aligned(io->pool_codes, 16) || !aligned(io->pool_scales, 16))) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
     LayerWs ws = layer_ws(mode, batch, workspace);
@@ -288,11 +302,26 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
         // a6: Top-512 of the pool, its scores read from the scan's score rows
         if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st)))
             return s;
+        // the pool's keys for the Reindex layers that follow, when the caller carries them
+        if (io->pool_codes &&
+            (s = launch_gather_pool(*cache, *batch, io->pool, io->pool_len, CSA2_POOL_MAX, io->pool_codes,
+                                    io->pool_scales, st)))
+            return s;
     } else if (mode == CSA2_MODE_REINDEX) {
         // a7: rescore the pool with this layer's indexer query, Top-512
         if ((s = prof(io->prof_begin))) return s;
-        if ((s = launch_index_pool(*cache, *batch, io->qi, io->w, io->pool, io->pool_len, CSA2_POOL_MAX,
-                                        ws.pool_scores, st)))
+        // the pool's keys in dense rows (the Full layer's copy, else copied here),
+        // scanned like the cache
+        const uint8_t *kc = io->pool_codes;
+        const float *ks = io->pool_scales;
+        if (!kc) {
+            if ((s = launch_gather_pool(*cache, *batch, io->pool, io->pool_len, CSA2_POOL_MAX, ws.pool_kcodes,
+                                        ws.pool_kscales, st)))
+                return s;
+            kc = ws.pool_kcodes;
+            ks = ws.pool_kscales;
+        }
+        if ((s = launch_index_dense(kc, ks, *batch, io->qi, io->w, io->pool_len, CSA2_POOL_MAX, ws.pool_scores, st)))
             return s;
         if ((s = prof(io->prof_end))) return s;
         if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st)))

@@ -59,6 +59,7 @@ struct F8Smem {
     uint32_t tmem;
     int abort;
     int32_t prefix[F8_PERSIST_ROWS + 1];
+    int32_t rowcnt[F8_PERSIST_ROWS];       // entries scored per row (persistent grid)
 };
 
 // Scales copied for the entries of a page whose id lies outside the cache:
@@ -156,10 +157,26 @@ __device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const
     }
 }
 
-template <bool PERSIST>
+// Entries scored by row r: every visible entry of the paged cache, or (DENSE)
+// the first pool_len[r] of a dense per-row copy of a candidate pool's keys.
+template <bool DENSE>
+__device__ __forceinline__ int64_t f8_row_entries(const csa2_batch &bt, const int32_t *pool_len, int64_t ld, int r)
+{
+    if (!DENSE) return visible_entries(bt, r);
+    const int64_t n = pool_len[r];
+    return n < 0 ? 0 : (n > ld ? ld : n);
+}
+
+// DENSE = false: row r scans the visible entries of the paged cache c.
+// DENSE = true: row r scans entries 0 .. pool_len[r] of rows of ld slots
+// stored one after the other in c.ik_codes / c.ik_scales (page j of row r is
+// page r * ld / 64 + j; no block table), scores only.
+template <bool PERSIST, bool DENSE>
 __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_batch bt,
                                                             const uint16_t *__restrict__ qi,
-                                                            const float *__restrict__ w, float *__restrict__ scores,
+                                                            const float *__restrict__ w,
+                                                            const int32_t *__restrict__ pool_len,
+                                                            float *__restrict__ scores,
                                                             float *__restrict__ block_max,
                                                             int32_t *__restrict__ n_visible, int64_t ld)
 {
@@ -191,12 +208,13 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
     pdl_launch_dependents();
     pdl_wait();
 
-    int64_t g0, g1;
+    int64_t g0, g1, nv_row = 0;                   // nv_row: the per-row grid's entry count
     if (PERSIST) {
         for (int r = tid; r < rows; r += F8_THREADS) {
-            const int64_t nv = visible_entries(bt, r);
+            const int64_t nv = f8_row_entries<DENSE>(bt, pool_len, ld, r);
+            S.rowcnt[r] = (int32_t)nv;
             S.prefix[r + 1] = (int32_t)((nv + F8_TILE - 1) / F8_TILE);
-            if (blockIdx.x == 0 && n_visible) n_visible[r] = (int32_t)nv;
+            if (!DENSE && blockIdx.x == 0 && n_visible) n_visible[r] = (int32_t)nv;
         }
         __syncthreads();
         if (tid == 0) {
@@ -209,9 +227,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
         g1 = total * (blockIdx.x + 1) / gridDim.x;
     } else {
         const int r = blockIdx.y;
-        const int64_t nv = visible_entries(bt, r);
+        const int64_t nv = f8_row_entries<DENSE>(bt, pool_len, ld, r);
         const int64_t T = (nv + F8_TILE - 1) / F8_TILE;
-        if (blockIdx.x == 0 && tid == 0 && n_visible) n_visible[r] = (int32_t)nv;
+        nv_row = nv;
+        if (!DENSE && blockIdx.x == 0 && tid == 0 && n_visible) n_visible[r] = (int32_t)nv;
         g0 = T * blockIdx.x / gridDim.x;
         g1 = T * (blockIdx.x + 1) / gridDim.x;
     }
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
             nt = g1 - g;
         }
         const int b = r / bt.nq;
-        const int64_t nvis = visible_entries(bt, r);
+        const int64_t nvis = PERSIST ? (int64_t)S.rowcnt[r] : nv_row;   // entries scored
 
         if (warp < 4) {
             // ---------------- producers: page ids of 32 tiles at a time (one lane per
@@ -255,7 +274,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         const int64_t e0 = e + 64 * h;
                         my_pg[h] = -2;                                // -2: beyond the visible entries
                         if (i + lane < nt && e0 < nvis) {
-                            const int32_t pg = __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
+                            const int32_t pg = DENSE ? (int32_t)(r * (ld >> 6) + (e0 >> 6))
+                                                     : __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
                             my_pg[h] = pg >= 0 && ((int64_t)pg + 1) * CSA2_PAGE <= c.num_slots ? pg : -1;
                         }
                     }
@@ -417,7 +437,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                     if (sc_cur != -INFINITY) sc = ((part[0] + part[1]) + (part[2] + part[3])) * sc_cur;
                     if (scores) scores[(int64_t)r * ld + p] = sc;
                 }
-                if (block_max) {
+                if (!DENSE && block_max) {
                     float m = valid ? sc : -INFINITY;
 #pragma unroll
                     for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -447,8 +467,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 static int g_sms = 0;
 static std::once_flag g_sms_once;
 
-int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
+template <bool DENSE>
+static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                     const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
+                     cudaStream_t st)
 {
     std::call_once(g_sms_once, [] {
         int dev = 0;
@@ -460,19 +482,87 @@ int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t 
     const size_t smem = sizeof(F8Smem) + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_index_f8<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_index_f8<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_index_f8<true, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_index_f8<false, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
-    const int64_t tiles_row = std::max<int64_t>(1, (bt.max_entries + F8_TILE - 1) / F8_TILE);
+    const int64_t per_row = DENSE ? ld : bt.max_entries;
+    const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
     if (rows <= F8_PERSIST_ROWS) {
         const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)rows * tiles_row, g_sms));
-        return launch_pdl(k_index_f8<true>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, scores, block_max,
-                          n_visible, ld);
+        return launch_pdl(k_index_f8<true, DENSE>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
+                          scores, block_max, n_visible, ld);
     }
     const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + rows - 1) / rows));
-    return launch_pdl(k_index_f8<false>, dim3(x, rows), dim3(F8_THREADS), smem, st, c, bt, qi, w, scores, block_max,
-                      n_visible, ld);
+    return launch_pdl(k_index_f8<false, DENSE>, dim3(x, rows), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
+                      scores, block_max, n_visible, ld);
+}
+
+int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
+{
+    return launch_f8<false>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st);
+}
+
+// Dense copy of the indexer keys of each row's candidate pool: slot e of row r
+// gets the codes and scale of position pool[r][e] (one thread per 16-byte
+// chunk, all of a row's lookups in flight at once).  A position that is not a
+// visible entry, or whose page id lies outside the cache, gets zero codes and
+// a -inf scale (it scores -inf) and is flagged.
+__global__ void __launch_bounds__(256) k_gather_pool(csa2_cache c, csa2_batch bt, const int32_t *__restrict__ pool,
+                                                     const int32_t *__restrict__ pool_len, int64_t ld,
+                                                     uint8_t *__restrict__ codes, float *__restrict__ scales)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t r = blockIdx.y;
+    const int64_t t = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const int64_t e = t >> 3;
+    const int ch = (int)(t & 7);
+    int64_t n = pool_len[r];
+    n = n < 0 ? 0 : (n > ld ? ld : n);
+    if (e >= n) return;
+    const int b = (int)(r / bt.nq);
+    const int64_t nvis = visible_entries(bt, r);
+    const int32_t p = __ldg(pool + r * ld + e);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    float s = -INFINITY;
+    if (p >= 0 && p < nvis) {
+        const int32_t pg = __ldg(c.block_table + (int64_t)b * c.max_pages + (p >> 6));
+        if (pg >= 0 && ((int64_t)pg + 1) * CSA2_PAGE <= c.num_slots) {
+            const int64_t slot = (int64_t)pg * CSA2_PAGE + (p & 63);
+            v = __ldg(reinterpret_cast<const uint4 *>(c.ik_codes + slot * 128) + ch);
+            s = __ldg(c.ik_scales + slot);
+        } else if (ch == 0) {
+            flag(c.status, CSA2_DEV_BAD_PAGE);
+        }
+    } else if (ch == 0) {
+        flag(c.status, CSA2_DEV_BAD_INDEX);
+    }
+    reinterpret_cast<uint4 *>(codes + (r * ld + e) * 128)[ch] = v;
+    if (ch == 0) scales[r * ld + e] = s;
+}
+
+int launch_gather_pool(const csa2_cache &c, const csa2_batch &bt, const int32_t *pool, const int32_t *pool_len,
+                       int64_t ld, uint8_t *codes, float *scales, cudaStream_t st)
+{
+    const int64_t rows = (int64_t)bt.batch * bt.nq;
+    if (rows == 0) return CSA2_OK;
+    return launch_pdl(k_gather_pool, dim3((unsigned)((ld * 8 + 255) / 256), (unsigned)rows), dim3(256), 0, st, c, bt,
+                      pool, pool_len, ld, codes, scales);
+}
+
+// Scores of the dense pool copy (rows of ld slots, codes [rows][ld][128] and
+// scales [rows][ld]) for slots 0 .. pool_len[r] of each row.
+int launch_index_dense(const uint8_t *codes, const float *scales, const csa2_batch &bt, const uint16_t *qi,
+                       const float *w, const int32_t *pool_len, int64_t ld, float *scores, cudaStream_t st)
+{
+    if (ld % CSA2_PAGE) return CSA2_ERR_SHAPE;
+    csa2_cache d = {};
+    d.ik_codes = const_cast<uint8_t *>(codes);
+    d.ik_scales = const_cast<float *>(scales);
+    d.num_slots = (int64_t)bt.batch * bt.nq * ld;
+    return launch_f8<true>(d, bt, qi, w, pool_len, scores, nullptr, nullptr, ld, st);
 }
 
 }  // namespace csa2

@@ -23,7 +23,11 @@ def _dev_normal_bf16(stream, start, count, dev, sigma=1.0):
 
 
 class DeviceWorkload:
-    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None):
+    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None, carry_pool_keys=True):
+        """carry_pool_keys: give the layers a carried copy of the pool's indexer keys
+        (written by the Full layer, read by Reindex layers) when the pattern has
+        Reindex layers; otherwise every Reindex call copies them into its workspace."""
+        self.carry_pool_keys = carry_pool_keys
         self.wl = wl
         self.dev = torch.device(device)
         self.rows = wl.batch * wl.nq
@@ -93,6 +97,10 @@ class DeviceWorkload:
         self.idx = torch.full((R, csa2.TOPK), -1, dtype=torch.int32, device=dev)
         self.pool = torch.full((R, csa2.POOL_MAX), -1, dtype=torch.int32, device=dev)
         self.pool_len = torch.zeros((R,), dtype=torch.int32, device=dev)
+        self.pool_keys = None
+        if self.carry_pool_keys and "reindex" in wl.layers:
+            self.pool_keys = (torch.empty((R, csa2.POOL_MAX, 128), dtype=torch.uint8, device=dev),
+                              torch.empty((R, csa2.POOL_MAX), dtype=torch.float32, device=dev))
         self.o = {l: torch.empty((R, 64, 512), dtype=torch.float32, device=dev) for l in self.layers}
         self.lse = {l: torch.empty((R, 64), dtype=torch.float32, device=dev) for l in self.layers}
         ws = max(csa2.csa2_layer_workspace_size(m, self.batch) for m in (0, 1, 2))
@@ -144,7 +152,7 @@ class DeviceWorkload:
         qi = self.qi.get(l, self.dummy_qi)
         w = self.w.get(l, self.dummy_w)
         return csa2.layer_io(self.q[l], qi, w, self.swa(l, new_rows), 1.0, self.idx, self.pool, self.pool_len,
-                             self.o[l], self.lse[l], prof=prof)
+                             self.o[l], self.lse[l], prof=prof, pool_keys=self.pool_keys)
 
     def run_layer(self, l, stream=None, prof=None, new_rows=None):
         """new_rows: optional window rows of the decode tokens, quantised into the

@@ -166,6 +166,11 @@ typedef struct csa2_layer_io {
                                     as an external node when captured; NULL
                                     for none                                   */
     void           *prof_end;    /* optional cudaEvent_t recorded just after it */
+    uint8_t        *pool_codes;  /* optional [B*Q][16384][128] and            */
+    float          *pool_scales; /* [B*Q][16384]: the indexer keys of the pool,
+                                    copied by FULL next to the pool and read by
+                                    REINDEX (both NULL: each REINDEX call copies
+                                    them into its workspace); 16-byte aligned   */
 } csa2_layer_io;
 
 /* ---- a1: compressor ------------------------------------------------------
