@@ -59,18 +59,20 @@ static_assert(AC_THREADS / 16 == AC_OWN, "sixteen threads per owned head");
 
 struct AcSmem {
     uint8_t k[AC_SLABS * AC_KEYS * 128];           // [slab of 64 dims][128 keys][128 B]
-    union {
-        uint8_t q[AC_SLABS * CSA2_HEADS * 128];    // [slab][64 heads][128 B]
-        uint8_t p[2 * 2 * CSA2_HEADS * 128];       // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB
-    } u;                                           // P arrives after the first cluster barrier,
-                                                   // when this CTA's first product is done with Q
+    uint8_t q[AC_SLABS * CSA2_HEADS * 128];        // [slab][64 heads][128 B]
+    uint8_t p[2 * 2 * CSA2_HEADS * 128];           // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB:
+                                                   // this CTA's heads written here, the others' rows
+                                                   // copied in by their owners
     float ps[AC_CL][AC_OWN][AC_KEYS];              // [source CTA][owned head][key] partial logits 32 KB
     uint32_t e2m1_pair[256][32];                   // byte -> bf16x2 of its two E2M1 codes, one
                                                    // copy per lane (bank = lane: no conflicts)  32 KB
     float kscale[AC_KEYS];                         // window row scale (1 for entries), -1: no key
-    uint64_t mbar;
+    uint64_t mbar;                                 // the products' commits
+    uint64_t pbar;                                 // the other CTAs' probability rows have landed
     uint32_t tmem;
 };
+constexpr uint32_t AC_P_ROWS_BYTES = AC_OWN * 128;                       // one CTA's rows of one half, one slab
+constexpr uint32_t AC_P_IN_BYTES = (AC_CL - 1) * 4 * AC_P_ROWS_BYTES;   // probability bytes received
 
 // ---------------------------------------------------------------- cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank()
@@ -98,18 +100,15 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_u4(uint32_t addr, const uint4 &v)
+// Bulk copy of `bytes` from this CTA's shared memory to shared memory of a CTA
+// of the cluster (cluster address), completing `bytes` on the mbarrier at the
+// cluster address `bar` (in the destination CTA).  Async proxy on both ends.
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
 {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
                  : "memory");
-}
-
-// Order this thread's generic writes to shared memory anywhere in the cluster
-// before later tensor-core (async proxy) reads of it.
-__device__ __forceinline__ void fence_proxy_async_cluster()
-{
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // a (bf16x2) * b (bf16x2), exact when the products are representable.
@@ -218,6 +217,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
     if (tid == 0) {
         tc::mbar_init(&S.mbar, 1);
+        tc::mbar_init(&S.pbar, 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&S.tmem, AC_TMEM_COLS);
@@ -330,7 +330,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int e = tid + AC_THREADS * i;
-        *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
+        *reinterpret_cast<uint4 *>(S.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
     }
     if (hf == 0) {
         S.kscale[key] = valid ? kscale : -1.0f;
@@ -353,7 +353,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
     // ---- partial S^T = K_d Q_d^T over this CTA's dims
     if (tid == 0) {
-        const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.u.q);
+        const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.q);
 #pragma unroll
         for (int kk = 0; kk < AC_DIMS / 16; kk++) {   // 16 dims per step
             const uint32_t off = (uint32_t)(kk >> 2) * (AC_KEYS * 128) + (uint32_t)(kk & 3) * 32u;
@@ -388,6 +388,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         flag(c.status, CSA2_DEV_TIMEOUT);
     }
     cluster_sync();                                // the partials of the owned heads are here
+    if (tid == 0) tc::mbar_arrive_expect_tx(&S.pbar, AC_P_IN_BYTES);   // the other CTAs' probability rows
 
     // ---- owned heads AC_OWN dq .. : sixteen threads per head, eight
     //      consecutive keys per thread
@@ -439,30 +440,44 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const uint32_t chunk16 = (uint32_t)((part & 7) ^ (h & 7)) << 4;
         const uint32_t off_hi = (uint32_t)(part >> 3) * (2 * CSA2_HEADS * 128) + (uint32_t)h * 128u + chunk16;
         const uint32_t off_lo = off_hi + CSA2_HEADS * 128;
-        const uint32_t p0 = tc::smem_u32(S.u.p);
-        const uint4 vhi = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
-        const uint4 vlo = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
-#pragma unroll
-        for (int dst = 0; dst < AC_CL; dst++) {
-            st_cluster_u4(cluster_map(p0 + off_hi, (uint32_t)dst), vhi);
-            st_cluster_u4(cluster_map(p0 + off_lo, (uint32_t)dst), vlo);
-        }
+        *reinterpret_cast<uint4 *>(S.p + off_hi) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
+        *reinterpret_cast<uint4 *>(S.p + off_lo) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         if (part == 0 && !fail) {
             part_ml[(base + h) * 2] = mx;
             part_ml[(base + h) * 2 + 1] = l;
         }
     }
-    fence_proxy_async_cluster();
-    tc::tc_fence_before();
-    cluster_sync();                                // P complete everywhere; partials no longer read
+    // this CTA's rows of P, written through the generic proxy, are read by the
+    // tensor core here and by the bulk copies to the other CTAs (async proxy)
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    bool p_ok = true;
+    if (tid == 0) {
+        // rows AC_OWN dq .. of each half (hi, lo) of each 64-key slab to every other CTA,
+        // completing on that CTA's pbar
+        const uint32_t p0 = tc::smem_u32(S.p), pb = tc::smem_u32(&S.pbar);
+#pragma unroll
+        for (int dst = 0; dst < AC_CL; dst++) {
+            if (dst == (int)dq) continue;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; q4++) {       // (slab, half) = (q4 >> 1, q4 & 1)
+                const uint32_t off = (uint32_t)(q4 >> 1) * (2 * CSA2_HEADS * 128) +
+                                     ((uint32_t)(q4 & 1) * CSA2_HEADS + AC_OWN * dq) * 128u;
+                bulk_to_peer(cluster_map(p0 + off, (uint32_t)dst), p0 + off, AC_P_ROWS_BYTES,
+                             cluster_map(pb, (uint32_t)dst));
+            }
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        p_ok = tc::mbar_wait(&S.pbar, 0);          // the other CTAs' rows have landed here
+    }
+    const bool p_fail = __syncthreads_or(!p_ok);
     tc::tc_fence_after();
     pdl_launch_dependents();                       // let the merge kernel be scheduled
 
     // ---- [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T: M-tiles of 128 dims, K = 128 keys,
     //      N = 128; tile mt in columns 128 mt .. +127 (S has been read out)
-    if (tid == 0 && !fail) {
-        tc::fence_proxy_async_smem();
-        const uint32_t k0 = tc::smem_u32(S.k), p0 = tc::smem_u32(S.u.p);
+    if (tid == 0 && !fail && !p_fail) {
+        const uint32_t k0 = tc::smem_u32(S.k), p0 = tc::smem_u32(S.p);
 #pragma unroll
         for (int mt = 0; mt < AC_MT; mt++) {
 #pragma unroll
@@ -476,7 +491,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         }
         tc::mma_commit(&S.mbar);
     }
-    if (!fail) {
+    if (p_fail && tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
+    if (!fail && !p_fail) {
         const bool fail2 = __syncthreads_or(!tc::mbar_wait(&S.mbar, 1));
         tc::tc_fence_after();
         if (!fail2) {
@@ -495,6 +511,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
             flag(c.status, CSA2_DEV_TIMEOUT);
         }
     }
+    // the bulk copies out of this CTA's shared memory have finished reading it
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
