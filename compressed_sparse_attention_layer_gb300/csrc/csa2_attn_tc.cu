@@ -16,13 +16,15 @@
 //      the window's fp32 row scale is applied to the logit and to the
 //      probability instead;
 //   2. partial S^T[128 keys x 64 heads] = K_d Q_d^T over its dims (M = keys,
-//      N = heads); each 32-head slice of it is stored straight into the
-//      shared memory of the CTA that owns those heads;
-//   3. after a cluster barrier CTA d sums the partials of heads
-//      32 d .. 32 d + 31 (in rank order, so every run gives the same logits),
-//      takes their max m_c and sum l_c over the chunk, and writes
-//      P = exp(S - m_c) as bf16 hi + lo (P = hi + lo to 2^-17) into the
-//      probability operand of every CTA of the cluster;
+//      N = heads), read out of tensor memory into shared memory; the 32-head
+//      slice each other CTA owns goes to it by one bulk shared-to-shared copy
+//      that completes on that CTA's mbarrier (no cluster-wide barrier, no
+//      cluster-scope proxy fence);
+//   3. CTA d sums the partials of heads 32 d .. 32 d + 31 (in rank order, so
+//      every run gives the same logits), takes their max m_c and sum l_c over
+//      the chunk, writes P = exp(S - m_c) as bf16 hi + lo (P = hi + lo to
+//      2^-17) into its own probability operand and bulk-copies those rows to
+//      the other CTA in the same way;
 //   4. [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T, reading the same key tile
 //      as an MN-major operand (V = K; M-tiles of 128 dims, K = 128 keys,
 //      N = 128); the epilogue adds the two halves;
@@ -59,20 +61,27 @@ static_assert(AC_THREADS / 16 == AC_OWN, "sixteen threads per owned head");
 
 struct AcSmem {
     uint8_t k[AC_SLABS * AC_KEYS * 128];           // [slab of 64 dims][128 keys][128 B]
-    uint8_t q[AC_SLABS * CSA2_HEADS * 128];        // [slab][64 heads][128 B]
+    union {
+        uint8_t q[AC_SLABS * CSA2_HEADS * 128];    // [slab][64 heads][128 B] 32 KB
+        float pout[CSA2_HEADS][AC_KEYS];           // this CTA's partial logits [head][key], written
+    } u;                                           // once the first product is done with Q
     uint8_t p[2 * 2 * CSA2_HEADS * 128];           // [slab of 64 keys][hi 64 | lo 64 rows][128 B] 32 KB:
                                                    // this CTA's heads written here, the others' rows
                                                    // copied in by their owners
-    float ps[AC_CL][AC_OWN][AC_KEYS];              // [source CTA][owned head][key] partial logits 32 KB
+    float ps[AC_CL][AC_OWN][AC_KEYS];              // [source CTA][owned head][key]: the other CTAs'
+                                                   // partial logits of this CTA's heads (copied in)
     uint32_t e2m1_pair[256][32];                   // byte -> bf16x2 of its two E2M1 codes, one
                                                    // copy per lane (bank = lane: no conflicts)  32 KB
     float kscale[AC_KEYS];                         // window row scale (1 for entries), -1: no key
     uint64_t mbar;                                 // the products' commits
+    uint64_t sbar;                                 // the other CTAs' partial logits have landed
     uint64_t pbar;                                 // the other CTAs' probability rows have landed
     uint32_t tmem;
 };
 constexpr uint32_t AC_P_ROWS_BYTES = AC_OWN * 128;                       // one CTA's rows of one half, one slab
 constexpr uint32_t AC_P_IN_BYTES = (AC_CL - 1) * 4 * AC_P_ROWS_BYTES;   // probability bytes received
+constexpr uint32_t AC_S_BYTES = AC_OWN * AC_KEYS * 4;                    // one CTA's partials of one owner
+constexpr uint32_t AC_S_IN_BYTES = (AC_CL - 1) * AC_S_BYTES;            // partial-logit bytes received
 
 // ---------------------------------------------------------------- cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank()
@@ -82,22 +91,11 @@ __device__ __forceinline__ uint32_t cluster_rank()
     return r;
 }
 
-// All threads of all CTAs of the cluster; release/acquire at cluster scope.
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
 {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
-}
-
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Bulk copy of `bytes` from this CTA's shared memory to shared memory of a CTA
@@ -217,10 +215,18 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
     if (tid == 0) {
         tc::mbar_init(&S.mbar, 1);
+        tc::mbar_init(&S.sbar, 1);
         tc::mbar_init(&S.pbar, 1);
         tc::fence_mbar_init();
     }
     if (warp == 0) tc::tmem_alloc(&S.tmem, AC_TMEM_COLS);
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(&S.sbar, AC_S_IN_BYTES);    // the other CTAs' partial logits
+        tc::mbar_arrive_expect_tx(&S.pbar, AC_P_IN_BYTES);    // and probability rows
+    }
+    // first half of a cluster barrier: this CTA's mbarriers are initialised; the
+    // matching wait comes before the first copy into another CTA
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     // E2M1 pair table: 2048 16-byte chunks of four copies each, consecutive per lane
 #pragma unroll
     for (int ch = tid; ch < 256 * 32 / 4; ch += AC_THREADS) {
@@ -330,7 +336,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 #pragma unroll
     for (int i = 0; i < 4; i++) {
         const int e = tid + AC_THREADS * i;
-        *reinterpret_cast<uint4 *>(S.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
+        *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
     }
     if (hf == 0) {
         S.kscale[key] = valid ? kscale : -1.0f;
@@ -353,7 +359,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
     // ---- partial S^T = K_d Q_d^T over this CTA's dims
     if (tid == 0) {
-        const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.q);
+        const uint32_t k0 = tc::smem_u32(S.k), q0 = tc::smem_u32(S.u.q);
 #pragma unroll
         for (int kk = 0; kk < AC_DIMS / 16; kk++) {   // 16 dims per step
             const uint32_t off = (uint32_t)(kk >> 2) * (AC_KEYS * 128) + (uint32_t)(kk & 3) * 32u;
@@ -363,13 +369,14 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         }
         tc::mma_commit(&S.mbar);
     }
-    // A CTA whose product timed out still passes both cluster barriers (the
-    // others wait there) but writes no output; the status word says why.
+    // A CTA whose product timed out still sends its (meaningless) partials and
+    // probabilities, so that the other CTAs' bounded waits complete, but writes
+    // no output; the status word says why.
     const bool fail = __syncthreads_or(!tc::mbar_wait(&S.mbar, 0));
     tc::tc_fence_after();
     if (!fail) {
         // this warp: keys of its lane quarter, heads col .. col + 64 / AC_SLABS - 1,
-        // each group of 16 heads stored into the shared memory of its owner
+        // into this CTA's partial logits [head][key] (Q is no longer read)
         constexpr int NG = 4 / AC_SLABS;           // groups of 16 heads per warp
         const uint32_t col = 64u / AC_SLABS * (uint32_t)(warp >> 2);
         uint32_t acc[NG][16];
@@ -378,17 +385,30 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         tc::tmem_ld_wait();
         const int kr = (warp & 3) * 32 + lane;
 #pragma unroll
-        for (int g = 0; g < NG; g++) {
-            const uint32_t h0 = col + 16u * g;
-            const uint32_t ra = cluster_map(tc::smem_u32(&S.ps[dq][h0 % AC_OWN][kr]), h0 / AC_OWN);
+        for (int g = 0; g < NG; g++)
 #pragma unroll
-            for (int j = 0; j < 16; j++) st_cluster_f32(ra + (uint32_t)j * (AC_KEYS * 4), acc[g][j]);
-        }
+            for (int j = 0; j < 16; j++) S.u.pout[col + 16 * g + j][kr] = __uint_as_float(acc[g][j]);
     } else if (tid == 0) {
         flag(c.status, CSA2_DEV_TIMEOUT);
     }
-    cluster_sync();                                // the partials of the owned heads are here
-    if (tid == 0) tc::mbar_arrive_expect_tx(&S.pbar, AC_P_IN_BYTES);   // the other CTAs' probability rows
+    // the partials of each other CTA's heads go to that CTA by one bulk copy (async
+    // proxy): generic writes fenced, then issued once every thread has written
+    tc::fence_proxy_async_smem();
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // the others' mbarriers exist
+    if (tid == 0) {
+        const uint32_t sb = tc::smem_u32(&S.sbar);
+#pragma unroll
+        for (int dst = 0; dst < AC_CL; dst++) {
+            if (dst == (int)dq) continue;
+            bulk_to_peer(cluster_map(tc::smem_u32(&S.ps[dq][0][0]), (uint32_t)dst),
+                         tc::smem_u32(&S.u.pout[AC_OWN * dst][0]), AC_S_BYTES, cluster_map(sb, (uint32_t)dst));
+        }
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    // the other CTAs' partials of this CTA's heads have landed
+    const bool s_fail = __syncthreads_or(!tc::mbar_wait(&S.sbar, 0));
+    if (s_fail && tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
 
     // ---- owned heads AC_OWN dq .. : sixteen threads per head, eight
     //      consecutive keys per thread
@@ -396,13 +416,14 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const int hl = tid >> 4, h = AC_OWN * (int)dq + hl, part = tid & 15;
         float4 v[AC_CL][2];
 #pragma unroll
-        for (int src = 0; src < AC_CL; src++) {
-            v[src][0] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part]);
-            v[src][1] = *reinterpret_cast<const float4 *>(&S.ps[src][hl][8 * part + 4]);
+        for (int src = 0; src < AC_CL; src++) {     // rank order: the same sum in every run
+            const float *row = src == (int)dq ? &S.u.pout[h][0] : &S.ps[src][hl][0];
+            v[src][0] = *reinterpret_cast<const float4 *>(row + 8 * part);
+            v[src][1] = *reinterpret_cast<const float4 *>(row + 8 * part + 4);
         }
-        float ks[8];                               // scales of keys 8 part .. +7 (-1: none)
-        *reinterpret_cast<float4 *>(ks) = *reinterpret_cast<const float4 *>(&S.kscale[8 * part]);
-        *reinterpret_cast<float4 *>(ks + 4) = *reinterpret_cast<const float4 *>(&S.kscale[8 * part + 4]);
+        const float4 ks0 = *reinterpret_cast<const float4 *>(&S.kscale[8 * part]);
+        const float4 ks1 = *reinterpret_cast<const float4 *>(&S.kscale[8 * part + 4]);
+        const float ks[8] = {ks0.x, ks0.y, ks0.z, ks0.w, ks1.x, ks1.y, ks1.z, ks1.w};   // -1: no key
         float lg[8];
         float mx = -INFINITY;
 #pragma unroll
@@ -442,7 +463,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const uint32_t off_lo = off_hi + CSA2_HEADS * 128;
         *reinterpret_cast<uint4 *>(S.p + off_hi) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
         *reinterpret_cast<uint4 *>(S.p + off_lo) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
-        if (part == 0 && !fail) {
+        if (part == 0 && !fail && !s_fail) {
             part_ml[(base + h) * 2] = mx;
             part_ml[(base + h) * 2 + 1] = l;
         }
@@ -476,7 +497,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
     // ---- [O_hi | O_lo]_d^T = V_d^T [P_hi | P_lo]^T: M-tiles of 128 dims, K = 128 keys,
     //      N = 128; tile mt in columns 128 mt .. +127 (S has been read out)
-    if (tid == 0 && !fail && !p_fail) {
+    if (tid == 0 && !fail && !s_fail && !p_fail) {
         const uint32_t k0 = tc::smem_u32(S.k), p0 = tc::smem_u32(S.p);
 #pragma unroll
         for (int mt = 0; mt < AC_MT; mt++) {
@@ -492,7 +513,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         tc::mma_commit(&S.mbar);
     }
     if (p_fail && tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
-    if (!fail && !p_fail) {
+    if (!fail && !s_fail && !p_fail) {
         const bool fail2 = __syncthreads_or(!tc::mbar_wait(&S.mbar, 1));
         tc::tc_fence_after();
         if (!fail2) {
