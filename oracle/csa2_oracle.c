@@ -167,6 +167,60 @@ void or_dequant_mxfp4(const uint8_t *codes, const uint8_t *scales, int64_t n, do
         }
 }
 
+/* FP4 main KV with one E4M3 scale per 16 elements: the block size and scale
+ * type that [P2] §4 and [P4] give for the FP4 cache ("16 channels share one
+ * E4M3 scale").  For a block with largest magnitude amax:
+ *   s  = e4m3(amax / 6)      one fp32 IEEE division, then the FP8 rounding
+ *                            (to nearest, ties to even, saturating at 448);
+ *   c_i = e2m1(x_i / s)      one fp32 IEEE division, then the E2M1 rounding
+ *                            (to nearest, ties to the even code, saturating
+ *                            at 6, sign bit kept);
+ * a block whose scale rounds to zero keeps only the elements' sign bits.
+ * codes: [n][256] in the MXFP4 nibble order; scales: [n][32] E4M3 bytes. */
+void or_quant_fp4_e4m3(const float *x, int64_t n, uint8_t *codes, uint8_t *scales)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; r++) {
+        const float *row = x + r * 512;
+        for (int b = 0; b < 32; b++) {
+            float amax = 0.0f;
+            for (int i = 0; i < 16; i++) {
+                float a = fabsf(row[b * 16 + i]);
+                if (a > amax) amax = a;
+            }
+            volatile float q = amax / 6.0f;           /* one fp32 rounding */
+            uint8_t sb = or_e4m3_encode(q);
+            scales[r * 32 + b] = sb;
+            float sv = (float)or_e4m3_value(sb);
+            for (int i = 0; i < 16; i += 2) {
+                uint8_t c[2];
+                for (int t = 0; t < 2; t++) {
+                    float v = row[b * 16 + i + t];
+                    if (sv == 0.0f) {
+                        c[t] = (uint8_t)(signbit(v) ? 8 : 0);
+                    } else {
+                        volatile float y = v / sv;    /* one fp32 rounding */
+                        c[t] = or_e2m1_encode((double)y);
+                    }
+                }
+                codes[r * 256 + (b * 16 + i) / 2] = (uint8_t)(c[0] | (c[1] << 4));
+            }
+        }
+    }
+}
+
+/* Exact decode of n entries of that format to doubles [n][512]. */
+void or_dequant_fp4_e4m3(const uint8_t *codes, const uint8_t *scales, int64_t n, double *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; r++)
+        for (int d = 0; d < 512; d++) {
+            uint8_t byte = codes[r * 256 + d / 2];
+            uint8_t c = (d & 1) ? (byte >> 4) : (byte & 15);
+            out[r * 512 + d] = or_e2m1_value(c) * or_e4m3_value(scales[r * 32 + d / 16]);
+        }
+}
+
 /* ------------------------------------------------------------------------ */
 /* a3: FP8 quantisation with a per-row fp32 scale (SWA KV, indexer keys)    */
 /* ------------------------------------------------------------------------ */

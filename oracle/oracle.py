@@ -71,6 +71,8 @@ def lib():
             L.or_mx_exponent.argtypes = [ctypes.c_float]
             L.or_quant_mxfp4.argtypes = [P, i64, P, P]
             L.or_dequant_mxfp4.argtypes = [P, P, i64, P]
+            L.or_quant_fp4_e4m3.argtypes = [P, i64, P, P]
+            L.or_dequant_fp4_e4m3.argtypes = [P, P, i64, P]
             L.or_quant_fp8.argtypes = [P, i64, i32, P, P]
             L.or_dequant_fp8.argtypes = [P, P, i64, i32, P]
             L.or_compress.argtypes = [P, P, P, i32, i64, P]
@@ -149,6 +151,27 @@ def dequant_mxfp4(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return out
 
 
+def quant_fp4_e4m3(x: np.ndarray):
+    """FP4 entries with one E4M3 scale per 16 elements: codes [n][256], scales [n][32]."""
+    x = _c(x, np.float32).reshape(-1, 512)
+    n = x.shape[0]
+    codes = np.empty((n, 256), np.uint8)
+    scales = np.empty((n, 32), np.uint8)
+    lib().or_quant_fp4_e4m3(_p(x), n, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequant_fp4_e4m3(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8).reshape(-1, 256)
+    scales = _c(scales, np.uint8).reshape(-1, 32)
+    out = np.empty((codes.shape[0], 512), np.float64)
+    lib().or_dequant_fp4_e4m3(_p(codes), _p(scales), codes.shape[0], _p(out))
+    return out
+
+
+KV_FORMATS = {0: (quant_mxfp4, dequant_mxfp4, 16), 1: (quant_fp4_e4m3, dequant_fp4_e4m3, 32)}
+
+
 def quant_fp8(x: np.ndarray):
     x = _c(x, np.float32)
     n, dim = x.shape
@@ -215,13 +238,14 @@ def swa_window(i: int, s: int = 0, W: int = SWA_W):
 
 
 def attention_keys(kv_codes, kv_scales, idx, swa_codes, swa_scales, t: int,
-                   swa_start: int = 0, W: int = SWA_W) -> np.ndarray:
-    """Dequantised key set of one query: the selected MXFP4 entries (idx != -1)
-    followed by the FP8 window rows of tokens [max(s, t-W+1), t]
-    ([P2] §5 window equation), token u held in ring row u % R."""
+                   swa_start: int = 0, W: int = SWA_W, kv_format: int = 0) -> np.ndarray:
+    """Dequantised key set of one query: the selected FP4 entries (idx != -1;
+    MXFP4 for kv_format 0, 16-element E4M3-scaled blocks for 1) followed by the
+    FP8 window rows of tokens [max(s, t-W+1), t] ([P2] §5 window equation),
+    token u held in ring row u % R."""
     sel = np.asarray(idx, np.int64)
     sel = sel[sel >= 0]
-    main = dequant_mxfp4(np.asarray(kv_codes)[sel], np.asarray(kv_scales)[sel])
+    main = KV_FORMATS[kv_format][1](np.asarray(kv_codes)[sel], np.asarray(kv_scales)[sel])
     R = swa_codes.shape[0]
     lo, hi = swa_window(t, swa_start, W)
     toks = np.arange(lo, hi + 1, dtype=np.int64)

@@ -172,3 +172,90 @@ def test_quant_fp8_rows():
     deq = oracle.dequant_fp8(c, s)
     bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s[:, None]) * (1 + 1e-6)
     assert (np.abs(deq - x) <= bound).all()
+
+
+# ---------------------------------------------------------------- FP4, 16-element blocks, E4M3 scale
+# The block size and scale type the pages give for the FP4 cache
+# ("DeepSeek-V4.1-Flash 架构详解" §4; "How DeepSeek V4.1 Flash beats 1.6T models"):
+# 16 elements share one E4M3 scale.
+def _brute_fp4_e4m3_block(vals):
+    """Independent reference: nearest-value searches over the full E4M3 and
+    E2M1 grids (torch for the fp32 divisions), ties to the even code."""
+    e4 = np.array([oracle.e4m3_value(c) for c in range(127)])          # positive finite codes
+    amax = np.float32(np.max(np.abs(vals)))
+    q = float((torch.tensor(amax) / torch.tensor(6.0, dtype=torch.float32)).item())
+    d = np.abs(e4 - q)
+    best = np.flatnonzero(d == d.min())
+    sb = int(best[0] if best.size == 1 else best[best % 2 == 0][0]) if q <= e4[-1] else 126
+    sv = np.float32(e4[sb])
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    codes = []
+    for v in vals:
+        if sv == 0:
+            codes.append(8 if np.signbit(v) else 0)
+            continue
+        y = float((torch.tensor(np.float32(v)) / torch.tensor(sv)).item())
+        dd = np.abs(grid - min(abs(y), 6.0))
+        cand = np.flatnonzero(dd == dd.min())
+        c = int(cand[0] if cand.size == 1 else cand[cand % 2 == 0][0])
+        codes.append(c | (8 if np.signbit(y) else 0))
+    return sb, codes
+
+
+def test_fp4_e4m3_hand_values():
+    x = np.zeros((1, 512), np.float32)
+    x[0, :16] = 1.0                          # s = e4m3(1/6) = 0.171875 (code 0x23), 1/s = 5.82 -> 6
+    blk = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -6.0, 0.0, -0.0, 3.0, 4.0, 1.5, 0.5, 2.0]
+    x[0, 16:32] = blk                        # amax 6 -> s = 1: the E2M1 ties land on even codes
+    x[0, 32:48] = 6.2                        # s = e4m3(1.0333) = 1.0: 6.2 saturates to 6
+    x[0, 48:64] = -0.0                       # amax 0: scale 0, sign bits only
+    x[0, 64:80] = 2.0 ** -16                 # amax / 6 rounds to 0 in E4M3: scale 0
+    codes, scales = oracle.quant_fp4_e4m3(x)
+    assert scales.shape == (1, 32) and codes.shape == (1, 256)
+    assert scales[0, 0] == 0x23 and oracle.e4m3_value(0x23) == 0.171875
+    assert all(codes[0, i] == 0x77 for i in range(8))
+    assert scales[0, 1] == 0x38                                         # 1.0
+    want = [7, 0, 2, 2, 4, 4, 6, 6, 15, 0, 8, 5, 6, 3, 1, 4]
+    got = [(codes[0, 8 + i // 2] >> (4 * (i % 2))) & 15 for i in range(16)]
+    assert got == want
+    assert scales[0, 2] == 0x38 and all(codes[0, 16 + i] == 0x77 for i in range(8))
+    assert scales[0, 3] == 0 and all(codes[0, 24 + i] == 0x88 for i in range(8))
+    assert scales[0, 4] == 0 and all(codes[0, 32 + i] == 0x00 for i in range(8))
+    deq = oracle.dequant_fp4_e4m3(codes, scales)[0]
+    assert np.all(deq[:16] == 6 * 0.171875)
+    assert np.array_equal(deq[16:32], [6, 0, 1, 1, 2, 2, 4, 4, -6, 0, 0, 3, 4, 1.5, 0.5, 2])
+
+
+def test_fp4_e4m3_matches_brute_force():
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((6, 512)).astype(np.float32)
+    x[1] *= np.float32(1e-3)
+    x[2] *= np.float32(3e3)                                              # scales near the top of E4M3
+    x[3, ::7] = 0.0
+    x[4] = np.round(x[4] * 4) / 4                                        # many exact grid points and ties
+    codes, scales = oracle.quant_fp4_e4m3(x)
+    for r in range(x.shape[0]):
+        for b in range(32):
+            sb, cs = _brute_fp4_e4m3_block(x[r, 16 * b:16 * b + 16])
+            assert scales[r, b] == sb, (r, b)
+            got = [(codes[r, 8 * b + i // 2] >> (4 * (i % 2))) & 15 for i in range(16)]
+            assert got == cs, (r, b)
+
+
+def test_fp4_e4m3_products_exact_in_bf16():
+    """Every (element code, scale code) product is a bf16 value: the attention
+    can dequantise this format exactly with one bf16 multiply."""
+    for sb in range(127):
+        s = oracle.e4m3_value(sb)
+        for c in range(16):
+            v = oracle.e2m1_value(c) * s
+            assert float(torch.tensor(v, dtype=torch.float64).to(torch.bfloat16).double()) == v
+
+
+def test_fp4_e4m3_bytes_per_entry():
+    # 512 E2M1 codes (256 B) + 32 E4M3 scales = 288 B per entry (MXFP4: 256 + 16 = 272 B)
+    x = np.ones((3, 512), np.float32)
+    c4, s4 = oracle.quant_fp4_e4m3(x)
+    cm, sm = oracle.quant_mxfp4(x)
+    assert c4.nbytes // 3 + s4.nbytes // 3 == 288
+    assert cm.nbytes // 3 + sm.nbytes // 3 == 272
