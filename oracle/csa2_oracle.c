@@ -59,6 +59,8 @@ double or_e2m1_value(uint8_t code)
 uint8_t or_e2m1_encode(double v)
 {
     double a = fabs(v);
+    if (a > 6.0)                        /* saturation: beyond 6 every distance is */
+        a = 6.0;                        /* the same in double precision for huge a */
     int best = 0;
     double best_d = INFINITY;
     for (int c = 0; c < 8; c++) {

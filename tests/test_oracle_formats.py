@@ -30,6 +30,11 @@ def test_e2m1_value_table():
     assert np.signbit(oracle.e2m1_value(8))
 
 
+def test_e2m1_saturates_far_beyond_the_grid():
+    for v in (6.5, 1e3, 1e30, 6.7e35, 3e38):
+        assert oracle.e2m1_encode(v) == 7 and oracle.e2m1_encode(-v) == 15
+
+
 def test_e2m1_roundtrip_all_codes():
     for c in range(16):
         assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
@@ -233,6 +238,8 @@ def test_fp4_e4m3_matches_brute_force():
     x[2] *= np.float32(3e3)                                              # scales near the top of E4M3
     x[3, ::7] = 0.0
     x[4] = np.round(x[4] * 4) / 4                                        # many exact grid points and ties
+    x[5, :40] = np.float32(3e38)                                         # quotients far beyond 6: saturate
+    x[5, 3] = np.float32(-1.7e38)
     codes, scales = oracle.quant_fp4_e4m3(x)
     for r in range(x.shape[0]):
         for b in range(32):
