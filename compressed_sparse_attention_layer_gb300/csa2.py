@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_HERE, "libcsa2.so")
 HEADS, HEAD_DIM, IDX_HEADS, IDX_DIM = 64, 512, 32, 128
 TOPK, BLOCK, POOL_BLOCKS, POOL_MAX, SWA_WINDOW, PAGE = 512, 8, 2048, 16384, 128, 64
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
+KV_MXFP4, KV_FP4_E4M3 = 0, 1                  # main-KV formats: scale bytes per entry 16 / 32
+KV_SCALE_BYTES = {KV_MXFP4: 16, KV_FP4_E4M3: 32}
 MODES = {"full": MODE_FULL, "reindex": MODE_REINDEX, "reuse": MODE_REUSE}
 DEV_BAD_PAGE, DEV_BAD_SLOT, DEV_TIMEOUT, DEV_BAD_INDEX = 1, 2, 4, 8
 
@@ -27,7 +29,8 @@ _vp, _i32, _i64, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ct
 
 class Cache(ctypes.Structure):
     _fields_ = [("kv_codes", _vp), ("kv_scales", _vp), ("ik_codes", _vp), ("ik_scales", _vp),
-                ("num_slots", _i64), ("block_table", _vp), ("max_pages", _i32), ("status", _vp)]
+                ("num_slots", _i64), ("block_table", _vp), ("max_pages", _i32), ("kv_format", _i32),
+                ("status", _vp)]
 
 
 class Batch(ctypes.Structure):
@@ -49,6 +52,7 @@ EXPORTS = {
     "csa2_compress": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i64, _vp, _vp]),
     "csa2_quant_mxfp4": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_quant_fp8": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "csa2_quant_fp4_e4m3": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_index_scores": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp, _vp,
                                          _vp, _i64, _vp]),
     "csa2_index_scores_pool": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp,
@@ -125,11 +129,12 @@ def _stream(stream):
 class PagedCache:
     """Device buffers of the layer-shared cache (caller-side allocation)."""
 
-    def __init__(self, num_pages: int, block_table: torch.Tensor, device="cuda"):
+    def __init__(self, num_pages: int, block_table: torch.Tensor, device="cuda", kv_format: int = KV_MXFP4):
         self.num_pages = int(num_pages)
+        self.kv_format = int(kv_format)
         S = self.num_pages * PAGE
         self.kv_codes = torch.zeros((S, 256), dtype=torch.uint8, device=device)
-        self.kv_scales = torch.zeros((S, 16), dtype=torch.uint8, device=device)
+        self.kv_scales = torch.zeros((S, KV_SCALE_BYTES[self.kv_format]), dtype=torch.uint8, device=device)
         self.ik_codes = torch.zeros((S, 128), dtype=torch.uint8, device=device)
         self.ik_scales = torch.ones((S,), dtype=torch.float32, device=device)
         self.block_table = block_table.to(device=device, dtype=torch.int32).contiguous()
@@ -142,7 +147,7 @@ class PagedCache:
     def struct(self) -> Cache:
         return Cache(_ptr(self.kv_codes), _ptr(self.kv_scales), _ptr(self.ik_codes), _ptr(self.ik_scales),
                      self.num_slots, _ptr(self.block_table, torch.int32), self.block_table.shape[1],
-                     _ptr(self.status))
+                     self.kv_format, _ptr(self.status))
 
     def slots(self, b: int, entries: torch.Tensor) -> torch.Tensor:
         """Slot ids of logical entries of sequence b (a host-side helper for appends)."""
@@ -171,6 +176,13 @@ def csa2_compress(C, Z, bias, m: int, out, stream=None):
 
 def csa2_quant_mxfp4(x, codes, scales, slots=None, status=None, stream=None):
     _check("csa2_quant_mxfp4", load().csa2_quant_mxfp4(
+        _ptr(x, torch.float32, "x"), x.shape[0], _ptr(slots, torch.int64, "slots"), _ptr(codes, torch.uint8),
+        _ptr(scales, torch.uint8), codes.shape[0], _ptr(status, torch.int32), _stream(stream)))
+
+
+def csa2_quant_fp4_e4m3(x, codes, scales, slots=None, status=None, stream=None):
+    """FP4 with one E4M3 scale per 16 elements: codes [S][256], scales [S][32]."""
+    _check("csa2_quant_fp4_e4m3", load().csa2_quant_fp4_e4m3(
         _ptr(x, torch.float32, "x"), x.shape[0], _ptr(slots, torch.int64, "slots"), _ptr(codes, torch.uint8),
         _ptr(scales, torch.uint8), codes.shape[0], _ptr(status, torch.int32), _stream(stream)))
 

@@ -15,6 +15,8 @@ int launch_quant_mxfp4(const float *, int64_t, const int64_t *, uint8_t *, uint8
                        cudaStream_t);
 int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, float *, int64_t, int32_t *,
                      cudaStream_t);
+int launch_quant_fp4_e4m3(const float *, int64_t, const int64_t *, uint8_t *, uint8_t *, int64_t, int32_t *,
+                          cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
                       float *, int32_t *, int64_t, cudaStream_t);
 int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, const int32_t *, int64_t, uint8_t *,
@@ -44,6 +46,7 @@ static int check_cache(const csa2_cache *c, bool need_kv, bool need_ik)
     if (need_kv && (!c->kv_codes || !c->kv_scales)) return CSA2_ERR_NULL;
     if (need_ik && (!c->ik_codes || !c->ik_scales)) return CSA2_ERR_NULL;
     if (c->num_slots <= 0 || c->num_slots % CSA2_PAGE || c->max_pages <= 0) return CSA2_ERR_SHAPE;
+    if (c->kv_format != CSA2_KV_MXFP4 && c->kv_format != CSA2_KV_FP4_E4M3) return CSA2_ERR_UNSUPPORTED;
     if (need_kv && (!aligned(c->kv_codes, 16) || !aligned(c->kv_scales, 16))) return CSA2_ERR_ALIGN;
     if (need_ik && (!aligned(c->ik_codes, 16) || !aligned(c->ik_scales, 16))) return CSA2_ERR_ALIGN;
     return CSA2_OK;
@@ -165,6 +168,17 @@ int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *c
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;
     if (!aligned(x, 16) || !aligned(codes, 16)) return CSA2_ERR_ALIGN;
     return launch_quant_mxfp4(x, n, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
+}
+
+int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t *codes, uint8_t *scales,
+                        int64_t num_slots, int32_t *status, csa2_stream_t stream)
+{
+    if (n < 0 || num_slots < 0) return CSA2_ERR_SHAPE;
+    if (n == 0) return CSA2_OK;
+    if (!x || !codes || !scales) return CSA2_ERR_NULL;
+    if (!slots && n > num_slots) return CSA2_ERR_RANGE;
+    if (!aligned(x, 16) || !aligned(codes, 16)) return CSA2_ERR_ALIGN;
+    return launch_quant_fp4_e4m3(x, n, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
 }
 
 int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,

@@ -124,19 +124,34 @@ __device__ __forceinline__ uint32_t pow2_bf16x2(int X)
     return h | (h << 16);
 }
 
-// Slab `hf` (local dims 64 hf .. 64 hf + 63, two MX blocks) of this CTA's
-// slice of an MXFP4 entry -> bf16 row of the key tile (exact): the table gives
-// the two E2M1 values of a byte with their signs (this lane's copy), one
-// bf16x2 multiply applies the block's 2^X.
+// Two e4m3 codes (low bytes of the halves of v) -> bf16x2 of their values:
+// sign and the 7 exponent/mantissa bits moved into bf16 position give the
+// value times 2^-120, which one exact multiply by 2^120 restores (subnormal
+// codes included).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v)
+{
+    const uint32_t bits = ((v & 0x007F007Fu) << 4) | ((v & 0x00800080u) << 8);
+    return bf16x2_mul(bits, 0x7B807B80u);          // 2^120 in both halves
+}
+
+// Slab `hf` (local dims 64 hf .. 64 hf + 63) of this CTA's slice of an FP4
+// entry -> bf16 row of the key tile (exact): the table gives the two E2M1
+// values of a byte with their signs (this lane's copy), one bf16x2 multiply
+// applies the block scale.  MXFP4: sc holds the two E8M0 bytes of the slab's
+// 32-element blocks (scale 2^X); FP4_E4M3: the four E4M3 bytes of its
+// 16-element blocks (every E2M1 x E4M3 product is a bf16 value).
+template <bool E4M3>
 __device__ __forceinline__ void store_main_key(uint8_t *ktile, uint32_t row, const uint4 (&c)[4], uint32_t sc,
                                                int hf, const uint32_t (*pair)[32], uint32_t lane)
 {
 #pragma unroll
-    for (int blk = 0; blk < 2; blk++) {            // 16 bytes = 32 elements = one MX block
-        const uint32_t f = pow2_bf16x2((int)((sc >> (8 * blk)) & 0xFFu) - 127);
+    for (int blk = 0; blk < 2; blk++) {            // 16 bytes = 32 elements
         const uint32_t w[4] = {c[blk].x, c[blk].y, c[blk].z, c[blk].w};
 #pragma unroll
         for (int j = 0; j < 4; j++) {              // 4 bytes = 8 elements -> one 16-byte chunk
+            uint32_t f;
+            if (E4M3) f = e4m3x2_to_bf16x2(((sc >> (8 * (2 * blk + (j >> 1)))) & 0xFFu) * 0x00010001u);
+            else f = pow2_bf16x2((int)((sc >> (8 * blk)) & 0xFFu) - 127);
             uint4 o;
             o.x = bf16x2_mul(pair[w[j] & 0xFFu][lane], f);
             o.y = bf16x2_mul(pair[(w[j] >> 8) & 0xFFu][lane], f);
@@ -156,16 +171,6 @@ __device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t byte)
     const uint32_t lo = byte & 15u, hi = (byte >> 4) & 15u;
     const uint32_t bits = ((lo & 7u) << 6) | ((lo & 8u) << 12) | ((hi & 7u) << 22) | ((hi & 8u) << 28);
     return bf16x2_mul(bits, 0x7E807E80u);          // 2^126 in both halves
-}
-
-// Two e4m3 codes (low bytes of the halves of v) -> bf16x2 of their values:
-// sign and the 7 exponent/mantissa bits moved into bf16 position give the
-// value times 2^-120, which one exact multiply by 2^120 restores (subnormal
-// codes included).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v)
-{
-    const uint32_t bits = ((v & 0x007F007Fu) << 4) | ((v & 0x00800080u) << 8);
-    return bf16x2_mul(bits, 0x7B807B80u);          // 2^120 in both halves
 }
 
 // Half `hf` of this CTA's slice of an FP8 window row -> bf16 row of the key
@@ -270,8 +275,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
                             reinterpret_cast<const uint4 *>(c.kv_codes + slot * 256 + AC_DIMS / 2 * dq) + 2 * hf;
                         kc[0] = __ldg(src);
                         kc[1] = __ldg(src + 1);
-                        ksc = __ldg(reinterpret_cast<const uint16_t *>(c.kv_scales + slot * 16 + AC_DIMS / 32 * dq) +
-                                    hf);
+                        ksc = c.kv_format == CSA2_KV_FP4_E4M3
+                                  ? __ldg(reinterpret_cast<const uint32_t *>(c.kv_scales + slot * 32 + AC_DIMS / 16 * dq) +
+                                          hf)
+                                  : __ldg(reinterpret_cast<const uint16_t *>(c.kv_scales + slot * 16 + AC_DIMS / 32 * dq) +
+                                          hf);
                         valid = true;
                     }
                 }
@@ -346,7 +354,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     // ---- dequantise into row `key` of the key tile
     if (valid) {
         if (window) store_window_key(S.k, key, kc, hf);
-        else store_main_key(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
+        else if (c.kv_format == CSA2_KV_FP4_E4M3) store_main_key<true>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
+        else store_main_key<false>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
     } else {
         zero_key(S.k, key, hf);
     }

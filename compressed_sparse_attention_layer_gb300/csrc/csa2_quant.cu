@@ -114,6 +114,53 @@ __global__ void __launch_bounds__(256) k_quant_mxfp4(const float *__restrict__ x
     scales[dst * 16 + blk] = (uint8_t)(X + 127);
 }
 
+// FP4 with one E4M3 scale per 16 elements ("DeepSeek-V4.1-Flash 架构详解" §4;
+// "How DeepSeek V4.1 Flash beats 1.6T models"): one thread per 16-element
+// block (64 B in, 8 B codes + 1 B scale out), 32 threads per entry.
+__global__ void __launch_bounds__(256) k_quant_fp4_e4m3(const float *__restrict__ x, int64_t n,
+                                                        const int64_t *__restrict__ slots,
+                                                        uint8_t *__restrict__ codes,
+                                                        uint8_t *__restrict__ scales, int64_t num_slots,
+                                                        int32_t *status)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (t >= n * 32) return;
+    const int64_t r = t >> 5;
+    const int blk = (int)(t & 31);
+    const int64_t dst = slots ? slots[r] : r;
+    if (dst < 0) return;
+    if (dst >= num_slots) {
+        if (blk == 0) flag(status, CSA2_DEV_BAD_SLOT);
+        return;
+    }
+    const float4 *src = reinterpret_cast<const float4 *>(x + r * CSA2_HEAD_DIM + blk * 16);
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float4 f = __ldg(src + i);
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t sb = f32x2_to_e4m3x2(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;   // amax / 6 >= 0
+    const float sv = e4m3_to_f32(sb);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const uint32_t sign = (__float_as_uint(v[i]) >> 31) << 3;
+        const uint32_t c = sv == 0.0f ? sign : e2m1_code(fabsf(__fdiv_rn(v[i], sv))) | sign;
+        packed[i >> 3] |= c << (4 * (i & 7));
+    }
+    *reinterpret_cast<uint2 *>(codes + dst * 256 + blk * 8) = make_uint2(packed[0], packed[1]);
+    scales[dst * 32 + blk] = (uint8_t)sb;
+}
+
 // One warp per row.  "DeepSeek-V4.1-Flash" research note §3.3 (FP8 SWA KV).
 template <int DIM>
 __global__ void __launch_bounds__(256) k_quant_fp8(const float *__restrict__ x, int64_t n,
@@ -172,6 +219,15 @@ int launch_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t 
     if (n == 0) return CSA2_OK;
     const int64_t threads = n * 16;
     return launch_pdl(k_quant_mxfp4, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, x, n, slots, codes,
+                      scales, num_slots, status);
+}
+
+int launch_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t *codes, uint8_t *scales,
+                          int64_t num_slots, int32_t *status, cudaStream_t st)
+{
+    if (n == 0) return CSA2_OK;
+    const int64_t threads = n * 32;
+    return launch_pdl(k_quant_fp4_e4m3, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, x, n, slots, codes,
                       scales, num_slots, status);
 }
 

@@ -33,7 +33,7 @@ class DeviceWorkload:
         self.rows = wl.batch * wl.nq
         self.layers = list(range(len(wl.layers))) if layers is None else list(layers)
         bt = torch.from_numpy(wl.block_table())
-        self.cache = csa2.PagedCache(wl.total_pages, bt, self.dev)
+        self.cache = csa2.PagedCache(wl.total_pages, bt, self.dev, kv_format=wl.kv_format)
         self.n_entries = torch.tensor([wl.entries(b) for b in range(wl.batch)], dtype=torch.int64, device=self.dev)
         self.q_pos = torch.from_numpy(np.concatenate([wl.q_pos(b) for b in range(wl.batch)])).to(self.dev)
         self.batch = csa2.batch_struct(self.n_entries, self.q_pos, wl.nq, wl.m, wl.max_entries)
@@ -62,8 +62,8 @@ class DeviceWorkload:
                     x = _dev_normal_bf16(wl._sid(T_C, b), e0 * 512, (e1 - e0) * 512, dev).float().view(e1 - e0, 512)
                 else:
                     x = self.compress_tokens(b, e0 * wl.m, e1 * wl.m)
-                csa2.csa2_quant_mxfp4(x, self.cache.kv_codes, self.cache.kv_scales, slots=slots,
-                                      status=self.cache.status)
+                quant = csa2.csa2_quant_fp4_e4m3 if wl.kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
+                quant(x, self.cache.kv_codes, self.cache.kv_scales, slots=slots, status=self.cache.status)
                 # indexer keys with planted rows
                 k = synth.normal_f32_torch(wl._sid(T_IK, b), e0 * 128, (e1 - e0) * 128, dev).view(e1 - e0, 128)
                 sel = (pos_d >= e0) & (pos_d < e1)

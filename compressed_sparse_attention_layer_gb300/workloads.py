@@ -52,6 +52,7 @@ class Workload:
     prefill_new: int = 0         # prefill: the last prefill_new tokens are the queries
     page_permute: bool = True
     swa_rows: int = W
+    kv_format: int = 0           # main KV: 0 MXFP4 (32-element blocks, E8M0), 1 FP4 with E4M3 per 16
 
     # ------------------------------------------------------------ geometry
     def entries(self, b: int) -> int:

@@ -28,12 +28,16 @@
  *
  * Cache layout (per compressed entry "slot"; one block-table page = 64 slots)
  * ---------------------------------------------------------------------------
- *   kv_codes  [num_slots][256]  MXFP4 E2M1 codes of the 512-dim main KV entry:
+ *   kv_codes  [num_slots][256]  FP4 E2M1 codes of the 512-dim main KV entry:
  *                               element 2i in the low nibble of byte i,
  *                               element 2i+1 in the high nibble; nibble bit 3
  *                               is the sign.  [P2] §4 (OCP MXFP4, E2M1).
- *   kv_scales [num_slots][16]   E8M0 scale byte (2^(byte-127)) of each
- *                               32-element block (OCP MX block size).
+ *   kv_scales [num_slots][16]   kv_format CSA2_KV_MXFP4: E8M0 scale byte
+ *                               (2^(byte-127)) of each 32-element block
+ *                               (OCP MX block size), 272 B per entry;
+ *             [num_slots][32]   kv_format CSA2_KV_FP4_E4M3: E4M3 scale byte of
+ *                               each 16-element block ([P2] §4 and [P4]: 16
+ *                               channels share one E4M3 scale), 288 B.
  *   ik_codes  [num_slots][128]  FP8 e4m3 codes of the 128-dim indexer key.
  *   ik_scales [num_slots]       fp32 per-entry scale of the indexer key.
  * Logical entry e of sequence b lives in slot
@@ -95,6 +99,10 @@ typedef struct CUstream_st *csa2_stream_t; /* same object as cudaStream_t */
 #define CSA2_MODE_REINDEX  1
 #define CSA2_MODE_REUSE    2
 
+/* main-KV formats (csa2_cache.kv_format) */
+#define CSA2_KV_MXFP4      0      /* 32-element blocks, E8M0 scale            */
+#define CSA2_KV_FP4_E4M3   1      /* 16-element blocks, E4M3 scale            */
+
 /* ---- descriptors -------------------------------------------------------- */
 
 /* The layer-shared global cache of compressed entries. */
@@ -106,6 +114,7 @@ typedef struct csa2_cache {
     int64_t        num_slots;    /* > 0, multiple of 64                      */
     const int32_t *block_table;  /* [batch][max_pages] page ids              */
     int32_t        max_pages;    /* row stride of block_table, > 0           */
+    int32_t        kv_format;    /* CSA2_KV_MXFP4 (0) or CSA2_KV_FP4_E4M3 (1) */
     int32_t       *status;       /* device status word (CSA2_DEV_*), or NULL */
 } csa2_cache;
 
@@ -196,6 +205,17 @@ CSA2_API int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bi
  *   codes  [num_slots][256], scales [num_slots][16]  (a csa2_cache's kv_*). */
 CSA2_API int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
                      uint8_t *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
+
+/* FP4 main KV with one E4M3 scale per 16-element block ([P2] §4 and [P4]:
+ * "16 channels share one E4M3 scale"; csa2_cache.kv_format CSA2_KV_FP4_E4M3).
+ * Per block: s = e4m3(amax / 6) (one fp32 IEEE division, then round to
+ * nearest even, saturating at 448); each element x becomes e2m1(x / s) (one
+ * fp32 IEEE division, nearest E2M1 value, ties to even, saturating at 6, sign
+ * bit copied); a block whose scale rounds to zero keeps only the sign bits.
+ *   x, slots, status, errors as csa2_quant_mxfp4;
+ *   codes  [num_slots][256] (same nibble order), scales [num_slots][32]. */
+CSA2_API int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
+                        uint8_t *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
 
 /* ---- a3: FP8 e4m3 quantisation with a per-row fp32 scale -----------------
  * s = amax / 448 (IEEE fp32 division; s = 1 when amax == 0); each element

@@ -27,7 +27,7 @@ class SeqOracle:
             self._ik = oracle.quant_fp8(self.wl.ik_src(self.b, 0, self.E, planted=self.planted))
         return self._ik
 
-    # main-KV entries at given positions (MXFP4 by the oracle's quantiser)
+    # main-KV entries at given positions (FP4 in the workload's format, by the oracle's quantiser)
     def kv(self, positions):
         wl, b = self.wl, self.b
         pos = np.asarray(positions, np.int64)
@@ -40,7 +40,7 @@ class SeqOracle:
                 C, Z = wl.cz_bits(b, int(p) * wl.m, (int(p) + 1) * wl.m)
                 rows.append(oracle.compress(C, Z, bias, wl.m))
             src = np.concatenate(rows) if rows else np.zeros((0, 512), np.float32)
-        return oracle.quant_mxfp4(src)
+        return oracle.KV_FORMATS[wl.kv_format][0](src)
 
     # the layer's window ring as the oracle quantises it
     def swa_ring(self, layer):
@@ -85,7 +85,8 @@ class SeqOracle:
         sel = sel[sel >= 0]
         kvc, kvs = self.kv(sel)
         swc, sws = ring if ring is not None else self.swa_ring(layer)
-        keys = oracle.attention_keys(kvc, kvs, np.arange(sel.size, dtype=np.int32), swc, sws, t)
+        keys = oracle.attention_keys(kvc, kvs, np.arange(sel.size, dtype=np.int32), swc, sws, t,
+                                     kv_format=self.wl.kv_format)
         q = self.wl.q_bits(layer, self.b, [i])[0]
         return oracle.attention(q, 1.0, keys)
 

@@ -57,6 +57,9 @@ def test_host_validation_without_gpu(lib):
                                 None, None) == -4                                # rows beyond the cache
     assert lib.csa2_quant_mxfp4(ctypes.c_void_p(8), 4, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 64,
                                 None, None) == -8                                # misaligned input
+    assert lib.csa2_quant_fp4_e4m3(None, 4, None, None, None, 64, None, None) == -1
+    assert lib.csa2_quant_fp4_e4m3(ctypes.c_void_p(8), 4, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 64,
+                                   None, None) == -8
     assert lib.csa2_topk(None, 10, None, 1, None, 0, None, None) == -2
     assert lib.csa2_topk(None, 10, None, 1, None, 5000, None, None) == -2
     assert lib.csa2_topk_blocks(None, 10, None, 1, 4096, None, None, None) == -2
@@ -65,11 +68,14 @@ def test_host_validation_without_gpu(lib):
     io = csa2.LayerIO()
     assert lib.csa2_layer(7, ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(io), None, 0, None) == -3
     assert lib.csa2_layer(0, ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(io), None, 0, None) == -1
-    cache = csa2.Cache(16, 16, 16, 16, 100, 16, 4, None)     # num_slots not a multiple of 64
+    cache = csa2.Cache(16, 16, 16, 16, 100, 16, 4, 0, None)  # num_slots not a multiple of 64
     assert lib.csa2_index_scores(ctypes.byref(cache), ctypes.byref(batch), 16, 16, 16, None, None, 8, None) == -2
-    cache = csa2.Cache(16, 16, 16, 16, 256, 16, 4, None)
+    cache = csa2.Cache(16, 16, 16, 16, 256, 16, 4, 0, None)
     batch = csa2.Batch(1, 1, 1, 0, 1000, 16, 16)             # more entries than 4 pages hold
     assert lib.csa2_index_scores(ctypes.byref(cache), ctypes.byref(batch), 16, 16, 16, None, None, 1000, None) == -4
+    cache = csa2.Cache(16, 16, 16, 16, 256, 16, 4, 7, None)  # unknown main-KV format
+    batch = csa2.Batch(1, 1, 1, 0, 100, 16, 16)
+    assert lib.csa2_index_scores(ctypes.byref(cache), ctypes.byref(batch), 16, 16, 16, None, None, 104, None) == -3
 
 
 def test_workspace_sizes(lib):

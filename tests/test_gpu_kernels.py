@@ -66,6 +66,32 @@ def test_quant_mxfp4_bit_exact():
     assert np.array_equal(got_c[perm[keep]], codes[keep]) and np.array_equal(got_s[perm[keep]], scales[keep])
 
 
+def test_quant_fp4_e4m3_bit_exact():
+    """FP4 with one E4M3 scale per 16 elements: bit-exact against the oracle,
+    including huge values (scale saturating at 448), signed zeros, subnormal
+    inputs (scale rounding to zero) and scattered destination slots."""
+    x = _special_rows(300, 512, 3)
+    x[6, :16] = 1.0
+    x[6, 16:32] = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -6.0, 0.0, -0.0, 3.0, 4.0, 1.5, 0.5, 2.0]
+    codes, scales = oracle.quant_fp4_e4m3(x)
+    xd = torch.from_numpy(x).cuda()
+    gc = torch.zeros((320, 256), dtype=torch.uint8, device="cuda")
+    gs = torch.zeros((320, 32), dtype=torch.uint8, device="cuda")
+    csa2.csa2_quant_fp4_e4m3(xd, gc, gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(gc[:300].cpu().numpy(), codes)
+    assert np.array_equal(gs[:300].cpu().numpy(), scales)
+    perm = np.random.default_rng(4).permutation(320)[:300].astype(np.int64)
+    perm[9] = -1
+    gc.zero_()
+    gs.zero_()
+    csa2.csa2_quant_fp4_e4m3(xd, gc, gs, slots=torch.from_numpy(perm).cuda())
+    torch.cuda.synchronize()
+    got_c, got_s = gc.cpu().numpy(), gs.cpu().numpy()
+    keep = perm >= 0
+    assert np.array_equal(got_c[perm[keep]], codes[keep]) and np.array_equal(got_s[perm[keep]], scales[keep])
+
+
 @pytest.mark.parametrize("dim", [128, 512])
 def test_quant_fp8_bit_exact(dim):
     x = _special_rows(257, dim, 3 + dim)

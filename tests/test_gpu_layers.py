@@ -186,3 +186,16 @@ def test_reindex_with_and_without_the_carried_pool_keys():
         assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
     for bb in range(wl.batch):
         _check_sequence(a, bb)
+
+
+def test_layers_with_fp4_e4m3_main_kv():
+    """The main KV in the 16-element / E4M3-scale FP4 format (csa2_cache.kv_format
+    = CSA2_KV_FP4_E4M3): selection and attention against the oracle, which
+    dequantises the same format, in every layer mode."""
+    wl = W.Workload("fp4_e4m3", 74, 3, [5000, 300, 20000], 1, ["full", "reuse", "reindex", "reuse"],
+                    planted_blocks=4, kv_format=1)
+    dw = DeviceWorkload(wl)
+    assert dw.cache.kv_scales.shape[1] == 32
+    _run_recording(dw)
+    for b in range(wl.batch):
+        _check_sequence(dw, b)
