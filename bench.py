@@ -39,6 +39,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=1 << 20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--kv-format", type=int, default=0, choices=[0, 1],
+                   help="main KV: 0 MXFP4 (32-element blocks, E8M0), 1 FP4 with an E4M3 scale per 16 elements")
     return p.parse_args()
 
 
@@ -125,7 +127,7 @@ class ClockSampler:
 class DecodeStep:
     """Device state and the launch sequence of one decode step."""
 
-    def __init__(self, batch, tokens, seed, device):
+    def __init__(self, batch, tokens, seed, device, kv_format=0):
         import numpy as np
         import torch
         from compressed_sparse_attention_layer_gb300 import csa2, synth
@@ -133,7 +135,7 @@ class DecodeStep:
         from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
 
         self.torch, self.csa2 = torch, csa2
-        self.wl = W.decode_1m(seed=seed, batch=batch, tokens=tokens)
+        self.wl = W.decode_1m(seed=seed, batch=batch, tokens=tokens, kv_format=kv_format)
         self.dw = DeviceWorkload(self.wl, device=device)
         wl, dw = self.wl, self.dw
         B, N = wl.batch, wl.tokens[0]
@@ -164,9 +166,10 @@ class DecodeStep:
 
     def enqueue(self, prof=True):
         csa2, dw, cache = self.csa2, self.dw, self.dw.cache
-        # a1: compress the new token (m = 1), a2: MXFP4 into the cache, a3: FP8 indexer key
+        # a1: compress the new token (m = 1), a2: FP4 main KV into the cache, a3: FP8 indexer key
         csa2.csa2_compress(self.C_new, self.Z_new, self.bias, 1, self.e_new)
-        csa2.csa2_quant_mxfp4(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
+        quant = csa2.csa2_quant_fp4_e4m3 if self.wl.kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
+        quant(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
         csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
         for l in dw.layers:
             # a3-a9: the layer; its attention call also quantises this layer's window
@@ -187,7 +190,7 @@ def run_native(args):
     build.build()
     csa2.load()
     dev = torch.device("cuda", local)
-    step = DecodeStep(args.batch, args.tokens, rank_seed(rank), dev)
+    step = DecodeStep(args.batch, args.tokens, rank_seed(rank), dev, kv_format=args.kv_format)
     B, N = step.wl.batch, step.wl.tokens[0]
 
     s = torch.cuda.Stream(device=dev)
@@ -302,6 +305,8 @@ def run_native(args):
         "config": {"workload": f"decode_1m: batch {B} x {N} tokens, m=1, 20-layer decoder stack "
                                "(Full+3 Reuse, 4x(Reindex+3 Reuse)), Top-512, SWA 128",
                    "batch": B, "context_tokens": N, "layers": len(step.wl.layers),
+                   "main_kv": ["MXFP4 (32-element blocks, E8M0 scale), 272 B/entry",
+                               "FP4 (16-element blocks, E4M3 scale), 288 B/entry"][args.kv_format],
                    "l2": "inputs larger than L2: the Full layer scans 1.1 GB of indexer keys per step",
                    "graph": "one CUDA graph per step"},
         "roofline": roofline, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,

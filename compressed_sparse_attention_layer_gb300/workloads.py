@@ -228,8 +228,9 @@ def prefill(seed: int = 3000, prefix: int = 65536, new: int = 8192) -> Workload:
                     swa_rows=new + W)
 
 
-def decode_1m(seed: int = 4000, batch: int = 8, tokens: int = 1 << 20, layers=None) -> Workload:
-    return Workload("decode_1m", seed, batch, [tokens] * batch, 1, list(layers or DECODER_STACK), planted_blocks=64)
+def decode_1m(seed: int = 4000, batch: int = 8, tokens: int = 1 << 20, layers=None, kv_format: int = 0) -> Workload:
+    return Workload("decode_1m", seed, batch, [tokens] * batch, 1, list(layers or DECODER_STACK), planted_blocks=64,
+                    kv_format=kv_format)
 
 
 def ragged_lengths(seed: int, batch: int, lo: int = 4096, hi: int = 1 << 20) -> List[int]:
