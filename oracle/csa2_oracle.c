@@ -407,19 +407,24 @@ int64_t or_block_pool(const double *score, int64_t n, int blk, int pmax, int32_t
  * nk == 0 gives o = 0 and lse = -inf.
  * [P2] §1 table (64 query heads x 512, top-k 512, SWA 128); [P3] §3.3 (the
  * window branch beside the compressed branch) and §4.3 (the compressed
- * entry serves as both key and value); one softmax over both branches. */
+ * entry serves as both key and value); one softmax over both branches.
+ *
+ * Options around it ([P3] §4.3 names a learnable attention sink and partial
+ * RoPE on the last 64 dims with the output rotated back):
+ *  - sink (NULL for none): per head a logit z_h that joins the softmax's
+ *    denominator without a value: o_h = sum_j e^l_j k_j / (e^z_h + sum_j e^l_j),
+ *    lse_h = log(e^z_h + sum_j e^l_j); z_h = -inf is no sink;
+ *  - rope_base > 0: the output's dims 448 + i and 480 + i (i < 32) are rotated
+ *    by -t * rope_base^(-i/32), t the query's token position:
+ *    (a, b) -> (a cos + b sin, -a sin + b cos). */
 void or_attention(const uint16_t *q, double sm_scale, const double *keys, int64_t nk,
-                  float *o, float *lse)
+                  const double *sink, double rope_base, int64_t t, float *o, float *lse)
 {
 #pragma omp parallel for schedule(static)
     for (int h = 0; h < 64; h++) {
-        if (nk == 0) {
-            for (int d = 0; d < 512; d++) o[h * 512 + d] = 0.0f;
-            lse[h] = -INFINITY;
-            continue;
-        }
-        double *l = (double *)malloc(sizeof(double) * (size_t)nk);
-        double mx = -INFINITY;
+        const double z = sink ? sink[h] : -INFINITY;
+        double *l = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+        double mx = z;
         for (int64_t j = 0; j < nk; j++) {
             double dot = 0.0;
             for (int d = 0; d < 512; d++)
@@ -427,14 +432,30 @@ void or_attention(const uint16_t *q, double sm_scale, const double *keys, int64_
             l[j] = sm_scale * dot;
             if (l[j] > mx) mx = l[j];
         }
-        double den = 0.0;
-        for (int64_t j = 0; j < nk; j++) den += exp(l[j] - mx);
-        for (int d = 0; d < 512; d++) {
-            double acc = 0.0;
-            for (int64_t j = 0; j < nk; j++) acc += exp(l[j] - mx) * keys[j * 512 + d];
-            o[h * 512 + d] = (float)(acc / den);
+        double out[512];
+        if (mx == -INFINITY) {               /* no key and no sink */
+            for (int d = 0; d < 512; d++) out[d] = 0.0;
+            lse[h] = -INFINITY;
+        } else {
+            double den = (z == -INFINITY) ? 0.0 : exp(z - mx);
+            for (int64_t j = 0; j < nk; j++) den += exp(l[j] - mx);
+            for (int d = 0; d < 512; d++) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < nk; j++) acc += exp(l[j] - mx) * keys[j * 512 + d];
+                out[d] = acc / den;
+            }
+            lse[h] = (float)(mx + log(den));
         }
-        lse[h] = (float)(mx + log(den));
+        if (rope_base > 0.0) {
+            for (int i = 0; i < 32; i++) {
+                const double th = (double)t * pow(rope_base, -(double)i / 32.0);
+                const double c = cos(th), sn = sin(th);
+                const double a = out[448 + i], b = out[480 + i];
+                out[448 + i] = a * c + b * sn;
+                out[480 + i] = -a * sn + b * c;
+            }
+        }
+        for (int d = 0; d < 512; d++) o[h * 512 + d] = (float)out[d];
         free(l);
     }
 }

@@ -83,7 +83,7 @@ def lib():
             L.or_topk.argtypes = [P, P, i64, i32, P]
             L.or_block_pool.restype = i64
             L.or_block_pool.argtypes = [P, i64, i32, i32, P]
-            L.or_attention.argtypes = [P, f64, P, i64, P, P]
+            L.or_attention.argtypes = [P, f64, P, i64, P, f64, i64, P, P]
             L.or_num_threads.restype = i32
             _lib = L
     return _lib
@@ -255,14 +255,28 @@ def attention_keys(kv_codes, kv_scales, idx, swa_codes, swa_scales, t: int,
     return np.concatenate([main, swa], axis=0)
 
 
-def attention(q_bits, sm_scale: float, keys: np.ndarray):
-    """o [64, 512] fp32, lse [64] fp32 of one query over dequantised keys."""
+def attention(q_bits, sm_scale: float, keys: np.ndarray, sink=None, rope_base: float = 0.0, t: int = 0):
+    """o [64, 512] fp32, lse [64] fp32 of one query over dequantised keys.
+    sink: optional per-head logits joining the softmax denominator; rope_base > 0:
+    the output's RoPE dims rotated back by the query position t (see the C source)."""
     q = _c(q_bits, np.uint16).reshape(64, 512)
     k = _c(keys, np.float64).reshape(-1, 512)
+    z = None if sink is None else _c(sink, np.float64).reshape(64)
     o = np.empty((64, 512), np.float32)
     lse = np.empty((64,), np.float32)
-    lib().or_attention(_p(q), float(sm_scale), _p(k), k.shape[0], _p(o), _p(lse))
+    lib().or_attention(_p(q), float(sm_scale), _p(k), k.shape[0], None if z is None else _p(z), float(rope_base),
+                       int(t), _p(o), _p(lse))
     return o, lse
+
+
+def dedup_selection(positions, t: int, m: int, swa_start: int = 0, W: int = SWA_W) -> np.ndarray:
+    """The selected positions without those whose token is also a window row
+    (m = 1 only: a compressed entry of m > 1 tokens is not a window row)."""
+    pos = np.asarray(positions, np.int64)
+    if m != 1:
+        return pos
+    lo, hi = swa_window(t, swa_start, W)
+    return pos[(pos < lo) | (pos > hi)]
 
 
 # ------------------------------------------------------------------ layers

@@ -206,3 +206,68 @@ def test_visibility_rule():
     assert oracle.n_visible(73727, 2, 36864) == 36864
     assert oracle.n_visible(65536, 2, 36864) == 32768
     assert oracle.n_visible(1048575, 1, 1048576) == 1048576
+
+
+# ---------------------------------------------------------------- attention options
+# [P3] §4.3 names a learnable attention sink and partial RoPE on the last 64
+# dims with the output rotated back; the window de-duplication is the option
+# of reading c12 (one softmax over both key sets by default).
+def _q_and_keys(seed, nk):
+    rng = np.random.default_rng(seed)
+    qb = torch.from_numpy((rng.standard_normal((64, 512)) / np.sqrt(512)).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    keys = rng.standard_normal((nk, 512))
+    return qb, keys
+
+
+def test_sink_minus_inf_is_no_sink():
+    qb, keys = _q_and_keys(31, 40)
+    o, lse = oracle.attention(qb, 1.0, keys)
+    o2, lse2 = oracle.attention(qb, 1.0, keys, sink=np.full(64, -np.inf))
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_sink_closed_forms():
+    qb, keys = _q_and_keys(32, 1)
+    q = torch.from_numpy(qb.view(np.int16)).view(torch.bfloat16).double().numpy()
+    z = np.linspace(-3, 3, 64)
+    o, lse = oracle.attention(qb, 1.0, keys, sink=z)
+    l = q @ keys[0]                                   # one key: o_h = k sigma(l_h - z_h)
+    w = 1.0 / (1.0 + np.exp(z - l))
+    assert np.allclose(o, w[:, None] * keys[0][None, :], rtol=1e-6, atol=1e-7)
+    assert np.allclose(lse, np.logaddexp(l, z), rtol=1e-6, atol=1e-6)
+    # many keys: lse with a sink = logaddexp(lse without it, z); o scales by the kept mass
+    qb, keys = _q_and_keys(33, 70)
+    o0, lse0 = oracle.attention(qb, 1.0, keys)
+    o1, lse1 = oracle.attention(qb, 1.0, keys, sink=z)
+    assert np.allclose(lse1, np.logaddexp(lse0.astype(np.float64), z), rtol=1e-6, atol=1e-6)
+    kept = np.exp(lse0.astype(np.float64) - np.logaddexp(lse0.astype(np.float64), z))
+    assert np.allclose(o1, o0 * kept[:, None], rtol=1e-5, atol=1e-7)
+    # no keys, a finite sink: o = 0, lse = z
+    o, lse = oracle.attention(qb, 1.0, np.zeros((0, 512)), sink=z)
+    assert np.all(o == 0) and np.allclose(lse, z.astype(np.float32))
+
+
+def test_output_rerotation():
+    qb, keys = _q_and_keys(34, 50)
+    o0, lse0 = oracle.attention(qb, 1.0, keys)
+    same, _ = oracle.attention(qb, 1.0, keys, rope_base=10000.0, t=0)
+    assert np.array_equal(same, o0)                                     # t = 0: identity
+    t = 987654
+    o1, lse1 = oracle.attention(qb, 1.0, keys, rope_base=10000.0, t=t)
+    assert np.array_equal(lse1, lse0)
+    assert np.array_equal(o1[:, :448], o0[:, :448])                     # only the last 64 dims move
+    # independent check: pairs (448+i, 480+i) as complex numbers times e^{-i t w_i}
+    w = 10000.0 ** (-np.arange(32) / 32.0)
+    zc = (o0[:, 448:480].astype(np.float64) + 1j * o0[:, 480:512]) * np.exp(-1j * np.mod(t * w, 2 * np.pi))
+    assert np.allclose(o1[:, 448:480], zc.real, atol=2e-7)
+    assert np.allclose(o1[:, 480:512], zc.imag, atol=2e-7)
+
+
+def test_dedup_selection():
+    t = 1000
+    sel = np.array([5, 871, 872, 873, 900, 999, 1000], np.int64)        # window of t: [873, 1000]
+    assert np.array_equal(oracle.dedup_selection(sel, t, 1), [5, 871, 872])
+    assert np.array_equal(oracle.dedup_selection(sel, t, 2), sel)      # compressed entries stay
+    assert np.array_equal(oracle.dedup_selection(sel, 50, 1), sel[sel > 50])
+    assert np.array_equal(oracle.dedup_selection(sel, t, 1, swa_start=950), [5, 871, 872, 873, 900])
