@@ -39,7 +39,8 @@ class Batch(ctypes.Structure):
 
 
 class Swa(ctypes.Structure):
-    _fields_ = [("codes", _vp), ("scales", _vp), ("rows", _i32), ("pad_", _i32), ("start", _vp), ("new_rows", _vp)]
+    _fields_ = [("codes", _vp), ("scales", _vp), ("rows", _i32), ("flags", _i32), ("start", _vp), ("new_rows", _vp),
+                ("sink", _vp), ("rope_base", _f32), ("pad_", _i32)]
 
 
 class LayerIO(ctypes.Structure):
@@ -160,11 +161,18 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
                  _ptr(q_pos, torch.int64, "q_pos"))
 
 
-def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None) -> Swa:
+ATTN_DEDUP_WINDOW = 1
+
+
+def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None, sink=None,
+               rope_base: float = 0.0, flags: int = 0) -> Swa:
     """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
-    into the ring by the attention call itself."""
+    into the ring by the attention call itself; sink: optional fp32 [64] per-head
+    sink logits; rope_base > 0 rotates the output's RoPE dims back by the query
+    position; flags: ATTN_DEDUP_WINDOW."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
-               0, _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"))
+               int(flags), _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"),
+               _ptr(sink, torch.float32, "sink"), float(rope_base), 0)
 
 
 # ---------------------------------------------------------------- entry points

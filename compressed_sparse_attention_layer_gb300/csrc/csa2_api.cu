@@ -67,6 +67,8 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
+    if (s->flags & ~CSA2_ATTN_DEDUP_WINDOW) return CSA2_ERR_UNSUPPORTED;
+    if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
     if (s->new_rows) {
         // the window of a query in a multi-token chunk holds other new tokens, which
         // must be in the ring before any query attends: quantise them first instead

@@ -262,10 +262,19 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     uint32_t ksc = 0;
     if (!window) {
         const int64_t vis = visible_entries(bt, r);   // issued alongside the index load
+        // window de-duplication (m = 1): a selected entry that is also a window row is dropped
+        int64_t dlo = 1, dhi = 0;
+        if ((swa.flags & CSA2_ATTN_DEDUP_WINDOW) && bt.m == 1) {
+            dhi = bt.q_pos[r];
+            const int64_t s0 = swa.start ? swa.start[b] : 0;
+            dlo = dhi - (CSA2_SWA_WINDOW - 1);
+            dlo = dlo < s0 ? s0 : dlo;
+            dlo = dlo < 0 ? 0 : dlo;
+        }
         const int j = chunk * AC_KEYS + key;
         if (j < k) {
             const int32_t p = idx[r * k + j];
-            if (p >= 0) {
+            if (p >= 0 && !(p >= dlo && p <= dhi)) {
                 if (p >= vis) {
                     if (hf == 0 && dq == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
                 } else {
@@ -549,12 +558,17 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     if (warp == 0) tc::tmem_dealloc(tmem, AC_TMEM_COLS);
 }
 
-// o = sum_c e^(m_c - M) O_c / sum_c e^(m_c - M) l_c, lse = M + log L; one CTA per
-// (row, 2 heads), thread = 4 consecutive dims (float4) of one head, all chunk
-// loads in flight.  Launched as a programmatic dependent of the attention
-// kernel: it is scheduled early and waits for that grid's results here.
+// o = sum_c e^(m_c - M) O_c / (sum_c e^(m_c - M) l_c + e^(z_h - M)), lse = M +
+// log of that denominator (z_h the head's sink logit, -inf without one); one
+// CTA per (row, 2 heads), thread = 4 consecutive dims (float4) of one head,
+// all chunk loads in flight.  With rope_base > 0 the RoPE dims 448+i and
+// 480+i of the output are rotated back by -t * rope_base^(-i/32) (angles in
+// double precision: t reaches 2^20).  Launched as a programmatic dependent of
+// the attention kernel: it is scheduled early and waits for that grid here.
 __global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml, int nchunks,
+                                                      const float *__restrict__ sink, float rope_base,
+                                                      const int64_t *__restrict__ q_pos,
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
     // the next kernel on the stream may be scheduled now; it waits for this grid
@@ -595,9 +609,41 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ 
             acc.w = fmaf(wgt, v[ch].w, acc.w);
         }
     }
+    const float z = sink ? sink[h] : -INFINITY;
+    if (z != -INFINITY) {
+        if (M == -INFINITY || z > M) {              // the sink sets the reference maximum
+            const float f = M == -INFINITY ? 0.0f : expf(M - z);
+            L = fmaf(L, f, 1.0f);
+            acc = make_float4(acc.x * f, acc.y * f, acc.z * f, acc.w * f);
+            M = z;
+        } else {
+            L += expf(z - M);
+        }
+    }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    *reinterpret_cast<float4 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 4 * tid) =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    float4 out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (rope_base > 0.0f && tid >= 96) {            // the warp holding dims 384..511
+        // dims 448+i (threads 112..119) pair with 480+i (threads 120..127), 8 lanes apart
+        const float4 other = make_float4(__shfl_xor_sync(0xffffffffu, out.x, 8), __shfl_xor_sync(0xffffffffu, out.y, 8),
+                                         __shfl_xor_sync(0xffffffffu, out.z, 8), __shfl_xor_sync(0xffffffffu, out.w, 8));
+        if (tid >= 112) {
+            const bool first = tid < 120;
+            const int i0 = 4 * (tid - (first ? 112 : 120));
+            const double t = (double)q_pos[r];
+            float rot[4];
+            const float mine[4] = {out.x, out.y, out.z, out.w}, oth[4] = {other.x, other.y, other.z, other.w};
+#pragma unroll
+            for (int c4 = 0; c4 < 4; c4++) {
+                double sd, cd;
+                sincos(t * pow((double)rope_base, -(double)(i0 + c4) / 32.0), &sd, &cd);
+                const float cs = (float)cd, sn = (float)sd;
+                // (a, b) -> (a cos + b sin, -a sin + b cos); this thread holds a (first) or b
+                rot[c4] = first ? fmaf(mine[c4], cs, oth[c4] * sn) : fmaf(mine[c4], cs, -oth[c4] * sn);
+            }
+            out = make_float4(rot[0], rot[1], rot[2], rot[3]);
+        }
+    }
+    *reinterpret_cast<float4 *>(o + (r * CSA2_HEADS + h) * CSA2_HEAD_DIM + 4 * tid) = out;
     if (tid == 0) lse[r * CSA2_HEADS + h] = L > 0.0f ? M + logf(L) : -INFINITY;
 }
 
@@ -656,7 +702,7 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
     cfg.attrs = at;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_combine, (const float *)part_o, (const float *)part_ml,
-                                             nchunks, o, lse);
+                                             nchunks, swa.sink, swa.rope_base, bt.q_pos, o, lse);
     if (e != cudaSuccess) {
         set_cuda_error(e);
         return CSA2_ERR_CUDA;

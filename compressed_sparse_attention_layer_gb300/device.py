@@ -98,6 +98,9 @@ class DeviceWorkload:
         self.pool = torch.full((R, csa2.POOL_MAX), -1, dtype=torch.int32, device=dev)
         self.pool_len = torch.zeros((R,), dtype=torch.int32, device=dev)
         self.pool_keys = None
+        # attention options passed to every layer call (csa2.swa_struct keywords:
+        # sink, rope_base, flags); none by default
+        self.attn_options = {}
         if self.carry_pool_keys and "reindex" in wl.layers:
             self.pool_keys = (torch.empty((R, csa2.POOL_MAX, 128), dtype=torch.uint8, device=dev),
                               torch.empty((R, csa2.POOL_MAX), dtype=torch.float32, device=dev))
@@ -139,7 +142,7 @@ class DeviceWorkload:
         self.swa_scales[l] = scales
 
     def swa(self, l, new_rows=None) -> csa2.Swa:
-        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows)
+        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows, **self.attn_options)
 
     def swa_new_rows(self, l) -> torch.Tensor:
         """fp32 [B][512]: the window row of each sequence's decode token (nq = 1)."""

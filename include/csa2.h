@@ -144,7 +144,7 @@ typedef struct csa2_swa {
     const uint8_t *codes;        /* [B][rows][512] e4m3                       */
     const float   *scales;       /* [B][rows] fp32 per-token scale            */
     int32_t        rows;         /* ring capacity, >= 128                     */
-    int32_t        pad_;
+    int32_t        flags;        /* CSA2_ATTN_* option bits                   */
     const int64_t *start;        /* [B] replay start s, or NULL               */
     const float   *new_rows;     /* NULL, or fp32 [B][512] (decode, Q = 1):   */
                                  /* the window row of each query's own token, */
@@ -152,7 +152,22 @@ typedef struct csa2_swa {
                                  /* into ring row q_pos % rows (codes and     */
                                  /* scale written, as csa2_quant_fp8 would)   */
                                  /* before it is attended; 16-byte aligned    */
+    const float   *sink;         /* NULL, or fp32 [64]: per-head sink logit z_h
+                                    joining the softmax denominator without a
+                                    value ([P3] §4.3): o_h = sum e^l k /
+                                    (e^z_h + sum e^l), lse_h = log(e^z_h +
+                                    sum e^l); -inf is no sink                 */
+    float          rope_base;    /* > 0: rotate the output's RoPE dims back by
+                                    the query position t ([P3] §4.3 partial
+                                    RoPE on the last 64 dims): dims 448+i and
+                                    480+i (i < 32) by -t * rope_base^(-i/32);
+                                    0: no rotation                             */
+    int32_t        pad_;
 } csa2_swa;
+
+/* csa2_swa.flags: drop the selected entries whose token is also in the
+ * query's window (m = 1; the window row stays) instead of attending to both. */
+#define CSA2_ATTN_DEDUP_WINDOW 1
 
 /* Per-layer inputs, outputs and carried selection state for csa2_layer. */
 typedef struct csa2_layer_io {

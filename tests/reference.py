@@ -79,16 +79,21 @@ class SeqOracle:
         codes, scales = self.ik()
         return oracle.index_scores(qi, w, codes, scales, positions=np.asarray(positions, np.int32))
 
-    def attention(self, layer, i, idx, ring=None):
+    def attention(self, layer, i, idx, ring=None, sink=None, rope_base=0.0, dedup=False):
+        """o, lse of query i over the selected entries idx and its window; sink,
+        rope_base and dedup (drop selected entries that are window rows) as in
+        oracle.attention / oracle.dedup_selection."""
         t, _ = self.visible(i)
         sel = np.asarray(idx, np.int64)
         sel = sel[sel >= 0]
+        if dedup:
+            sel = oracle.dedup_selection(sel, t, self.wl.m)
         kvc, kvs = self.kv(sel)
         swc, sws = ring if ring is not None else self.swa_ring(layer)
         keys = oracle.attention_keys(kvc, kvs, np.arange(sel.size, dtype=np.int32), swc, sws, t,
                                      kv_format=self.wl.kv_format)
         q = self.wl.q_bits(layer, self.b, [i])[0]
-        return oracle.attention(q, 1.0, keys)
+        return oracle.attention(q, 1.0, keys, sink=sink, rope_base=rope_base, t=t)
 
     def layers(self, i, upto=None):
         """Expected (idx, o, lse) of query i for each layer, run in order."""

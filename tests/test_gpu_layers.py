@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import oracle
+from compressed_sparse_attention_layer_gb300 import csa2
 from compressed_sparse_attention_layer_gb300 import workloads as W
 from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
 from tests.reference import SeqOracle, attn_close, topk_valid
@@ -199,3 +200,31 @@ def test_layers_with_fp4_e4m3_main_kv():
     _run_recording(dw)
     for b in range(wl.batch):
         _check_sequence(dw, b)
+
+
+@pytest.mark.parametrize("tokens", [[300, 5000, 1000], [200, 200000, 1100]])
+def test_attention_options_sink_rotation_dedup(tokens):
+    """Per-head sink logits, the output's RoPE dims rotated back by the query
+    position and the de-duplication of selected entries that are also window
+    rows (m = 1), in Full / Reuse / Reindex layers, against the oracle with the
+    same options.  Short contexts select every visible entry, so the window's
+    rows are all duplicates there."""
+    wl = W.Workload("attn_opts", 75, 3, tokens, 1, ["full", "reuse", "reindex"], planted_blocks=2)
+    dw = DeviceWorkload(wl)
+    g = np.random.default_rng(75)
+    sink = g.normal(2.0, 3.0, 64).astype(np.float32)
+    sink[:4] = [-np.inf, 40.0, -40.0, 0.0]          # no sink, a sink that dominates, one that vanishes
+    dw.attn_options = dict(sink=torch.from_numpy(sink).to(dw.dev), rope_base=10000.0,
+                           flags=csa2.ATTN_DEDUP_WINDOW)
+    _run_recording(dw)
+    for b in range(wl.batch):
+        so = SeqOracle(wl, b)
+        for l in range(len(wl.layers)):
+            o_ref, lse_ref = so.attention(l, 0, dw.hist_idx[l][b], sink=sink, rope_base=10000.0, dedup=True)
+            ok, info = attn_close(dw.o[l][b].cpu().numpy(), dw.lse[l][b].cpu().numpy(), o_ref, lse_ref)
+            assert ok, (b, l, info)
+    # the selection itself is unchanged by the options
+    plain = DeviceWorkload(wl)
+    _run_recording(plain)
+    for l in range(len(wl.layers)):
+        assert np.array_equal(plain.hist_idx[l], dw.hist_idx[l]), l
