@@ -171,11 +171,27 @@ class DecodeStep:
         quant = csa2.csa2_quant_fp4_e4m3 if self.wl.kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
         quant(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
         csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
-        for l in dw.layers:
+        self.enqueue_layers(dw.layers, prof)
+
+    def enqueue_layers(self, layers, prof=False):
+        for l in layers:
             # a3-a9: the layer; its attention call also quantises this layer's window
             # row of the new token into the ring (csa2_swa.new_rows)
             full = self.wl.layers[l] == "full"
-            dw.run_layer(l, prof=self.scan_ev if (prof and full) else None, new_rows=self.swa_new[l])
+            self.dw.run_layer(l, prof=self.scan_ev if (prof and full) else None, new_rows=self.swa_new[l])
+
+    def layer_bytes(self):
+        """Algorithmic bytes per query token of each layer mode: what the method
+        must read and write (indexer keys scanned or rescored, the selected main-KV
+        entries, the window rows, q / qi / w, the pool or indices, o and lse)."""
+        wl = self.wl
+        E = wl.entries(0)
+        kv = 256 + self.csa2.KV_SCALE_BYTES[wl.kv_format]      # codes + block scales per entry
+        attn = 512 * kv + 128 * 516 + 64 * 512 * 2 + 64 * 512 * 4 + 64 * 4
+        pool = min(self.csa2.POOL_MAX, E)
+        return {"full": E * 132 + (E // 8) * 4 + 32 * 128 * 2 + 32 * 4 + attn,
+                "reindex": pool * 132 + pool * 4 + 32 * 128 * 2 + 32 * 4 + attn,
+                "reuse": 512 * 4 + attn}
 
 
 def run_native(args):
@@ -232,6 +248,30 @@ def run_native(args):
             g.replay()
         torch.cuda.synchronize()
         scan_ms.append(step.scan_ev[0].elapsed_time(step.scan_ev[1]))
+    # per layer mode: the step's layers of one mode captured back to back in a
+    # graph of their own (the same launches, the same programmatic overlap
+    # between consecutive layers), replayed after the timed region
+    per_mode_ms = {}
+    for mode in ("full", "reindex", "reuse"):
+        ls = [l for l in step.dw.layers if step.wl.layers[l] == mode]
+        if not ls:
+            continue
+        reps = max(1, 8 // len(ls))
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm, stream=s):
+            for _ in range(reps):
+                step.enqueue_layers(ls)
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(5):
+            with torch.cuda.stream(s):
+                ev0.record(s)
+                gm.replay()
+                ev1.record(s)
+            torch.cuda.synchronize()
+            t.append(ev0.elapsed_time(ev1) / (reps * len(ls)))
+        per_mode_ms[mode] = (len(ls), statistics.median(t))
+        del gm
     ms_total = reduce_max(ms, dev, world)
     ms_step = ms_total / args.steps
     value = throughput(world, B, args.steps, ms_total / 1e3)
@@ -293,6 +333,23 @@ def run_native(args):
                 "kernel": "index scan (Full layer)", "kernel_ms": scan_avg,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks else "fallback"}
 
+    # per layer mode: median layer time, query tokens/s of that layer alone, and its
+    # algorithmic bytes over that time against the same peak
+    lb = step.layer_bytes()
+    per_mode = {}
+    for mode, (n, lms) in per_mode_ms.items():
+        gbs = B * lb[mode] / (lms * 1e-3) / 1e9
+        per_mode[mode] = {"layers": n, "us_per_layer": 1e3 * lms, "query_tokens_per_s": B / (lms * 1e-3),
+                          "algo_bytes_per_token": lb[mode], "achieved_gbs": gbs, "frac": gbs / peak}
+    stack_bytes = sum(lb[m] for m in step.wl.layers)
+    rest = ms_step - sum(n * lms for n, lms in per_mode_ms.values())
+    per_mode["stack"] = {"us": 1e3 * ms_step, "algo_bytes_per_token": stack_bytes,
+                         "achieved_gbs": B * stack_bytes / (ms_step * 1e-3) / 1e9,
+                         "frac": B * stack_bytes / (ms_step * 1e-3) / 1e9 / peak,
+                         "us_outside_layers": 1e3 * rest,
+                         "note": "layer times: each mode's layers of the step captured back to back in a "
+                                 "graph of their own; outside: the new token's quantisation and launch gaps"}
+
     cpu = None
     if not args.no_cpu_baseline:
         cpu = cpu_baseline(step.wl)
@@ -309,7 +366,7 @@ def run_native(args):
                                "FP4 (16-element blocks, E4M3 scale), 288 B/entry"][args.kv_format],
                    "l2": "inputs larger than L2: the Full layer scans 1.1 GB of indexer keys per step",
                    "graph": "one CUDA graph per step"},
-        "roofline": roofline, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
+        "roofline": roofline, "per_layer_mode": per_mode, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -162,6 +162,7 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
 
 
 ATTN_DEDUP_WINDOW = 1
+ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
 
 
 def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None, sink=None,
@@ -169,7 +170,7 @@ def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=N
     """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
     into the ring by the attention call itself; sink: optional fp32 [64] per-head
     sink logits; rope_base > 0 rotates the output's RoPE dims back by the query
-    position; flags: ATTN_DEDUP_WINDOW."""
+    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
                int(flags), _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"),
                _ptr(sink, torch.float32, "sink"), float(rope_base), 0)

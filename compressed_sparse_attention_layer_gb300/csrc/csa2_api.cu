@@ -32,7 +32,7 @@ int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
-                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t);
+                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
 size_t attn_workspace_bytes(int64_t rows);
 int topk_max_k();
 int64_t topk_max_len();
@@ -67,7 +67,7 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
-    if (s->flags & ~CSA2_ATTN_DEDUP_WINDOW) return CSA2_ERR_UNSUPPORTED;
+    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS)) return CSA2_ERR_UNSUPPORTED;
     if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
     if (s->new_rows) {
         // the window of a query in a multi-token chunk holds other new tokens, which
@@ -260,7 +260,7 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
     if (!aligned(q, 16) || !aligned(o, 16)) return CSA2_ERR_ALIGN;
     return launch_attn(*cache, *batch, q, sm_scale, idx, k, *swa, o, lse, workspace, workspace_bytes,
-                       (cudaStream_t)stream);
+                       (cudaStream_t)stream, false);
 }
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
@@ -344,8 +344,9 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
             return s;
     }
     // a8 (REUSE) keeps io->idx as it is; a9 for every mode
+    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call
     return launch_attn(*cache, *batch, io->q, io->sm_scale, io->idx, CSA2_TOPK, io->swa, io->o, io->lse,
-                       ws.attn, ws.attn_bytes, st);
+                       ws.attn, ws.attn_bytes, st, mode == CSA2_MODE_REUSE && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS));
 }
 
 }  // extern "C"

@@ -204,7 +204,7 @@ __device__ __forceinline__ void zero_key(uint8_t *ktile, uint32_t row, int hf)
 __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_CL == 4 ? 2 : 1)
     k_attn_tc(csa2_cache c, csa2_batch bt, const uint16_t *__restrict__ q, float sm_scale,
               const int32_t *__restrict__ idx, int k, csa2_swa swa, float *__restrict__ part_o,
-              float *__restrict__ part_ml, int nchunks)
+              float *__restrict__ part_ml, int nchunks, int early)
 {
     extern __shared__ uint8_t smem_raw[];
     AcSmem &S = *reinterpret_cast<AcSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -238,29 +238,23 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const uint32_t v = e2m1x2_to_bf16x2((uint32_t)ch >> 3);
         reinterpret_cast<uint4 *>(&S.e2m1_pair[0][0])[ch] = make_uint4(v, v, v, v);
     }
-    // Launched as a programmatic dependent of the previous kernel on the stream:
-    // everything above touches only this CTA's own state; inputs are read below,
-    // after that kernel has completed.
-    pdl_wait();
-
-    // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
-    constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
-    uint4 qv[4];
-    {
-        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM + AC_DIMS * dq);
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int e = tid + AC_THREADS * i;
-            qv[i] = __ldg(src + (e / QCH) * (CSA2_HEAD_DIM / 8) + (e % QCH));
-        }
-    }
-
-    // ---- this thread's key: locate it and start loading its 64 dims
+    // ---- this thread's key: locate it and load its 64 dims
     float kscale = 1.0f;          // multiplies the logit and the probability (window rows)
     bool valid = false;
     uint4 kc[4];
     uint32_t ksc = 0;
-    if (!window) {
+    int64_t t = 0, lo = 0;
+    int kn = -1;                  // the query's own token in the window chunk (when in it)
+    if (window) {
+        t = bt.q_pos[r];
+        const int64_t s0 = swa.start ? swa.start[b] : 0;
+        lo = t - (CSA2_SWA_WINDOW - 1);
+        lo = lo < s0 ? s0 : lo;
+        lo = lo < 0 ? 0 : lo;
+        kn = (int)(t - lo);
+    }
+    // the selected entry of this thread's key (main KV)
+    auto load_selected = [&]() {
         const int64_t vis = visible_entries(bt, r);   // issued alongside the index load
         // window de-duplication (m = 1): a selected entry that is also a window row is dropped
         int64_t dlo = 1, dhi = 0;
@@ -294,52 +288,104 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
                 }
             }
         }
-    } else {
-        const int64_t t = bt.q_pos[r];
-        const int64_t s0 = swa.start ? swa.start[b] : 0;
-        int64_t lo = t - (CSA2_SWA_WINDOW - 1);
-        lo = lo < s0 ? s0 : lo;
-        lo = lo < 0 ? 0 : lo;
-        const int kn = (int)(t - lo);                 // the query's own token (when it is in the window)
-        if (swa.new_rows && kn >= 0 && kn < AC_KEYS && (warp & 3) == (kn >> 5)) {
-            // this warp holds the new token's key in lane kn % 32: the whole warp takes
-            // the row's largest magnitude; the 16 lanes that loaded this thread-slab's
-            // dims (float4 chunks base .. base + 15 of the row) each quantise four of
-            // them exactly as the FP8 quantiser would and store them to the ring; the
-            // key's lane collects the 16 words
-            const float4 *nr = reinterpret_cast<const float4 *>(swa.new_rows + r * CSA2_HEAD_DIM);
-            float4 v[4];
-            float amax = 0.0f;
+    };
+    // a window row other than the query's own token's
+    auto load_window_row = [&]() {
+        if (lo + key <= t && key != kn) {
+            const int64_t off = (int64_t)b * swa.rows + (lo + key) % swa.rows;
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(swa.codes + off * CSA2_HEAD_DIM + AC_DIMS * dq) + 4 * hf;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; c4++) {
-                v[c4] = __ldg(nr + c4 * 32 + lane);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[c4].x), fabsf(v[c4].y)), fmaxf(fabsf(v[c4].z), fabsf(v[c4].w))));
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float sc = fp8_row_scale(amax);
-            const int base = (AC_DIMS * (int)dq + 64 * hf) / 4;          // first float4 of the slab
-            const int cb = base >> 5, lb = base & 31;                     // its register and lane
-            const float4 x = cb == 0 ? v[0] : cb == 1 ? v[1] : cb == 2 ? v[2] : v[3];
-            const uint32_t wd = f32x2_to_e4m3x2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc)) |
-                                (f32x2_to_e4m3x2(__fdiv_rn(x.z, sc), __fdiv_rn(x.w, sc)) << 16);
-            const int64_t off = (int64_t)b * swa.rows + t % swa.rows;
-            if (lane >= lb && lane < lb + 16)
-                reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(swa.codes) + off * CSA2_HEAD_DIM)[base + (lane - lb)] = wd;
-            uint32_t got[16];
-#pragma unroll
-            for (int q2 = 0; q2 < 16; q2++) got[q2] = __shfl_sync(0xffffffffu, wd, lb + q2);
-            if (key == kn) {
-#pragma unroll
-                for (int i = 0; i < 4; i++) kc[i] = make_uint4(got[4 * i], got[4 * i + 1], got[4 * i + 2], got[4 * i + 3]);
-                if (dq == 0 && hf == 0) const_cast<float *>(swa.scales)[off] = sc;
-                kscale = sc;
-                valid = true;
-            }
+            for (int i = 0; i < 4; i++) kc[i] = __ldg(src + i);
+            kscale = swa.scales[off];
+            valid = true;
         }
-        if (lo + key <= t && !(swa.new_rows && key == kn)) {
-            const int64_t row = (lo + key) % swa.rows;
-            const int64_t off = (int64_t)b * swa.rows + row;
+    };
+    // dequantise the loaded key into row `key` of the key tile (zeros if none)
+    auto store_key = [&]() {
+        if (valid) {
+            if (window) store_window_key(S.k, key, kc, hf);
+            else if (c.kv_format == CSA2_KV_FP4_E4M3) store_main_key<true>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
+            else store_main_key<false>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
+        } else {
+            zero_key(S.k, key, hf);
+        }
+        if (hf == 0) S.kscale[key] = valid ? kscale : -1.0f;
+    };
+
+    // Launched as a programmatic dependent of the previous kernel on the stream:
+    // everything before the wait touches only this CTA's own state, except with
+    // `early`, where the caller has guaranteed that the index array, the selected
+    // entries and the window rows other than the query's own token were written
+    // before that kernel's predecessors (a Reuse layer after another layer call):
+    // those keys are then loaded and dequantised while that kernel finishes.
+    bool stored = false;
+    if (early) {
+        if (window) load_window_row();
+        else load_selected();
+        __syncthreads();                           // the pair table is ready
+        if (!window || key != kn) {
+            store_key();
+            stored = true;
+        }
+    }
+    pdl_wait();
+
+    // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
+    constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
+    uint4 qv[4];
+    {
+        const uint4 *src = reinterpret_cast<const uint4 *>(q + r * CSA2_HEADS * CSA2_HEAD_DIM + AC_DIMS * dq);
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int e = tid + AC_THREADS * i;
+            qv[i] = __ldg(src + (e / QCH) * (CSA2_HEAD_DIM / 8) + (e % QCH));
+        }
+    }
+    if (!early) {
+        if (window) load_window_row();
+        else load_selected();
+    }
+    if (window && kn >= 0 && kn < AC_KEYS) {
+        if (swa.new_rows) {
+            if ((warp & 3) == (kn >> 5)) {
+                // this warp holds the new token's key in lane kn % 32: the whole warp takes
+                // the row's largest magnitude; the 16 lanes that loaded this thread-slab's
+                // dims (float4 chunks base .. base + 15 of the row) each quantise four of
+                // them exactly as the FP8 quantiser would and store them to the ring; the
+                // key's lane collects the 16 words
+                const float4 *nr = reinterpret_cast<const float4 *>(swa.new_rows + r * CSA2_HEAD_DIM);
+                float4 v[4];
+                float amax = 0.0f;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) {
+                    v[c4] = __ldg(nr + c4 * 32 + lane);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[c4].x), fabsf(v[c4].y)), fmaxf(fabsf(v[c4].z), fabsf(v[c4].w))));
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sc = fp8_row_scale(amax);
+                const int base = (AC_DIMS * (int)dq + 64 * hf) / 4;          // first float4 of the slab
+                const int cb = base >> 5, lb = base & 31;                     // its register and lane
+                const float4 x = cb == 0 ? v[0] : cb == 1 ? v[1] : cb == 2 ? v[2] : v[3];
+                const uint32_t wd = f32x2_to_e4m3x2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc)) |
+                                    (f32x2_to_e4m3x2(__fdiv_rn(x.z, sc), __fdiv_rn(x.w, sc)) << 16);
+                const int64_t off = (int64_t)b * swa.rows + t % swa.rows;
+                if (lane >= lb && lane < lb + 16)
+                    reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(swa.codes) + off * CSA2_HEAD_DIM)[base + (lane - lb)] = wd;
+                uint32_t got[16];
+#pragma unroll
+                for (int q2 = 0; q2 < 16; q2++) got[q2] = __shfl_sync(0xffffffffu, wd, lb + q2);
+                if (key == kn) {
+#pragma unroll
+                    for (int i = 0; i < 4; i++) kc[i] = make_uint4(got[4 * i], got[4 * i + 1], got[4 * i + 2], got[4 * i + 3]);
+                    if (dq == 0 && hf == 0) const_cast<float *>(swa.scales)[off] = sc;
+                    kscale = sc;
+                    valid = true;
+                }
+            }
+        } else if (key == kn) {                    // the own token's row, written before this call
+            const int64_t off = (int64_t)b * swa.rows + t % swa.rows;
             const uint4 *src =
                 reinterpret_cast<const uint4 *>(swa.codes + off * CSA2_HEAD_DIM + AC_DIMS * dq) + 4 * hf;
 #pragma unroll
@@ -355,19 +401,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         const int e = tid + AC_THREADS * i;
         *reinterpret_cast<uint4 *>(S.u.q + tc::sw128_offset(e / QCH, 8 * (e % QCH), CSA2_HEADS)) = qv[i];
     }
-    if (hf == 0) {
-        S.kscale[key] = valid ? kscale : -1.0f;
-    }
     __syncthreads();                               // the pair table is ready
-
-    // ---- dequantise into row `key` of the key tile
-    if (valid) {
-        if (window) store_window_key(S.k, key, kc, hf);
-        else if (c.kv_format == CSA2_KV_FP4_E4M3) store_main_key<true>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
-        else store_main_key<false>(S.k, key, kc, ksc, hf, S.e2m1_pair, (uint32_t)lane);
-    } else {
-        zero_key(S.k, key, hf);
-    }
+    if (!stored) store_key();
 
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -655,7 +690,8 @@ size_t attn_workspace_bytes(int64_t rows)
 }
 
 int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, float sm_scale, const int32_t *idx,
-                int k, const csa2_swa &swa, float *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st)
+                int k, const csa2_swa &swa, float *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
+                bool early)
 {
     const int64_t rows = (int64_t)bt.batch * bt.nq;
     if (rows == 0) return CSA2_OK;
@@ -684,7 +720,7 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
         ac.attrs = pdl;
         ac.numAttrs = 1;
         const cudaError_t e = cudaLaunchKernelEx(&ac, k_attn_tc, c, bt, q, sm_scale, idx, k, swa, part_o, part_ml,
-                                                 nchunks);
+                                                 nchunks, (int)early);
         if (e != cudaSuccess) {
             set_cuda_error(e);
             return CSA2_ERR_CUDA;

@@ -101,6 +101,9 @@ class DeviceWorkload:
         # attention options passed to every layer call (csa2.swa_struct keywords:
         # sink, rope_base, flags); none by default
         self.attn_options = {}
+        # Reuse layers load their keys while the previous layer finishes
+        # (csa2.ATTN_EARLY_INPUTS): the layers are called one after the other
+        self.early_inputs = True
         if self.carry_pool_keys and "reindex" in wl.layers:
             self.pool_keys = (torch.empty((R, csa2.POOL_MAX, 128), dtype=torch.uint8, device=dev),
                               torch.empty((R, csa2.POOL_MAX), dtype=torch.float32, device=dev))
@@ -142,7 +145,11 @@ class DeviceWorkload:
         self.swa_scales[l] = scales
 
     def swa(self, l, new_rows=None) -> csa2.Swa:
-        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows, **self.attn_options)
+        opts = dict(self.attn_options)
+        if self.early_inputs and self.wl.layers[l] == "reuse":
+            # every layer call follows the previous one on the stream (run / run_layer in order)
+            opts["flags"] = opts.get("flags", 0) | csa2.ATTN_EARLY_INPUTS
+        return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows, **opts)
 
     def swa_new_rows(self, l) -> torch.Tensor:
         """fp32 [B][512]: the window row of each sequence's decode token (nq = 1)."""

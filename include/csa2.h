@@ -168,6 +168,16 @@ typedef struct csa2_swa {
 /* csa2_swa.flags: drop the selected entries whose token is also in the
  * query's window (m = 1; the window row stays) instead of attending to both. */
 #define CSA2_ATTN_DEDUP_WINDOW 1
+/* csa2_swa.flags, honoured by csa2_layer in REUSE mode (ignored elsewhere):
+ * the caller guarantees that the previous call into this library on the same
+ * stream was csa2_layer, and that the index array, the main-KV entries it
+ * selects, the window rows other than each query's own token and the batch
+ * description were all written before that call's attention.  The attention
+ * then loads and dequantises those keys while the previous layer's last kernel
+ * is still running (q and new_rows are still read only after that kernel has
+ * completed).  A decode stack that calls csa2_layer layer after layer, with
+ * the window rows of its own tokens passed as new_rows, satisfies it. */
+#define CSA2_ATTN_EARLY_INPUTS 2
 
 /* Per-layer inputs, outputs and carried selection state for csa2_layer. */
 typedef struct csa2_layer_io {

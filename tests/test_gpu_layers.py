@@ -228,3 +228,26 @@ def test_attention_options_sink_rotation_dedup(tokens):
     _run_recording(plain)
     for l in range(len(wl.layers)):
         assert np.array_equal(plain.hist_idx[l], dw.hist_idx[l]), l
+
+
+def test_reuse_keys_loaded_early_bit_identical():
+    """Reuse layers that load and dequantise their keys while the previous
+    layer's merge is still running (csa2.ATTN_EARLY_INPUTS) give the same o and
+    lse, bit for bit, as Reuse layers that load them after it; the window rows
+    of the decode tokens are quantised inside the calls in both."""
+    wl = W.Workload("early", 76, 3, [6000, 700, 90000], 1,
+                    ["full", "reuse", "reuse", "reindex", "reuse"], planted_blocks=4)
+    runs = []
+    for early in (False, True):
+        dw = DeviceWorkload(wl)
+        dw.early_inputs = early
+        for l in dw.layers:
+            dw.run_layer(l, new_rows=dw.swa_new_rows(l))
+        torch.cuda.synchronize()
+        assert int(dw.cache.status[0]) == 0
+        runs.append(dw)
+    a, b = runs
+    for l in a.layers:
+        assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
+        assert torch.equal(a.lse[l].view(torch.int32), b.lse[l].view(torch.int32)), l
+        assert torch.equal(a.swa_codes[l], b.swa_codes[l]), l
