@@ -335,25 +335,37 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
 
 // ---------------------------------------------------------------- one CTA per row, keys in registers
 // Rows of up to RS_MAX = 16,384 keys: 1,024 threads hold 16 consecutive slots
-// each (thread t: slots 16 t .. 16 t + 15) as order keys in registers.  The
-// k-th largest key T is found by a radix select on (key - kmin) over the
-// row's actual range, 8 bits per round from the top, each round counted in
-// per-warp shared-memory histograms (no atomics across warps) and summed per
-// bin; one packed block scan of (count > T, count == T) then places every
-// selected slot: rank = slots above T before it + the ties before it, ties
-// taken lowest slot first -- so the output is in ascending slot order and
-// identical on every run.
+// each (thread t: slots 16 t .. 16 t + 15) as order keys in registers.
+//  1. A lower bound L of the k-th largest key (k <= 512): the 512 groups of
+//     32 keys (one register index of one warp) each hold a key >= their
+//     maximum, so at least 512 keys are >= L = the smallest group maximum.
+//     Only keys >= L are counted below (typically a few percent of the row).
+//  2. A radix select on (key - L) over [L, kmax], 11 bits per round from the
+//     top, counted in one shared-memory histogram of 2,048 bins; the bin that
+//     holds the k-th largest key is found by one block scan of the bin counts.
+//     Once that bin holds at most 32 keys, one warp ranks them directly.
+//  3. One packed block scan of (count > T, count == T) places every selected
+//     slot: rank = slots above T before it + the ties before it, ties taken
+//     lowest slot first -- so the output is in ascending slot order and
+//     identical on every run.
 constexpr int RS_THREADS = 1024;
 constexpr int RS_PER = 16;
 constexpr int RS_MAX = RS_THREADS * RS_PER;
+constexpr int RS_BITS = 11;
+constexpr int RS_BINS = 1 << RS_BITS;
+constexpr int RS_GROUPS = RS_MAX / 32;         // groups of the lower bound (k <= RS_GROUPS)
+constexpr int RS_DIRECT = 32;                  // a bin of at most this many keys is ranked directly
 
-struct __align__(16) RsShared {                // 16-byte vector accesses to hist and tot
-    uint32_t hist[RS_THREADS / 32][256];   // per-warp digit counts
-    uint32_t tot[256];                     // digit counts of the block
-    uint32_t warp_u[RS_THREADS / 32];
-    uint32_t kmin, kmax;
-    uint32_t digit;
+struct __align__(16) RsShared {
+    uint32_t hist[RS_BINS];                    // digit counts of the round
+    uint32_t warp_u[RS_THREADS / 32];          // block scan partials
+    uint32_t wmin[RS_THREADS / 32], wmax[RS_THREADS / 32];
+    uint32_t direct[RS_DIRECT];                // the keys of a small bin
+    uint32_t ndirect;
+    uint32_t digit, bin_count;
     int above;
+    uint32_t T;
+    int need_eq;
 };
 
 // Block-wide exclusive scan of one 32-bit value per thread (1,024 threads).
@@ -398,93 +410,104 @@ __device__ int rs_select(const uint32_t (&key)[RS_PER], uint32_t valid, int n, i
             if (valid >> j & 1u) emit((int)off++, j);
         return n;
     }
-    // ---- the valid keys' range
-    uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+    // ---- 1. group maxima (an invalid slot counts as key 0): L and kmax
+    uint32_t gmin = 0xFFFFFFFFu, gmax = 0u;
 #pragma unroll
-    for (int j = 0; j < RS_PER; j++)
-        if (valid >> j & 1u) {
-            mn = min(mn, key[j]);
-            mx = max(mx, key[j]);
-        }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int j = 0; j < RS_PER; j++) {
+        const uint32_t g = __reduce_max_sync(0xffffffffu, (valid >> j & 1u) ? key[j] : 0u);
+        gmin = min(gmin, g);
+        gmax = max(gmax, g);
     }
-    if (tid == 0) {
-        sh.kmin = 0xFFFFFFFFu;
-        sh.kmax = 0u;
-    }
-    __syncthreads();
     if (lane == 0) {
-        atomicMin(&sh.kmin, mn);
-        atomicMax(&sh.kmax, mx);
+        sh.wmin[wid] = gmin;
+        sh.wmax[wid] = gmax;
     }
+    if (tid == 0) sh.ndirect = 0u;
     __syncthreads();
-    const uint32_t kmin = sh.kmin, range = sh.kmax - kmin;
-    const int nbits = range ? 32 - __clz(range) : 0;
-    uint32_t prefix = 0, mask = 0;                     // over rel = key - kmin
+    uint32_t L = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll 8
+    for (int w = 0; w < RS_THREADS / 32; w++) {
+        L = min(L, sh.wmin[w]);
+        kmax = max(kmax, sh.wmax[w]);
+    }
+    if (k > RS_GROUPS) L = 0u;                         // the bound holds for k <= RS_GROUPS only
+    // ---- 2. radix select over rel = key - L of the keys >= L
+    uint32_t cand = 0;                                 // this thread's keys >= L
+#pragma unroll
+    for (int j = 0; j < RS_PER; j++) cand |= (uint32_t)((valid >> j & 1u) && key[j] >= L) << j;
+    const uint32_t range = kmax - L;
+    int top = range ? 32 - __clz(range) : 0;
+    uint32_t prefix = 0, mask = 0;
     int kk = k;
+    bool direct = false;
 #pragma unroll 1
-    for (int top = nbits; top > 0; top -= 8) {
-        const int width = top < 8 ? top : 8;
+    while (top > 0) {
+        const int width = top < RS_BITS ? top : RS_BITS;
         const int shift = top - width;
         const uint32_t dmask = (1u << width) - 1u;
-        *reinterpret_cast<uint4 *>(&sh.hist[wid][4 * lane]) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(&sh.hist[wid][128 + 4 * lane]) = make_uint4(0u, 0u, 0u, 0u);
-        if (tid < 256) sh.tot[tid] = 0u;
-        __syncwarp();
+        sh.hist[tid] = 0u;
+        sh.hist[tid + RS_THREADS] = 0u;
+        __syncthreads();
 #pragma unroll
         for (int j = 0; j < RS_PER; j++) {
-            const uint32_t rel = key[j] - kmin;
-            if ((valid >> j & 1u) && (rel & mask) == prefix) atomicAdd(&sh.hist[wid][(rel >> shift) & dmask], 1u);
+            const uint32_t rel = key[j] - L;
+            if ((cand >> j & 1u) && (rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
         }
         __syncthreads();
-        {
-            // every thread sums one bin over 8 warps' counts, four groups per bin
-            const int bin = tid & 255, grp = tid >> 8;
-            uint32_t t = 0;
-#pragma unroll
-            for (int w2 = 0; w2 < 8; w2++) t += sh.hist[8 * grp + w2][bin];
-            if (t) atomicAdd(&sh.tot[bin], t);
-        }
-        __syncthreads();
-        if (wid == 0) {
-            // lane L holds bins 8 L .. 8 L + 7; keys above a bin = the bins of the higher lanes
-            // (a suffix sum) + this lane's higher bins
-            const uint4 t0 = *reinterpret_cast<const uint4 *>(&sh.tot[8 * lane]);   // RsShared is 16-aligned
-            const uint4 t1 = *reinterpret_cast<const uint4 *>(&sh.tot[8 * lane + 4]);
-            const uint32_t c[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-            uint32_t csum = 0;
-#pragma unroll
-            for (int q = 0; q < 8; q++) csum += c[q];
-            uint32_t incl = csum;                      // sum over lanes >= this one
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
-                if (lane + o < 32) incl += y;
-            }
-            uint32_t acc = incl - csum;                // keys in the bins of the higher lanes
-            if (acc < (uint32_t)kk && incl >= (uint32_t)kk) {
-#pragma unroll
-                for (int q = 7; q >= 0; q--) {
-                    if (acc + c[q] >= (uint32_t)kk) {
-                        sh.digit = (uint32_t)(8 * lane + q);
-                        sh.above = (int)acc;
-                        break;
-                    }
-                    acc += c[q];
-                }
-            }
+        // thread t: bins 2047 - 2t (higher) and 2046 - 2t; counts of the higher
+        // bins by one exclusive scan in descending bin order
+        const uint32_t c_hi = sh.hist[RS_BINS - 1 - 2 * tid], c_lo = sh.hist[RS_BINS - 2 - 2 * tid];
+        const uint32_t ex = rs_exclusive_scan(c_hi + c_lo, sh);
+        if (ex < (uint32_t)kk && ex + c_hi + c_lo >= (uint32_t)kk) {
+            const bool hi = ex + c_hi >= (uint32_t)kk;
+            sh.digit = (uint32_t)(RS_BINS - 1 - 2 * tid - (hi ? 0 : 1));
+            sh.above = (int)(hi ? ex : ex + c_hi);
+            sh.bin_count = hi ? c_hi : c_lo;
         }
         __syncthreads();
         prefix |= sh.digit << shift;
         mask |= dmask << shift;
         kk -= sh.above;
-        // digit, above and tot are rewritten only after another block barrier
+        top = shift;
+        if (top > 0 && sh.bin_count <= (uint32_t)RS_DIRECT) {
+            direct = true;
+            break;
+        }
+        // digit, above and bin_count are rewritten only after another block barrier
     }
-    const uint32_t T = prefix + kmin;
-    const int need_eq = kk;                            // ties with T that are selected, lowest slots first
+    uint32_t T;
+    int need_eq;
+    if (direct) {
+        // the bin's keys (at most RS_DIRECT) into shared memory; one warp ranks them
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++) {
+            const uint32_t rel = key[j] - L;
+            if ((cand >> j & 1u) && (rel & mask) == prefix) sh.direct[atomicAdd(&sh.ndirect, 1u)] = key[j];
+        }
+        __syncthreads();
+        if (wid == 0) {
+            const int nd = (int)sh.ndirect;
+            const uint32_t v = lane < nd ? sh.direct[lane] : 0u;
+            int gt = 0, ge = 0;
+            for (int i = 0; i < nd; i++) {
+                const uint32_t u = sh.direct[i];
+                gt += u > v;
+                ge += u >= v;
+            }
+            // the kk-th largest of the bin: fewer than kk above it, at least kk from it up
+            if (lane < nd && gt < kk && ge >= kk) {
+                sh.T = v;                              // every lane that matches holds the same value
+                sh.need_eq = kk - gt;
+            }
+        }
+        __syncthreads();
+        T = sh.T;
+        need_eq = sh.need_eq;
+    } else {
+        T = prefix + L;
+        need_eq = kk;                                  // ties with T that are selected, lowest slots first
+    }
+    // ---- 3. placement
     uint32_t gt = 0, eq = 0;
 #pragma unroll
     for (int j = 0; j < RS_PER; j++)

@@ -193,6 +193,32 @@ def test_topk_rows_of_at_most_16384_bit_exact():
             assert np.array_equal(got[r], want), (r, use_cand)
 
 
+def test_topk_rows_threshold_cases_bit_exact():
+    """The one-CTA select's bound-and-radix path: distinct values (the k-th
+    largest in a small bin, ranked directly), ties exactly at the k-th value,
+    scores concentrated like the indexer's (positive, a narrow range), a row
+    whose group maxima exclude almost everything, a negative row, and k larger
+    than the 512 groups of the bound."""
+    rng = np.random.default_rng(23)
+    rows, ld = 6, 16384
+    s = rng.standard_normal((rows, ld)).astype(np.float32)
+    v = np.sort(s[1])[::-1][511]
+    s[1, rng.choice(np.flatnonzero(s[1] < v), 5, replace=False)] = v       # ties at the threshold
+    s[2] = (rng.gamma(2.0, 0.3, ld) * rng.uniform(0.9, 1.1, ld)).astype(np.float32) + np.float32(3.0)
+    s[3] = np.float32(1.0)
+    s[3, rng.choice(ld, 600, replace=False)] = rng.uniform(2.0, 3.0, 600).astype(np.float32)
+    s[4] = -np.abs(s[4]) - np.float32(1.0)
+    lens = np.array([16384, 16384, 16384, 16384, 16000, 16384], np.int32)
+    for k in (512, 1500):
+        out = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+        csa2.csa2_topk(torch.from_numpy(s).cuda(), torch.from_numpy(lens).cuda(), k, out)
+        got = out.cpu().numpy()
+        for r in range(rows):
+            n = lens[r]
+            want = oracle.topk(s[r, :n].astype(np.float64), None, k=k)
+            assert np.array_equal(got[r], want), (r, k)
+
+
 def test_topk_blocks_bit_exact():
     rng = np.random.default_rng(10)
     rows = 4
