@@ -14,22 +14,30 @@
 // path sustains above 6 TB/s with fewer bytes in flight.  The indexer query is
 // the B operand split into two e4m3 parts per head, hi = e4m3(q'), lo =
 // e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  hi and lo are
-// stacked as one N = 64 operand (rows 0-31 hi, 32-63 lo), so each K step is
-// one MMA that reads the key tile once; the fp32 D[128 entries x 64] in
-// tensor memory holds A.hi in columns 0-31 and A.lo in 32-63, and the
-// epilogue adds them, applies ReLU, w_h * 2^e_h and the entry's scale.
+// two operands of 32 rows per query; each K step multiplies the key tile by
+// both into the same fp32 sums (D = A.hi + A.lo), so tensor memory holds one
+// column per head, and the epilogue applies ReLU, w_h * 2^e_h and the entry's
+// scale.
 //
-// A tile is 256 entries (four pages): two M = 128 halves per K step.  Warp
-// roles (448 threads): warps 0-3 copy key tiles into a 6-stage ring (sixteen
+// Several queries of one sequence (QG = 2 or 4: draft tokens of a
+// multi-token decode step, or the new tokens of a prefill chunk) share each
+// key tile: their operands are stacked along N (N = 32 QG per part), so a tile
+// is read from memory once for all of them, and each query keeps its own visible range
+// (a score past it is not written, a block maximum covers visible entries only).
+//
+// A tile is 256 entries (four pages): two M = 128 halves per K step into a
+// tensor-memory accumulator slot of 2 x 32 QG columns (512 columns hold 8, 4
+// or 2 slots, so tile parity gives every slot one issuer).  Warp
+// roles (448 threads): warps 0-3 copy key tiles into a ring of stages (sixteen
 // 16-byte chunks per thread per tile), warps 0-1 also the entries' fp32
 // scales into the same stage, so that no role waits on a dependent global
-// load per tile; warps 4-11 drain four tensor-memory accumulators (warp w:
-// half (w - 4) / 4, TMEM lane quarter w % 4) and free a stage once they have
-// read its scales (its MMAs are complete by then); warp 12 writes the query
-// operand of each row, and lane 0 of warps 12 and 13 issue the MMAs of the
+// load per tile; warps 4-11 drain the accumulator slots (warp w: half
+// (w - 4) / 4, TMEM lane quarter w % 4) and free a stage once they have read
+// its scales (its MMAs are complete by then); warps 12 and 13 write the query
+// operands of each group, and lane 0 of warps 12 and 13 issue the MMAs of the
 // even and odd tiles (one issuing thread that also waits on barriers between
 // tiles leaves the tensor pipe idle half the time).  A persistent grid walks
-// one global list of (row, tile) items so ragged batches stay balanced.
+// one global list of (query group, tile) items so ragged batches stay balanced.
 #include <algorithm>
 #include <mutex>
 
@@ -39,27 +47,39 @@
 namespace csa2 {
 
 constexpr int F8_TILE = 256;               // entries per tile: 4 pages, two MMA halves of M = 128
-constexpr int F8_STAGES = 6;               // 32 KB of codes per stage
-constexpr int F8_ACC = 4;                  // tensor-memory accumulators of 128 columns (2 halves x hi | lo)
 constexpr int F8_PROD = 128;               // producer threads (warps 0-3)
 constexpr int F8_EPI_WARP = 4;             // epilogue warps 4-11: half (w - 4) / 4, lane quarter w % 4
 constexpr int F8_EPI = 8;
-constexpr int F8_MMA_WARP = 12;            // MMA issuers: warps 12 and 13
+constexpr int F8_MMA_WARP = 12;            // operand writers and MMA issuers: warps 12 and 13
 constexpr int F8_THREADS = 448;
-constexpr int F8_PERSIST_ROWS = 256;
-constexpr uint32_t F8_IDESC = tc::idesc_e4m3(128, 64);
+constexpr int F8_PERSIST_ROWS = 256;       // query groups of the persistent grid
+constexpr uint32_t F8_TMEM_COLS = 512;
 
+template <int QG>
+struct F8Cfg {
+    static constexpr int STAGES = QG == 1 ? 6 : (QG == 2 ? 5 : 4);    // 32 KB of codes per stage
+    static constexpr int N = 32 * QG;                                 // MMA N: every head of every query
+    static constexpr int SLOT_COLS = 2 * N;                           // accumulator of a tile (two halves)
+    static constexpr int SLOTS = (int)F8_TMEM_COLS / SLOT_COLS;       // 8, 4, 2: even, so that each slot
+    static constexpr int ISSUERS = 2;                                 // belongs to one issuer (tile parity)
+    static constexpr int WRITERS = QG >= 2 ? 2 : 1;                   // query-operand warps
+    static constexpr uint32_t IDESC = tc::idesc_e4m3(128, N);
+    static_assert(QG == 1 || QG == 2 || QG == 4, "1, 2 or 4 queries per group");
+};
+
+template <int QG>
 struct F8Smem {
-    uint8_t a[F8_STAGES][F8_TILE * 128];   // e4m3 keys, 128-byte swizzle (cp.async); rows 128 h .. of half h
-    uint8_t b[2][64 * 128];                // query hi (rows 0-31) and lo (rows 32-63), per segment parity
-    float sc[F8_STAGES][F8_TILE];          // fp32 scales of the stage's entries (cp.async)
-    float wq[2][32];                       // w_h * 2^e_h, per segment parity
-    uint64_t full[F8_STAGES], empty[F8_STAGES], tfull[F8_ACC], tempty[F8_ACC];
+    static constexpr int ST = F8Cfg<QG>::STAGES, SL = F8Cfg<QG>::SLOTS;
+    uint8_t a[ST][F8_TILE * 128];          // e4m3 keys, 128-byte swizzle (cp.async); rows 128 h .. of half h
+    uint8_t b[2][QG * 64 * 128];           // per segment parity: hi rows 32 q + h, then lo rows 32 QG + 32 q + h
+    float sc[ST][F8_TILE];                 // fp32 scales of the stage's entries (cp.async)
+    float wq[2][QG][32];                   // w_h * 2^e_h of each query, per segment parity
+    uint64_t full[ST], empty[ST], tfull[SL], tempty[SL];
     uint64_t bfree[2], wready[2], wfree[2];
     uint32_t tmem;
     int abort;
     int32_t prefix[F8_PERSIST_ROWS + 1];
-    int32_t rowcnt[F8_PERSIST_ROWS];       // entries scored per row (persistent grid)
+    int32_t rowcnt[F8_PERSIST_ROWS];       // entries scanned per query group (persistent grid)
 };
 
 // Scales copied for the entries of a page whose id lies outside the cache:
@@ -112,10 +132,11 @@ __device__ __forceinline__ uint32_t sw128_b8(uint32_t row, uint32_t k)
     return row * 128u + ((((k >> 4) ^ (row & 7u)) << 4) | (k & 15u));
 }
 
-// The two-part e4m3 query operand of row r and w_h * 2^e_h, written by one
-// warp; lane h = head h.  Two passes over the head's 128 dims (the maximum,
+// The two-part e4m3 query operand of row r (hi rows at bh, lo rows at bl, 32
+// each, 8-row aligned) and w_h * 2^e_h, written by one warp; lane h = head h.  Two passes over the head's 128 dims (the maximum,
 // then the conversion) keep half of it in registers at a time.
-__device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const uint16_t *qr, const float *wr)
+__device__ __forceinline__ void write_query_operand(uint8_t *bh, uint8_t *bl, float *wq, const uint16_t *qr,
+                                                    const float *wr)
 {
     const int h = threadIdx.x & 31;
     const uint4 *src = reinterpret_cast<const uint4 *>(qr + h * 128);
@@ -152,8 +173,8 @@ __device__ __forceinline__ void write_query_operand(uint8_t *b, float *wq, const
             }
         }
         const uint32_t k = (uint32_t)i * 8;        // first dim of this 16-dim chunk
-        *reinterpret_cast<uint4 *>(b + sw128_b8(h, k)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
-        *reinterpret_cast<uint4 *>(b + sw128_b8(32 + h, k)) = make_uint4(low[0], low[1], low[2], low[3]);
+        *reinterpret_cast<uint4 *>(bh + sw128_b8(h, k)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
+        *reinterpret_cast<uint4 *>(bl + sw128_b8(h, k)) = make_uint4(low[0], low[1], low[2], low[3]);
     }
 }
 
@@ -167,11 +188,32 @@ __device__ __forceinline__ int64_t f8_row_entries(const csa2_batch &bt, const in
     return n < 0 ? 0 : (n > ld ? ld : n);
 }
 
-// DENSE = false: row r scans the visible entries of the paged cache c.
-// DENSE = true: row r scans entries 0 .. pool_len[r] of rows of ld slots
-// stored one after the other in c.ik_codes / c.ik_scales (page j of row r is
-// page r * ld / 64 + j; no block table), scores only.
-template <bool PERSIST, bool DENSE>
+// Query group g of QG consecutive queries of one sequence: its first row r0,
+// its sequence b, its number of queries qn (the last group of a sequence may
+// be partial) and the entries it scans (the largest of its rows').
+template <int QG, bool DENSE>
+__device__ __forceinline__ int64_t f8_group(const csa2_batch &bt, const int32_t *pool_len, int64_t ld, int g,
+                                            int &r0, int &b, int &qn)
+{
+    const int gps = (bt.nq + QG - 1) / QG;         // groups per sequence
+    b = g / gps;
+    const int i0 = (g - b * gps) * QG;
+    r0 = b * bt.nq + i0;
+    qn = bt.nq - i0 < QG ? bt.nq - i0 : QG;
+    int64_t n = 0;
+    for (int q = 0; q < qn; q++) {
+        const int64_t e = f8_row_entries<DENSE>(bt, pool_len, ld, r0 + q);
+        n = e > n ? e : n;
+    }
+    return n;
+}
+
+// DENSE = false: row r scans the visible entries of the paged cache c, in
+// groups of QG rows of one sequence.
+// DENSE = true (QG = 1): row r scans entries 0 .. pool_len[r] of rows of ld
+// slots stored one after the other in c.ik_codes / c.ik_scales (page j of row
+// r is page r * ld / 64 + j; no block table), scores only.
+template <bool PERSIST, bool DENSE, int QG>
 __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_batch bt,
                                                             const uint16_t *__restrict__ qi,
                                                             const float *__restrict__ w,
@@ -180,57 +222,62 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                                                             float *__restrict__ block_max,
                                                             int32_t *__restrict__ n_visible, int64_t ld)
 {
+    using Cfg = F8Cfg<QG>;
+    constexpr int ST = Cfg::STAGES, SL = Cfg::SLOTS, N = Cfg::N;
+    static_assert(!DENSE || QG == 1, "a dense pool copy has one query per row");
     extern __shared__ uint8_t smem_raw[];
-    F8Smem &S = *reinterpret_cast<F8Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    F8Smem<QG> &S = *reinterpret_cast<F8Smem<QG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = bt.batch * bt.nq;
+    const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
 
     if (tid == 0) {
-        for (int i = 0; i < F8_STAGES; i++) {
+        for (int i = 0; i < ST; i++) {
             tc::mbar_init(&S.full[i], F8_PROD);
             tc::mbar_init(&S.empty[i], F8_EPI);      // the epilogue warps, after the tile's MMAs and scale reads
         }
-        for (int i = 0; i < F8_ACC; i++) {
+        for (int i = 0; i < SL; i++) {
             tc::mbar_init(&S.tfull[i], 1);
-            tc::mbar_init(&S.tempty[i], F8_EPI);
+            tc::mbar_init(&S.tempty[i], F8_EPI);     // the epilogue warps, once they have read it
         }
         for (int i = 0; i < 2; i++) {
-            tc::mbar_init(&S.bfree[i], 2);           // both MMA issuers
-            tc::mbar_init(&S.wready[i], 32);
+            tc::mbar_init(&S.bfree[i], Cfg::ISSUERS);
+            tc::mbar_init(&S.wready[i], 32 * Cfg::WRITERS);
             tc::mbar_init(&S.wfree[i], F8_EPI);
         }
         S.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_ACC * 128);
+    if (warp == F8_MMA_WARP) tc::tmem_alloc(&S.tmem, F8_TMEM_COLS);
     // launched as a programmatic dependent: the set-up above is local; the
     // batch, cache and queries are read below, once the previous kernel is done
     pdl_launch_dependents();
     pdl_wait();
 
-    int64_t g0, g1, nv_row = 0;                   // nv_row: the per-row grid's entry count
+    int64_t g0, g1, nv_grp = 0;                   // nv_grp: the per-group grid's entry count
+    if (!DENSE && blockIdx.x == 0 && (PERSIST || blockIdx.y == 0) && n_visible)
+        for (int r = tid; r < rows; r += F8_THREADS) n_visible[r] = (int32_t)visible_entries(bt, r);
     if (PERSIST) {
-        for (int r = tid; r < rows; r += F8_THREADS) {
-            const int64_t nv = f8_row_entries<DENSE>(bt, pool_len, ld, r);
-            S.rowcnt[r] = (int32_t)nv;
-            S.prefix[r + 1] = (int32_t)((nv + F8_TILE - 1) / F8_TILE);
-            if (!DENSE && blockIdx.x == 0 && n_visible) n_visible[r] = (int32_t)nv;
+        for (int gi = tid; gi < groups; gi += F8_THREADS) {
+            int r0, b, qn;
+            const int64_t nv = f8_group<QG, DENSE>(bt, pool_len, ld, gi, r0, b, qn);
+            S.rowcnt[gi] = (int32_t)nv;
+            S.prefix[gi + 1] = (int32_t)((nv + F8_TILE - 1) / F8_TILE);
         }
         __syncthreads();
         if (tid == 0) {
             S.prefix[0] = 0;
-            for (int r = 0; r < rows; r++) S.prefix[r + 1] += S.prefix[r];
+            for (int gi = 0; gi < groups; gi++) S.prefix[gi + 1] += S.prefix[gi];
         }
         __syncthreads();
-        const int64_t total = S.prefix[rows];
+        const int64_t total = S.prefix[groups];
         g0 = total * blockIdx.x / gridDim.x;
         g1 = total * (blockIdx.x + 1) / gridDim.x;
     } else {
-        const int r = blockIdx.y;
-        const int64_t nv = f8_row_entries<DENSE>(bt, pool_len, ld, r);
+        int r0, b, qn;
+        const int64_t nv = f8_group<QG, DENSE>(bt, pool_len, ld, (int)blockIdx.y, r0, b, qn);
         const int64_t T = (nv + F8_TILE - 1) / F8_TILE;
-        nv_row = nv;
-        if (!DENSE && blockIdx.x == 0 && tid == 0 && n_visible) n_visible[r] = (int32_t)nv;
+        nv_grp = nv;
         g0 = T * blockIdx.x / gridDim.x;
         g1 = T * (blockIdx.x + 1) / gridDim.x;
     }
@@ -240,24 +287,29 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
     const uint32_t tmem = S.tmem;
     volatile int *abort = &S.abort;
 
-    // every role walks the same segments (consecutive tiles of one row)
-    int r = PERSIST ? 0 : (int)blockIdx.y;
+    // every role walks the same segments (consecutive tiles of one query group)
+    int grp = PERSIST ? 0 : (int)blockIdx.y;
     int64_t g = g0, it = 0;
     int seg = 0;
-    int64_t last_tile = -1;
+    int last_slot = -1;
+    uint32_t last_par = 0;
 
     while (g < g1 && !*abort) {
         int64_t j0, nt;
         if (PERSIST) {
-            while (S.prefix[r + 1] <= g) r++;
-            j0 = g - S.prefix[r];
-            nt = std::min<int64_t>(g1, S.prefix[r + 1]) - g;
+            while (S.prefix[grp + 1] <= g) grp++;
+            j0 = g - S.prefix[grp];
+            nt = std::min<int64_t>(g1, S.prefix[grp + 1]) - g;
         } else {
             j0 = g;
             nt = g1 - g;
         }
-        const int b = r / bt.nq;
-        const int64_t nvis = PERSIST ? (int64_t)S.rowcnt[r] : nv_row;   // entries scored
+        // the group's sequence, first row and query count (QG = 1: the row itself)
+        const int gps = QG == 1 ? 1 : (bt.nq + QG - 1) / QG;
+        const int b = QG == 1 ? grp / bt.nq : grp / gps;
+        const int r0 = QG == 1 ? grp : b * bt.nq + (grp - b * gps) * QG;
+        const int qn = QG == 1 ? 1 : min(QG, bt.nq - (grp - b * gps) * QG);
+        const int64_t nvis = PERSIST ? (int64_t)S.rowcnt[grp] : nv_grp;   // entries scanned
 
         if (warp < 4) {
             // ---------------- producers: page ids of 32 tiles at a time (one lane per
@@ -274,7 +326,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         const int64_t e0 = e + 64 * h;
                         my_pg[h] = -2;                                // -2: beyond the visible entries
                         if (i + lane < nt && e0 < nvis) {
-                            const int32_t pg = DENSE ? (int32_t)(r * (ld >> 6) + (e0 >> 6))
+                            const int32_t pg = DENSE ? (int32_t)(r0 * (ld >> 6) + (e0 >> 6))
                                                      : __ldg(c.block_table + (int64_t)b * c.max_pages + (e0 >> 6));
                             my_pg[h] = pg >= 0 && ((int64_t)pg + 1) * CSA2_PAGE <= c.num_slots ? pg : -1;
                         }
@@ -284,8 +336,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 #pragma unroll
                 for (int h = 0; h < 4; h++) pgs[h] = __shfl_sync(0xffffffffu, my_pg[h], (int)(i & 31));
                 const int64_t ti = it + i;
-                const int stage = (int)(ti % F8_STAGES);
-                const int k = (int)(ti / F8_STAGES);
+                const int stage = (int)(ti % ST);
+                const int k = (int)(ti / ST);
                 const bool ok = k == 0 || tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) {
@@ -314,14 +366,14 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 cp_async_arrive(&S.full[stage]);
             }
         } else if (warp >= F8_MMA_WARP) {
-            // ---------------- query operand (warp 8) + MMA issue: lane 0 of warp 8 takes the
-            // even tiles, lane 0 of warp 9 the odd ones (one issuing thread cannot keep
-            // the tensor pipe busy while it also waits on barriers)
+            // ---------------- query operands (warps 12 and 13 split the group's queries)
+            // and MMA issue (lane 0 of warp 12: even tiles, of warp 13: odd tiles; warp
+            // 12 all of them when there is a single issuer)
             const int is = warp - F8_MMA_WARP;
             bool ok = true;
-            if (is == 0) {
+            if (is < Cfg::WRITERS) {
                 // the operand and weights of segment seg-2 must be done with: its MMAs
-                // completed (bfree, both issuers) and the epilogue finished its tiles (wfree)
+                // completed (bfree) and the epilogue finished its tiles (wfree)
                 if (seg >= 2 && lane == 0) {
                     const uint32_t par = (uint32_t)(((seg >> 1) - 1) & 1);
                     ok = tc::mbar_wait_or_abort(&S.bfree[seg & 1], par, abort) &&
@@ -329,55 +381,67 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (ok) {
-                    write_query_operand(S.b[seg & 1], S.wq[seg & 1], qi + (int64_t)r * 4096, w + (int64_t)r * 32);
+                    for (int q = is; q < qn; q += Cfg::WRITERS)
+                        write_query_operand(S.b[seg & 1] + q * (32 * 128), S.b[seg & 1] + (N + 32 * q) * 128,
+                                            S.wq[seg & 1][q], qi + (int64_t)(r0 + q) * 4096, w + (int64_t)(r0 + q) * 32);
                     tc::fence_proxy_async_smem();
                     tc::mbar_arrive(&S.wready[seg & 1]);
                 }
-            } else if (lane == 0) {
-                ok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
             }
-            if (!ok) {
-                if (lane == 0) {
-                    *abort = 1;
-                    flag(c.status, CSA2_DEV_TIMEOUT);
-                }
-            } else {
-                __syncwarp();
-                if (lane == 0) {
-                    const uint32_t a0 = tc::smem_u32(S.a[0]);
-                    const uint32_t b0 = tc::smem_u32(S.b[seg & 1]);
-                    for (int64_t i = (is - it) & 1; i < nt; i += 2) {   // tiles ti = it + i with ti % 2 == is
-                        const int64_t ti = it + i;
-                        const int stage = (int)(ti % F8_STAGES);
-                        const int acc = (int)(ti % F8_ACC);
-                        if (!tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / F8_STAGES) & 1), abort) ||
-                            (ti >= F8_ACC &&
-                             !tc::mbar_wait_or_abort(&S.tempty[acc], (uint32_t)(((ti / F8_ACC) - 1) & 1), abort))) {
-                            *abort = 1;
-                            flag(c.status, CSA2_DEV_TIMEOUT);
-                            break;
-                        }
-                        // the producers' cp.async writes, acquired through the barrier, made
-                        // visible to the tensor core's (async-proxy) operand reads
-                        tc::fence_proxy_async_smem();
-                        tc::tc_fence_after();
-                        const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
-#pragma unroll
-                        for (int hf = 0; hf < 2; hf++)       // two halves of 128 entries
-#pragma unroll
-                            for (int kk = 0; kk < 4; kk++)   // K = 128 codes in steps of 32; N = hi | lo
-                                tc::mma_f8(tmem + (uint32_t)acc * 128u + 64u * hf,
-                                           tc::smem_desc(as + hf * (128 * 128) + kk * 32, 16, 1024, tc::kSwizzle128B),
-                                           tc::smem_desc(b0 + kk * 32, 16, 1024, tc::kSwizzle128B), F8_IDESC,
-                                           kk > 0);
-                        // the stage is released by the epilogue, which reads its scales only
-                        // after this commit: the MMAs are done with the codes by then
-                        tc::mma_commit(&S.tfull[acc]);
-                        last_tile = ti;
+            if (is < Cfg::ISSUERS) {
+                if (lane == 0 && ok) ok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) {
+                    if (lane == 0) {
+                        *abort = 1;
+                        flag(c.status, CSA2_DEV_TIMEOUT);
                     }
-                    tc::mma_commit(&S.bfree[seg & 1]);
+                } else {
+                    if (lane == 0) {
+                        const uint32_t a0 = tc::smem_u32(S.a[0]);
+                        const uint32_t b0 = tc::smem_u32(S.b[seg & 1]);
+                        for (int64_t i = (is - it) & 1; i < nt; i += 2) {   // tiles ti with ti % 2 == is
+                            const int64_t ti = it + i;
+                            const int stage = (int)(ti % ST);
+                            if (!tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort)) {
+                                *abort = 1;
+                                flag(c.status, CSA2_DEV_TIMEOUT);
+                                break;
+                            }
+                            // the producers' cp.async writes, acquired through the barrier, made
+                            // visible to the tensor core's (async-proxy) operand reads
+                            tc::fence_proxy_async_smem();
+                            const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
+                            const int slot = (int)(ti % SL);
+                            if (ti >= SL &&
+                                !tc::mbar_wait_or_abort(&S.tempty[slot], (uint32_t)(((ti / SL) - 1) & 1), abort)) {
+                                *abort = 1;
+                                flag(c.status, CSA2_DEV_TIMEOUT);
+                                break;
+                            }
+                            tc::tc_fence_after();
+#pragma unroll
+                            for (int hf = 0; hf < 2; hf++)       // two halves of 128 entries
+#pragma unroll
+                                for (int kk = 0; kk < 4; kk++)   // K = 128 codes in steps of 32
+#pragma unroll
+                                    for (int part = 0; part < 2; part++)   // hi, then lo into the same sums
+                                        tc::mma_f8(tmem + (uint32_t)(slot * Cfg::SLOT_COLS + hf * N),
+                                                   tc::smem_desc(as + hf * (128 * 128) + kk * 32, 16, 1024,
+                                                                 tc::kSwizzle128B),
+                                                   tc::smem_desc(b0 + (uint32_t)(part * N * 128) + kk * 32, 16, 1024,
+                                                                 tc::kSwizzle128B),
+                                                   Cfg::IDESC, (kk | part) > 0);
+                            // the stage is released by the epilogue, which reads its scales only
+                            // after this commit: the MMAs are done with the codes by then
+                            tc::mma_commit(&S.tfull[slot]);
+                            last_slot = slot;
+                            last_par = (uint32_t)((ti / SL) & 1);
+                        }
+                        tc::mma_commit(&S.bfree[seg & 1]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         } else {
             // ---------------- epilogue: warps 4-11, half (warp - 4) / 4, TMEM lanes by warp % 4
@@ -390,17 +454,19 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
                 break;
             }
-            const float *wv = S.wq[seg & 1];              // broadcast shared-memory reads
+            int64_t nvq[QG];                              // each query's own visible range
+#pragma unroll
+            for (int q = 0; q < QG; q++) nvq[q] = q < qn ? (QG == 1 ? nvis : f8_row_entries<DENSE>(bt, pool_len, ld, r0 + q)) : 0;
             const int64_t rowp = (int64_t)hf * 128 + qd * 32 + lane;
             for (int64_t i = 0; i < nt; i++) {
                 const int64_t ti = it + i;
-                const int acc = (int)(ti % F8_ACC);
-                const int stage = (int)(ti % F8_STAGES);
+                const int stage = (int)(ti % ST);
+                const int slot = (int)(ti % SL);
                 // the MMAs of tile ti are done, so its stage's data has landed: the wait on
                 // full[stage] returns at once and acquires the producers' scale copies (the
                 // stage cannot refill before this warp's arrival on empty[stage] below)
-                bool ok = tc::mbar_wait_or_abort(&S.tfull[acc], (uint32_t)((ti / F8_ACC) & 1), abort) &&
-                          tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / F8_STAGES) & 1), abort);
+                bool ok = tc::mbar_wait_or_abort(&S.tfull[slot], (uint32_t)((ti / SL) & 1), abort) &&
+                          tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) {
                         *abort = 1;
@@ -409,39 +475,46 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)acc * 128u + 64u * (uint32_t)hf;
+                const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16) + (uint32_t)(slot * Cfg::SLOT_COLS + hf * N);
                 const float sc_cur = S.sc[stage][rowp];
                 const int64_t p = (j0 + i) * F8_TILE + rowp;
-                const bool valid = p < nvis;
-                float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};             // four independent chains
+                float res[QG];
 #pragma unroll
-                for (int c16 = 0; c16 < 2; c16++) {                    // heads 16 c16 .. 16 c16 + 15
-                    uint32_t dh[16], dl[16];
-                    tc::tmem_ld16(ta + 16u * c16, dh);
-                    tc::tmem_ld16(ta + 32u + 16u * c16, dl);
-                    tc::tmem_ld_wait();
+                for (int q = 0; q < QG; q++) {
+                    const float *wv = S.wq[seg & 1][q];       // broadcast shared-memory reads
+                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent chains
+                    if (q < qn) {
+                        uint32_t d[32];                         // q's 32 heads: hi . k + lo . k
+                        tc::tmem_ld32(ta + 32u * q, d);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        const float x = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
-                        part[j & 3] = fmaf(wv[16 * c16 + j], fmaxf(x, 0.0f), part[j & 3]);
+                        for (int j = 0; j < 32; j++)
+                            part[j & 3] = fmaf(wv[j], fmaxf(__uint_as_float(d[j]), 0.0f), part[j & 3]);
                     }
+                    res[q] = (part[0] + part[1]) + (part[2] + part[3]);
                 }
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    tc::mbar_arrive(&S.tempty[acc]);
+                    tc::mbar_arrive(&S.tempty[slot]);
                     tc::mbar_arrive(&S.empty[stage]);
                 }
-                float sc = -INFINITY;
-                if (valid) {
-                    if (sc_cur != -INFINITY) sc = ((part[0] + part[1]) + (part[2] + part[3])) * sc_cur;
-                    if (scores) scores[(int64_t)r * ld + p] = sc;
-                }
-                if (!DENSE && block_max) {
-                    float m = valid ? sc : -INFINITY;
 #pragma unroll
-                    for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if ((lane & 7) == 0 && valid) block_max[(int64_t)r * (ld / 8) + (p >> 3)] = m;
+                for (int q = 0; q < QG; q++) {
+                    if (q >= qn) break;
+                    const bool valid = p < nvq[q];
+                    const int64_t rq = r0 + q;
+                    float sc = -INFINITY;
+                    if (valid) {
+                        if (sc_cur != -INFINITY) sc = res[q] * sc_cur;
+                        if (scores) scores[rq * ld + p] = sc;
+                    }
+                    if (!DENSE && block_max) {
+                        float m = valid ? sc : -INFINITY;
+#pragma unroll
+                        for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if ((lane & 7) == 0 && valid) block_max[rq * (ld / 8) + (p >> 3)] = m;
+                    }
                 }
             }
             __syncwarp();
@@ -455,18 +528,46 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
     // ---- teardown: nothing in flight may outlive the CTA's shared and tensor memory
     if (warp < 4) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
-    if (*abort && (tid == F8_MMA_WARP * 32 || tid == (F8_MMA_WARP + 1) * 32) && last_tile >= 0)
-        tc::mbar_wait(&S.tfull[last_tile % F8_ACC], (uint32_t)((last_tile / F8_ACC) & 1), 1u << 20);
+    if (*abort && (tid == F8_MMA_WARP * 32 || tid == (F8_MMA_WARP + 1) * 32) && last_slot >= 0)
+        tc::mbar_wait(&S.tfull[last_slot], last_par, 1u << 20);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == F8_MMA_WARP) tc::tmem_dealloc(tmem, F8_ACC * 128);
+    if (warp == F8_MMA_WARP) tc::tmem_dealloc(tmem, F8_TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host side
 static int g_sms = 0;
 static std::once_flag g_sms_once;
 
+template <bool DENSE, int QG>
+static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
+                       const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
+                       cudaStream_t st)
+{
+    const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
+    const size_t smem = sizeof(F8Smem<QG>) + 1024;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(k_index_f8<true, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_index_f8<false, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr = true;
+    }
+    const int64_t per_row = DENSE ? ld : bt.max_entries;
+    const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
+    if (groups <= F8_PERSIST_ROWS) {
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, g_sms));
+        return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
+                          scores, block_max, n_visible, ld);
+    }
+    if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
+    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + groups - 1) / groups));
+    return launch_pdl(k_index_f8<false, DENSE, QG>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
+                      pool_len, scores, block_max, n_visible, ld);
+}
+
+// Queries per group: the largest of 4, 2, 1 that the per-sequence query count
+// fills (a dense pool copy holds one query's keys per row).
 template <bool DENSE>
 static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                      const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
@@ -478,24 +579,9 @@ static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     });
     if (g_sms <= 0) return CSA2_ERR_CUDA;
-    const int rows = bt.batch * bt.nq;
-    const size_t smem = sizeof(F8Smem) + 1024;
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_index_f8<true, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_index_f8<false, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
-    const int64_t per_row = DENSE ? ld : bt.max_entries;
-    const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
-    if (rows <= F8_PERSIST_ROWS) {
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)rows * tiles_row, g_sms));
-        return launch_pdl(k_index_f8<true, DENSE>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
-                          scores, block_max, n_visible, ld);
-    }
-    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + rows - 1) / rows));
-    return launch_pdl(k_index_f8<false, DENSE>, dim3(x, rows), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
-                      scores, block_max, n_visible, ld);
+    if (DENSE || bt.nq < 2) return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
+    if (bt.nq < 4) return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
+    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
 }
 
 int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,

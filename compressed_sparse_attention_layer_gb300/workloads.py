@@ -233,6 +233,14 @@ def decode_1m(seed: int = 4000, batch: int = 8, tokens: int = 1 << 20, layers=No
                     kv_format=kv_format)
 
 
+def decode_multi(seed: int = 6000, batch: int = 8, tokens: int = 1 << 20, q: int = 4, layers=None,
+                 planted_blocks: int = 64) -> Workload:
+    """Multi-token decode (draft tokens verified in one step): the last q
+    tokens of each sequence are queries, each with its own causal range."""
+    return Workload("decode_multi", seed, batch, [tokens] * batch, 1, list(layers or DECODER_STACK),
+                    planted_blocks=planted_blocks, nq=q, prefill_new=q, swa_rows=W + q)
+
+
 def ragged_lengths(seed: int, batch: int, lo: int = 4096, hi: int = 1 << 20) -> List[int]:
     rng = np.random.default_rng(synth.stream_id(seed, T_LEN))
     return [int(math.floor(math.exp(v))) for v in rng.uniform(math.log(lo), math.log(hi), batch)]

@@ -251,3 +251,18 @@ def test_reuse_keys_loaded_early_bit_identical():
         assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
         assert torch.equal(a.lse[l].view(torch.int32), b.lse[l].view(torch.int32)), l
         assert torch.equal(a.swa_codes[l], b.swa_codes[l]), l
+
+
+@pytest.mark.parametrize("q", [2, 3, 5])
+def test_layer_multi_query_decode(q):
+    """Several query tokens per sequence (a multi-token decode step): the Full
+    layer's scan serves groups of 2 or 4 queries from each key tile (the last
+    group of a sequence partial for q = 3, 5); every query keeps its own causal
+    range, selection and attention, checked against the oracle in every layer."""
+    wl = W.Workload("mq", 77 + q, 2, [30000, 9000], 1, ["full", "reuse", "reindex"], planted_blocks=4,
+                    nq=q, prefill_new=q, swa_rows=W.W + q)
+    dw = DeviceWorkload(wl)
+    _run_recording(dw)
+    for b in range(wl.batch):
+        for i in range(q):
+            _check_sequence(dw, b, i)
