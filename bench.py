@@ -41,6 +41,9 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--kv-format", type=int, default=0, choices=[0, 1],
                    help="main KV: 0 MXFP4 (32-element blocks, E8M0), 1 FP4 with an E4M3 scale per 16 elements")
+    p.add_argument("--queries", type=int, default=1,
+                   help="query tokens per sequence per step (>1: a multi-token decode step, e.g. draft "
+                        "tokens verified together; the Full layer's scan serves them from one read)")
     return p.parse_args()
 
 
@@ -127,7 +130,7 @@ class ClockSampler:
 class DecodeStep:
     """Device state and the launch sequence of one decode step."""
 
-    def __init__(self, batch, tokens, seed, device, kv_format=0):
+    def __init__(self, batch, tokens, seed, device, kv_format=0, queries=1):
         import numpy as np
         import torch
         from compressed_sparse_attention_layer_gb300 import csa2, synth
@@ -135,26 +138,38 @@ class DecodeStep:
         from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
 
         self.torch, self.csa2 = torch, csa2
-        self.wl = W.decode_1m(seed=seed, batch=batch, tokens=tokens, kv_format=kv_format)
+        if queries == 1:
+            self.wl = W.decode_1m(seed=seed, batch=batch, tokens=tokens, kv_format=kv_format)
+        else:
+            self.wl = W.decode_multi(seed=seed, batch=batch, tokens=tokens, q=queries)
+            self.wl.kv_format = kv_format
         self.dw = DeviceWorkload(self.wl, device=device)
         wl, dw = self.wl, self.dw
-        B, N = wl.batch, wl.tokens[0]
+        # several new tokens: their window rows are written by the FP8 quantiser
+        # right before each layer call, so keys may not be read ahead of it
+        dw.early_inputs = queries == 1
+        B, N, Q = wl.batch, wl.tokens[0], queries
+        self.queries = Q
         dev = dw.dev
-        # the new token of each sequence is entry N-1 / window row (N-1) % 128
-        self.new_slots = torch.stack([dw.entry_slots(b, N - 1, N) for b in range(B)]).view(B)
-        self.C_new = torch.cat([synth.normal_bf16_torch(wl._sid(W.T_C, b), (N - 1) * 512, 512, dev)
-                                for b in range(B)]).view(B, 512)
+        # the new tokens of each sequence are entries N-Q .. N-1, window rows (N-Q+i) % R
+        self.new_slots = torch.stack([dw.entry_slots(b, N - Q, N) for b in range(B)]).view(B * Q)
+        self.C_new = torch.cat([synth.normal_bf16_torch(wl._sid(W.T_C, b), (N - Q) * 512, Q * 512, dev)
+                                for b in range(B)]).view(B * Q, 512)
         self.Z_new = torch.zeros_like(self.C_new)
         self.bias = torch.zeros((1, 512), dtype=torch.float32, device=dev)
-        self.ik_new = torch.cat([synth.normal_f32_torch(wl._sid(W.T_IK, b), (N - 1) * 128, 128, dev)
-                                 for b in range(B)]).view(B, 128)
-        self.swa_new = {l: torch.cat([synth.normal_bf16_torch(wl._sid(W.T_SWA, b, l), (N - 1) * 512, 512, dev)
-                                      for b in range(B)]).view(B, 512).float() for l in dw.layers}
-        self.e_new = torch.empty((B, 512), dtype=torch.float32, device=dev)
+        self.ik_new = torch.cat([synth.normal_f32_torch(wl._sid(W.T_IK, b), (N - Q) * 128, Q * 128, dev)
+                                 for b in range(B)]).view(B * Q, 128)
+        self.swa_new = {l: torch.cat([synth.normal_bf16_torch(wl._sid(W.T_SWA, b, l), (N - Q) * 512, Q * 512, dev)
+                                      for b in range(B)]).view(B * Q, 512).float() for l in dw.layers}
+        R = wl.swa_rows
+        self.ring_slots = torch.tensor([b * R + (N - Q + i) % R for b in range(B) for i in range(Q)],
+                                       dtype=torch.int64, device=dev)
+        self.e_new = torch.empty((B * Q, 512), dtype=torch.float32, device=dev)
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 3 + sum({"full": 6, "reindex": 4, "reuse": 2}[m] for m in wl.layers)
+        self.launches = 3 + sum({"full": 6, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
+            (len(wl.layers) if Q > 1 else 0)
         # the step's host inputs for the end-to-end leg (new token + every layer's queries)
         self.h2d = [(self.C_new, None), (self.ik_new, None)]
         for l in dw.layers:
@@ -176,22 +191,30 @@ class DecodeStep:
     def enqueue_layers(self, layers, prof=False):
         for l in layers:
             # a3-a9: the layer; its attention call also quantises this layer's window
-            # row of the new token into the ring (csa2_swa.new_rows)
+            # row of the new token into the ring (csa2_swa.new_rows); several new
+            # tokens per sequence: the FP8 quantiser writes their rows first
             full = self.wl.layers[l] == "full"
-            self.dw.run_layer(l, prof=self.scan_ev if (prof and full) else None, new_rows=self.swa_new[l])
+            if self.queries > 1:
+                dw = self.dw
+                self.csa2.csa2_quant_fp8(self.swa_new[l], dw.swa_codes[l].view(-1, 512), dw.swa_scales[l].view(-1),
+                                         slots=self.ring_slots, status=dw.cache.status)
+            self.dw.run_layer(l, prof=self.scan_ev if (prof and full) else None,
+                              new_rows=self.swa_new[l] if self.queries == 1 else None)
 
     def layer_bytes(self):
-        """Algorithmic bytes per query token of each layer mode: what the method
-        must read and write (indexer keys scanned or rescored, the selected main-KV
-        entries, the window rows, q / qi / w, the pool or indices, o and lse)."""
-        wl = self.wl
+        """Algorithmic bytes per step and sequence of each layer mode: what the
+        method must read and write -- the indexer keys scanned (once for all the
+        sequence's query tokens) or rescored, and per query token the selected
+        main-KV entries, the window rows, q / qi / w, the pool or indices, o and
+        lse."""
+        wl, Q = self.wl, self.queries
         E = wl.entries(0)
         kv = 256 + self.csa2.KV_SCALE_BYTES[wl.kv_format]      # codes + block scales per entry
         attn = 512 * kv + 128 * 516 + 64 * 512 * 2 + 64 * 512 * 4 + 64 * 4
         pool = min(self.csa2.POOL_MAX, E)
-        return {"full": E * 132 + (E // 8) * 4 + 32 * 128 * 2 + 32 * 4 + attn,
-                "reindex": pool * 132 + pool * 4 + 32 * 128 * 2 + 32 * 4 + attn,
-                "reuse": 512 * 4 + attn}
+        return {"full": E * 132 + Q * ((E // 8) * 4 + 32 * 128 * 2 + 32 * 4 + attn),
+                "reindex": Q * (pool * 132 + pool * 4 + 32 * 128 * 2 + 32 * 4 + attn),
+                "reuse": Q * (512 * 4 + attn)}
 
 
 def run_native(args):
@@ -206,8 +229,8 @@ def run_native(args):
     build.build()
     csa2.load()
     dev = torch.device("cuda", local)
-    step = DecodeStep(args.batch, args.tokens, rank_seed(rank), dev, kv_format=args.kv_format)
-    B, N = step.wl.batch, step.wl.tokens[0]
+    step = DecodeStep(args.batch, args.tokens, rank_seed(rank), dev, kv_format=args.kv_format, queries=args.queries)
+    B, N, Q = step.wl.batch, step.wl.tokens[0], args.queries
 
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
@@ -274,7 +297,7 @@ def run_native(args):
         del gm
     ms_total = reduce_max(ms, dev, world)
     ms_step = ms_total / args.steps
-    value = throughput(world, B, args.steps, ms_total / 1e3)
+    value = throughput(world, B * Q, args.steps, ms_total / 1e3)
 
     # ---- end to end: pinned host inputs copied in, outputs copied out, every step
     e2e = None
@@ -296,7 +319,7 @@ def run_native(args):
                     h.copy_(d, non_blocking=True)
             s.synchronize()
         el = time.perf_counter() - t0
-        e2e = {"value": throughput(world, B, args.steps, reduce_max(el, dev, world)), "unit": UNIT,
+        e2e = {"value": throughput(world, B * Q, args.steps, reduce_max(el, dev, world)), "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes}
 
     if rank != 0:
@@ -315,7 +338,7 @@ def run_native(args):
     E = step.wl.entries(0)
     # algorithmic bytes per launch: 128 B codes + 4 B scale per entry read, 4 B per 8 entries
     # of block maxima written, the 8 KB query + 128 B weights per row
-    algo_bytes = B * (E * 132 + (E // 8) * 4 + 8192 + 128)
+    algo_bytes = B * (E * 132 + Q * ((E // 8) * 4 + 8192 + 128))   # keys read once for the Q queries
     scan_avg = statistics.median(scan_ms) if scan_ms else None
     achieved = algo_bytes / (scan_avg * 1e-3) / 1e9 if scan_avg else None
     traffic = None
@@ -339,11 +362,11 @@ def run_native(args):
     per_mode = {}
     for mode, (n, lms) in per_mode_ms.items():
         gbs = B * lb[mode] / (lms * 1e-3) / 1e9
-        per_mode[mode] = {"layers": n, "us_per_layer": 1e3 * lms, "query_tokens_per_s": B / (lms * 1e-3),
-                          "algo_bytes_per_token": lb[mode], "achieved_gbs": gbs, "frac": gbs / peak}
+        per_mode[mode] = {"layers": n, "us_per_layer": 1e3 * lms, "query_tokens_per_s": B * Q / (lms * 1e-3),
+                          "algo_bytes_per_token": lb[mode] / Q, "achieved_gbs": gbs, "frac": gbs / peak}
     stack_bytes = sum(lb[m] for m in step.wl.layers)
     rest = ms_step - sum(n * lms for n, lms in per_mode_ms.values())
-    per_mode["stack"] = {"us": 1e3 * ms_step, "algo_bytes_per_token": stack_bytes,
+    per_mode["stack"] = {"us": 1e3 * ms_step, "algo_bytes_per_token": stack_bytes / Q,
                          "achieved_gbs": B * stack_bytes / (ms_step * 1e-3) / 1e9,
                          "frac": B * stack_bytes / (ms_step * 1e-3) / 1e9 / peak,
                          "us_outside_layers": 1e3 * rest,
@@ -359,8 +382,10 @@ def run_native(args):
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3/bf16",
         "data": "synthetic (seeded counter-based generator; 64 planted blocks per sequence)",
-        "config": {"workload": f"decode_1m: batch {B} x {N} tokens, m=1, 20-layer decoder stack "
-                               "(Full+3 Reuse, 4x(Reindex+3 Reuse)), Top-512, SWA 128",
+        "config": {"workload": (f"decode_1m: batch {B} x {N} tokens" if Q == 1 else
+                                f"decode_multi: batch {B} x {N} tokens, {Q} query tokens per sequence per step") +
+                               ", m=1, 20-layer decoder stack (Full+3 Reuse, 4x(Reindex+3 Reuse)), Top-512, SWA 128",
+                   "queries_per_sequence": Q,
                    "batch": B, "context_tokens": N, "layers": len(step.wl.layers),
                    "main_kv": ["MXFP4 (32-element blocks, E8M0 scale), 272 B/entry",
                                "FP4 (16-element blocks, E4M3 scale), 288 B/entry"][args.kv_format],

@@ -13,21 +13,24 @@
 // 8 KB pages the TMA stream saturates near 5.3 TB/s while the load-store
 // path sustains above 6 TB/s with fewer bytes in flight.  The indexer query is
 // the B operand split into two e4m3 parts per head, hi = e4m3(q'), lo =
-// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  hi and lo are
-// two operands of 32 rows per query; each K step multiplies the key tile by
-// both into the same fp32 sums (D = A.hi + A.lo), so tensor memory holds one
-// column per head, and the epilogue applies ReLU, w_h * 2^e_h and the entry's
-// scale.
+// e4m3(q' - hi), q' = q * 2^-e_h with max|q'| in [128, 256).  With one or
+// two queries per tile hi and lo are stacked as one operand (rows 64 q .. hi,
+// 64 q + 32 .. lo of query q), so each K step is one MMA that reads the key
+// tile once and the epilogue adds the hi and lo columns; with four, they are
+// two operands whose MMAs accumulate into the same fp32 sums (D = A.hi + A.lo),
+// one column per head, which halves the epilogue's tensor-memory reads where
+// the epilogue is the bottleneck.  The epilogue applies ReLU, w_h * 2^e_h and
+// the entry's scale.
 //
 // Several queries of one sequence (QG = 2 or 4: draft tokens of a
 // multi-token decode step, or the new tokens of a prefill chunk) share each
-// key tile: their operands are stacked along N (N = 32 QG per part), so a tile
-// is read from memory once for all of them, and each query keeps its own visible range
+// key tile: their operands are stacked along N, so a tile is read from
+// memory once for all of them, and each query keeps its own visible range
 // (a score past it is not written, a block maximum covers visible entries only).
 //
 // A tile is 256 entries (four pages): two M = 128 halves per K step into a
-// tensor-memory accumulator slot of 2 x 32 QG columns (512 columns hold 8, 4
-// or 2 slots, so tile parity gives every slot one issuer).  Warp
+// tensor-memory accumulator slot of 2N columns (512 columns hold 4, 2 or 2
+// slots: tile parity gives every slot one issuer).  Warp
 // roles (448 threads): warps 0-3 copy key tiles into a ring of stages (sixteen
 // 16-byte chunks per thread per tile), warps 0-1 also the entries' fp32
 // scales into the same stage, so that no role waits on a dependent global
@@ -58,20 +61,27 @@ constexpr uint32_t F8_TMEM_COLS = 512;
 template <int QG>
 struct F8Cfg {
     static constexpr int STAGES = QG == 1 ? 6 : (QG == 2 ? 5 : 4);    // 32 KB of codes per stage
-    static constexpr int N = 32 * QG;                                 // MMA N: every head of every query
+    // hi and lo query parts: stacked along N (one MMA per K step, the epilogue
+    // adds the two columns; the fewest MMA instructions) while two tile slots of
+    // 2 x 64 QG columns fit in tensor memory, else accumulated into the same
+    // columns by two MMAs per K step (half the epilogue's reads)
+    static constexpr bool STACKED = QG <= 2;
+    static constexpr int N = (STACKED ? 64 : 32) * QG;                // MMA N
+    static constexpr int PARTS = STACKED ? 1 : 2;                     // MMAs per K step and half
     static constexpr int SLOT_COLS = 2 * N;                           // accumulator of a tile (two halves)
-    static constexpr int SLOTS = (int)F8_TMEM_COLS / SLOT_COLS;       // 8, 4, 2: even, so that each slot
+    static constexpr int SLOTS = (int)F8_TMEM_COLS / SLOT_COLS;       // 4, 2, 2: even, so that each slot
     static constexpr int ISSUERS = 2;                                 // belongs to one issuer (tile parity)
     static constexpr int WRITERS = QG >= 2 ? 2 : 1;                   // query-operand warps
     static constexpr uint32_t IDESC = tc::idesc_e4m3(128, N);
     static_assert(QG == 1 || QG == 2 || QG == 4, "1, 2 or 4 queries per group");
+    static_assert(SLOTS >= 2 && SLOTS % 2 == 0, "an even number of tile slots");
 };
 
 template <int QG>
 struct F8Smem {
     static constexpr int ST = F8Cfg<QG>::STAGES, SL = F8Cfg<QG>::SLOTS;
     uint8_t a[ST][F8_TILE * 128];          // e4m3 keys, 128-byte swizzle (cp.async); rows 128 h .. of half h
-    uint8_t b[2][QG * 64 * 128];           // per segment parity: hi rows 32 q + h, then lo rows 32 QG + 32 q + h
+    uint8_t b[2][QG * 64 * 128];           // per segment parity: the hi and lo rows of every query
     float sc[ST][F8_TILE];                 // fp32 scales of the stage's entries (cp.async)
     float wq[2][QG][32];                   // w_h * 2^e_h of each query, per segment parity
     uint64_t full[ST], empty[ST], tfull[SL], tempty[SL];
@@ -381,9 +391,14 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (ok) {
-                    for (int q = is; q < qn; q += Cfg::WRITERS)
-                        write_query_operand(S.b[seg & 1] + q * (32 * 128), S.b[seg & 1] + (N + 32 * q) * 128,
-                                            S.wq[seg & 1][q], qi + (int64_t)(r0 + q) * 4096, w + (int64_t)(r0 + q) * 32);
+                    for (int q = is; q < qn; q += Cfg::WRITERS) {
+                        // stacked: query q's hi rows 64 q .., lo rows 64 q + 32 ..; accumulated:
+                        // hi rows 32 q .., lo rows 32 QG + 32 q ..
+                        uint8_t *bh = S.b[seg & 1] + (Cfg::STACKED ? 64 * q : 32 * q) * 128;
+                        uint8_t *bl = S.b[seg & 1] + (Cfg::STACKED ? 64 * q + 32 : 32 * QG + 32 * q) * 128;
+                        write_query_operand(bh, bl, S.wq[seg & 1][q], qi + (int64_t)(r0 + q) * 4096,
+                                            w + (int64_t)(r0 + q) * 32);
+                    }
                     tc::fence_proxy_async_smem();
                     tc::mbar_arrive(&S.wready[seg & 1]);
                 }
@@ -425,7 +440,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 #pragma unroll
                                 for (int kk = 0; kk < 4; kk++)   // K = 128 codes in steps of 32
 #pragma unroll
-                                    for (int part = 0; part < 2; part++)   // hi, then lo into the same sums
+                                    for (int part = 0; part < Cfg::PARTS; part++)   // (hi, then lo)
                                         tc::mma_f8(tmem + (uint32_t)(slot * Cfg::SLOT_COLS + hf * N),
                                                    tc::smem_desc(as + hf * (128 * 128) + kk * 32, 16, 1024,
                                                                  tc::kSwizzle128B),
@@ -454,9 +469,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
                 break;
             }
-            int64_t nvq[QG];                              // each query's own visible range
+            int32_t nvq[QG];                              // each query's own visible range (< 2^31)
 #pragma unroll
-            for (int q = 0; q < QG; q++) nvq[q] = q < qn ? (QG == 1 ? nvis : f8_row_entries<DENSE>(bt, pool_len, ld, r0 + q)) : 0;
+            for (int q = 0; q < QG; q++)
+                nvq[q] = QG == 1 ? (int32_t)nvis : (q < qn ? (int32_t)f8_row_entries<DENSE>(bt, pool_len, ld, r0 + q) : 0);
             const int64_t rowp = (int64_t)hf * 128 + qd * 32 + lane;
             for (int64_t i = 0; i < nt; i++) {
                 const int64_t ti = it + i;
@@ -483,7 +499,22 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 for (int q = 0; q < QG; q++) {
                     const float *wv = S.wq[seg & 1][q];       // broadcast shared-memory reads
                     float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent chains
-                    if (q < qn) {
+                    if constexpr (Cfg::STACKED) {
+                      if (q < qn) {
+#pragma unroll
+                        for (int c16 = 0; c16 < 2; c16++) {    // heads 16 c16 .. 16 c16 + 15: hi + lo columns
+                            uint32_t dh[16], dl[16];
+                            tc::tmem_ld16(ta + 64u * q + 16u * c16, dh);
+                            tc::tmem_ld16(ta + 64u * q + 32u + 16u * c16, dl);
+                            tc::tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 16; j++) {
+                                const float x = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
+                                part[j & 3] = fmaf(wv[16 * c16 + j], fmaxf(x, 0.0f), part[j & 3]);
+                            }
+                        }
+                      }
+                    } else if (q < qn) {
                         uint32_t d[32];                         // q's 32 heads: hi . k + lo . k
                         tc::tmem_ld32(ta + 32u * q, d);
                         tc::tmem_ld_wait();
