@@ -495,34 +495,46 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 const float sc_cur = S.sc[stage][rowp];
                 const int64_t p = (j0 + i) * F8_TILE + rowp;
                 float res[QG];
+                if constexpr (Cfg::STACKED) {
 #pragma unroll
-                for (int q = 0; q < QG; q++) {
-                    const float *wv = S.wq[seg & 1][q];       // broadcast shared-memory reads
-                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four independent chains
-                    if constexpr (Cfg::STACKED) {
-                      if (q < qn) {
+                    for (int q = 0; q < QG; q++) {
+                        const float *wv = S.wq[seg & 1][q];   // broadcast shared-memory reads
+                        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // four independent chains
+                        if (q < qn) {
 #pragma unroll
-                        for (int c16 = 0; c16 < 2; c16++) {    // heads 16 c16 .. 16 c16 + 15: hi + lo columns
-                            uint32_t dh[16], dl[16];
-                            tc::tmem_ld16(ta + 64u * q + 16u * c16, dh);
-                            tc::tmem_ld16(ta + 64u * q + 32u + 16u * c16, dl);
-                            tc::tmem_ld_wait();
+                            for (int c16 = 0; c16 < 2; c16++) {   // heads 16 c16 .. 16 c16 + 15: hi + lo columns
+                                uint32_t dh[16], dl[16];
+                                tc::tmem_ld16(ta + 64u * q + 16u * c16, dh);
+                                tc::tmem_ld16(ta + 64u * q + 32u + 16u * c16, dl);
+                                tc::tmem_ld_wait();
 #pragma unroll
-                            for (int j = 0; j < 16; j++) {
-                                const float x = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
-                                part[j & 3] = fmaf(wv[16 * c16 + j], fmaxf(x, 0.0f), part[j & 3]);
+                                for (int j = 0; j < 16; j++) {
+                                    const float x = __uint_as_float(dh[j]) + __uint_as_float(dl[j]);
+                                    part[j & 3] = fmaf(wv[16 * c16 + j], fmaxf(x, 0.0f), part[j & 3]);
+                                }
                             }
                         }
-                      }
-                    } else if (q < qn) {
-                        uint32_t d[32];                         // q's 32 heads: hi . k + lo . k
-                        tc::tmem_ld32(ta + 32u * q, d);
-                        tc::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; j++)
-                            part[j & 3] = fmaf(wv[j], fmaxf(__uint_as_float(d[j]), 0.0f), part[j & 3]);
+                        res[q] = (part[0] + part[1]) + (part[2] + part[3]);
                     }
-                    res[q] = (part[0] + part[1]) + (part[2] + part[3]);
+                } else {
+                    // one column per head (hi . k + lo . k); two queries' columns in
+                    // flight per tensor-memory wait
+#pragma unroll
+                    for (int q = 0; q < QG; q += 2) {
+                        uint32_t d0[32], d1[32];
+                        tc::tmem_ld32(ta + 32u * q, d0);
+                        tc::tmem_ld32(ta + 32u * (q + 1), d1);
+                        tc::tmem_ld_wait();
+                        const float *w0 = S.wq[seg & 1][q], *w1 = S.wq[seg & 1][q + 1];
+                        float p0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, p1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                        for (int j = 0; j < 32; j++) {
+                            p0[j & 3] = fmaf(w0[j], fmaxf(__uint_as_float(d0[j]), 0.0f), p0[j & 3]);
+                            p1[j & 3] = fmaf(w1[j], fmaxf(__uint_as_float(d1[j]), 0.0f), p1[j & 3]);
+                        }
+                        res[q] = (p0[0] + p0[1]) + (p0[2] + p0[3]);
+                        res[q + 1] = (p1[0] + p1[1]) + (p1[2] + p1[3]);
+                    }
                 }
                 tc::tc_fence_before();
                 __syncwarp();
@@ -580,16 +592,21 @@ static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t
     const size_t smem = sizeof(F8Smem<QG>) + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_index_f8<true, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if constexpr (QG == 1)
+            cudaFuncSetAttribute(k_index_f8<true, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         cudaFuncSetAttribute(k_index_f8<false, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         attr = true;
     }
     const int64_t per_row = DENSE ? ld : bt.max_entries;
     const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
-    if (groups <= F8_PERSIST_ROWS) {
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, g_sms));
-        return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w, pool_len,
-                          scores, block_max, n_visible, ld);
+    // the persistent grid (ragged single-query batches) for QG = 1; query groups
+    // (equal lengths within a sequence) take a grid of CTAs per group
+    if constexpr (QG == 1) {
+        if (groups <= F8_PERSIST_ROWS) {
+            const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, g_sms));
+            return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
+                              pool_len, scores, block_max, n_visible, ld);
+        }
     }
     if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
     const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + groups - 1) / groups));
