@@ -399,7 +399,7 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-KERNEL_VERSION = "f8-cpasync-scan-v4"
+KERNEL_VERSION = "f8-cpasync-scan-v5"
 
 
 # ---------------------------------------------------------------- CPU oracle

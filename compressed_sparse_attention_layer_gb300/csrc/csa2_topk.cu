@@ -134,13 +134,20 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         for (int i = tid; i < m; i += TK_THREADS) emit((int)(lo + i), lo + i);
         return;
     }
-    // ---- the row's key range (cluster-wide), digits relative to its minimum
+    // ---- a lower bound L of the k-th largest key and the row's maximum
+    // (cluster-wide): the keys of TPG consecutive threads form a group (the
+    // cluster has CL * TK_THREADS / TPG >= k groups); every non-empty group
+    // holds a key >= its maximum, so at least k keys are >= L = the smallest
+    // group maximum (an empty group makes L = 0, no bound).  Digits are
+    // relative to L and only keys >= L are counted.
     {
-        uint32_t mn = 0xFFFFFFFFu, mx = 0u;
-        for (int i = tid; i < m; i += TK_THREADS) {
-            mn = min(mn, keys[i]);
-            mx = max(mx, keys[i]);
-        }
+        int tpg = (CL * TK_THREADS) / k;                 // threads per group, a power of two <= 32
+        tpg = tpg >= 32 ? 32 : (tpg >= 16 ? 16 : (tpg >= 8 ? 8 : (tpg >= 4 ? 4 : (tpg >= 2 ? 2 : 1))));
+        uint32_t gm = 0u, mx = 0u;
+        for (int i = tid; i < m; i += TK_THREADS) gm = max(gm, keys[i]);
+        for (int o = 1; o < tpg; o <<= 1) gm = max(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        uint32_t mn = k <= (CL * TK_THREADS) ? gm : 0u;  // the bound needs k groups
+        mx = gm;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
             mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -166,7 +173,7 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
     }
     const uint32_t range = kmax - kmin;
     const int nbits = range ? 32 - __clz(range) : 1;
-    uint32_t prefix = 0, mask = 0;                   // over rel = key - kmin
+    uint32_t prefix = 0, mask = 0;                   // over rel = key - kmin, keys >= kmin only
     int kk = k;
 #pragma unroll 1
     for (int top = nbits; top > 0; top -= 11) {
@@ -176,8 +183,8 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         for (int b = tid; b < 2048; b += TK_THREADS) sh.hist[b] = 0;
         __syncthreads();
         for (int i = tid; i < m; i += TK_THREADS) {
-            const uint32_t rel = keys[i] - kmin;
-            if ((rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
+            const uint32_t key = keys[i], rel = key - kmin;
+            if (key >= kmin && (rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
         }
         cluster.sync();                              // every slice counted
         uint32_t d;
