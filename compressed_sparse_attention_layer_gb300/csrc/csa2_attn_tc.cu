@@ -320,6 +320,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     // before that kernel's predecessors (a Reuse layer after another layer call):
     // those keys are then loaded and dequantised while that kernel finishes.
     bool stored = false;
+    uint32_t ring_word = 0;                        // the new token's window row, stored at the end
+    int64_t ring_idx = -1, ring_scale_idx = -1;
     if (early) {
         if (window) load_window_row();
         else load_selected();
@@ -370,18 +372,22 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
                 const float4 x = cb == 0 ? v[0] : cb == 1 ? v[1] : cb == 2 ? v[2] : v[3];
                 const uint32_t wd = f32x2_to_e4m3x2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc)) |
                                     (f32x2_to_e4m3x2(__fdiv_rn(x.z, sc), __fdiv_rn(x.w, sc)) << 16);
-                const int64_t off = (int64_t)b * swa.rows + t % swa.rows;
-                if (lane >= lb && lane < lb + 16)
-                    reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(swa.codes) + off * CSA2_HEAD_DIM)[base + (lane - lb)] = wd;
-                uint32_t got[16];
-#pragma unroll
-                for (int q2 = 0; q2 < 16; q2++) got[q2] = __shfl_sync(0xffffffffu, wd, lb + q2);
+                // each of the 16 lanes puts its four codes, widened exactly to bf16, into
+                // the key tile's row kn itself (no gathering into the key's lane); the
+                // ring row is stored at the end of the kernel
+                if (lane >= lb && lane < lb + 16) {
+                    ring_word = wd;
+                    ring_idx = (int64_t)((b * (int64_t)swa.rows + t % swa.rows) * (CSA2_HEAD_DIM / 4)) + base + (lane - lb);
+                    const uint2 kb = make_uint2(e4m3x2_to_bf16x2(__byte_perm(wd, 0, 0x4140)),
+                                                e4m3x2_to_bf16x2(__byte_perm(wd, 0, 0x4342)));
+                    *reinterpret_cast<uint2 *>(S.k + tc::sw128_offset((uint32_t)kn, 64 * hf + 4 * (lane - lb), AC_KEYS)) = kb;
+                }
                 if (key == kn) {
-#pragma unroll
-                    for (int i = 0; i < 4; i++) kc[i] = make_uint4(got[4 * i], got[4 * i + 1], got[4 * i + 2], got[4 * i + 3]);
-                    if (dq == 0 && hf == 0) const_cast<float *>(swa.scales)[off] = sc;
+                    if (dq == 0 && hf == 0) ring_scale_idx = (int64_t)b * swa.rows + t % swa.rows;
                     kscale = sc;
                     valid = true;
+                    stored = true;                 // its row of the key tile is written above
+                    if (hf == 0) S.kscale[key] = sc;
                 }
             }
         } else if (key == kn) {                    // the own token's row, written before this call
@@ -585,6 +591,9 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
             flag(c.status, CSA2_DEV_TIMEOUT);
         }
     }
+    // the new token's FP8 window row (codes and scale) into the ring
+    if (ring_idx >= 0) reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(swa.codes))[ring_idx] = ring_word;
+    if (ring_scale_idx >= 0) const_cast<float *>(swa.scales)[ring_scale_idx] = kscale;
     // the bulk copies out of this CTA's shared memory have finished reading it
     if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     tc::tc_fence_before();
