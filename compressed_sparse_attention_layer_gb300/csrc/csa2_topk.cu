@@ -38,6 +38,12 @@ struct TkShared {
     uint32_t digit;
     int above;
     uint32_t kmin, kmax;                   // this CTA's key range
+    int ncand;                             // keys >= the bound, compacted
+    uint32_t bin_count;                    // cluster-wide keys in the crossing bin
+    uint32_t ndirect;                      // rank 0: keys of a small crossing bin gathered here
+    uint32_t direct[32];
+    uint32_t T;
+    int need_eq;
 };
 
 // 32-bit load from the same shared-memory variable in CTA `rank` of the cluster.
@@ -112,6 +118,7 @@ __device__ void cluster_digit(cg::cluster_group &cluster, TkShared &sh, int kk, 
             if (acc + c[j] >= kk) {
                 sh.digit = (uint32_t)(BPR * slice + BPR - 1 - (tid * PER + j));
                 sh.above = acc;
+                sh.bin_count = (uint32_t)c[j];
                 break;
             }
             acc += c[j];
@@ -126,8 +133,8 @@ __device__ void cluster_digit(cg::cluster_group &cluster, TkShared &sh, int kk, 
 // emit(rank, slot) for every selected slot of this slice, rank ascending with
 // the slot across the whole row.
 template <int CL, class Emit>
-__device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys, int64_t lo, int m, int64_t n,
-                               int k, TkShared &sh, Emit emit)
+__device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys, uint32_t *cand, int64_t lo, int m,
+                               int64_t n, int k, TkShared &sh, Emit emit)
 {
     const int tid = threadIdx.x;
     if (n <= k) {                                    // everything is selected: rank = slot
@@ -173,18 +180,35 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
     }
     const uint32_t range = kmax - kmin;
     const int nbits = range ? 32 - __clz(range) : 1;
+    // this CTA's keys >= the bound, compacted (thread by thread) so that every
+    // radix round reads only them
+    {
+        int cnt = 0;
+        for (int i = tid; i < m; i += TK_THREADS) cnt += keys[i] >= kmin;
+        int tot = 0;
+        int pos = block_exclusive_scan<TK_THREADS>(cnt, sh.warp_sums, &tot);
+        for (int i = tid; i < m; i += TK_THREADS) {
+            const uint32_t key = keys[i];
+            if (key >= kmin) cand[pos++] = key;
+        }
+        if (tid == 0) sh.ncand = tot;
+        __syncthreads();
+    }
+    const int nc = sh.ncand;
     uint32_t prefix = 0, mask = 0;                   // over rel = key - kmin, keys >= kmin only
     int kk = k;
+    bool direct = false;
+    if (tid == 0) sh.ndirect = 0u;                   // (cluster-synchronised before any use)
 #pragma unroll 1
-    for (int top = nbits; top > 0; top -= 11) {
+    for (int top = nbits; top > 0;) {
         const int width = top < 11 ? top : 11;
         const int shift = top - width;
         const uint32_t dmask = (1u << width) - 1u;
         for (int b = tid; b < 2048; b += TK_THREADS) sh.hist[b] = 0;
         __syncthreads();
-        for (int i = tid; i < m; i += TK_THREADS) {
-            const uint32_t key = keys[i], rel = key - kmin;
-            if (key >= kmin && (rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
+        for (int i = tid; i < nc; i += TK_THREADS) {
+            const uint32_t rel = cand[i] - kmin;
+            if ((rel & mask) == prefix) atomicAdd(&sh.hist[(rel >> shift) & dmask], 1u);
         }
         cluster.sync();                              // every slice counted
         uint32_t d;
@@ -193,10 +217,44 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         prefix |= d << shift;
         mask |= dmask << shift;
         kk -= above;
+        top = shift;
+        if (top > 0 && sh.bin_count <= 32u) {
+            // a crossing bin of at most 32 keys (cluster-wide): gathered in rank 0,
+            // whose first warp ranks them directly
+            uint32_t *cnt0 = cluster.map_shared_rank(&sh.ndirect, 0);
+            uint32_t *dir0 = cluster.map_shared_rank(sh.direct, 0);
+            for (int i = tid; i < nc; i += TK_THREADS) {
+                const uint32_t rel = cand[i] - kmin;
+                if ((rel & mask) == prefix) dir0[atomicAdd(cnt0, 1u) & 31u] = cand[i];
+            }
+            cluster.sync();                          // every key gathered
+            if (cluster.block_rank() == 0 && tid < 32) {
+                const int nd = (int)(sh.ndirect < 32u ? sh.ndirect : 32u);
+                const uint32_t v = tid < nd ? sh.direct[tid] : 0u;
+                int gt = 0, ge = 0;
+                for (int i = 0; i < nd; i++) {
+                    const uint32_t u = sh.direct[i];
+                    gt += u > v;
+                    ge += u >= v;
+                }
+                // the kk-th largest of the bin (every lane holding it writes the same)
+                if (tid < nd && gt < kk && ge >= kk) {
+                    sh.T = v;
+                    sh.need_eq = kk - gt;
+                }
+            }
+            cluster.sync();                          // T written
+            direct = true;
+            break;
+        }
         cluster.sync();                              // every CTA done reading before the reset
     }
-    const uint32_t T = prefix + kmin;
-    const int need_eq = kk;                          // ties with T that are selected, lowest slots first
+    uint32_t T = prefix + kmin;
+    int need_eq = kk;                                // ties with T that are selected, lowest slots first
+    if (direct) {
+        T = *cluster.map_shared_rank(&sh.T, 0);
+        need_eq = *cluster.map_shared_rank(&sh.need_eq, 0);
+    }
 
     // ---- counts of this thread's chunk, of this slice, and of the slices before it
     const int chunk = ((m + TK_THREADS - 1) / TK_THREADS) | 1;    // odd: no bank conflicts
@@ -208,9 +266,11 @@ __device__ void cluster_select(cg::cluster_group &cluster, const uint32_t *keys,
         gt += u > T;
         eq += u == T;
     }
-    int tot_gt = 0, tot_eq = 0;
-    const int gt_local = block_exclusive_scan<TK_THREADS>(gt, sh.warp_sums, &tot_gt);
-    const int eq_local = block_exclusive_scan<TK_THREADS>(eq, sh.warp_sums, &tot_eq);
+    // one scan of both counts packed in 16-bit halves (a slice holds at most 16,384 keys)
+    int tot_pk = 0;
+    const int pk = block_exclusive_scan<TK_THREADS>((gt << 16) | eq, sh.warp_sums, &tot_pk);
+    const int gt_local = pk >> 16, eq_local = pk & 0xFFFF;
+    const int tot_gt = tot_pk >> 16, tot_eq = tot_pk & 0xFFFF;
     if (tid == 0) {
         sh.cnt[0] = tot_gt;
         sh.cnt[1] = tot_eq;
@@ -260,6 +320,10 @@ __device__ __forceinline__ void stage_keys(uint32_t *keys, const float *row, int
     }
 }
 
+// Keys of one CTA's slice of a row of ld slots (its staged keys, then as many
+// again for the compacted candidates): the dynamic shared memory is twice that.
+__host__ __device__ __forceinline__ int64_t slice_cap(int64_t ld, int cl) { return ((ld + cl - 1) / cl + 3) & ~(int64_t)3; }
+
 // Slice of a row of n keys held by cluster rank q: a multiple of 4 keys so
 // that slices of 16-byte aligned rows stay aligned.
 __device__ __forceinline__ void slice_of(int64_t n, int cl, int q, int64_t &lo, int &m)
@@ -293,7 +357,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(const float *__restrict__ s
     __syncthreads();
     int32_t *o = out + r * k;
     const int32_t *cr = cand ? cand + r * ld : nullptr;
-    cluster_select<CL>(cluster, keys, lo, m, n, k, sh, [&](int j, int64_t i) {
+    cluster_select<CL>(cluster, keys, keys + slice_cap(ld, CL), lo, m, n, k, sh, [&](int j, int64_t i) {
         if (j < k) o[j] = cr ? cr[i] : (int32_t)i;
     });
     const int64_t nsel = n < k ? n : k;
@@ -325,7 +389,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
     __syncthreads();
     int32_t *pr = pool + r * (int64_t)pmax * 8;
     const int nsel = (int)(nb < pmax ? nb : pmax);
-    cluster_select<CL>(cluster, keys, lo, m, nb, pmax, sh, [&](int j, int64_t blk) {
+    cluster_select<CL>(cluster, keys, keys + slice_cap(ld_blocks, CL), lo, m, nb, pmax, sh, [&](int j, int64_t blk) {
         if (j >= pmax) return;
 #pragma unroll
         for (int t = 0; t < 8; t++) {
@@ -625,7 +689,7 @@ static int launch_cluster(K kernel, int cl, int64_t ld, int32_t rows, cudaStream
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rows * (unsigned)cl);
     cfg.blockDim = dim3(TK_THREADS);
-    cfg.dynamicSmemBytes = (size_t)((((ld + cl - 1) / cl + 3) & ~(int64_t)3) * 4);
+    cfg.dynamicSmemBytes = (size_t)(2 * slice_cap(ld, cl) * 4);
     cfg.stream = st;
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -650,7 +714,7 @@ static int topk_cl(const float *scores, int64_t ld, const int32_t *len, int32_t 
 {
     static bool attr = false;                        // raise the limit once, before any graph capture
     if (!attr) {
-        cudaFuncSetAttribute(k_topk<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SLICE * 4);
+        cudaFuncSetAttribute(k_topk<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * TK_SLICE * 4);
         attr = true;
     }
     return launch_cluster(k_topk<CL>, CL, ld, rows, st, scores, ld, len, cand, (int)k, out);
@@ -662,7 +726,7 @@ static int blocks_cl(const float *block_max, int64_t ld_blocks, const int32_t *n
 {
     static bool attr = false;
     if (!attr) {
-        cudaFuncSetAttribute(k_topk_blocks<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, TK_SLICE * 4);
+        cudaFuncSetAttribute(k_topk_blocks<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * TK_SLICE * 4);
         attr = true;
     }
     return launch_cluster(k_topk_blocks<CL>, CL, ld_blocks, rows, st, block_max, ld_blocks, n_visible, (int)pmax,
