@@ -45,6 +45,8 @@ def parse():
                    choices=["decode_1m", "decode_small", "decode_group", "decode_ragged", "prefill"],
                    help="decode_1m (default: the headline, batch 8 x 1M tokens); the other four synthetic "
                         "workloads run the same step for their own shapes (prefill: one 8,192-token chunk)")
+    p.add_argument("--bf16-scores", action="store_true",
+                   help="Full and Reindex layers select on bf16-rounded index scores (csa2.LAYER_SCORES_BF16)")
     p.add_argument("--queries", type=int, default=1,
                    help="query tokens per sequence per step (>1: a multi-token decode step, e.g. draft "
                         "tokens verified together; the Full layer's scan serves them from one read)")
@@ -268,6 +270,8 @@ def run_native(args):
     step = DecodeStep(args.batch, args.tokens, seed, dev, kv_format=args.kv_format, queries=args.queries,
                       workload=args.workload)
     B, N, Q = step.wl.batch, step.wl.tokens[0], step.queries
+    if args.bf16_scores:
+        step.dw.layer_flags = csa2.LAYER_SCORES_BF16
 
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
@@ -453,8 +457,9 @@ def run_native(args):
                  f"m={wl.m}, {len(wl.layers)} layers {'/'.join(sorted(set(wl.layers)))}, Top-512, SWA 128")
     inputs_bytes = sum(wl.entries(b) for b in range(B)) * 132
 
-    metric = METRIC if args.workload == "decode_1m" and Q == 1 else \
-        f"CSA2 query-tokens/s, {args.workload}" + (f", {Q} query tokens per sequence" if Q > 1 else "")
+    metric = METRIC if args.workload == "decode_1m" and Q == 1 and not args.bf16_scores else \
+        f"CSA2 query-tokens/s, {args.workload}" + (f", {Q} query tokens per sequence" if Q > 1 else "") + \
+        (", bf16 index scores" if args.bf16_scores else "")
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -469,7 +474,8 @@ def run_native(args):
                           "keys per step") if inputs_bytes >= (256 << 20) else
                          (f"L2 flushed (512 MB write) before every timed step; the step's indexer keys are "
                           f"{inputs_bytes / 1e6:.1f} MB"),
-                   "graph": "one CUDA graph per step"},
+                   "graph": "one CUDA graph per step",
+                   "index_scores": "bf16 (selection on rounded scores)" if args.bf16_scores else "fp32"},
         "roofline": roofline, "per_layer_mode": per_mode, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
         "cpu_baseline": cpu,
     }

@@ -44,7 +44,7 @@ class Swa(ctypes.Structure):
 
 
 class LayerIO(ctypes.Structure):
-    _fields_ = [("q", _vp), ("qi", _vp), ("w", _vp), ("swa", Swa), ("sm_scale", _f32), ("pad_", _i32),
+    _fields_ = [("q", _vp), ("qi", _vp), ("w", _vp), ("swa", Swa), ("sm_scale", _f32), ("flags", _i32),
                 ("idx", _vp), ("pool", _vp), ("pool_len", _vp), ("o", _vp), ("lse", _vp),
                 ("prof_begin", _vp), ("prof_end", _vp), ("pool_codes", _vp), ("pool_scales", _vp)]
 
@@ -162,6 +162,7 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
 
 
 ATTN_DEDUP_WINDOW = 1
+LAYER_SCORES_BF16 = 1      # csa2_layer_io.flags: selection on bf16-rounded index scores
 ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
 
 
@@ -249,14 +250,16 @@ def csa2_layer_workspace_size(mode: int, batch: Batch) -> int:
     return int(load().csa2_layer_workspace_size(mode, ctypes.byref(batch)))
 
 
-def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None, pool_keys=None) -> LayerIO:
+def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None, pool_keys=None,
+             flags: int = 0) -> LayerIO:
     """prof: optional (begin, end) pair of recorded torch.cuda.Event(enable_timing=True).
     pool_keys: optional (codes uint8 [rows][16384][128], scales fp32 [rows][16384]) carried
-    copy of the pool's indexer keys (written by a Full layer, read by Reindex layers)."""
+    copy of the pool's indexer keys (written by a Full layer, read by Reindex layers).
+    flags: LAYER_SCORES_BF16 or 0."""
     pb, pe = (prof[0].cuda_event, prof[1].cuda_event) if prof else (None, None)
     pkc, pks = pool_keys if pool_keys is not None else (None, None)
     return LayerIO(_ptr(q, torch.bfloat16, "q"), _ptr(qi, torch.bfloat16, "qi"), _ptr(w, torch.float32, "w"),
-                   swa, float(sm_scale), 0, _ptr(idx, torch.int32, "idx"), _ptr(pool, torch.int32, "pool"),
+                   swa, float(sm_scale), int(flags), _ptr(idx, torch.int32, "idx"), _ptr(pool, torch.int32, "pool"),
                    _ptr(pool_len, torch.int32, "pool_len"), _ptr(o, torch.float32, "o"),
                    _ptr(lse, torch.float32, "lse"), pb, pe, _ptr(pkc, torch.uint8, "pool codes"),
                    _ptr(pks, torch.float32, "pool scales"))

@@ -18,17 +18,17 @@ int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, fl
 int launch_quant_fp4_e4m3(const float *, int64_t, const int64_t *, uint8_t *, uint8_t *, int64_t, int32_t *,
                           cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
-                      float *, int32_t *, int64_t, cudaStream_t);
+                      float *, int32_t *, int64_t, cudaStream_t, bool bf16_scores = false);
 int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, const int32_t *, int64_t, uint8_t *,
                        float *, cudaStream_t);
 int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const uint16_t *, const float *,
-                       const int32_t *, int64_t, float *, cudaStream_t);
+                       const int32_t *, int64_t, float *, cudaStream_t, bool bf16_scores = false);
 int launch_index_pool(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
                            const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
-                cudaStream_t);
+                cudaStream_t, bool bf16_scores = false);
 int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int32_t *, int32_t, int32_t,
-                     int32_t *, cudaStream_t);
+                     int32_t *, cudaStream_t, bool bf16_scores = false);
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
@@ -281,6 +281,8 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
     if (!io->pool_codes != !io->pool_scales) return CSA2_ERR_NULL;
+    if (io->flags & ~CSA2_LAYER_SCORES_BF16) return CSA2_ERR_UNSUPPORTED;
+    const bool bf16 = (io->flags & CSA2_LAYER_SCORES_BF16) != 0;
     if (io->pool_codes && (!aligned(io->pool_codes, 16) || !aligned(io->pool_scales, 16))) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
@@ -308,7 +310,8 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (mode == CSA2_MODE_FULL) {
         // a4: scores of every visible entry and the per-block maxima
         if ((s = prof(io->prof_begin))) return s;
-        if ((s = launch_index_scan(*cache, *batch, io->qi, io->w, ws.scores, ws.block_max, ws.n_visible, ld, st)))
+        if ((s = launch_index_scan(*cache, *batch, io->qi, io->w, ws.scores, ws.block_max, ws.n_visible, ld, st,
+                                   bf16)))
             return s;
         if ((s = prof(io->prof_end))) return s;
         // a5: the best 2,048 blocks of 8 -> candidate pool
@@ -316,7 +319,8 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
                                     io->pool_len, st)))
             return s;
         // a6: Top-512 of the pool, its scores read from the scan's score rows
-        if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st)))
+        if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st,
+                                  bf16)))
             return s;
         // the pool's keys for the Reindex layers that follow, when the caller carries them
         if (io->pool_codes &&
@@ -337,10 +341,12 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
             kc = ws.pool_kcodes;
             ks = ws.pool_kscales;
         }
-        if ((s = launch_index_dense(kc, ks, *batch, io->qi, io->w, io->pool_len, CSA2_POOL_MAX, ws.pool_scores, st)))
+        if ((s = launch_index_dense(kc, ks, *batch, io->qi, io->w, io->pool_len, CSA2_POOL_MAX, ws.pool_scores, st,
+                                    bf16)))
             return s;
         if ((s = prof(io->prof_end))) return s;
-        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st)))
+        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st,
+                             bf16)))
             return s;
     }
     // a8 (REUSE) keeps io->idx as it is; a9 for every mode

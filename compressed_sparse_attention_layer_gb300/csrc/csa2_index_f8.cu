@@ -41,6 +41,8 @@
 // even and odd tiles (one issuing thread that also waits on barriers between
 // tiles leaves the tensor pipe idle half the time).  A persistent grid walks
 // one global list of (query group, tile) items so ragged batches stay balanced.
+#include <cuda_bf16.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -230,7 +232,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                                                             const int32_t *__restrict__ pool_len,
                                                             float *__restrict__ scores,
                                                             float *__restrict__ block_max,
-                                                            int32_t *__restrict__ n_visible, int64_t ld)
+                                                            int32_t *__restrict__ n_visible, int64_t ld,
+                                                            int bf16_scores)
 {
     using Cfg = F8Cfg<QG>;
     constexpr int ST = Cfg::STAGES, SL = Cfg::SLOTS, N = Cfg::N;
@@ -550,7 +553,13 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                     float sc = -INFINITY;
                     if (valid) {
                         if (sc_cur != -INFINITY) sc = res[q] * sc_cur;
-                        if (scores) scores[rq * ld + p] = sc;
+                        if (bf16_scores) {             // kept as bf16 (nearest even); maxima of the rounded
+                            const __nv_bfloat16 hb = __float2bfloat16_rn(sc);
+                            sc = __bfloat162float(hb);
+                            if (scores) reinterpret_cast<__nv_bfloat16 *>(scores)[rq * ld + p] = hb;
+                        } else if (scores) {
+                            scores[rq * ld + p] = sc;
+                        }
                     }
                     if (!DENSE && block_max) {
                         float m = valid ? sc : -INFINITY;
@@ -586,7 +595,7 @@ static std::once_flag g_sms_once;
 template <bool DENSE, int QG>
 static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                        const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
-                       cudaStream_t st)
+                       cudaStream_t st, bool bf16)
 {
     const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
     const size_t smem = sizeof(F8Smem<QG>) + 1024;
@@ -605,13 +614,13 @@ static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t
         if (groups <= F8_PERSIST_ROWS) {
             const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, g_sms));
             return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
-                              pool_len, scores, block_max, n_visible, ld);
+                              pool_len, scores, block_max, n_visible, ld, (int)bf16);
         }
     }
     if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
     const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + groups - 1) / groups));
     return launch_pdl(k_index_f8<false, DENSE, QG>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
-                      pool_len, scores, block_max, n_visible, ld);
+                      pool_len, scores, block_max, n_visible, ld, (int)bf16);
 }
 
 // Queries per group: the largest of 4, 2, 1 that the per-sequence query count
@@ -619,7 +628,7 @@ static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t
 template <bool DENSE>
 static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                      const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
-                     cudaStream_t st)
+                     cudaStream_t st, bool bf16)
 {
     std::call_once(g_sms_once, [] {
         int dev = 0;
@@ -627,15 +636,17 @@ static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *
         cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
     });
     if (g_sms <= 0) return CSA2_ERR_CUDA;
-    if (DENSE || bt.nq < 2) return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
-    if (bt.nq < 4) return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
-    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st);
+    if (DENSE || bt.nq < 2)
+        return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
+    if (bt.nq < 4) return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
+    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
 }
 
 int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
-                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st)
+                      float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st,
+                      bool bf16_scores)
 {
-    return launch_f8<false>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st);
+    return launch_f8<false>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st, bf16_scores);
 }
 
 // Dense copy of the indexer keys of each row's candidate pool: slot e of row r
@@ -689,14 +700,15 @@ int launch_gather_pool(const csa2_cache &c, const csa2_batch &bt, const int32_t 
 // Scores of the dense pool copy (rows of ld slots, codes [rows][ld][128] and
 // scales [rows][ld]) for slots 0 .. pool_len[r] of each row.
 int launch_index_dense(const uint8_t *codes, const float *scales, const csa2_batch &bt, const uint16_t *qi,
-                       const float *w, const int32_t *pool_len, int64_t ld, float *scores, cudaStream_t st)
+                       const float *w, const int32_t *pool_len, int64_t ld, float *scores, cudaStream_t st,
+                       bool bf16_scores)
 {
     if (ld % CSA2_PAGE) return CSA2_ERR_SHAPE;
     csa2_cache d = {};
     d.ik_codes = const_cast<uint8_t *>(codes);
     d.ik_scales = const_cast<float *>(scales);
     d.num_slots = (int64_t)bt.batch * bt.nq * ld;
-    return launch_f8<true>(d, bt, qi, w, pool_len, scores, nullptr, nullptr, ld, st);
+    return launch_f8<true>(d, bt, qi, w, pool_len, scores, nullptr, nullptr, ld, st, bf16_scores);
 }
 
 }  // namespace csa2

@@ -608,10 +608,26 @@ __device__ int rs_select(const uint32_t (&key)[RS_PER], uint32_t valid, int n, i
 // (row[i]) when ind is NULL, else gathered (src[ind[i]]; an index outside
 // [0, src_len) reads as -inf).  Returns the valid mask (slots < n).
 __device__ __forceinline__ uint32_t rs_load(const float *__restrict__ row, const int32_t *__restrict__ ind,
-                                            int64_t src_len, int n, uint32_t (&key)[RS_PER])
+                                            int64_t src_len, int n, uint32_t (&key)[RS_PER], bool bf16)
 {
     const int s0 = RS_PER * threadIdx.x;
     uint32_t valid = 0;
+    if (bf16) {                                    // bf16 score rows (same slots, two bytes each)
+        const uint16_t *row16 = reinterpret_cast<const uint16_t *>(row);
+        int32_t p[RS_PER];
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++) p[j] = s0 + j < n ? (ind ? __ldg(ind + s0 + j) : s0 + j) : -1;
+#pragma unroll
+        for (int j = 0; j < RS_PER; j++) {
+            key[j] = 0u;
+            if (s0 + j < n) {
+                const bool ok = p[j] >= 0 && (!ind || p[j] < src_len);
+                key[j] = order_key(ok ? bf16_to_f32(__ldg(row16 + p[j])) : -INFINITY);
+                valid |= 1u << j;
+            }
+        }
+        return valid;
+    }
     if (!ind) {
         if (s0 + RS_PER <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
 #pragma unroll
@@ -655,7 +671,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__rest
                                                               const int32_t *__restrict__ ind, int64_t ld,
                                                               const int32_t *__restrict__ len,
                                                               const int32_t *__restrict__ cand, int k,
-                                                              int32_t *__restrict__ out)
+                                                              int32_t *__restrict__ out, int bf16)
 {
     __shared__ RsShared sh;
     pdl_launch_dependents();
@@ -665,8 +681,12 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__rest
     n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
     const int n = (int)n64;
     uint32_t key[RS_PER];
-    const uint32_t valid = ind ? rs_load(scores + r * src_len, ind + r * ld, src_len, n, key)
-                               : rs_load(scores + r * ld, nullptr, 0, n, key);
+    // row offsets in elements of the score type (fp32, or bf16 with bf16 != 0)
+    const float *srow = bf16 ? reinterpret_cast<const float *>(reinterpret_cast<const uint16_t *>(scores) +
+                                                               r * (ind ? src_len : ld))
+                             : scores + r * (ind ? src_len : ld);
+    const uint32_t valid = ind ? rs_load(srow, ind + r * ld, src_len, n, key, bf16 != 0)
+                               : rs_load(srow, nullptr, 0, n, key, bf16 != 0);
     int32_t *o = out + r * k;
     const int32_t *cr = cand ? cand + r * ld : nullptr;
     const int s0 = RS_PER * threadIdx.x;
@@ -734,13 +754,14 @@ static int blocks_cl(const float *block_max, int64_t ld_blocks, const int32_t *n
 }
 
 int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
-                int32_t k, int32_t *out, cudaStream_t st)
+                int32_t k, int32_t *out, cudaStream_t st, bool bf16_scores)
 {
     if (rows == 0) return CSA2_OK;
     if (ld <= RS_MAX) {
         return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, (int64_t)0,
-                          (const int32_t *)nullptr, ld, len, cand, (int)k, out);
+                          (const int32_t *)nullptr, ld, len, cand, (int)k, out, (int)bf16_scores);
     }
+    if (bf16_scores) return CSA2_ERR_UNSUPPORTED;      // bf16 rows: the one-CTA select only
     switch (topk_cluster_for(ld)) {
     case 1: return topk_cl<1>(scores, ld, len, rows, cand, k, out, st);
     case 2: return topk_cl<2>(scores, ld, len, rows, cand, k, out, st);
@@ -753,12 +774,12 @@ int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t row
 // full score row (scores[r][pool[r][i]], rows of ld_scores), reported as
 // positions, ascending.
 int launch_topk_pool(const float *scores, int64_t ld_scores, const int32_t *pool, int64_t ld_pool,
-                     const int32_t *pool_len, int32_t rows, int32_t k, int32_t *out, cudaStream_t st)
+                     const int32_t *pool_len, int32_t rows, int32_t k, int32_t *out, cudaStream_t st, bool bf16_scores)
 {
     if (rows == 0) return CSA2_OK;
     if (ld_pool > RS_MAX) return CSA2_ERR_SHAPE;
     return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, ld_scores, pool, ld_pool,
-                      pool_len, pool, (int)k, out);
+                      pool_len, pool, (int)k, out, (int)bf16_scores);
 }
 
 int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,

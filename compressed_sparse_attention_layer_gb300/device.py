@@ -101,6 +101,7 @@ class DeviceWorkload:
         # attention options passed to every layer call (csa2.swa_struct keywords:
         # sink, rope_base, flags); none by default
         self.attn_options = {}
+        self.layer_flags = 0             # csa2.LAYER_* bits for every layer call
         # Reuse layers load their keys while the previous layer finishes
         # (csa2.ATTN_EARLY_INPUTS): the layers are called one after the other
         self.early_inputs = True
@@ -162,7 +163,7 @@ class DeviceWorkload:
         qi = self.qi.get(l, self.dummy_qi)
         w = self.w.get(l, self.dummy_w)
         return csa2.layer_io(self.q[l], qi, w, self.swa(l, new_rows), 1.0, self.idx, self.pool, self.pool_len,
-                             self.o[l], self.lse[l], prof=prof, pool_keys=self.pool_keys)
+                             self.o[l], self.lse[l], prof=prof, pool_keys=self.pool_keys, flags=self.layer_flags)
 
     def run_layer(self, l, stream=None, prof=None, new_rows=None):
         """new_rows: optional window rows of the decode tokens, quantised into the

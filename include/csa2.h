@@ -179,6 +179,15 @@ typedef struct csa2_swa {
  * the window rows of its own tokens passed as new_rows, satisfies it. */
 #define CSA2_ATTN_EARLY_INPUTS 2
 
+/* csa2_layer_io.flags: FULL and REINDEX layers keep the index scores in bf16
+ * (each fp32 score rounded to nearest even) and select on them: the block
+ * maxima are those of the rounded scores and the Top-512 ranks the rounded
+ * scores (ties to the lower position).  The pages report that a BF16 score
+ * path doubles Top-K speed at 99.7 % recall ("DeepSeek-V4 report explainer"
+ * §10.2); this is that trade, outside the fp32 parity rule: near-ties at the
+ * threshold may resolve differently from fp32 scores. */
+#define CSA2_LAYER_SCORES_BF16 1
+
 /* Per-layer inputs, outputs and carried selection state for csa2_layer. */
 typedef struct csa2_layer_io {
     const uint16_t *q;           /* bf16 [B*Q][64][512] attention queries      */
@@ -186,7 +195,7 @@ typedef struct csa2_layer_io {
     const float    *w;           /* [B*Q][32] indexer head weights             */
     csa2_swa        swa;         /* this layer's window                        */
     float           sm_scale;    /* multiplies q.k (1 if q is pre-scaled)     */
-    int32_t         pad_;
+    int32_t         flags;       /* CSA2_LAYER_* option bits (0: none)        */
     int32_t        *idx;         /* [B*Q][512] selection (written by FULL and
                                     REINDEX, read by every mode)              */
     int32_t        *pool;        /* [B*Q][16384] candidate pool (written by
