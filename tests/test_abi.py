@@ -78,6 +78,26 @@ def test_host_validation_without_gpu(lib):
     assert lib.csa2_index_scores(ctypes.byref(cache), ctypes.byref(batch), 16, 16, 16, None, None, 104, None) == -3
 
 
+def test_layer_option_flags_validated_on_the_host(lib):
+    """Unknown csa2_layer_io.flags or csa2_swa.flags bits are refused before any
+    launch (fake aligned device pointers: nothing is dereferenced)."""
+    from compressed_sparse_attention_layer_gb300 import csa2
+    P = ctypes.c_void_p(1 << 12)
+    cache = csa2.Cache(P, P, P, P, 1 << 12, P, 64, 0, None)
+    batch = csa2.Batch(1, 1, 1, 0, 1000, P, P)
+    def io(layer_flags=0, swa_flags=0):
+        s = csa2.Swa(P, P, 128, swa_flags, None, None, None, 0.0, 0)
+        return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None, None, None)
+    for bad in (io(layer_flags=2), io(layer_flags=1 << 30), io(swa_flags=4)):
+        assert lib.csa2_layer(csa2.MODES["full"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(bad),
+                              P, 1 << 30, None) == -3
+    # a negative RoPE base is a shape error
+    s = csa2.Swa(P, P, 128, 0, None, None, None, -1.0, 0)
+    neg = csa2.LayerIO(P, P, P, s, 1.0, 0, P, P, P, P, P, None, None, None, None)
+    assert lib.csa2_layer(csa2.MODES["reuse"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(neg),
+                          P, 1 << 30, None) == -2
+
+
 def test_workspace_sizes(lib):
     from compressed_sparse_attention_layer_gb300 import csa2
     b = csa2.Batch(8, 1, 1, 0, 1 << 20, None, None)
