@@ -187,14 +187,33 @@ class DecodeStep:
             e.record()                       # materialise the CUDA events
         self.launches = 3 + sum({"full": 6, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
             (len(wl.layers) if Q > 1 else 0)
-        # the step's host inputs for the end-to-end leg (new token + every layer's queries)
-        self.h2d = [(self.C_new, None), (self.ik_new, None)]
+        # the step's host-fed inputs (new tokens, every layer's queries and window
+        # rows) in one device buffer and its outputs (every layer's o and lse) in
+        # another, so that the end-to-end leg moves each direction with one copy
+        ins = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
         for l in dw.layers:
-            self.h2d.append((dw.q[l], None))
-            self.h2d.append((self.swa_new[l], None))
+            ins += [(dw.q, l), (self.swa_new, l)]
             if l in dw.qi:
-                self.h2d += [(dw.qi[l], None), (dw.w[l], None)]
-        self.d2h = [dw.o[l] for l in dw.layers] + [dw.lse[l] for l in dw.layers]
+                ins += [(dw.qi, l), (dw.w, l)]
+        self.in_dev = self._gather(ins)
+        self.out_dev = self._gather([(dw.o, l) for l in dw.layers] + [(dw.lse, l) for l in dw.layers])
+        self.h2d = [(self.in_dev, None)]
+        self.d2h = [self.out_dev]
+
+    def _gather(self, refs):
+        """One device byte buffer holding the tensors refs name (container, key),
+        each 256-byte aligned; the containers are rebound to views of it."""
+        torch = self.torch
+        sizes = [(c[k].numel() * c[k].element_size() + 255) // 256 * 256 for c, k in refs]
+        buf = torch.empty(sum(sizes), dtype=torch.uint8, device=self.dw.dev)
+        off = 0
+        for (c, k), n in zip(refs, sizes):
+            t = c[k]
+            v = buf[off: off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            c[k] = v
+            off += n
+        return buf
 
     def enqueue(self, prof=True):
         csa2, dw, cache = self.csa2, self.dw, self.dw.cache
