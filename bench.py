@@ -188,17 +188,21 @@ class DecodeStep:
         self.launches = 3 + sum({"full": 6, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
             (len(wl.layers) if Q > 1 else 0)
         # the step's host-fed inputs (new tokens, every layer's queries and window
-        # rows) in one device buffer and its outputs (every layer's o and lse) in
-        # another, so that the end-to-end leg moves each direction with one copy
-        ins = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
-        for l in dw.layers:
-            ins += [(dw.q, l), (self.swa_new, l)]
-            if l in dw.qi:
-                ins += [(dw.qi, l), (dw.w, l)]
-        self.in_dev = self._gather(ins)
-        self.out_dev = self._gather([(dw.o, l) for l in dw.layers] + [(dw.lse, l) for l in dw.layers])
-        self.h2d = [(self.in_dev, None)]
-        self.d2h = [self.out_dev]
+        # rows) and its outputs (every layer's o and lse) in two device buffers
+        # each -- the first layer's inputs / the rest, the first half of the
+        # layers' outputs / the rest -- so that the end-to-end leg copies in
+        # while the first layer runs and copies out while the second half runs
+        layers = list(dw.layers)
+        self.half = max(1, len(layers) // 2)
+        ins0 = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
+        ins1 = []
+        for i, l in enumerate(layers):
+            refs = [(dw.q, l), (self.swa_new, l)] + ([(dw.qi, l), (dw.w, l)] if l in dw.qi else [])
+            (ins0 if i == 0 else ins1).extend(refs)
+        self.in_dev = [self._gather(ins0)] + ([self._gather(ins1)] if ins1 else [])
+        outs = [[(dw.o, l), (dw.lse, l)] for l in layers]
+        self.out_dev = [self._gather(sum(outs[:self.half], []))] + \
+            ([self._gather(sum(outs[self.half:], []))] if len(layers) > self.half else [])
 
     def _gather(self, refs):
         """One device byte buffer holding the tensors refs name (container, key),
@@ -223,6 +227,40 @@ class DecodeStep:
         quant(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
         csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
         self.enqueue_layers(dw.layers, prof)
+
+    def enqueue_e2e(self, host_in, host_out, s2, s3):
+        """The step with its copies, for capture on the current stream: the first
+        layer's inputs first, the other layers' on s2 while the first layer runs;
+        the first half of the outputs on s3 while the second half of the layers
+        runs, the rest at the end."""
+        torch, dw, csa2, cache = self.torch, self.dw, self.csa2, self.dw.cache
+        s = torch.cuda.current_stream()
+        ev_in, ev_mid = torch.cuda.Event(), torch.cuda.Event()
+        if len(self.in_dev) > 1:
+            s2.wait_stream(s)
+            with torch.cuda.stream(s2):
+                self.in_dev[1].copy_(host_in[1], non_blocking=True)
+                ev_in.record(s2)
+        self.in_dev[0].copy_(host_in[0], non_blocking=True)
+        csa2.csa2_compress(self.C_new, self.Z_new, self.bias, self.wl.m, self.e_new)
+        quant = csa2.csa2_quant_fp4_e4m3 if self.wl.kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
+        quant(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
+        csa2.csa2_quant_fp8(self.ik_new, cache.ik_codes, cache.ik_scales, slots=self.new_slots, status=cache.status)
+        layers = list(dw.layers)
+        for i, l in enumerate(layers):
+            if i == 1:
+                s.wait_event(ev_in)
+            self.enqueue_layers([l])
+            if i == self.half - 1 and len(self.out_dev) > 1:
+                ev_mid.record(s)
+                s3.wait_event(ev_mid)
+                with torch.cuda.stream(s3):
+                    host_out[0].copy_(self.out_dev[0], non_blocking=True)
+        host_out[-1].copy_(self.out_dev[-1], non_blocking=True)
+        if len(self.in_dev) > 1:
+            s.wait_stream(s2)
+        if len(self.out_dev) > 1:
+            s.wait_stream(s3)
 
     def enqueue_layers(self, layers, prof=False):
         for l in layers:
@@ -377,27 +415,34 @@ def run_native(args):
     value = throughput(world, B * Q, args.steps, ms_total / 1e3)
 
     # ---- end to end: pinned host inputs copied in, outputs copied out, every step
+    # (one graph per step with its copies; within a step the copies overlap the
+    # layers that do not need them)
     e2e = None
     if not args.no_e2e:
-        host_in = [(x.cpu().pin_memory(), x) for x, _ in step.h2d]
-        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in step.d2h]
-        h2d_bytes = sum(h.numel() * h.element_size() for h, _ in host_in)
+        host_in = [x.cpu().pin_memory() for x in step.in_dev]
+        host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in step.out_dev]
+        h2d_bytes = sum(h.numel() * h.element_size() for h in host_in)
         d2h_bytes = sum(h.numel() * h.element_size() for h in host_out)
+        s2, s3 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=s):
+            step.enqueue_e2e(host_in, host_out, s2, s3)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            with torch.cuda.stream(s):
+                ge.replay()
+        torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             with torch.cuda.stream(s):
-                for h, d in host_in:
-                    d.copy_(h, non_blocking=True)
-                g.replay()
-                for h, d in zip(host_out, step.d2h):
-                    h.copy_(d, non_blocking=True)
+                ge.replay()
             s.synchronize()
         el = time.perf_counter() - t0
         e2e = {"value": throughput(world, B * Q, args.steps, reduce_max(el, dev, world)), "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes}
+        del ge
 
     if rank != 0:
         if world > 1:
