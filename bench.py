@@ -276,39 +276,54 @@ class DecodeStep:
                               new_rows=self.swa_new[l] if self.queries == 1 else None)
 
     def rows_visible(self):
-        """Entries visible to each query row of the step (causal, m tokens per entry)."""
-        wl = self.wl
-        out = []
-        for b in range(wl.batch):
-            E = wl.entries(b)
-            out += [min(E, (int(t) + 1) // wl.m) for t in wl.q_pos(b)]
-        return out
+        return rows_visible(self.wl)
 
     def layer_bytes(self):
-        """Algorithmic bytes per step of each layer mode, all sequences: what the
-        method must read and write -- the indexer keys scanned (once for all of a
-        sequence's query tokens) or rescored, and per query token the selected
-        main-KV entries, the window rows, q / qi / w, the pool or indices, o and
-        lse."""
-        wl = self.wl
-        kv = 256 + self.csa2.KV_SCALE_BYTES[wl.kv_format]      # codes + block scales per entry
-        attn = 512 * kv + 128 * 516 + 64 * 512 * 2 + 64 * 512 * 4 + 64 * 4
-        vis = self.rows_visible()
-        keys = sum(wl.entries(b) for b in range(wl.batch)) * 132
-        full = keys + sum((v // 8) * 4 + 32 * 128 * 2 + 32 * 4 + attn for v in vis)
-        reindex = sum(min(self.csa2.POOL_MAX, v) * 136 + 32 * 128 * 2 + 32 * 4 + attn for v in vis)
-        reuse = len(vis) * (512 * 4 + attn)
-        return {"full": full, "reindex": reindex, "reuse": reuse}
+        return layer_bytes(self.wl)
 
     def scan_work(self):
-        """The Full layer scan's algorithmic work per launch: HBM bytes (keys once
-        per sequence, block maxima, queries) or, for a prefill chunk, where the
-        keys stay in L2 and the products bound it, e4m3 FLOPs."""
-        wl, vis = self.wl, self.rows_visible()
-        if wl.nq > 4:
-            return "tensor", sum(vis) * 32 * 128 * 2.0
-        return "hbm", float(sum(wl.entries(b) for b in range(wl.batch)) * 132 +
-                            sum((v // 8) * 4 + 8192 + 128 for v in vis))
+        return scan_work(self.wl)
+
+
+# ---------------------------------------------------------------- algorithmic work
+KV_SCALE_BYTES = {0: 16, 1: 32}     # main-KV block-scale bytes per entry: MXFP4, FP4 with E4M3 per 16
+POOL_MAX = 16384                    # candidate pool: 2,048 blocks of 8
+
+
+def rows_visible(wl):
+    """Entries visible to each query row of the step (causal, m tokens per entry)."""
+    out = []
+    for b in range(wl.batch):
+        E = wl.entries(b)
+        out += [min(E, (int(t) + 1) // wl.m) for t in wl.q_pos(b)]
+    return out
+
+
+def layer_bytes(wl):
+    """Algorithmic bytes per step of each layer mode, all sequences: what the
+    method must read and write -- the indexer keys scanned (once for all of a
+    sequence's query tokens) or rescored, and per query token the selected
+    main-KV entries, the window rows, q / qi / w, the pool or indices, o and
+    lse."""
+    kv = 256 + KV_SCALE_BYTES[wl.kv_format]                  # codes + block scales per entry
+    attn = 512 * kv + 128 * 516 + 64 * 512 * 2 + 64 * 512 * 4 + 64 * 4
+    vis = rows_visible(wl)
+    keys = sum(wl.entries(b) for b in range(wl.batch)) * 132
+    full = keys + sum((v // 8) * 4 + 32 * 128 * 2 + 32 * 4 + attn for v in vis)
+    reindex = sum(min(POOL_MAX, v) * 136 + 32 * 128 * 2 + 32 * 4 + attn for v in vis)
+    reuse = len(vis) * (512 * 4 + attn)
+    return {"full": full, "reindex": reindex, "reuse": reuse}
+
+
+def scan_work(wl):
+    """The Full layer scan's algorithmic work per launch: HBM bytes (keys once
+    per sequence, block maxima, queries) or, for a prefill chunk, where the
+    keys stay in L2 and the products bound it, e4m3 FLOPs."""
+    vis = rows_visible(wl)
+    if wl.nq > 4:
+        return "tensor", sum(vis) * 32 * 128 * 2.0
+    return "hbm", float(sum(wl.entries(b) for b in range(wl.batch)) * 132 +
+                        sum((v // 8) * 4 + 8192 + 128 for v in vis))
 
 
 def run_native(args):
