@@ -604,12 +604,12 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 
 // o = sum_c e^(m_c - M) O_c / (sum_c e^(m_c - M) l_c + e^(z_h - M)), lse = M +
 // log of that denominator (z_h the head's sink logit, -inf without one); one
-// CTA per (row, 2 heads), thread = 4 consecutive dims (float4) of one head,
+// CTA per (row, 2 or 8 heads), thread = 4 consecutive dims (float4) of one head,
 // all chunk loads in flight.  With rope_base > 0 the RoPE dims 448+i and
 // 480+i of the output are rotated back by -t * rope_base^(-i/32) (angles in
 // double precision: t reaches 2^20).  Launched as a programmatic dependent of
 // the attention kernel: it is scheduled early and waits for that grid here.
-__global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ part_o,
+__global__ void __launch_bounds__(1024) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml, int nchunks,
                                                       const float *__restrict__ sink, float rope_base,
                                                       const int64_t *__restrict__ q_pos,
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float *__restrict__ 
     pdl_wait();
     const int64_t r = blockIdx.x;
     const int tid = threadIdx.x & 127;
-    const int h = blockIdx.y * 2 + (threadIdx.x >> 7);
+    const int h = blockIdx.y * (int)(blockDim.x >> 7) + (threadIdx.x >> 7);   // 128 threads per head
     float mc[AC_MAX_CHUNKS], lc[AC_MAX_CHUNKS];
     float4 v[AC_MAX_CHUNKS];
     float M = -INFINITY;
@@ -738,8 +738,11 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
     int s = launch_status();
     if (s) return s;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)rows, CSA2_HEADS / 2);
-    cfg.blockDim = dim3(256);
+    // decode (few rows): eight heads per CTA, few CTAs to schedule after the
+    // wait; many rows: two heads per CTA, more CTAs resident per SM
+    const int heads_per_cta = rows <= 256 ? 8 : 2;
+    cfg.gridDim = dim3((unsigned)rows, CSA2_HEADS / heads_per_cta);
+    cfg.blockDim = dim3(heads_per_cta * 128);
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
