@@ -460,6 +460,39 @@ void or_attention(const uint16_t *q, double sm_scale, const double *keys, int64_
     }
 }
 
+/* RMSNorm and forward partial RoPE of nvec 512-dim vectors, vecs of them per
+ * row sharing the row's token position pos[row] ([P3] §4.3: queries and
+ * compressed KV are RMS-normalised before the core attention; RoPE acts on the
+ * last 64 dims only):
+ *   y_d = x_d / sqrt((1/512) sum_e x_e^2 + eps) * gamma_d   (gamma NULL: 1);
+ *   rope_base > 0: for i < 32 the pair (y[448 + i], y[480 + i]) turns by the
+ *   angle +t * rope_base^(-i/32), t = pos[row]:
+ *     (a, b) -> (a cos - b sin, a sin + b cos),
+ *   the inverse of the output rotation in or_attention. */
+void or_norm_rope(const double *x, int64_t nvec, int vecs, const double *gamma, double eps,
+                  const int64_t *pos, double rope_base, double *out)
+{
+    for (int64_t v = 0; v < nvec; v++) {
+        const double *xv = x + v * 512;
+        double *y = out + v * 512;
+        double ms = 0.0;
+        for (int d = 0; d < 512; d++) ms += xv[d] * xv[d];
+        ms /= 512.0;
+        const double rms = sqrt(ms + eps);
+        for (int d = 0; d < 512; d++) y[d] = xv[d] / rms * (gamma ? gamma[d] : 1.0);
+        if (rope_base > 0.0) {
+            const double t = (double)pos[v / vecs];
+            for (int i = 0; i < 32; i++) {
+                const double th = t * pow(rope_base, -(double)i / 32.0);
+                const double c = cos(th), sn = sin(th);
+                const double a = y[448 + i], b = y[480 + i];
+                y[448 + i] = a * c - b * sn;
+                y[480 + i] = a * sn + b * c;
+            }
+        }
+    }
+}
+
 int or_num_threads(void)
 {
 #ifdef _OPENMP

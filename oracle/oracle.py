@@ -84,6 +84,7 @@ def lib():
             L.or_block_pool.restype = i64
             L.or_block_pool.argtypes = [P, i64, i32, i32, P]
             L.or_attention.argtypes = [P, f64, P, i64, P, f64, i64, P, P]
+            L.or_norm_rope.argtypes = [P, i64, i32, P, f64, P, f64, P]
             L.or_num_threads.restype = i32
             _lib = L
     return _lib
@@ -267,6 +268,20 @@ def attention(q_bits, sm_scale: float, keys: np.ndarray, sink=None, rope_base: f
     lib().or_attention(_p(q), float(sm_scale), _p(k), k.shape[0], None if z is None else _p(z), float(rope_base),
                        int(t), _p(o), _p(lse))
     return o, lse
+
+
+def norm_rope(x, gamma=None, eps: float = 1e-6, pos=None, rope_base: float = 0.0) -> np.ndarray:
+    """float64 [rows][vecs][512]: RMSNorm of every 512-dim vector, then the
+    forward RoPE of its last 64 dims at the row's position (see the C source)."""
+    xx = _c(x, np.float64)
+    assert xx.ndim == 3 and xx.shape[2] == 512
+    rows, vecs = xx.shape[0], xx.shape[1]
+    g = None if gamma is None else _c(gamma, np.float64).reshape(512)
+    p = np.zeros((max(rows, 1),), np.int64) if pos is None else _c(pos, np.int64).reshape(rows)
+    out = np.empty_like(xx)
+    lib().or_norm_rope(_p(xx), rows * vecs, max(vecs, 1), None if g is None else _p(g), float(eps), _p(p),
+                       float(rope_base), _p(out))
+    return out
 
 
 def dedup_selection(positions, t: int, m: int, swa_start: int = 0, W: int = SWA_W) -> np.ndarray:

@@ -271,3 +271,78 @@ def test_dedup_selection():
     assert np.array_equal(oracle.dedup_selection(sel, t, 2), sel)      # compressed entries stay
     assert np.array_equal(oracle.dedup_selection(sel, 50, 1), sel[sel > 50])
     assert np.array_equal(oracle.dedup_selection(sel, t, 1, swa_start=950), [5, 871, 872, 873, 900])
+
+
+# ---------------------------------------------------------------- norm / RoPE prologue
+def test_norm_rope_closed_forms():
+    # a constant vector c: mean square c^2, y = c / sqrt(c^2 + eps) * gamma
+    x = np.full((2, 3, 512), -2.0)
+    assert np.allclose(oracle.norm_rope(x, eps=0.0), -1.0, rtol=0, atol=1e-15)
+    assert np.allclose(oracle.norm_rope(x, eps=1.0), -2.0 / np.sqrt(5.0), rtol=0, atol=1e-15)
+    g = np.linspace(0.5, 1.5, 512)
+    assert np.allclose(oracle.norm_rope(x, gamma=g, eps=0.0)[1, 2], -g, rtol=0, atol=1e-15)
+    # a one-hot vector e_d * s: mean square s^2 / 512, so y_d = sqrt(512) (eps = 0)
+    x = np.zeros((1, 1, 512))
+    x[0, 0, 17] = 0.25
+    y = oracle.norm_rope(x, eps=0.0)
+    assert abs(y[0, 0, 17] - np.sqrt(512.0)) < 1e-12 and np.count_nonzero(y) == 1
+    # a zero vector with eps > 0 stays zero
+    assert np.all(oracle.norm_rope(np.zeros((1, 1, 512)), eps=1e-6) == 0.0)
+
+
+def test_norm_rope_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((5, 4, 512)) * rng.uniform(0.01, 100.0, (5, 4, 1))
+    pos = rng.integers(0, 1 << 20, 5)
+    y = oracle.norm_rope(x, eps=0.0, pos=pos, rope_base=10000.0)
+    # the rotation keeps every pair's length, so the RMS stays 1
+    assert np.allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-12)
+    assert np.allclose(oracle.norm_rope(3.5 * x, eps=0.0, pos=pos, rope_base=10000.0), y, rtol=1e-12, atol=1e-12)
+    # dims below 448 are untouched by the rotation
+    y0 = oracle.norm_rope(x, eps=0.0)
+    assert np.array_equal(y[..., :448], y0[..., :448])
+
+
+def test_norm_rope_worked_angles():
+    # position 1: pair 0 turns by exactly 1 rad, pair 16 by 10000^(-1/2) = 0.01 rad
+    x = np.zeros((1, 1, 512))
+    x[0, 0, 448] = 1.0          # (a, b) = (1, 0) for pair 0
+    x[0, 0, 480 + 16] = 1.0     # (a, b) = (0, 1) for pair 16
+    y = oracle.norm_rope(x, eps=0.0, pos=[1], rope_base=10000.0)[0, 0] / np.sqrt(256.0)
+    assert abs(y[448] - 0.5403023058681398) < 1e-15 and abs(y[480] - 0.8414709848078965) < 1e-15
+    # (0, 1) -> (-sin, cos) at 0.01 rad
+    assert abs(y[448 + 16] + 0.009999833334166664) < 1e-15 and abs(y[480 + 16] - 0.9999500004166653) < 1e-15
+    # position 0 rotates nothing
+    y0 = oracle.norm_rope(x, eps=0.0, pos=[0], rope_base=10000.0)
+    assert np.array_equal(y0, oracle.norm_rope(x, eps=0.0))
+
+
+def test_norm_rope_relative_positions():
+    # dot(rope(q, t), rope(k, s)) depends on t - s only, and equals the
+    # unrotated dot product at t = s
+    rng = np.random.default_rng(42)
+    q = rng.standard_normal((1, 1, 512))
+    k = rng.standard_normal((1, 1, 512))
+
+    def dot(t, s):
+        a = oracle.norm_rope(q, eps=0.0, pos=[t], rope_base=10000.0)[0, 0]
+        b = oracle.norm_rope(k, eps=0.0, pos=[s], rope_base=10000.0)[0, 0]
+        return float(a @ b)
+
+    base = float(oracle.norm_rope(q, eps=0.0)[0, 0] @ oracle.norm_rope(k, eps=0.0)[0, 0])
+    assert abs(dot(5000, 5000) - base) < 1e-9
+    assert abs(dot(700, 200) - dot(10700, 10200)) < 1e-9
+    assert abs(dot(700, 200) - base) > 1e-3
+
+
+def test_norm_rope_inverts_the_output_rotation():
+    # one key, rotated forward at position t, attended by a query at t: the
+    # softmax weight is 1, so the output is the key, rotated back to where it was
+    rng = np.random.default_rng(43)
+    t = 777777
+    k = rng.standard_normal((1, 1, 512))
+    kn = oracle.norm_rope(k, eps=1e-6)
+    kr = oracle.norm_rope(k, eps=1e-6, pos=[t], rope_base=10000.0)
+    qb, _ = _q_and_keys(44, 1)
+    o, _ = oracle.attention(qb, 1.0, kr.reshape(1, 512), rope_base=10000.0, t=t)
+    assert np.allclose(o, np.broadcast_to(kn.reshape(1, 512), (64, 512)), rtol=0, atol=2e-6)
