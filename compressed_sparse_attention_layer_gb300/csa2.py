@@ -54,6 +54,7 @@ EXPORTS = {
     "csa2_quant_mxfp4": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_quant_fp8": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_quant_fp4_e4m3": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "csa2_norm_rope": (ctypes.c_int, [_vp, _i64, _i32, _vp, _f32, _vp, _f32, _vp, _vp, _vp]),
     "csa2_index_scores": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp, _vp,
                                          _vp, _i64, _vp]),
     "csa2_index_scores_pool": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp,
@@ -202,6 +203,17 @@ def csa2_quant_fp8(x, codes, scales, slots=None, status=None, stream=None):
         _ptr(x, torch.float32, "x"), x.shape[0], x.shape[1], _ptr(slots, torch.int64, "slots"),
         _ptr(codes, torch.uint8), _ptr(scales, torch.float32), codes.shape[0], _ptr(status, torch.int32),
         _stream(stream)))
+
+
+def csa2_norm_rope(x, out, gamma=None, eps: float = 1e-6, pos=None, rope_base: float = 0.0, stream=None):
+    """RMSNorm and forward partial RoPE of x fp32 [rows][vecs][512] into out
+    (fp32 or bf16, same shape; out may be x when fp32); pos int64 [rows]."""
+    assert x.dim() == 3 and x.shape[2] == 512 and tuple(out.shape) == tuple(x.shape)
+    f32 = out.dtype == torch.float32
+    _check("csa2_norm_rope", load().csa2_norm_rope(
+        _ptr(x, torch.float32, "x"), x.shape[0], x.shape[1], _ptr(gamma, torch.float32, "gamma"), float(eps),
+        _ptr(pos, torch.int64, "pos"), float(rope_base), _ptr(out, torch.float32, "out") if f32 else None,
+        None if f32 else _ptr(out, torch.bfloat16, "out"), _stream(stream)))
 
 
 def csa2_index_scores(cache: Cache, batch: Batch, qi, w, scores=None, block_max=None, n_visible=None,

@@ -2,6 +2,8 @@
 // kernel launches and the per-layer driver.  No entry point allocates memory.
 #include <cuda_runtime.h>
 
+#include <cmath>
+
 #include "csa2_internal.cuh"
 
 namespace csa2 {
@@ -17,6 +19,8 @@ int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, fl
                      cudaStream_t);
 int launch_quant_fp4_e4m3(const float *, int64_t, const int64_t *, uint8_t *, uint8_t *, int64_t, int32_t *,
                           cudaStream_t);
+int launch_norm_rope(const float *, int64_t, int, const float *, float, const int64_t *, float, float *, uint16_t *,
+                     cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
                       float *, int32_t *, int64_t, cudaStream_t, bool bf16_scores = false);
 int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, const int32_t *, int64_t, uint8_t *,
@@ -192,6 +196,20 @@ int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots,
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;
     if (!aligned(x, 16) || !aligned(codes, 4)) return CSA2_ERR_ALIGN;
     return launch_quant_fp8(x, n, dim, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
+}
+
+int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const float *gamma, float eps, const int64_t *pos,
+                   float rope_base, float *out_f32, uint16_t *out_bf16, csa2_stream_t stream)
+{
+    if (rows < 0 || vecs < 1 || !(eps >= 0.0f) || !std::isfinite(eps) || !(rope_base >= 0.0f) ||
+        !std::isfinite(rope_base) || rows * (int64_t)vecs >= ((int64_t)1 << 34))
+        return CSA2_ERR_SHAPE;
+    if (rows == 0) return CSA2_OK;
+    if (!x || (!out_f32) == (!out_bf16) || (rope_base > 0.0f && !pos)) return CSA2_ERR_NULL;
+    if (!aligned(x, 16) || (gamma && !aligned(gamma, 16)) || (out_f32 && !aligned(out_f32, 16)) ||
+        (out_bf16 && !aligned(out_bf16, 8)))
+        return CSA2_ERR_ALIGN;
+    return launch_norm_rope(x, rows, vecs, gamma, eps, pos, rope_base, out_f32, out_bf16, (cudaStream_t)stream);
 }
 
 int csa2_index_scores(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi, const float *w,

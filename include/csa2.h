@@ -261,6 +261,33 @@ CSA2_API int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots
 CSA2_API int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
                    float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
 
+/* ---- RMSNorm and forward partial RoPE of the attention inputs ------------
+ * [P3] §4.3: queries and compressed KV are RMS-normalised before the core
+ * attention, and RoPE acts on the last 64 of the 512 dims only (the output is
+ * rotated back by csa2_swa.rope_base).  For every 512-dim vector x of row r
+ * (vecs vectors per row, all at token position pos[r]):
+ *   y = x / sqrt(mean_d(x_d^2) + eps) * gamma
+ *   then, when rope_base > 0, for i < 32 the pair (y[448+i], y[480+i]) is
+ *   rotated by +pos[r] * rope_base^(-i/32):  (a, b) -> (a cos - b sin,
+ *   a sin + b cos) -- the inverse of the output rotation of csa2_swa.
+ * Queries: rows = B*Q tokens, vecs = 64 heads, bf16 output (csa2_layer_io.q).
+ * KV: rows = entries, vecs = 1, fp32 output for the quantisers; the position
+ * of a compressed entry is the caller's choice.
+ *   x        fp32 [rows][vecs][512], 16-byte aligned; may equal out_f32
+ *   gamma    fp32 [512] RMSNorm weight, 16-byte aligned, or NULL for ones
+ *   eps      >= 0, finite
+ *   pos      int64 [rows] (may be NULL when rope_base == 0)
+ *   out_f32  fp32 [rows][vecs][512] (16-byte aligned) or NULL
+ *   out_bf16 bf16 [rows][vecs][512] (8-byte aligned) or NULL: exactly one of
+ *            the two outputs (CSA2_ERR_NULL otherwise)
+ * Computed in fp32 (IEEE square root and division) with the angles reduced
+ * in double precision; the bf16 output is rounded to nearest even.
+ * CSA2_ERR_SHAPE for rows < 0, vecs < 1, rows * vecs >= 2^34, eps or
+ * rope_base negative or not finite. */
+CSA2_API int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const float *gamma, float eps,
+                   const int64_t *pos, float rope_base, float *out_f32, uint16_t *out_bf16,
+                   csa2_stream_t stream);
+
 /* ---- a4: lightning-indexer scores over every visible entry ---------------
  * score(p) = sum_h w[h] * ReLU(qi[h] . k_p), k_p = e4m3(code_p) * scale_p,
  * for every entry p visible to each query; block_max[b8] = max over the

@@ -107,3 +107,26 @@ def test_workspace_sizes(lib):
     assert full >= 8 * (1 << 20) * 4 + 8 * (1 << 17) * 4 + 8 * 16384 * 4
     assert full > reindex >= 8 * 16384 * 4 and reuse < reindex
     assert lib.csa2_layer_workspace_size(5, ctypes.byref(b)) == 0
+
+
+def test_norm_rope_validated_on_the_host(lib):
+    """csa2_norm_rope refuses bad shapes, missing or doubled outputs and
+    misaligned pointers before any launch (fake pointers, never dereferenced)."""
+    P, Q = ctypes.c_void_p(1 << 12), ctypes.c_void_p((1 << 12) + 8)
+    f = lib.csa2_norm_rope
+    assert f(P, 0, 64, None, 1e-6, None, 1e4, P, None, None) == 0               # nothing to do
+    assert f(P, -1, 64, None, 1e-6, P, 1e4, P, None, None) == -2
+    assert f(P, 4, 0, None, 1e-6, P, 1e4, P, None, None) == -2
+    assert f(P, 1 << 30, 1 << 4, None, 1e-6, P, 1e4, P, None, None) == -2       # 2^34 vectors
+    assert f(P, 4, 64, None, -1e-6, P, 1e4, P, None, None) == -2
+    assert f(P, 4, 64, None, float("nan"), P, 1e4, P, None, None) == -2
+    assert f(P, 4, 64, None, 1e-6, P, -1.0, P, None, None) == -2
+    assert f(P, 4, 64, None, 1e-6, P, float("inf"), P, None, None) == -2
+    assert f(None, 4, 64, None, 1e-6, P, 1e4, P, None, None) == -1
+    assert f(P, 4, 64, None, 1e-6, None, 1e4, P, None, None) == -1              # RoPE needs positions
+    assert f(P, 4, 64, None, 1e-6, P, 1e4, None, None, None) == -1              # no output
+    assert f(P, 4, 64, None, 1e-6, P, 1e4, P, P, None) == -1                    # two outputs
+    assert f(Q, 4, 64, None, 1e-6, P, 1e4, P, None, None) == -8                # x not 16-byte aligned
+    assert f(P, 4, 64, Q, 1e-6, P, 1e4, P, None, None) == -8                    # gamma
+    assert f(P, 4, 64, None, 1e-6, P, 1e4, Q, None, None) == -8                 # fp32 output
+    assert f(P, 4, 64, None, 1e-6, P, 1e4, None, ctypes.c_void_p((1 << 12) + 4), None) == -8

@@ -386,3 +386,59 @@ def test_index_scores_pool_gathered():
         assert np.all(np.isneginf(got[b, :lens[b]][~ok]))
         assert np.all(np.isnan(got[b, lens[b]:]))
     assert int(dw.cache.status[0]) & csa2.DEV_BAD_INDEX
+
+
+def _norm_rope_tol(ref):
+    """Per-element bound for the fp32 kernel against the fp64 oracle: the
+    fp32 mean square (16 products per lane, a 5-level shuffle tree) and the
+    scale carry <= ~1e-6 relative; the rotation adds the fp32 angle and
+    sin / cos errors (<= 3e-7 absolute) times the pair's size.  So 4e-6 times
+    |y_d| outside the RoPE dims and times |y_448+i| + |y_480+i| inside them."""
+    mag = np.abs(ref).copy()
+    pair = np.abs(ref[..., 448:480]) + np.abs(ref[..., 480:512])
+    mag[..., 448:480] = pair
+    mag[..., 480:512] = pair
+    return 4e-6 * mag
+
+
+@pytest.mark.parametrize("rows,vecs,rope_base,use_gamma", [(37, 64, 10000.0, True), (1000, 1, 10000.0, False),
+                                                            (5, 3, 0.0, True), (1, 64, 1e6, False)])
+def test_norm_rope_matches_oracle(rows, vecs, rope_base, use_gamma):
+    rng = np.random.default_rng(rows * 100 + vecs)
+    x = (rng.standard_normal((rows, vecs, 512)) * np.exp(rng.uniform(-6, 6, (rows, vecs, 1)))).astype(np.float32)
+    x[0, 0] = 0.0                                           # zero vector: stays zero (eps > 0)
+    pos = rng.integers(0, 1 << 20, rows).astype(np.int64)
+    pos[0] = 0
+    pos[-1] = (1 << 20) - 1
+    gamma = rng.uniform(0.5, 1.5, 512).astype(np.float32) if use_gamma else None
+    eps = 1e-6
+    ref = oracle.norm_rope(x, gamma, eps, pos, rope_base)
+    tol = _norm_rope_tol(ref)
+    xd = torch.from_numpy(x).cuda()
+    gd = None if gamma is None else torch.from_numpy(gamma).cuda()
+    pd = torch.from_numpy(pos).cuda()
+    out = torch.empty_like(xd)
+    csa2.csa2_norm_rope(xd, out, gd, eps, pd, rope_base)
+    ob = torch.empty(xd.shape, dtype=torch.bfloat16, device="cuda")
+    csa2.csa2_norm_rope(xd, ob, gd, eps, pd, rope_base)
+    torch.cuda.synchronize()
+    y = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(y - ref) <= tol), float(np.max(np.abs(y - ref) - tol))
+    assert np.all(y[0, 0] == 0.0)
+    # bf16 output: the same values rounded once more (half an ulp of bf16 = 2^-8 relative)
+    yb = ob.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(yb - ref) <= 2.0 ** -8 * np.abs(ref) + tol)
+    # in place (out = x) gives the same bits as out of place
+    csa2.csa2_norm_rope(xd, xd, gd, eps, pd, rope_base)
+    torch.cuda.synchronize()
+    assert torch.equal(xd, out)
+
+
+def test_norm_rope_empty_and_bad_arguments():
+    x = torch.zeros((0, 64, 512), device="cuda")
+    csa2.csa2_norm_rope(x, torch.empty_like(x), None, 1e-6, None, 10000.0)     # rows = 0: nothing to do
+    x = torch.ones((2, 1, 512), device="cuda")
+    with pytest.raises(csa2.Csa2Error):
+        csa2.csa2_norm_rope(x, torch.empty_like(x), None, 1e-6, None, 10000.0)  # rope without positions
+    with pytest.raises(csa2.Csa2Error):
+        csa2.csa2_norm_rope(x, torch.empty_like(x), None, -1.0, None, 0.0)      # negative eps
