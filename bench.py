@@ -42,9 +42,10 @@ def parse():
     p.add_argument("--kv-format", type=int, default=0, choices=[0, 1],
                    help="main KV: 0 MXFP4 (32-element blocks, E8M0), 1 FP4 with an E4M3 scale per 16 elements")
     p.add_argument("--workload", default="decode_1m",
-                   choices=["decode_1m", "decode_small", "decode_group", "decode_ragged", "prefill"],
+                   choices=["decode_1m", "decode_small", "decode_group", "decode_ragged", "prefill", "norm_rope"],
                    help="decode_1m (default: the headline, batch 8 x 1M tokens); the other four synthetic "
-                        "workloads run the same step for their own shapes (prefill: one 8,192-token chunk)")
+                        "workloads run the same step for their own shapes (prefill: one 8,192-token chunk); "
+                        "norm_rope times the input prologue alone (RMSNorm + RoPE of a prefill chunk's queries)")
     p.add_argument("--bf16-scores", action="store_true",
                    help="Full and Reindex layers select on bf16-rounded index scores (csa2.LAYER_SCORES_BF16)")
     p.add_argument("--queries", type=int, default=1,
@@ -631,6 +632,87 @@ def cpu_baseline(wl, target_s=10.0):
                       f"first); {n} tokens in {secs:.1f} s of oracle time"}
 
 
+def run_norm_rope(args):
+    """The attention inputs' prologue (csa2_norm_rope) on a prefill chunk's
+    queries: 8,192 tokens x 64 heads of 512 fp32 dims, RMS-normalised and
+    rotated at their positions, written as bf16.  HBM bound: 2,048 B read and
+    1,024 B written per vector (1.61 GB per launch, above L2)."""
+    import torch
+    from compressed_sparse_attention_layer_gb300 import build, csa2, synth
+    world, rank, local = dist_env()
+    if rank != 0:
+        return                                  # one GPU: the prologue does not shard across ranks here
+    torch.cuda.set_device(local)
+    build.build()
+    csa2.load()
+    dev = torch.device("cuda", local)
+    T, H = 8192, 64
+    x = synth.normal_f32_torch(7100, 0, T * H * 512, dev).view(T, H, 512)
+    gamma = (1.0 + 0.1 * synth.normal_f32_torch(7101, 0, 512, dev)).contiguous()
+    pos = torch.arange(65536, 65536 + T, dtype=torch.int64, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def launch():
+        csa2.csa2_norm_rope(x, out, gamma, 1e-6, pos, 10000.0, stream=s)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(3, args.warmup)):
+            launch()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0.record(s)
+    for _ in range(args.steps):
+        launch()
+    e1.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    nvec = T * H
+    # end to end: pinned host input copied in, the prologue, bf16 result copied out
+    hx = torch.empty((T, H, 512), dtype=torch.float32, pin_memory=True)
+    hx.copy_(x)
+    ho = torch.empty((T, H, 512), dtype=torch.bfloat16, pin_memory=True)
+    torch.cuda.synchronize()
+    for k in range(args.steps + 2):
+        if k == 2:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        with torch.cuda.stream(s):
+            x.copy_(hx, non_blocking=True)
+            launch()
+            ho.copy_(out, non_blocking=True)
+    s.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    algo = nvec * (2048 + 1024)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    achieved = algo / (ms * 1e-3) / 1e9
+    line = {"metric": "CSA2 input prologue (RMSNorm + partial RoPE) vectors/s, 8,192 tokens x 64 heads",
+            "value": nvec / (ms * 1e-3), "unit": "vectors/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": "norm_rope: 8,192 query tokens x 64 heads x 512 dims, fp32 in, bf16 out, "
+                                   "positions 65,536.., rope_base 10,000",
+                       "l2": "inputs larger than L2 (1.07 GB read per launch)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "k_norm_rope",
+                         "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks
+                         else "fallback"},
+            "clocks": clk,
+            "e2e": {"value": nvec / e2e_s, "unit": "vectors/s", "h2d_bytes_per_step": hx.numel() * 4,
+                    "d2h_bytes_per_step": ho.numel() * 2},
+            "gpu_launches": args.steps, "cpu_baseline": None}
+    print(json.dumps(line))
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -660,5 +742,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.workload == "norm_rope":
+        run_norm_rope(a)
     else:
         run_native(a)
