@@ -606,12 +606,12 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
 // log of that denominator (z_h the head's sink logit, -inf without one); one
 // CTA per (row, 2 or 8 heads), thread = 4 consecutive dims (float4) of one head,
 // all chunk loads in flight.  With rope_base > 0 the RoPE dims 448+i and
-// 480+i of the output are rotated back by -t * rope_base^(-i/32) (angles in
-// double precision: t reaches 2^20).  Launched as a programmatic dependent of
+// 480+i of the output are rotated back by -t * rope_base^(-i/32) (angles
+// reduced exactly in integer turns: t reaches 2^20).  Launched as a programmatic dependent of
 // the attention kernel: it is scheduled early and waits for that grid here.
 __global__ void __launch_bounds__(1024) k_attn_combine(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_ml, int nchunks,
-                                                      const float *__restrict__ sink, float rope_base,
+                                                      const float *__restrict__ sink, int rope, RopeTurns turns,
                                                       const int64_t *__restrict__ q_pos,
                                                       float *__restrict__ o, float *__restrict__ lse)
 {
@@ -666,21 +666,20 @@ __global__ void __launch_bounds__(1024) k_attn_combine(const float *__restrict__
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     float4 out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (rope_base > 0.0f && tid >= 96) {            // the warp holding dims 384..511
+    if (rope && tid >= 96) {                        // the warp holding dims 384..511
         // dims 448+i (threads 112..119) pair with 480+i (threads 120..127), 8 lanes apart
         const float4 other = make_float4(__shfl_xor_sync(0xffffffffu, out.x, 8), __shfl_xor_sync(0xffffffffu, out.y, 8),
                                          __shfl_xor_sync(0xffffffffu, out.z, 8), __shfl_xor_sync(0xffffffffu, out.w, 8));
         if (tid >= 112) {
             const bool first = tid < 120;
             const int i0 = 4 * (tid - (first ? 112 : 120));
-            const double t = (double)q_pos[r];
+            const int64_t t = q_pos[r];
             float rot[4];
             const float mine[4] = {out.x, out.y, out.z, out.w}, oth[4] = {other.x, other.y, other.z, other.w};
 #pragma unroll
             for (int c4 = 0; c4 < 4; c4++) {
-                double sd, cd;
-                sincos(t * pow((double)rope_base, -(double)(i0 + c4) / 32.0), &sd, &cd);
-                const float cs = (float)cd, sn = (float)sd;
+                float sn, cs;
+                rope_sincos(t, turns.phi[i0 + c4], &sn, &cs);
                 // (a, b) -> (a cos + b sin, -a sin + b cos); this thread holds a (first) or b
                 rot[c4] = first ? fmaf(mine[c4], cs, oth[c4] * sn) : fmaf(mine[c4], cs, -oth[c4] * sn);
             }
@@ -750,7 +749,8 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
     cfg.attrs = at;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_attn_combine, (const float *)part_o, (const float *)part_ml,
-                                             nchunks, swa.sink, swa.rope_base, bt.q_pos, o, lse);
+                                             nchunks, swa.sink, swa.rope_base > 0.0f ? 1 : 0,
+                                             rope_turns(swa.rope_base), bt.q_pos, o, lse);
     if (e != cudaSuccess) {
         set_cuda_error(e);
         return CSA2_ERR_CUDA;

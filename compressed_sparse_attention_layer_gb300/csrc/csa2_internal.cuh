@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cmath>
+
 #include "csa2.h"
 
 namespace csa2 {
@@ -88,6 +90,38 @@ __device__ __forceinline__ int64_t visible_entries(const csa2_batch &bt, int64_t
     if (n > bt.max_entries) n = bt.max_entries;
     if (n < 0) n = 0;
     return n;
+}
+
+// ---------------------------------------------------------------- RoPE angles
+// The RoPE pair i (dims 448+i, 480+i) turns by t * theta_i, theta_i =
+// rope_base^(-i/32), at token position t.  phi[i] holds theta_i / 2π as a
+// 64-bit binary fraction (computed on the host in double precision), so that
+// t * phi[i] modulo 2^64 is the angle reduced modulo 2π, exact for every
+// int64 t up to phi's own rounding (relative 2^-53): no floating-point
+// reduction of angles that reach 2^20 rad, and no double-precision work on
+// the device.
+struct RopeTurns {
+    uint64_t phi[32];
+};
+
+inline RopeTurns rope_turns(float rope_base)
+{
+    RopeTurns r;
+    for (int i = 0; i < 32; i++) {
+        // theta_i <= 1, so theta_i / 2π < 1 and the fraction fits 64 bits
+        const double f = rope_base > 0.0f ? pow((double)rope_base, -(double)i / 32.0) / 6.283185307179586 : 0.0;
+        r.phi[i] = (uint64_t)ldexp(f, 64);
+    }
+    return r;
+}
+
+// sin and cos of t * theta for one pair: the top 32 bits of the turn fraction,
+// read as signed, are the angle in units of 2^-31 π, in [-π, π).
+__device__ __forceinline__ void rope_sincos(int64_t t, uint64_t phi, float *s, float *c)
+{
+    const uint64_t turns = (uint64_t)t * phi;
+    const float x = (float)(int32_t)(uint32_t)(turns >> 32) * 4.656612873077393e-10f;   // 2^-31
+    sincospif(x, s, c);
 }
 
 // FP8 e4m3 byte -> float (exact).

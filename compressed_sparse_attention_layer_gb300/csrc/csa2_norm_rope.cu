@@ -8,19 +8,13 @@
 // vector, each lane four float4 loads (dims 4·lane + 128·c), the mean square
 // by warp shuffle.  The RoPE pair (448+i, 480+i) sits in lanes 16+i/4 and
 // 24+i/4 of the last chunk, so one shuffle across 8 lanes brings each lane its
-// partner.  Angles: t·θ_i in double (t reaches 2^20, θ_0 = 1), reduced to
-// [-π, π] in double, then sin / cos of the reduced fp32 angle.
+// partner.  Angles: t·θ_i reduced modulo 2π exactly in 64-bit integer turns
+// (rope_sincos), then sin / cos in fp32.
 #include <cuda_bf16.h>
-
-#include <cmath>
 
 #include "csa2_internal.cuh"
 
 namespace csa2 {
-
-struct RopeTheta {
-    double th[32];   // rope_base^(-i/32), computed on the host in double precision
-};
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 {
@@ -32,7 +26,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 // before it writes them.
 __global__ void __launch_bounds__(256) k_norm_rope(const float *x, int64_t nvec, int vecs,
                                                    const float *__restrict__ gamma, float eps,
-                                                   const int64_t *__restrict__ pos, int rope, RopeTheta theta,
+                                                   const int64_t *__restrict__ pos, int rope, RopeTurns turns,
                                                    float *out_f32, uint16_t *out_bf16)
 {
     pdl_launch_dependents();
@@ -73,17 +67,14 @@ __global__ void __launch_bounds__(256) k_norm_rope(const float *x, int64_t nvec,
         p.z = __shfl_xor_sync(0xffffffffu, a[3].z, 8);
         p.w = __shfl_xor_sync(0xffffffffu, a[3].w, 8);
         if (lane >= 16) {
-            const double t = (double)pos[v / vecs];
+            const int64_t t = pos[v / vecs];
             const bool first = lane < 24;
             float *own = &a[3].x;
             const float *par = &p.x;
 #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const double ang = t * theta.th[4 * (lane & 7) + j];
-                const double turns = rint(ang * 0.15915494309189535);   // ang / 2π, nearest integer
-                const float r = (float)fma(-turns, 6.283185307179586, ang);
                 float s, co;
-                sincosf(r, &s, &co);
+                rope_sincos(t, turns.phi[4 * (lane & 7) + j], &s, &co);
                 // (u, w) -> (u cos - w sin, u sin + w cos), u the first half
                 own[j] = first ? own[j] * co - par[j] * s : par[j] * s + own[j] * co;
             }
@@ -105,11 +96,10 @@ int launch_norm_rope(const float *x, int64_t rows, int vecs, const float *gamma,
 {
     const int64_t nvec = rows * vecs;
     if (nvec == 0) return CSA2_OK;
-    RopeTheta theta;
-    for (int i = 0; i < 32; i++) theta.th[i] = rope_base > 0.0f ? pow((double)rope_base, -(double)i / 32.0) : 0.0;
+    const RopeTurns turns = rope_turns(rope_base);
     const unsigned grid = (unsigned)((nvec + 7) / 8);
     return launch_pdl(k_norm_rope, dim3(grid), dim3(256), 0, st, x, nvec, vecs, gamma, eps, pos,
-                      rope_base > 0.0f ? 1 : 0, theta, out_f32, out_bf16);
+                      rope_base > 0.0f ? 1 : 0, turns, out_f32, out_bf16);
 }
 
 }  // namespace csa2
