@@ -565,6 +565,7 @@ def run_native(args):
 
 
 KERNEL_VERSION = "f8-cpasync-scan-v5"
+NORM_ROPE_VERSION = "norm-rope-int-turns-v1"   # the prologue kernel whose ncu traffic profiles/ records
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -695,6 +696,14 @@ def run_norm_rope(args):
         pass
     peak = peaks.get("hbm_gbs", 6800.0)
     achieved = algo / (ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic_norm_rope.json")) as f:
+            tp = json.load(f)
+        if tp.get("kernel_version") == NORM_ROPE_VERSION:
+            traffic = tp["bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
     line = {"metric": "CSA2 input prologue (RMSNorm + partial RoPE) vectors/s, 8,192 tokens x 64 heads",
             "value": nvec / (ms * 1e-3), "unit": "vectors/s", "n_gpus": 1, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -703,7 +712,7 @@ def run_norm_rope(args):
                                    "positions 65,536.., rope_base 10,000",
                        "l2": "inputs larger than L2 (1.07 GB read per launch)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "k_norm_rope",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": "k_norm_rope",
                          "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured)" if "hbm_gbs" in peaks
                          else "fallback"},
             "clocks": clk,
