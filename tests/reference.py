@@ -79,10 +79,11 @@ class SeqOracle:
         codes, scales = self.ik()
         return oracle.index_scores(qi, w, codes, scales, positions=np.asarray(positions, np.int32))
 
-    def attention(self, layer, i, idx, ring=None, sink=None, rope_base=0.0, dedup=False):
+    def attention(self, layer, i, idx, ring=None, sink=None, rope_base=0.0, dedup=False, q_bits=None):
         """o, lse of query i over the selected entries idx and its window; sink,
         rope_base and dedup (drop selected entries that are window rows) as in
-        oracle.attention / oracle.dedup_selection."""
+        oracle.attention / oracle.dedup_selection; q_bits: the query's bf16 bits
+        [64][512] in place of the workload's own."""
         t, _ = self.visible(i)
         sel = np.asarray(idx, np.int64)
         sel = sel[sel >= 0]
@@ -92,7 +93,7 @@ class SeqOracle:
         swc, sws = ring if ring is not None else self.swa_ring(layer)
         keys = oracle.attention_keys(kvc, kvs, np.arange(sel.size, dtype=np.int32), swc, sws, t,
                                      kv_format=self.wl.kv_format)
-        q = self.wl.q_bits(layer, self.b, [i])[0]
+        q = self.wl.q_bits(layer, self.b, [i])[0] if q_bits is None else q_bits
         return oracle.attention(q, 1.0, keys, sink=sink, rope_base=rope_base, t=t)
 
     def layers(self, i, upto=None):

@@ -230,6 +230,35 @@ def test_attention_options_sink_rotation_dedup(tokens):
         assert np.array_equal(plain.hist_idx[l], dw.hist_idx[l]), l
 
 
+def test_normed_rotated_queries_feed_the_layers():
+    """Queries RMS-normalised and rotated at their positions by csa2_norm_rope
+    (fp32 raw queries in, bf16 out; the RMSNorm weight carries the 1/sqrt(512)
+    softmax scale) feed Full / Reuse / Reindex layers whose output is rotated
+    back.  The oracle normalises and rotates in double precision, rounds to
+    bf16 and attends.  Where the fp32 and fp64 values straddle a bf16 rounding
+    boundary a query element differs by one bf16 unit; attn_close's tolerance
+    covers that."""
+    wl = W.Workload("qnorm", 78, 2, [5000, 40000], 1, ["full", "reuse", "reindex"], planted_blocks=2)
+    dw = DeviceWorkload(wl)
+    g = np.random.default_rng(78)
+    gamma = (g.uniform(0.5, 1.5, 512) / np.sqrt(512.0)).astype(np.float32)
+    raw = {l: (3.0 * g.standard_normal((dw.rows, 64, 512))).astype(np.float32) for l in dw.layers}
+    gd = torch.from_numpy(gamma).to(dw.dev)
+    for l in dw.layers:
+        csa2.csa2_norm_rope(torch.from_numpy(raw[l]).to(dw.dev), dw.q[l], gd, 1e-6, dw.q_pos, 10000.0)
+    dw.attn_options = dict(rope_base=10000.0)
+    _run_recording(dw)
+    for b in range(wl.batch):
+        so = SeqOracle(wl, b)
+        t = int(wl.q_pos(b)[0])
+        for l in dw.layers:
+            qn = oracle.norm_rope(raw[l][b:b + 1], gamma, 1e-6, [t], 10000.0)[0]
+            qb = torch.from_numpy(qn).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            o_ref, lse_ref = so.attention(l, 0, dw.hist_idx[l][b], rope_base=10000.0, q_bits=qb)
+            ok, info = attn_close(dw.o[l][b].cpu().numpy(), dw.lse[l][b].cpu().numpy(), o_ref, lse_ref)
+            assert ok, (b, l, info)
+
+
 def test_reuse_keys_loaded_early_bit_identical():
     """Reuse layers that load and dequantise their keys while the previous
     layer's merge is still running (csa2.ATTN_EARLY_INPUTS) give the same o and
