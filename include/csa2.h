@@ -280,8 +280,9 @@ CSA2_API int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_
  *   out_f32  fp32 [rows][vecs][512] (16-byte aligned) or NULL
  *   out_bf16 bf16 [rows][vecs][512] (8-byte aligned) or NULL: exactly one of
  *            the two outputs (CSA2_ERR_NULL otherwise)
- * Computed in fp32 (IEEE square root and division) with the angles reduced
- * in double precision; the bf16 output is rounded to nearest even.
+ * Computed in fp32 (IEEE square root and division); each angle is reduced
+ * modulo 2π exactly as a 64-bit integer count of turns before its sine and
+ * cosine are taken in fp32; the bf16 output is rounded to nearest even.
  * CSA2_ERR_SHAPE for rows < 0, vecs < 1, rows * vecs >= 2^34, eps or
  * rope_base negative or not finite. */
 CSA2_API int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const float *gamma, float eps,
