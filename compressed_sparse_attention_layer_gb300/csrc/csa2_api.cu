@@ -202,7 +202,7 @@ int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const float *gamm
                    float rope_base, float *out_f32, uint16_t *out_bf16, csa2_stream_t stream)
 {
     if (rows < 0 || vecs < 1 || !(eps >= 0.0f) || !std::isfinite(eps) || !(rope_base >= 0.0f) ||
-        !std::isfinite(rope_base) || rows * (int64_t)vecs >= ((int64_t)1 << 34))
+        !std::isfinite(rope_base) || rows > ((((int64_t)1 << 34) - 1) / vecs))   // rows * vecs < 2^34
         return CSA2_ERR_SHAPE;
     if (rows == 0) return CSA2_OK;
     if (!x || (!out_f32) == (!out_bf16) || (rope_base > 0.0f && !pos)) return CSA2_ERR_NULL;

@@ -118,6 +118,8 @@ def test_norm_rope_validated_on_the_host(lib):
     assert f(P, -1, 64, None, 1e-6, P, 1e4, P, None, None) == -2
     assert f(P, 4, 0, None, 1e-6, P, 1e4, P, None, None) == -2
     assert f(P, 1 << 30, 1 << 4, None, 1e-6, P, 1e4, P, None, None) == -2       # 2^34 vectors
+    assert f(P, (1 << 30) - 1, 1 << 4, None, 1e-6, None, 0.0, None, None, None) == -1   # 2^34 - 16: in range
+    assert f(P, 1 << 62, 1 << 30, None, 1e-6, P, 1e4, P, None, None) == -2      # the product would overflow
     assert f(P, 4, 64, None, -1e-6, P, 1e4, P, None, None) == -2
     assert f(P, 4, 64, None, float("nan"), P, 1e4, P, None, None) == -2
     assert f(P, 4, 64, None, 1e-6, P, -1.0, P, None, None) == -2
