@@ -168,7 +168,7 @@ int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int32
 int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *codes, uint8_t *scales,
                      int64_t num_slots, int32_t *status, csa2_stream_t stream)
 {
-    if (n < 0 || num_slots < 0) return CSA2_ERR_SHAPE;
+    if (n < 0 || n > INT32_MAX || num_slots < 0) return CSA2_ERR_SHAPE;
     if (n == 0) return CSA2_OK;
     if (!x || !codes || !scales) return CSA2_ERR_NULL;
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;
@@ -179,7 +179,7 @@ int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, uint8_t *c
 int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t *codes, uint8_t *scales,
                         int64_t num_slots, int32_t *status, csa2_stream_t stream)
 {
-    if (n < 0 || num_slots < 0) return CSA2_ERR_SHAPE;
+    if (n < 0 || n > INT32_MAX || num_slots < 0) return CSA2_ERR_SHAPE;
     if (n == 0) return CSA2_OK;
     if (!x || !codes || !scales) return CSA2_ERR_NULL;
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;
@@ -190,7 +190,7 @@ int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t
 int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
                    float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream)
 {
-    if (n < 0 || num_slots < 0 || (dim != 128 && dim != 512)) return CSA2_ERR_SHAPE;
+    if (n < 0 || n > INT32_MAX || num_slots < 0 || (dim != 128 && dim != 512)) return CSA2_ERR_SHAPE;
     if (n == 0) return CSA2_OK;
     if (!x || !codes || !scales) return CSA2_ERR_NULL;
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;

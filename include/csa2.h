@@ -232,7 +232,7 @@ CSA2_API int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bi
  * to [-127, 127], stored as E8M0 byte X + 127; each element x becomes the
  * E2M1 value nearest to x * 2^-X (ties to even mantissa, saturating at 6),
  * its sign bit copying x's.  [P2] §4; OCP MX block 32 / E8M0.
- *   x      fp32 [n][512] (finite values)
+ *   x      fp32 [n][512] (finite values), n <= 2^31 - 1 (CSA2_ERR_SHAPE beyond)
  *   slots  int64 [n] destination slot of each row, or NULL for row i -> slot i;
  *          a negative slot skips the row; a slot >= num_slots is skipped and
  *          flagged CSA2_DEV_BAD_SLOT in *status (status may be NULL).
@@ -256,7 +256,7 @@ CSA2_API int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots
  * code = e4m3(x / s) (IEEE fp32 division, round to nearest even, saturating
  * at 448, sign kept).  Used for the SWA rows ([P1] §3.3, [P2] §4) and the
  * indexer keys.
- *   x fp32 [n][dim], dim in {128, 512}; slots as for csa2_quant_mxfp4;
+ *   x fp32 [n][dim], dim in {128, 512}, n <= 2^31 - 1; slots as for csa2_quant_mxfp4;
  *   codes [num_slots][dim], scales [num_slots]. */
 CSA2_API int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
                    float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);

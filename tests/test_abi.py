@@ -58,6 +58,13 @@ def test_host_validation_without_gpu(lib):
     assert lib.csa2_quant_mxfp4(ctypes.c_void_p(8), 4, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 64,
                                 None, None) == -8                                # misaligned input
     assert lib.csa2_quant_fp4_e4m3(None, 4, None, None, None, 64, None, None) == -1
+    big = 1 << 31                                   # more rows than one launch grid covers
+    assert lib.csa2_quant_mxfp4(ctypes.c_void_p(16), big, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                ctypes.c_void_p(16), 64, None, None) == -2
+    assert lib.csa2_quant_fp4_e4m3(ctypes.c_void_p(16), big, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                   ctypes.c_void_p(16), 64, None, None) == -2
+    assert lib.csa2_quant_fp8(ctypes.c_void_p(16), big, 128, ctypes.c_void_p(16), ctypes.c_void_p(16),
+                              ctypes.c_void_p(16), 64, None, None) == -2
     assert lib.csa2_quant_fp4_e4m3(ctypes.c_void_p(8), 4, None, ctypes.c_void_p(16), ctypes.c_void_p(16), 64,
                                    None, None) == -8
     assert lib.csa2_topk(None, 10, None, 1, None, 0, None, None) == -2
