@@ -723,13 +723,70 @@ def run_norm_rope(args):
             "e2e": {"value": nvec / e2e_s, "unit": "vectors/s", "h2d_bytes_per_step": hx.numel() * 4,
                     "d2h_bytes_per_step": ho.numel() * 2},
             "gpu_launches": args.steps, "cpu_baseline": None}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = norm_rope_cpu_baseline()
     print(json.dumps(line))
+
+
+def norm_rope_cpu_baseline(reps=20):
+    """The oracle's RMSNorm + RoPE on the host: 256 of the chunk's tokens x 64
+    heads, repeated reps times (about 1.5 s), inputs prepared outside the timing."""
+    import numpy as np
+    import oracle
+    from compressed_sparse_attention_layer_gb300 import synth
+    oracle.build()
+    T, H = 256, 64
+    x = synth.normal_f32(7100, 0, T * H * 512).reshape(T, H, 512)
+    gamma = (1.0 + 0.1 * synth.normal_f32(7101, 0, 512)).astype(np.float32)
+    pos = np.arange(65536, 65536 + T, dtype=np.int64)
+    oracle.norm_rope(x, gamma, 1e-6, pos, 10000.0)          # warm-up (library load)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.norm_rope(x, gamma, 1e-6, pos, 10000.0)
+    secs = time.perf_counter() - t0
+    return {"value": reps * T * H / secs, "unit": "vectors/s", "cores": 1, "kind": "oracle",
+            "sample": f"{T} of the 8,192 query tokens x {H} heads, {reps}x ({reps * T * H} vectors in "
+                      f"{secs:.1f} s, single-threaded)"}
+
+
+def run_reference_norm_rope(args):
+    """The oracle's RMSNorm + RoPE on a bounded sample of the prologue
+    workload: each step 256 of the chunk's 8,192 query tokens (x 64 heads)."""
+    import numpy as np
+    import oracle
+    from compressed_sparse_attention_layer_gb300 import synth
+    oracle.build()
+    T, H = 256, 64
+    x = synth.normal_f32(7100, 0, T * H * 512).reshape(T, H, 512)
+    gamma = (1.0 + 0.1 * synth.normal_f32(7101, 0, 512)).astype(np.float32)
+    pos = np.arange(65536, 65536 + T, dtype=np.int64)
+    for _ in range(max(1, min(args.warmup, 1))):
+        oracle.norm_rope(x, gamma, 1e-6, pos, 10000.0)
+    tot = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.norm_rope(x, gamma, 1e-6, pos, 10000.0)
+        tot += time.perf_counter() - t0
+    value = args.steps * T * H / tot
+    sample = f"each step: {T} of the 8,192 query tokens x {H} heads ({T * H} vectors), single-threaded oracle"
+    print(json.dumps({"impl": "reference", "metric": "CSA2 input prologue (RMSNorm + partial RoPE) vectors/s, "
+                      "8,192 tokens x 64 heads", "value": value, "unit": "vectors/s", "n_gpus": 1,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic", "config": {"workload": "norm_rope: 8,192 query tokens x 64 heads x "
+                                                                  "512 dims (sampled)"},
+                      "cpu_baseline": {"value": value, "unit": "vectors/s", "cores": 1, "kind": "oracle",
+                                       "sample": sample},
+                      "e2e": {"value": value, "unit": "vectors/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    if args.workload == "norm_rope":
+        return run_reference_norm_rope(args)
     import oracle
     from compressed_sparse_attention_layer_gb300 import workloads as W
     oracle.build()
