@@ -442,3 +442,38 @@ def test_norm_rope_empty_and_bad_arguments():
         csa2.csa2_norm_rope(x, torch.empty_like(x), None, 1e-6, None, 10000.0)  # rope without positions
     with pytest.raises(csa2.Csa2Error):
         csa2.csa2_norm_rope(x, torch.empty_like(x), None, -1.0, None, 0.0)      # negative eps
+
+
+def _prologue_gamma():
+    """The RMSNorm weight of the benchmark's prologue workload (host generator)."""
+    return (1.0 + 0.1 * synth.normal_f32(7101, 0, 512)).astype(np.float32)
+
+
+def _norm_rope_full_size_check(out_rows, picks, H):
+    """The oracle on the sampled vectors of the full-size prologue (inputs from
+    the host generator) against the kernel's bf16 rows out_rows
+    [len(picks)][512]: bf16 rounding plus the fp32 bound of _norm_rope_tol."""
+    x = np.stack([synth.normal_f32(7100, int(v) * 512, 512) for v in picks]).reshape(len(picks), 1, 512)
+    pos = (65536 + np.asarray(picks) // H).astype(np.int64)
+    ref = oracle.norm_rope(x, _prologue_gamma(), 1e-6, pos, 10000.0)[:, 0]
+    return np.abs(out_rows - ref) <= 2.0 ** -8 * np.abs(ref) + _norm_rope_tol(ref)
+
+
+def test_norm_rope_full_size_sampled():
+    """The prologue in the launch the benchmark times (8,192 query tokens x 64
+    heads of 512 fp32 dims, bf16 out, positions from 65,536, rope_base
+    10,000): 512 sampled vectors, the first and last among them, against the
+    oracle."""
+    T, H = 8192, 64
+    dev = torch.device("cuda")
+    x = synth.normal_f32_torch(7100, 0, T * H * 512, dev).view(T, H, 512)
+    rng = np.random.default_rng(8192)
+    picks = rng.choice(T * H, 512, replace=False)
+    picks[:2] = [0, T * H - 1]
+    pos = torch.arange(65536, 65536 + T, dtype=torch.int64, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    csa2.csa2_norm_rope(x, out, torch.from_numpy(_prologue_gamma()).to(dev), 1e-6, pos, 10000.0)
+    torch.cuda.synchronize()
+    got = out.view(T * H, 512)[torch.from_numpy(picks).to(dev)].float().cpu().numpy().astype(np.float64)
+    ok = _norm_rope_full_size_check(got, picks, H)
+    assert ok.all(), int((~ok).sum())
