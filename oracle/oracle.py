@@ -16,6 +16,10 @@ of one CSA2 layer in the order the pages give them:
 * every layer   -- attention over the selected entries plus its own FP8
   sliding window under one softmax ([P2] §3, §5 window equation; [P3] §3.3).
 
+Around the layer: the input prologue (RMSNorm of the queries and compressed
+KV, then RoPE on their last 64 dims; [P3] §4.3) and the attention options
+(sink, output re-rotation, window de-duplication).
+
 Parity status of each function is listed in the design notes; the one
 unpinned item is the 890-byte/token decomposition (a footprint reading, not a
 function of this module).
