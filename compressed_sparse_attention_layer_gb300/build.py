@@ -1,12 +1,15 @@
 """Build the CSA2 CUDA library (libcsa2.so) in place with nvcc for sm_103a.
 
 Each translation unit is compiled in parallel; the objects are linked into
-one shared library next to this file.  Rebuilds only what changed.
+one shared library next to this file.  Rebuilds only what changed: objects
+live in a build folder named for a hash of the compiler flags, and the
+library is relinked when its objects or its flags change.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import subprocess
 
@@ -27,8 +30,12 @@ def _headers():
     return glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _flags_key(extra) -> str:
+    return hashlib.sha1("\0".join([NVCC, *ARCH, *FLAGS, *extra]).encode()).hexdigest()[:12]
+
+
+def _compile(src: str, extra, objdir: str) -> str:
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     deps = [src] + _headers()
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(d) for d in deps):
         return obj
@@ -40,17 +47,26 @@ def _compile(src: str, extra) -> str:
 
 
 def build(verbose: bool = False, extra=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+    key = _flags_key(list(extra))
+    objdir = os.path.join(BUILD, key)
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, list(extra)), srcs))
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
+        objs = list(ex.map(lambda s: _compile(s, list(extra), objdir), srcs))
+    # the library remembers the flags and sources it was linked from
+    stamp = LIB + ".build"
+    want = key + "\n" + "\n".join(os.path.basename(o) for o in objs) + "\n"
+    have = open(stamp).read() if os.path.exists(stamp) else ""
+    if not os.path.exists(LIB) or have != want or \
+            os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp, "w") as f:
+            f.write(want)
     if verbose:
         print("built", LIB)
     return LIB

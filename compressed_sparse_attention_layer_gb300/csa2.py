@@ -58,7 +58,8 @@ EXPORTS = {
     "csa2_index_scores": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp, _vp,
                                          _vp, _i64, _vp]),
     "csa2_index_scores_pool": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp,
-                                              _vp, _i64, _vp, _vp]),
+                                              _vp, _i64, _vp, _vp, _sz, _vp]),
+    "csa2_index_scores_pool_workspace_size": (_sz, [ctypes.POINTER(Batch), _i64]),
     "csa2_topk": (ctypes.c_int, [_vp, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
     "csa2_topk_blocks": (ctypes.c_int, [_vp, _i64, _vp, _i32, _i32, _vp, _vp, _vp]),
     "csa2_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _f32, _vp, _i32,
@@ -224,11 +225,22 @@ def csa2_index_scores(cache: Cache, batch: Batch, qi, w, scores=None, block_max=
         _stream(stream)))
 
 
-def csa2_index_scores_pool(cache: Cache, batch: Batch, qi, w, pool, pool_len, scores, stream=None):
+def csa2_index_scores_pool_workspace_size(batch: Batch, ld: int) -> int:
+    return int(load().csa2_index_scores_pool_workspace_size(ctypes.byref(batch), int(ld)))
+
+
+def csa2_index_scores_pool(cache: Cache, batch: Batch, qi, w, pool, pool_len, scores, workspace=None, stream=None):
+    """workspace: uint8 device buffer of csa2_index_scores_pool_workspace_size bytes (allocated
+    here through torch when None)."""
+    ld = pool.shape[-1]
+    if workspace is None:
+        workspace = torch.empty(csa2_index_scores_pool_workspace_size(batch, ld), dtype=torch.uint8,
+                                device=pool.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
     _check("csa2_index_scores_pool", load().csa2_index_scores_pool(
         ctypes.byref(cache), ctypes.byref(batch), _ptr(qi, torch.bfloat16, "qi"), _ptr(w, torch.float32, "w"),
-        _ptr(pool, torch.int32, "pool"), _ptr(pool_len, torch.int32, "pool_len"), pool.shape[-1],
-        _ptr(scores, torch.float32, "scores"), _stream(stream)))
+        _ptr(pool, torch.int32, "pool"), _ptr(pool_len, torch.int32, "pool_len"), ld,
+        _ptr(scores, torch.float32, "scores"), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def csa2_topk(scores, lens, k: int, out, cand=None, stream=None):

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 #include "csa2_internal.cuh"
 
@@ -10,6 +12,58 @@ namespace csa2 {
 
 static thread_local int g_last_cuda_error = 0;
 void set_cuda_error(cudaError_t e) { g_last_cuda_error = (int)e; }
+
+// ---------------------------------------------------------------- per-device set-up
+namespace {
+constexpr int kMaxDevices = 64;
+struct KernelAttr {
+    int dev;
+    const void *fn;
+    size_t bytes;
+};
+std::mutex g_dev_mu;
+std::vector<KernelAttr> g_kernel_attrs;     // (device, kernel) limits already raised
+int g_dev_sms[kMaxDevices] = {};
+}  // namespace
+
+int kernel_smem_limit(const void *kernel, size_t bytes, int carveout)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    for (const KernelAttr &a : g_kernel_attrs)
+        if (a.dev == dev && a.fn == kernel && a.bytes >= bytes) return CSA2_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && carveout >= 0)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return CSA2_ERR_CUDA;
+    }
+    for (KernelAttr &a : g_kernel_attrs)
+        if (a.dev == dev && a.fn == kernel) {
+            a.bytes = bytes;
+            return CSA2_OK;
+        }
+    g_kernel_attrs.push_back({dev, kernel, bytes});
+    return CSA2_OK;
+}
+
+int device_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (dev < kMaxDevices && g_dev_sms[dev] > 0) return g_dev_sms[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) g_dev_sms[dev] = n;
+    return n;
+}
 
 // launchers defined in the kernel files
 int launch_compress(const uint16_t *, const uint16_t *, const float *, int, int64_t, float *, cudaStream_t);
@@ -27,8 +81,6 @@ int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, 
                        float *, cudaStream_t);
 int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const uint16_t *, const float *,
                        const int32_t *, int64_t, float *, cudaStream_t, bool bf16_scores = false);
-int launch_index_pool(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *,
-                           const int32_t *, const int32_t *, int64_t, float *, cudaStream_t);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
                 cudaStream_t, bool bf16_scores = false);
 int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int32_t *, int32_t, int32_t,
@@ -92,8 +144,9 @@ static inline int64_t score_ld(const csa2_batch *b)
 
 // FULL workspace: scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
 //                 | attention workspace
-// REINDEX:        pool scores [rows][16384] | pool key codes [rows][16384][128]
-//                 | pool key scales [rows][16384] | attention workspace
+// REINDEX:        pool scores [rows][16384] | (only without a carried copy of
+//                 the pool's keys: pool key codes [rows][16384][128] | pool key
+//                 scales [rows][16384]) | attention workspace
 struct LayerWs {
     float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr, *pool_kscales = nullptr;
     uint8_t *pool_kcodes = nullptr;
@@ -102,7 +155,7 @@ struct LayerWs {
     size_t attn_bytes = 0, total = 0;
 };
 
-static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
+static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base, bool pool_copy)
 {
     LayerWs w;
     const int64_t rows = (int64_t)b->batch * b->nq;
@@ -121,15 +174,24 @@ static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
     }
     if (mode == CSA2_MODE_REINDEX) {
         w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
-        // the pool's keys, when the caller carries no copy of them (the size
-        // query counts them: the layer may be called either way)
-        w.pool_kcodes = (uint8_t *)take((size_t)rows * CSA2_POOL_MAX * 128);
-        w.pool_kscales = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+        // the pool's keys, when the caller carries no copy of them
+        if (pool_copy) {
+            w.pool_kcodes = (uint8_t *)take((size_t)rows * CSA2_POOL_MAX * 128);
+            w.pool_kscales = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
+        }
     }
     w.attn_bytes = attn_workspace_bytes(rows);
     w.attn = take(w.attn_bytes);
     w.total = off;
     return w;
+}
+
+// Workspace a csa2_layer call with these arguments needs: a Reindex layer
+// reserves room for the pool's keys only when io carries no copy of them.
+size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_io *io)
+{
+    if (!b || b->batch < 1 || b->nq < 1 || mode < 0 || mode > 2) return 0;
+    return layer_ws(mode, b, nullptr, !(io && io->pool_codes)).total;
 }
 
 }  // namespace csa2
@@ -223,16 +285,37 @@ int csa2_index_scores(const csa2_cache *cache, const csa2_batch *batch, const ui
     return launch_index_scan(*cache, *batch, qi, w, scores, block_max, n_visible, ld, (cudaStream_t)stream);
 }
 
+// The pool's indexer keys gathered into dense rows of ld slots (codes, then
+// scales), the layout the Reindex layers scan.
+static size_t pool_keys_bytes(int64_t rows, int64_t ld)
+{
+    return align256((size_t)rows * ld * 128) + align256((size_t)rows * ld * 4);
+}
+
+size_t csa2_index_scores_pool_workspace_size(const csa2_batch *batch, int64_t ld)
+{
+    if (!batch || batch->batch < 1 || batch->nq < 1 || ld <= 0 || ld % CSA2_PAGE || ld > (int64_t)1 << 24) return 0;
+    return pool_keys_bytes((int64_t)batch->batch * batch->nq, ld);
+}
+
 int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi,
                            const float *w, const int32_t *pool, const int32_t *pool_len, int64_t ld,
-                           float *scores, csa2_stream_t stream)
+                           float *scores, void *workspace, size_t workspace_bytes, csa2_stream_t stream)
 {
     int s = check_cache(cache, false, true);
     if (s) return s;
     if ((s = check_batch(batch, cache))) return s;
     if (!qi || !w || !pool || !pool_len || !scores) return CSA2_ERR_NULL;
-    if (ld <= 0 || ld > (int64_t)1 << 24) return CSA2_ERR_SHAPE;
-    return launch_index_pool(*cache, *batch, qi, w, pool, pool_len, ld, scores, (cudaStream_t)stream);
+    if (ld <= 0 || ld % CSA2_PAGE || ld > (int64_t)1 << 24) return CSA2_ERR_SHAPE;
+    const int64_t rows = (int64_t)batch->batch * batch->nq;
+    if (!workspace || workspace_bytes < pool_keys_bytes(rows, ld)) return CSA2_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return CSA2_ERR_ALIGN;
+    const cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *codes = static_cast<uint8_t *>(workspace);
+    float *kscales = reinterpret_cast<float *>(codes + align256((size_t)rows * ld * 128));
+    // the same two kernels as a Reindex layer: gather the pool's keys, scan them densely
+    if ((s = launch_gather_pool(*cache, *batch, pool, pool_len, ld, codes, kscales, st))) return s;
+    return launch_index_dense(codes, kscales, *batch, qi, w, pool_len, ld, scores, st);
 }
 
 int csa2_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
@@ -283,8 +366,9 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
 {
-    if (!batch || batch->batch < 1 || batch->nq < 1 || mode < 0 || mode > 2) return 0;
-    return layer_ws(mode, batch, nullptr).total;
+    // the most a call of this mode needs: a Reindex layer given no carried copy
+    // of the pool's keys copies them into its workspace
+    return layer_workspace_need(mode, batch, nullptr);
 }
 
 int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, const csa2_layer_io *io,
@@ -304,7 +388,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (io->pool_codes && (!aligned(io->pool_codes, 16) || !aligned(io->pool_scales, 16))) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
-    LayerWs ws = layer_ws(mode, batch, workspace);
+    LayerWs ws = layer_ws(mode, batch, workspace, !io->pool_codes);
     if (ws.total && (!workspace || workspace_bytes < ws.total)) return CSA2_ERR_WORKSPACE;
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
 

@@ -710,12 +710,7 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
     const int nchunks = (k + AC_KEYS - 1) / AC_KEYS + 1;
     const size_t smem = sizeof(AcSmem) + 1024;
     if (rows > 65535) return CSA2_ERR_SHAPE;       // rows run along the grid's y dimension
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        attr = true;
-    }
+    if (const int s = kernel_smem_limit((const void *)k_attn_tc, smem, 100)) return s;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;

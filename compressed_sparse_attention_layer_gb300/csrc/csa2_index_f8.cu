@@ -44,7 +44,6 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "csa2_internal.cuh"
 #include "csa2_tc.cuh"
@@ -589,36 +588,30 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 }
 
 // ---------------------------------------------------------------- host side
-static int g_sms = 0;
-static std::once_flag g_sms_once;
-
 template <bool DENSE, int QG>
 static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                        const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
-                       cudaStream_t st, bool bf16)
+                       cudaStream_t st, bool bf16, int sms)
 {
     const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
     const size_t smem = sizeof(F8Smem<QG>) + 1024;
-    static bool attr = false;
-    if (!attr) {
-        if constexpr (QG == 1)
-            cudaFuncSetAttribute(k_index_f8<true, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaFuncSetAttribute(k_index_f8<false, DENSE, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr = true;
-    }
+    int s = CSA2_OK;
+    if constexpr (QG == 1)
+        s = kernel_smem_limit((const void *)k_index_f8<true, DENSE, QG>, smem);
+    if (s || (s = kernel_smem_limit((const void *)k_index_f8<false, DENSE, QG>, smem))) return s;
     const int64_t per_row = DENSE ? ld : bt.max_entries;
     const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
     // the persistent grid (ragged single-query batches) for QG = 1; query groups
     // (equal lengths within a sequence) take a grid of CTAs per group
     if constexpr (QG == 1) {
         if (groups <= F8_PERSIST_ROWS) {
-            const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, g_sms));
+            const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, sms));
             return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
                               pool_len, scores, block_max, n_visible, ld, (int)bf16);
         }
     }
     if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
-    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)g_sms + groups - 1) / groups));
+    const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)sms + groups - 1) / groups));
     return launch_pdl(k_index_f8<false, DENSE, QG>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
                       pool_len, scores, block_max, n_visible, ld, (int)bf16);
 }
@@ -630,16 +623,13 @@ static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *
                      const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
                      cudaStream_t st, bool bf16)
 {
-    std::call_once(g_sms_once, [] {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    });
-    if (g_sms <= 0) return CSA2_ERR_CUDA;
+    const int sms = device_sms();
+    if (sms <= 0) return CSA2_ERR_CUDA;
     if (DENSE || bt.nq < 2)
-        return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
-    if (bt.nq < 4) return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
-    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16);
+        return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
+    if (bt.nq < 4)
+        return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
+    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
 }
 
 int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,

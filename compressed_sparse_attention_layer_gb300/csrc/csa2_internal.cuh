@@ -50,6 +50,21 @@ inline int launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
 
 inline int ceil_div_i(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Per-device kernel set-up (thread-safe): raises `kernel`'s dynamic
+// shared-memory limit to `bytes` on the current device -- the limit is a
+// property of the kernel on each device -- the first time a launch there
+// needs it, and with carveout >= 0 also sets its preferred shared-memory
+// carveout (percent).  CSA2_ERR_CUDA if the runtime refuses.
+int kernel_smem_limit(const void *kernel, size_t bytes, int carveout = -1);
+
+// Number of SMs of the current device (looked up once per device); 0 if the
+// runtime cannot say.
+int device_sms();
+
+// Workspace bytes csa2_layer needs for these arguments (io may be NULL: the
+// most any call of the mode needs); 0 for invalid arguments.
+size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_io *io);
+
 inline bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 // ---------------------------------------------------------------- device side

@@ -25,8 +25,10 @@ extern "C" int csa2_layer_noalloc(int32_t mode, const csa2_cache *cache, const c
                                   const csa2_layer_io *io, csa2_stream_t stream)
 {
     if (!batch) return CSA2_ERR_NULL;
-    // reject work whose scratch does not fit before touching the device
-    const size_t need = csa2_layer_workspace_size(mode, batch);
+    // reject work whose scratch does not fit before touching the device (a
+    // Reindex layer given the Full layer's copy of the pool's keys needs no room
+    // for them)
+    const size_t need = csa2::layer_workspace_need(mode, batch, io);
     if (need > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_WORKSPACE;
 
     int dev = -1;

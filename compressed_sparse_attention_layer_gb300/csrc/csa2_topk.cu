@@ -732,11 +732,7 @@ template <int CL>
 static int topk_cl(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
                    int32_t k, int32_t *out, cudaStream_t st)
 {
-    static bool attr = false;                        // raise the limit once, before any graph capture
-    if (!attr) {
-        cudaFuncSetAttribute(k_topk<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * TK_SLICE * 4);
-        attr = true;
-    }
+    if (const int s = kernel_smem_limit((const void *)k_topk<CL>, 2 * TK_SLICE * 4)) return s;
     return launch_cluster(k_topk<CL>, CL, ld, rows, st, scores, ld, len, cand, (int)k, out);
 }
 
@@ -744,11 +740,7 @@ template <int CL>
 static int blocks_cl(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
                      int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaFuncSetAttribute(k_topk_blocks<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * TK_SLICE * 4);
-        attr = true;
-    }
+    if (const int s = kernel_smem_limit((const void *)k_topk_blocks<CL>, 2 * TK_SLICE * 4)) return s;
     return launch_cluster(k_topk_blocks<CL>, CL, ld_blocks, rows, st, block_max, ld_blocks, n_visible, (int)pmax,
                           pool, pool_len);
 }

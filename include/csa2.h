@@ -305,12 +305,24 @@ CSA2_API int csa2_index_scores(const csa2_cache *cache, const csa2_batch *batch,
                       int64_t ld, csa2_stream_t stream);
 
 /* Reindex variant ([P2] §3.2: later layers rescore only the pool): scores of
- * the entries listed in pool[r][0 .. pool_len[r]).
- *   pool int32 [B*Q][ld] ascending positions; pool_len int32 [B*Q] (<= ld);
- *   scores fp32 [B*Q][ld] (slot i of row r = score of pool[r][i]). */
+ * the entries listed in pool[r][0 .. pool_len[r]), by the kernels a Reindex
+ * layer uses: the pool's indexer keys are gathered into dense rows of the
+ * workspace, then scanned like the cache.
+ *   pool int32 [B*Q][ld] positions; pool_len int32 [B*Q] (clamped to [0, ld]);
+ *   scores fp32 [B*Q][ld] (slot i of row r = score of pool[r][i]; a position
+ *   at or beyond the query's visible entries, or on a page outside the cache,
+ *   scores -inf and is flagged CSA2_DEV_BAD_INDEX / CSA2_DEV_BAD_PAGE);
+ *   ld a multiple of 64, <= 2^24 (CSA2_ERR_SHAPE otherwise);
+ *   workspace >= csa2_index_scores_pool_workspace_size(batch, ld) bytes,
+ *   256-byte aligned (CSA2_ERR_WORKSPACE / CSA2_ERR_ALIGN otherwise). */
 CSA2_API int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *batch, const uint16_t *qi,
                            const float *w, const int32_t *pool, const int32_t *pool_len,
-                           int64_t ld, float *scores, csa2_stream_t stream);
+                           int64_t ld, float *scores, void *workspace, size_t workspace_bytes,
+                           csa2_stream_t stream);
+
+/* Workspace of csa2_index_scores_pool: B*Q*ld*132 bytes (rounded up to 256-byte
+ * sections); 0 for an invalid batch or ld. */
+CSA2_API size_t csa2_index_scores_pool_workspace_size(const csa2_batch *batch, int64_t ld);
 
 /* ---- a5/a6: Top-K selection ---------------------------------------------
  * For each of `rows` rows: the k slots i < len[r] with the largest scores
@@ -369,6 +381,9 @@ CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch 
                const csa2_layer_io *io, void *workspace, size_t workspace_bytes,
                csa2_stream_t stream);
 
+/* The most workspace a csa2_layer call of this mode needs (a REINDEX call whose
+ * io->pool_codes is NULL copies the pool's keys into its workspace; with the
+ * carried copy it needs B*Q*16384*132 bytes less); 0 for invalid arguments. */
 CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch);
 
 /* ---- allocation-free layer call --------------------------------------------
@@ -379,12 +394,17 @@ CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
  * workspace: the scratch is one static device array of
  * CSA2_NOALLOC_SCRATCH_BYTES (16 MiB) compiled into the library, held on
  * every GPU that loads the library until the process exits.
- * - Returns CSA2_ERR_WORKSPACE, before any device work, when
- *   csa2_layer_workspace_size(mode, batch) exceeds CSA2_NOALLOC_SCRATCH_BYTES
- *   (for example a Full layer over 8 x 1M entries); use csa2_layer there.
+ * - Returns CSA2_ERR_WORKSPACE, before any device work, when the scratch this
+ *   call needs exceeds CSA2_NOALLOC_SCRATCH_BYTES (for example a Full layer
+ *   over 8 x 1M entries, or a Reindex layer of 8 or more query rows whose
+ *   io->pool_codes is NULL); use csa2_layer there.  A Reindex layer given the
+ *   Full layer's copy of the pool's keys needs only its scores and attention
+ *   scratch (about 5.8 MB at 8 rows).
  * - The first call on a device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress); make that first call before any
- *   stream capture.  `stream` must belong to the current device.
+ *   stream capture.  `stream` must belong to the current device.  The cached
+ *   address is good for the life of the device's primary context: after
+ *   cudaDeviceReset, do not call this entry point again in the process.
  * - Every call on a device shares the one array, which keeps the previous
  *   call's contents (nothing in it needs to start at zero).  Calls whose
  *   work overlaps on the GPU (other streams, other host threads) race on it

@@ -2,8 +2,14 @@
 
 Bit-exact: quantisers, Top-K given identical scores, pool construction.
 Tolerances (floating point): compressor rounds once from double precision on
-both sides; indexer scores rel 1e-5 (fp32 accumulation of exact products vs
-double); attention max-abs 2e-3 and rel-L2 1e-3 given identical indices.
+both sides; indexer scores rel 1e-5 -- the scan splits each head of the bf16
+query into two e4m3 parts, hi = e4m3(q 2^-e) and lo = e4m3(q 2^-e - hi) with
+max|q 2^-e| in [128, 256): an element within about 2^-10 of its head's
+largest keeps its bf16 value exactly, a smaller one is carried to an absolute
+error of at most 2^-17 of that largest element (lo's subnormal step); the
+products of the key codes with hi and lo accumulate in fp32 on the tensor
+cores, against the oracle's double precision; attention max-abs 2e-3 and
+rel-L2 1e-3 given identical indices.
 """
 import numpy as np
 import pytest

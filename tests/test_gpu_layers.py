@@ -2,8 +2,10 @@
 
 Parity bar: Reuse propagation bit-exact; Top-K
 valid (every selected index scores >= the oracle's k-th score - 1e-3|score|)
-with >= 99.5% overlap; attention within max-abs 2e-3 / rel-L2 1e-3 against the
-oracle's attention over the indices the layer selected, in every layer.
+with >= 99.5% overlap, at both levels of a Full layer's hierarchy (the pool's
+blocks against the oracle's best 2,048 blocks of 8, the Top-512 against the
+oracle's); attention within max-abs 2e-3 / rel-L2 1e-3 against the oracle's
+attention over the indices the layer selected, in every layer.
 """
 import numpy as np
 import pytest
@@ -16,6 +18,26 @@ from compressed_sparse_attention_layer_gb300.device import DeviceWorkload
 from tests.reference import SeqOracle, attn_close, topk_valid
 
 pytestmark = pytest.mark.gpu
+
+
+def _pool_valid(pool_gpu, pool_ref, scores, nvis):
+    """The block level of the hierarchy ([P1] §3.2, [P2] §3.2: the best 2,048
+    blocks of 8): the GPU pool covers whole visible blocks, each kept block's
+    oracle block maximum is >= the oracle's 2,048th block maximum - 1e-3|.|,
+    and >= 99.5 % of the oracle's blocks are kept."""
+    blocks = np.unique(pool_gpu // 8)
+    want = np.concatenate([np.arange(8 * k, min(8 * k + 8, nvis)) for k in blocks]) if blocks.size else blocks
+    if not np.array_equal(np.sort(pool_gpu), want):
+        return False, "pool is not the visible positions of whole blocks"
+    nb = (nvis + 7) // 8
+    bmax = np.full(nb * 8, -np.inf)
+    bmax[:nvis] = scores[:nvis]
+    bmax = bmax.reshape(nb, 8).max(axis=1)
+    ref_blocks = np.unique(pool_ref // 8)
+    kth = np.sort(bmax[ref_blocks])[0]                     # the weakest block the oracle keeps
+    ok = bool(np.all(bmax[blocks] >= kth - 1e-3 * abs(kth)))
+    ov = np.intersect1d(blocks, ref_blocks).size / max(ref_blocks.size, 1)
+    return ok and ov >= 0.995 and blocks.size == ref_blocks.size, (ok, ov, blocks.size, ref_blocks.size)
 
 
 def _check_sequence(dw, b, i=0):
@@ -32,8 +54,12 @@ def _check_sequence(dw, b, i=0):
             kth = np.sort(scores[pool_ref])[::-1][min(511, pool_ref.size - 1)]
             ok, info = topk_valid(got_idx, lambda s: scores[s], kth, idx_ref)
             assert ok, (l, mode, info)
-            # pool: same size; the planted blocks are in it
+            # pool: the same size, valid and overlapping the oracle's at the block level
             assert dw.hist_pool_len[l][r] == pool_ref.size
+            n = int(dw.hist_pool_len[l][r])
+            pool_gpu = dw.hist_pool[l][r, :n].cpu().numpy()
+            ok, info = _pool_valid(pool_gpu, pool_ref, scores, so.visible(i)[1])
+            assert ok, (l, "pool", info)
         elif mode == "reindex":
             idx_ref, ps = so.reindex(l, i, pool_ref)
             kth = np.sort(ps)[::-1][min(511, ps.size - 1)]
@@ -49,11 +75,13 @@ def _check_sequence(dw, b, i=0):
 
 
 def _run_recording(dw):
-    dw.hist_idx, dw.hist_pool_len = {}, {}
+    dw.hist_idx, dw.hist_pool_len, dw.hist_pool = {}, {}, {}
 
     def rec(l):
         dw.hist_idx[l] = dw.idx.cpu().numpy().copy()
         dw.hist_pool_len[l] = dw.pool_len.cpu().numpy().copy()
+        if dw.wl.layers[l] == "full":
+            dw.hist_pool[l] = dw.pool.clone()          # on the device: rows are read as checked
 
     dw.run(on_layer=rec)
     torch.cuda.synchronize()
@@ -144,6 +172,38 @@ def test_layer_decode_1m_sampled():
     pool_len = dw.pool_len.cpu().numpy()
     for b in range(wl.batch):
         assert np.isin(wl.planted_positions(b), pool[b][: pool_len[b]]).all()
+    del dw
+    torch.cuda.empty_cache()
+
+
+def test_decode_step_deterministic():
+    """The same 20-layer decode step over 8 x 1,048,576 tokens, run twice from
+    the same state: every layer's idx, the pool, o and lse are bitwise equal
+    (fixed reduction orders everywhere, no atomics on the data path)."""
+    wl = W.decode_1m()
+    dw = DeviceWorkload(wl)
+    runs = []
+    for _ in range(2):
+        dw.idx.fill_(-1)
+        dw.pool.fill_(-1)
+        dw.pool_len.zero_()
+        rec = {}
+
+        def keep(l):
+            rec[l] = (dw.idx.clone(), dw.o[l].clone(), dw.lse[l].clone())
+
+        for l in dw.layers:
+            dw.run_layer(l, new_rows=dw.swa_new_rows(l))
+            keep(l)
+        torch.cuda.synchronize()
+        runs.append((rec, dw.pool.clone(), dw.pool_len.clone()))
+    (a, pa, la), (b, pb, lb) = runs
+    assert torch.equal(pa, pb) and torch.equal(la, lb)
+    for l in dw.layers:
+        assert torch.equal(a[l][0], b[l][0]), (l, "idx")
+        assert torch.equal(a[l][1].view(torch.int32), b[l][1].view(torch.int32)), (l, "o")
+        assert torch.equal(a[l][2].view(torch.int32), b[l][2].view(torch.int32)), (l, "lse")
+    assert int(dw.cache.status[0]) == 0
     del dw
     torch.cuda.empty_cache()
 

@@ -4,9 +4,10 @@ A caller that cannot hand the library a workspace buffer (a plugin whose host
 program owns all device memory, a serving loop that allocates nothing after
 start-up) uses this entry point; its scratch is a static device array of
 CSA2_NOALLOC_SCRATCH_BYTES inside the library.  These checks compare it with
-csa2_layer given a caller workspace, on the same inputs, for two calls in a
-row (the array keeps the previous call's contents), and check that work too
-large for the array is refused before anything runs.
+csa2_layer given a caller workspace, on the same inputs, for two passes with
+an unrelated workload run through the array in between (the array keeps the
+previous call's contents, so the second pass starts from unrelated data), and
+check that work too large for the array is refused before anything runs.
 
 Collected last on purpose (file name), so a run that stops at the first
 failure has already run every other test.
@@ -53,6 +54,18 @@ def _run(dw, use_noalloc):
     return out
 
 
+def _same(got, want, tag):
+    for l in want:
+        assert np.array_equal(got[l][0], want[l][0]), (tag, l, "indices")
+        assert np.array_equal(got[l][1], want[l][1]), (tag, l, "pool sizes")
+        for r in range(got[l][2].shape[0]):
+            ok, info = attn_close(got[l][2][r], got[l][3][r], want[l][2][r], want[l][3][r])
+            assert ok, (tag, l, r, info)
+        # the kernels are deterministic: the scratch's earlier contents change no bit
+        assert np.array_equal(got[l][2].view(np.int32), want[l][2].view(np.int32)), (tag, l, "o bits")
+        assert np.array_equal(got[l][3].view(np.int32), want[l][3].view(np.int32)), (tag, l, "lse bits")
+
+
 def test_noalloc_layer_matches_layer_twice():
     wl = W.Workload("noalloc", 4242, 3, [4096, 2500, 20000], 1,
                     ["full", "reuse", "reindex", "reuse"], planted_blocks=4)
@@ -60,15 +73,13 @@ def test_noalloc_layer_matches_layer_twice():
     for mode in (0, 1, 2):
         assert csa2.csa2_layer_workspace_size(mode, dw.batch) <= SCRATCH_BYTES
     want = _run(dw, use_noalloc=False)
-    for call in range(2):
-        got = _run(dw, use_noalloc=True)
-        for l in dw.layers:
-            assert np.array_equal(got[l][0], want[l][0]), (call, l, "indices")
-            assert np.array_equal(got[l][1], want[l][1]), (call, l, "pool sizes")
-            for r in range(dw.rows):
-                ok, info = attn_close(got[l][2][r], got[l][3][r], want[l][2][r], want[l][3][r])
-                assert ok, (call, l, r, info)
-    assert int(dw.cache.status[0]) == 0
+    _same(_run(dw, use_noalloc=True), want, "first pass")
+    # an unrelated workload (other seed, shapes, layer pattern) through the array
+    other = DeviceWorkload(W.Workload("noalloc_other", 9191, 2, [9000, 30000], 1,
+                                      ["full", "reindex", "reuse"], planted_blocks=2))
+    _run(other, use_noalloc=True)
+    _same(_run(dw, use_noalloc=True), want, "after another workload")
+    assert int(dw.cache.status[0]) == 0 and int(other.cache.status[0]) == 0
 
 
 def test_noalloc_refuses_work_beyond_its_scratch():
@@ -78,3 +89,11 @@ def test_noalloc_refuses_work_beyond_its_scratch():
     cache, io = csa2.Cache(), csa2.LayerIO()
     st = lib.csa2_layer_noalloc(0, ctypes.byref(cache), ctypes.byref(big), ctypes.byref(io), None)
     assert st == -5                                              # CSA2_ERR_WORKSPACE, nothing launched
+    # a Reindex layer of 8 rows: refused without the carried pool keys (their copy
+    # does not fit), accepted past the size check with them (it then fails on the
+    # NULL cache, still before any launch)
+    st = lib.csa2_layer_noalloc(1, ctypes.byref(cache), ctypes.byref(big), ctypes.byref(io), None)
+    assert st == -5
+    io.pool_codes, io.pool_scales = 1 << 12, 1 << 12
+    st = lib.csa2_layer_noalloc(1, ctypes.byref(cache), ctypes.byref(big), ctypes.byref(io), None)
+    assert st == -1                                              # CSA2_ERR_NULL from csa2_layer's checks
