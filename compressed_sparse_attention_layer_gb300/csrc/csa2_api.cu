@@ -2,6 +2,7 @@
 // kernel launches and the per-layer driver.  No entry point allocates memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -53,6 +54,10 @@ int kernel_smem_limit(const void *kernel, size_t bytes, int carveout)
     return CSA2_OK;
 }
 
+static constexpr uint32_t kDefaultWaitPolls = 1u << 24;
+static std::atomic<uint32_t> g_wait_polls{kDefaultWaitPolls};
+uint32_t wait_polls() { return g_wait_polls.load(std::memory_order_relaxed); }
+
 int device_sms()
 {
     int dev = 0;
@@ -88,8 +93,9 @@ int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
-                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
+                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool, uint8_t *, int);
 size_t attn_workspace_bytes(int64_t rows);
+size_t attn_tile_bytes(int64_t rows);
 int topk_max_k();
 int64_t topk_max_len();
 
@@ -123,7 +129,7 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
-    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS)) return CSA2_ERR_UNSUPPORTED;
+    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS | CSA2_ATTN_EARLY_TILES)) return CSA2_ERR_UNSUPPORTED;
     if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
     if (s->new_rows) {
         // the window of a query in a multi-token chunk holds other new tokens, which
@@ -217,6 +223,12 @@ const char *csa2_status_string(int32_t s)
 }
 
 int32_t csa2_last_cuda_error(void) { return g_last_cuda_error; }
+
+int csa2_debug_set_wait_limit(uint32_t polls)
+{
+    g_wait_polls.store(polls ? polls : kDefaultWaitPolls, std::memory_order_relaxed);
+    return CSA2_OK;
+}
 
 int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int32_t m, int64_t n_tok,
                   float *out, csa2_stream_t stream)
@@ -361,7 +373,13 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
     if (!aligned(q, 16) || !aligned(o, 16)) return CSA2_ERR_ALIGN;
     return launch_attn(*cache, *batch, q, sm_scale, idx, k, *swa, o, lse, workspace, workspace_bytes,
-                       (cudaStream_t)stream, false);
+                       (cudaStream_t)stream, false, nullptr, 0);
+}
+
+size_t csa2_layer_kv_tiles_size(const csa2_batch *batch)
+{
+    if (!batch || batch->batch < 1 || batch->nq < 1) return 0;
+    return attn_tile_bytes((int64_t)batch->batch * batch->nq);
 }
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
@@ -386,6 +404,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (io->flags & ~CSA2_LAYER_SCORES_BF16) return CSA2_ERR_UNSUPPORTED;
     const bool bf16 = (io->flags & CSA2_LAYER_SCORES_BF16) != 0;
     if (io->pool_codes && (!aligned(io->pool_codes, 16) || !aligned(io->pool_scales, 16))) return CSA2_ERR_ALIGN;
+    if (io->kv_tiles && !aligned(io->kv_tiles, 16)) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
     LayerWs ws = layer_ws(mode, batch, workspace, !io->pool_codes);
@@ -452,9 +471,14 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
             return s;
     }
     // a8 (REUSE) keeps io->idx as it is; a9 for every mode
-    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call
+    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call;
+    // carried key tiles are written by the selecting modes and read by REUSE (before the dependency
+    // wait with CSA2_ATTN_EARLY_TILES)
+    const bool reuse = mode == CSA2_MODE_REUSE;
+    const int tile_mode = !io->kv_tiles ? 0 : !reuse ? 1 : (io->swa.flags & CSA2_ATTN_EARLY_TILES) ? 3 : 2;
     return launch_attn(*cache, *batch, io->q, io->sm_scale, io->idx, CSA2_TOPK, io->swa, io->o, io->lse,
-                       ws.attn, ws.attn_bytes, st, mode == CSA2_MODE_REUSE && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS));
+                       ws.attn, ws.attn_bytes, st, reuse && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS), io->kv_tiles,
+                       tile_mode);
 }
 
 }  // extern "C"

@@ -224,6 +224,9 @@ __device__ __forceinline__ int64_t f8_group(const csa2_batch &bt, const int32_t 
 // DENSE = true (QG = 1): row r scans entries 0 .. pool_len[r] of rows of ld
 // slots stored one after the other in c.ik_codes / c.ik_scales (page j of row
 // r is page r * ld / 64 + j; no block table), scores only.
+// `polls` bounds each pipeline wait: when one runs out the CTA sets its abort
+// flag and CSA2_DEV_TIMEOUT, every role leaves its loop, and the teardown
+// awaits the CTA's own copies and last MMA commit before freeing memory.
 template <bool PERSIST, bool DENSE, int QG>
 __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_batch bt,
                                                             const uint16_t *__restrict__ qi,
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                                                             float *__restrict__ scores,
                                                             float *__restrict__ block_max,
                                                             int32_t *__restrict__ n_visible, int64_t ld,
-                                                            int bf16_scores)
+                                                            int bf16_scores, uint32_t polls)
 {
     using Cfg = F8Cfg<QG>;
     constexpr int ST = Cfg::STAGES, SL = Cfg::SLOTS, N = Cfg::N;
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 const int64_t ti = it + i;
                 const int stage = (int)(ti % ST);
                 const int k = (int)(ti / ST);
-                const bool ok = k == 0 || tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort);
+                const bool ok = k == 0 || tc::mbar_wait_or_abort(&S.empty[stage], (uint32_t)((k - 1) & 1), abort, polls);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) {
                         *abort = 1;
@@ -388,8 +391,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 // completed (bfree) and the epilogue finished its tiles (wfree)
                 if (seg >= 2 && lane == 0) {
                     const uint32_t par = (uint32_t)(((seg >> 1) - 1) & 1);
-                    ok = tc::mbar_wait_or_abort(&S.bfree[seg & 1], par, abort) &&
-                         tc::mbar_wait_or_abort(&S.wfree[seg & 1], par, abort);
+                    ok = tc::mbar_wait_or_abort(&S.bfree[seg & 1], par, abort, polls) &&
+                         tc::mbar_wait_or_abort(&S.wfree[seg & 1], par, abort, polls);
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (ok) {
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 }
             }
             if (is < Cfg::ISSUERS) {
-                if (lane == 0 && ok) ok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
+                if (lane == 0 && ok) ok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort, polls);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) {
                     if (lane == 0) {
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         for (int64_t i = (is - it) & 1; i < nt; i += 2) {   // tiles ti with ti % 2 == is
                             const int64_t ti = it + i;
                             const int stage = (int)(ti % ST);
-                            if (!tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort)) {
+                            if (!tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort, polls)) {
                                 *abort = 1;
                                 flag(c.status, CSA2_DEV_TIMEOUT);
                                 break;
@@ -431,7 +434,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                             const uint32_t as = a0 + (uint32_t)stage * (F8_TILE * 128);
                             const int slot = (int)(ti % SL);
                             if (ti >= SL &&
-                                !tc::mbar_wait_or_abort(&S.tempty[slot], (uint32_t)(((ti / SL) - 1) & 1), abort)) {
+                                !tc::mbar_wait_or_abort(&S.tempty[slot], (uint32_t)(((ti / SL) - 1) & 1), abort, polls)) {
                                 *abort = 1;
                                 flag(c.status, CSA2_DEV_TIMEOUT);
                                 break;
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
         } else {
             // ---------------- epilogue: warps 4-11, half (warp - 4) / 4, TMEM lanes by warp % 4
             const int qd = warp & 3, hf = (warp - F8_EPI_WARP) >> 2;
-            const bool wok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort);
+            const bool wok = tc::mbar_wait_or_abort(&S.wready[seg & 1], (uint32_t)((seg >> 1) & 1), abort, polls);
             if (!__all_sync(0xffffffffu, wok)) {
                 if (lane == 0) {
                     *abort = 1;
@@ -483,8 +486,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                 // the MMAs of tile ti are done, so its stage's data has landed: the wait on
                 // full[stage] returns at once and acquires the producers' scale copies (the
                 // stage cannot refill before this warp's arrival on empty[stage] below)
-                bool ok = tc::mbar_wait_or_abort(&S.tfull[slot], (uint32_t)((ti / SL) & 1), abort) &&
-                          tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort);
+                bool ok = tc::mbar_wait_or_abort(&S.tfull[slot], (uint32_t)((ti / SL) & 1), abort, polls) &&
+                          tc::mbar_wait_or_abort(&S.full[stage], (uint32_t)((ti / ST) & 1), abort, polls);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) {
                         *abort = 1;
@@ -607,13 +610,13 @@ static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t
         if (groups <= F8_PERSIST_ROWS) {
             const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, sms));
             return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
-                              pool_len, scores, block_max, n_visible, ld, (int)bf16);
+                              pool_len, scores, block_max, n_visible, ld, (int)bf16, wait_polls());
         }
     }
     if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
     const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)sms + groups - 1) / groups));
     return launch_pdl(k_index_f8<false, DENSE, QG>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
-                      pool_len, scores, block_max, n_visible, ld, (int)bf16);
+                      pool_len, scores, block_max, n_visible, ld, (int)bf16, wait_polls());
 }
 
 // Queries per group: the largest of 4, 2, 1 that the per-sequence query count

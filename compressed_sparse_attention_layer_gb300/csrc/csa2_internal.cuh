@@ -61,6 +61,10 @@ int kernel_smem_limit(const void *kernel, size_t bytes, int carveout = -1);
 // runtime cannot say.
 int device_sms();
 
+// Polls a bounded device wait makes before it gives up (kernel argument of
+// the tcgen05 kernels): 2^24 unless csa2_debug_set_wait_limit changed it.
+uint32_t wait_polls();
+
 // Workspace bytes csa2_layer needs for these arguments (io may be NULL: the
 // most any call of the mode needs); 0 for invalid arguments.
 size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_io *io);

@@ -178,6 +178,12 @@ typedef struct csa2_swa {
  * completed).  A decode stack that calls csa2_layer layer after layer, with
  * the window rows of its own tokens passed as new_rows, satisfies it. */
 #define CSA2_ATTN_EARLY_INPUTS 2
+/* csa2_swa.flags, honoured by csa2_layer in REUSE mode with io->kv_tiles: the
+ * caller guarantees that the carried key tiles were written before the
+ * previous call into this library on the stream (by an earlier FULL or REINDEX
+ * call, not by the call just before this one), so they are bulk-copied while
+ * the previous layer's last kernel is still running. */
+#define CSA2_ATTN_EARLY_TILES  4
 
 /* csa2_layer_io.flags: FULL and REINDEX layers keep the index scores in bf16
  * (each fp32 score rounded to nearest even) and select on them: the block
@@ -214,6 +220,20 @@ typedef struct csa2_layer_io {
                                     copied by FULL next to the pool and read by
                                     REINDEX (both NULL: each REINDEX call copies
                                     them into its workspace); 16-byte aligned   */
+    uint8_t        *kv_tiles;    /* optional carried state of
+                                    csa2_layer_kv_tiles_size(batch) bytes,
+                                    16-byte aligned: the dequantised (bf16)
+                                    main-KV entries of the selection and their
+                                    validity, in the attention kernel's own
+                                    layout.  FULL and REINDEX write them for the
+                                    indices they select; REUSE reads them in
+                                    place of the cache, so a REUSE call given
+                                    kv_tiles must follow (on the same stream)
+                                    the FULL or REINDEX call that selected
+                                    io->idx with the same batch and cache, with
+                                    no other selecting call in between.  NULL:
+                                    every call gathers and dequantises the
+                                    entries itself.  Contents are opaque.       */
 } csa2_layer_io;
 
 /* ---- a1: compressor ------------------------------------------------------
@@ -381,6 +401,13 @@ CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch 
                const csa2_layer_io *io, void *workspace, size_t workspace_bytes,
                csa2_stream_t stream);
 
+/* Bytes of csa2_layer_io.kv_tiles for this batch: 528,384 per query row (the
+ * 512 selected entries as bf16 dims plus their validity); 0 for an invalid
+ * batch.  The Reuse layers of a decoder group attend to the same entries as
+ * the layer that selected them ([P2] §3 mode table), so they can take them
+ * dequantised. */
+CSA2_API size_t csa2_layer_kv_tiles_size(const csa2_batch *batch);
+
 /* The most workspace a csa2_layer call of this mode needs (a REINDEX call whose
  * io->pool_codes is NULL copies the pool's keys into its workspace; with the
  * carried copy it needs B*Q*16384*132 bytes less); 0 for invalid arguments. */
@@ -412,6 +439,19 @@ CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
 #define CSA2_NOALLOC_SCRATCH_BYTES (16u << 20)
 CSA2_API int csa2_layer_noalloc(int32_t mode, const csa2_cache *cache, const csa2_batch *batch,
                                 const csa2_layer_io *io, csa2_stream_t stream);
+
+/* ---- failure-path test hook ------------------------------------------------
+ * No counterpart in the source pages.  Every wait of the tensor-core kernels
+ * (the index scan's pipeline, the attention's products) gives up after a
+ * bounded number of polls: the kernel then skips the work that depended on
+ * it, sets CSA2_DEV_TIMEOUT in the cache's status word and returns normally
+ * (its in-flight copies and products are still awaited with a long limit
+ * before its shared and tensor memory are released, so the context stays
+ * usable; outputs of that call are undefined).  This sets the poll count for
+ * launches made after it, process-wide (0 restores the default of 2^24, about
+ * a second); a small count makes those waits run out, which is how the tests
+ * drive the timeout path without a fault. */
+CSA2_API int csa2_debug_set_wait_limit(uint32_t polls);
 
 /* ---- errors -------------------------------------------------------------- */
 CSA2_API const char *csa2_status_string(int32_t status);   /* static string, never NULL */
