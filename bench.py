@@ -186,7 +186,7 @@ class DecodeStep:
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 3 + sum({"full": 5, "reindex": 3, "reuse": 1}[m] for m in wl.layers) + \
+        self.launches = 3 + sum({"full": 4, "reindex": 3, "reuse": 1}[m] for m in wl.layers) + \
             (len(wl.layers) if Q > 1 else 0)
         # the step's host-fed inputs (new tokens, every layer's queries and window
         # rows) and its outputs (every layer's o and lse) in two device buffers
@@ -222,7 +222,7 @@ class DecodeStep:
 
     def enqueue(self, prof=True):
         csa2, dw, cache = self.csa2, self.dw, self.dw.cache
-        # a1: compress the new token (m = 1), a2: FP4 main KV into the cache, a3: FP8 indexer key
+        # compress the new token (m = 1), its FP4 main KV into the cache, its FP8 indexer key
         csa2.csa2_compress(self.C_new, self.Z_new, self.bias, self.wl.m, self.e_new)
         quant = csa2.csa2_quant_fp4_e4m3 if self.wl.kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
         quant(self.e_new, cache.kv_codes, cache.kv_scales, slots=self.new_slots, status=cache.status)
@@ -265,7 +265,7 @@ class DecodeStep:
 
     def enqueue_layers(self, layers, prof=False):
         for l in layers:
-            # a3-a9: the layer; its attention call also quantises this layer's window
+            # the layer; its attention call also quantises this layer's window
             # row of the new token into the ring (csa2_swa.new_rows); several new
             # tokens per sequence: the FP8 quantiser writes their rows first
             full = self.wl.layers[l] == "full"

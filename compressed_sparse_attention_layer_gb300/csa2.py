@@ -46,8 +46,7 @@ class Swa(ctypes.Structure):
 class LayerIO(ctypes.Structure):
     _fields_ = [("q", _vp), ("qi", _vp), ("w", _vp), ("swa", Swa), ("sm_scale", _f32), ("flags", _i32),
                 ("idx", _vp), ("pool", _vp), ("pool_len", _vp), ("o", _vp), ("lse", _vp),
-                ("prof_begin", _vp), ("prof_end", _vp), ("pool_codes", _vp), ("pool_scales", _vp),
-                ("kv_tiles", _vp)]
+                ("prof_begin", _vp), ("prof_end", _vp), ("kv_tiles", _vp)]
 
 
 EXPORTS = {
@@ -278,21 +277,17 @@ def csa2_layer_workspace_size(mode: int, batch: Batch) -> int:
     return int(load().csa2_layer_workspace_size(mode, ctypes.byref(batch)))
 
 
-def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None, pool_keys=None,
+def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None,
              flags: int = 0, kv_tiles=None) -> LayerIO:
     """prof: optional (begin, end) pair of recorded torch.cuda.Event(enable_timing=True).
-    pool_keys: optional (codes uint8 [rows][16384][128], scales fp32 [rows][16384]) carried
-    copy of the pool's indexer keys (written by a Full layer, read by Reindex layers).
     flags: LAYER_SCORES_BF16 or 0.
     kv_tiles: optional uint8 buffer of csa2_layer_kv_tiles_size bytes: the selection's
     dequantised entries, written by Full / Reindex layers and read by the Reuse layers after them."""
     pb, pe = (prof[0].cuda_event, prof[1].cuda_event) if prof else (None, None)
-    pkc, pks = pool_keys if pool_keys is not None else (None, None)
     return LayerIO(_ptr(q, torch.bfloat16, "q"), _ptr(qi, torch.bfloat16, "qi"), _ptr(w, torch.float32, "w"),
                    swa, float(sm_scale), int(flags), _ptr(idx, torch.int32, "idx"), _ptr(pool, torch.int32, "pool"),
                    _ptr(pool_len, torch.int32, "pool_len"), _ptr(o, torch.float32, "o"),
-                   _ptr(lse, torch.float32, "lse"), pb, pe, _ptr(pkc, torch.uint8, "pool codes"),
-                   _ptr(pks, torch.float32, "pool scales"), _ptr(kv_tiles, torch.uint8, "kv tiles"))
+                   _ptr(lse, torch.float32, "lse"), pb, pe, _ptr(kv_tiles, torch.uint8, "kv tiles"))
 
 
 def csa2_layer_kv_tiles_size(batch: Batch) -> int:

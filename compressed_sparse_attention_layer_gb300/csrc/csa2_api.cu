@@ -88,6 +88,9 @@ int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const
                        const int32_t *, int64_t, float *, cudaStream_t, bool bf16_scores = false);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
                 cudaStream_t, bool bf16_scores = false);
+int launch_reindex(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, const int32_t *,
+                   const int32_t *, int, int32_t *, bool, void *, cudaStream_t);
+size_t reindex_workspace_bytes(int64_t rows);
 int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int32_t *, int32_t, int32_t,
                      int32_t *, cudaStream_t, bool bf16_scores = false);
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
@@ -148,20 +151,20 @@ static inline int64_t score_ld(const csa2_batch *b)
     return ld > 0 ? ld : 8;
 }
 
-// FULL workspace: scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
-//                 | attention workspace
-// REINDEX:        pool scores [rows][16384] | (only without a carried copy of
-//                 the pool's keys: pool key codes [rows][16384][128] | pool key
-//                 scales [rows][16384]) | attention workspace
+// FULL workspace:    scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
+//                    | attention workspace
+// REINDEX workspace: the pool's rescored keys [rows][16384] and group minima
+//                    | attention workspace
+// REUSE workspace:   attention workspace
 struct LayerWs {
-    float *scores = nullptr, *block_max = nullptr, *pool_scores = nullptr, *pool_kscales = nullptr;
-    uint8_t *pool_kcodes = nullptr;
+    float *scores = nullptr, *block_max = nullptr;
     int32_t *n_visible = nullptr;
+    void *rx = nullptr;
     void *attn = nullptr;
     size_t attn_bytes = 0, total = 0;
 };
 
-static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base, bool pool_copy)
+static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
 {
     LayerWs w;
     const int64_t rows = (int64_t)b->batch * b->nq;
@@ -178,26 +181,18 @@ static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base, bool pool
         w.block_max = (float *)take((size_t)rows * (ld / 8) * 4);
         w.n_visible = (int32_t *)take((size_t)rows * 4);
     }
-    if (mode == CSA2_MODE_REINDEX) {
-        w.pool_scores = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
-        // the pool's keys, when the caller carries no copy of them
-        if (pool_copy) {
-            w.pool_kcodes = (uint8_t *)take((size_t)rows * CSA2_POOL_MAX * 128);
-            w.pool_kscales = (float *)take((size_t)rows * CSA2_POOL_MAX * 4);
-        }
-    }
+    if (mode == CSA2_MODE_REINDEX) w.rx = take(reindex_workspace_bytes(rows));
     w.attn_bytes = attn_workspace_bytes(rows);
     w.attn = take(w.attn_bytes);
     w.total = off;
     return w;
 }
 
-// Workspace a csa2_layer call with these arguments needs: a Reindex layer
-// reserves room for the pool's keys only when io carries no copy of them.
-size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_io *io)
+// Workspace a csa2_layer call with these arguments needs.
+size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_io *)
 {
     if (!b || b->batch < 1 || b->nq < 1 || mode < 0 || mode > 2) return 0;
-    return layer_ws(mode, b, nullptr, !(io && io->pool_codes)).total;
+    return layer_ws(mode, b, nullptr).total;
 }
 
 }  // namespace csa2
@@ -384,8 +379,6 @@ size_t csa2_layer_kv_tiles_size(const csa2_batch *batch)
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
 {
-    // the most a call of this mode needs: a Reindex layer given no carried copy
-    // of the pool's keys copies them into its workspace
     return layer_workspace_need(mode, batch, nullptr);
 }
 
@@ -400,14 +393,13 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if ((s = check_swa(&io->swa, batch))) return s;
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
-    if (!io->pool_codes != !io->pool_scales) return CSA2_ERR_NULL;
     if (io->flags & ~CSA2_LAYER_SCORES_BF16) return CSA2_ERR_UNSUPPORTED;
     const bool bf16 = (io->flags & CSA2_LAYER_SCORES_BF16) != 0;
-    if (io->pool_codes && (!aligned(io->pool_codes, 16) || !aligned(io->pool_scales, 16))) return CSA2_ERR_ALIGN;
     if (io->kv_tiles && !aligned(io->kv_tiles, 16)) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
+    if (mode != CSA2_MODE_REUSE && !aligned(io->pool, 16)) return CSA2_ERR_ALIGN;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
-    LayerWs ws = layer_ws(mode, batch, workspace, !io->pool_codes);
+    LayerWs ws = layer_ws(mode, batch, workspace);
     if (ws.total && (!workspace || workspace_bytes < ws.total)) return CSA2_ERR_WORKSPACE;
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
 
@@ -429,48 +421,30 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
         return CSA2_OK;
     };
     if (mode == CSA2_MODE_FULL) {
-        // a4: scores of every visible entry and the per-block maxima
+        // scores of every visible entry and the per-block maxima
         if ((s = prof(io->prof_begin))) return s;
         if ((s = launch_index_scan(*cache, *batch, io->qi, io->w, ws.scores, ws.block_max, ws.n_visible, ld, st,
                                    bf16)))
             return s;
         if ((s = prof(io->prof_end))) return s;
-        // a5: the best 2,048 blocks of 8 -> candidate pool
+        // the best 2,048 blocks of 8 -> candidate pool
         if ((s = launch_topk_blocks(ws.block_max, ld / 8, ws.n_visible, rows, CSA2_POOL_BLOCKS, io->pool,
                                     io->pool_len, st)))
             return s;
-        // a6: Top-512 of the pool, its scores read from the scan's score rows
+        // Top-512 of the pool, its scores read from the scan's score rows
         if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st,
                                   bf16)))
             return s;
-        // the pool's keys for the Reindex layers that follow, when the caller carries them
-        if (io->pool_codes &&
-            (s = launch_gather_pool(*cache, *batch, io->pool, io->pool_len, CSA2_POOL_MAX, io->pool_codes,
-                                    io->pool_scales, st)))
-            return s;
     } else if (mode == CSA2_MODE_REINDEX) {
-        // a7: rescore the pool with this layer's indexer query, Top-512
+        // rescore the pool (its blocks' keys read from the cache) with this
+        // layer's indexer query and take its Top-512
         if ((s = prof(io->prof_begin))) return s;
-        // the pool's keys in dense rows (the Full layer's copy, else copied here),
-        // scanned like the cache
-        const uint8_t *kc = io->pool_codes;
-        const float *ks = io->pool_scales;
-        if (!kc) {
-            if ((s = launch_gather_pool(*cache, *batch, io->pool, io->pool_len, CSA2_POOL_MAX, ws.pool_kcodes,
-                                        ws.pool_kscales, st)))
-                return s;
-            kc = ws.pool_kcodes;
-            ks = ws.pool_kscales;
-        }
-        if ((s = launch_index_dense(kc, ks, *batch, io->qi, io->w, io->pool_len, CSA2_POOL_MAX, ws.pool_scores, st,
-                                    bf16)))
+        if ((s = launch_reindex(*cache, *batch, io->qi, io->w, io->pool, io->pool_len, CSA2_TOPK, io->idx, bf16,
+                                ws.rx, st)))
             return s;
         if ((s = prof(io->prof_end))) return s;
-        if ((s = launch_topk(ws.pool_scores, CSA2_POOL_MAX, io->pool_len, rows, io->pool, CSA2_TOPK, io->idx, st,
-                             bf16)))
-            return s;
     }
-    // a8 (REUSE) keeps io->idx as it is; a9 for every mode
+    // REUSE keeps io->idx as it is; the attention for every mode
     // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call;
     // carried key tiles are written by the selecting modes and read by REUSE (before the dependency
     // wait with CSA2_ATTN_EARLY_TILES)

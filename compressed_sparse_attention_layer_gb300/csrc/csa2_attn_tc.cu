@@ -1,4 +1,4 @@
-// a9: sparse MQA + sliding-window attention on the tcgen05 tensor cores.
+// Sparse MQA + sliding-window attention on the tcgen05 tensor cores.
 //
 // Every key is its own value ("DeepSeek-V4 report explainer" §4.3) and one
 // softmax covers the selected entries and the window ("DeepSeek-V4.1-Flash
@@ -91,11 +91,6 @@ __device__ __forceinline__ uint32_t cluster_rank()
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // a (bf16x2) * b (bf16x2), exact when the products are representable.

@@ -1,4 +1,4 @@
-// a4: the Full layer's lightning-indexer scan, e4m3 keys streamed into shared
+// The Full layer's lightning-indexer scan, e4m3 keys streamed into shared
 // memory by cp.async and multiplied on the kind::f8f6f4 tensor cores.
 //
 // score(p) = s_p * sum_h w_h ReLU(qi_h . code_p) and the maximum of each
@@ -45,6 +45,7 @@
 
 #include <algorithm>
 
+#include "csa2_index_common.cuh"
 #include "csa2_internal.cuh"
 #include "csa2_tc.cuh"
 
@@ -104,90 +105,6 @@ __device__ __align__(16) float g_neg_inf_scales[64] = {
     -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
     -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY,
     -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY, -INFINITY};
-
-// 16-byte global -> shared copy through the load-store path (L1 bypassed).
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// Arrive on the mbarrier once every cp.async this thread issued so far has
-// landed (the barrier's expected count includes this arrival).
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
-{
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-
-// e_h with max|q_h| * 2^-e_h in [128, 256).
-__device__ __forceinline__ int head_exponent(float amax)
-{
-    if (!(amax > 0.0f)) return 0;
-    const uint32_t u = __float_as_uint(amax);
-    const int ex = (int)((u >> 23) & 0xFF);
-    const int fl = ex ? ex - 127 : (31 - __clz(u & 0x7FFFFF)) - 149;
-    const int e = fl - 7;
-    return e < -126 ? -126 : (e > 120 ? 120 : e);
-}
-
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Byte offset of element k of row `row` in a K-major 128-byte-swizzled tile of
-// one-byte elements (128 elements per row).
-__device__ __forceinline__ uint32_t sw128_b8(uint32_t row, uint32_t k)
-{
-    return row * 128u + ((((k >> 4) ^ (row & 7u)) << 4) | (k & 15u));
-}
-
-// The two-part e4m3 query operand of row r (hi rows at bh, lo rows at bl, 32
-// each, 8-row aligned) and w_h * 2^e_h, written by one warp; lane h = head h.  Two passes over the head's 128 dims (the maximum,
-// then the conversion) keep half of it in registers at a time.
-__device__ __forceinline__ void write_query_operand(uint8_t *bh, uint8_t *bl, float *wq, const uint16_t *qr,
-                                                    const float *wr)
-{
-    const int h = threadIdx.x & 31;
-    const uint4 *src = reinterpret_cast<const uint4 *>(qr + h * 128);
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const uint4 raw = __ldg(src + i);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int j = 0; j < 4; j++) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[j] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w4[j] & 0xFFFF0000u)));
-        }
-    }
-    const int e = head_exponent(amax);
-    const float f = exp2i(-e);
-    wq[h] = wr[h] * exp2i(e);
-#pragma unroll 2
-    for (int i = 0; i < 16; i += 2) {               // 16 dims per 16-byte chunk of the operand
-        uint32_t hiw[4], low[4];
-#pragma unroll
-        for (int half = 0; half < 2; half++) {
-            const uint4 raw = __ldg(src + i + half);
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int j = 0; j < 4; j += 2) {
-                float v[4] = {__uint_as_float(w4[j] << 16) * f, __uint_as_float(w4[j] & 0xFFFF0000u) * f,
-                              __uint_as_float(w4[j + 1] << 16) * f, __uint_as_float(w4[j + 1] & 0xFFFF0000u) * f};
-                const uint32_t h01 = e4m3x2(v[0], v[1]), h23 = e4m3x2(v[2], v[3]);
-                const float r0 = v[0] - e4m3_to_f32(h01 & 0xFF), r1 = v[1] - e4m3_to_f32(h01 >> 8);
-                const float r2 = v[2] - e4m3_to_f32(h23 & 0xFF), r3 = v[3] - e4m3_to_f32(h23 >> 8);
-                hiw[half * 2 + j / 2] = h01 | (h23 << 16);
-                low[half * 2 + j / 2] = e4m3x2(r0, r1) | (e4m3x2(r2, r3) << 16);
-            }
-        }
-        const uint32_t k = (uint32_t)i * 8;        // first dim of this 16-dim chunk
-        *reinterpret_cast<uint4 *>(bh + sw128_b8(h, k)) = make_uint4(hiw[0], hiw[1], hiw[2], hiw[3]);
-        *reinterpret_cast<uint4 *>(bl + sw128_b8(h, k)) = make_uint4(low[0], low[1], low[2], low[3]);
-    }
-}
 
 // Entries scored by row r: every visible entry of the paged cache, or (DENSE)
 // the first pool_len[r] of a dense per-row copy of a candidate pool's keys.

@@ -1,4 +1,4 @@
-// a1-a3: the CSA compressor and the MXFP4 / FP8 quantisers.
+// The CSA compressor and the MXFP4 / FP8 quantisers.
 //
 // These kernels are memory bound (a few bytes read per byte written), so the
 // design goal is coalesced 16-byte accesses and enough threads in flight:

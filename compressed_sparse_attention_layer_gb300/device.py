@@ -23,14 +23,9 @@ def _dev_normal_bf16(stream, start, count, dev, sigma=1.0):
 
 
 class DeviceWorkload:
-    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None, carry_pool_keys=True,
-                 carry_kv_tiles=True):
-        """carry_pool_keys: give the layers a carried copy of the pool's indexer keys
-        (written by the Full layer, read by Reindex layers) when the pattern has
-        Reindex layers; otherwise every Reindex call copies them into its workspace.
-        carry_kv_tiles: give the layers the carried dequantised entries of the selection
+    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None, carry_kv_tiles=True):
+        """carry_kv_tiles: give the layers the carried dequantised entries of the selection
         (written by Full / Reindex layers, read by the Reuse layers after them)."""
-        self.carry_pool_keys = carry_pool_keys
         self.carry_kv_tiles = carry_kv_tiles
         self.wl = wl
         self.dev = torch.device(device)
@@ -101,7 +96,6 @@ class DeviceWorkload:
         self.idx = torch.full((R, csa2.TOPK), -1, dtype=torch.int32, device=dev)
         self.pool = torch.full((R, csa2.POOL_MAX), -1, dtype=torch.int32, device=dev)
         self.pool_len = torch.zeros((R,), dtype=torch.int32, device=dev)
-        self.pool_keys = None
         # attention options passed to every layer call (csa2.swa_struct keywords:
         # sink, rope_base, flags); none by default
         self.attn_options = {}
@@ -109,9 +103,6 @@ class DeviceWorkload:
         # Reuse layers load their keys while the previous layer finishes
         # (csa2.ATTN_EARLY_INPUTS): the layers are called one after the other
         self.early_inputs = True
-        if self.carry_pool_keys and "reindex" in wl.layers:
-            self.pool_keys = (torch.empty((R, csa2.POOL_MAX, 128), dtype=torch.uint8, device=dev),
-                              torch.empty((R, csa2.POOL_MAX), dtype=torch.float32, device=dev))
         # the selection's dequantised entries, carried from each Full / Reindex layer to
         # the Reuse layers after it (528 KB per query row: decode-sized batches only)
         self.kv_tiles = None
@@ -179,7 +170,7 @@ class DeviceWorkload:
         qi = self.qi.get(l, self.dummy_qi)
         w = self.w.get(l, self.dummy_w)
         return csa2.layer_io(self.q[l], qi, w, self.swa(l, new_rows), 1.0, self.idx, self.pool, self.pool_len,
-                             self.o[l], self.lse[l], prof=prof, pool_keys=self.pool_keys, flags=self.layer_flags,
+                             self.o[l], self.lse[l], prof=prof, flags=self.layer_flags,
                              kv_tiles=self.kv_tiles)
 
     def run_layer(self, l, stream=None, prof=None, new_rows=None):

@@ -205,21 +205,22 @@ typedef struct csa2_layer_io {
     int32_t        *idx;         /* [B*Q][512] selection (written by FULL and
                                     REINDEX, read by every mode)              */
     int32_t        *pool;        /* [B*Q][16384] candidate pool (written by
-                                    FULL, read by REINDEX)                    */
+                                    FULL, read by REINDEX: blocks of 8
+                                    consecutive positions from multiples of 8,
+                                    the last possibly shorter; a REINDEX pool
+                                    not of that form has the offending blocks
+                                    scored -inf and flagged CSA2_DEV_BAD_INDEX);
+                                    16-byte aligned                           */
     int32_t        *pool_len;    /* [B*Q]                                     */
     float          *o;           /* [B*Q][64][512] attention output           */
     float          *lse;         /* [B*Q][64] natural-log sum of exp          */
     void           *prof_begin;  /* optional cudaEvent_t recorded on the stream
                                     just before the layer's index kernel (the
-                                    Full scan / the Reindex pool rescoring),
+                                    Full scan / the Reindex pool rescoring and
+                                    selection),
                                     as an external node when captured; NULL
                                     for none                                   */
     void           *prof_end;    /* optional cudaEvent_t recorded just after it */
-    uint8_t        *pool_codes;  /* optional [B*Q][16384][128] and            */
-    float          *pool_scales; /* [B*Q][16384]: the indexer keys of the pool,
-                                    copied by FULL next to the pool and read by
-                                    REINDEX (both NULL: each REINDEX call copies
-                                    them into its workspace); 16-byte aligned   */
     uint8_t        *kv_tiles;    /* optional carried state of
                                     csa2_layer_kv_tiles_size(batch) bytes,
                                     16-byte aligned: the dequantised (bf16)
@@ -236,7 +237,7 @@ typedef struct csa2_layer_io {
                                     entries itself.  Contents are opaque.       */
 } csa2_layer_io;
 
-/* ---- a1: compressor ------------------------------------------------------
+/* ---- compressor ----------------------------------------------------------
  * e_j[d] = sum_{i<m} softmax_i(Z[jm+i][d] + bias[i][d]) * C[jm+i][d]
  * [P3] §3.1 (softmax-weighted pooling of m tokens with a learned bias);
  * [P2] §2 (C, Z projected per layer), §3.1-3.2 (m = 2 encoder, m = 1 decoder,
@@ -247,7 +248,7 @@ typedef struct csa2_layer_io {
 CSA2_API int csa2_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int32_t m,
                   int64_t n_tok, float *out, csa2_stream_t stream);
 
-/* ---- a2: MXFP4 quantisation of main-KV entries ----------------------------
+/* ---- MXFP4 quantisation of main-KV entries --------------------------------
  * Per 32-element block: X = floor(log2(amax)) - 2 (0 if amax == 0), clamped
  * to [-127, 127], stored as E8M0 byte X + 127; each element x becomes the
  * E2M1 value nearest to x * 2^-X (ties to even mantissa, saturating at 6),
@@ -271,7 +272,7 @@ CSA2_API int csa2_quant_mxfp4(const float *x, int64_t n, const int64_t *slots, u
 CSA2_API int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots, uint8_t *codes,
                         uint8_t *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
 
-/* ---- a3: FP8 e4m3 quantisation with a per-row fp32 scale -----------------
+/* ---- FP8 e4m3 quantisation with a per-row fp32 scale ---------------------
  * s = amax / 448 (IEEE fp32 division; s = 1 when amax == 0); each element
  * code = e4m3(x / s) (IEEE fp32 division, round to nearest even, saturating
  * at 448, sign kept).  Used for the SWA rows ([P1] §3.3, [P2] §4) and the
@@ -309,7 +310,7 @@ CSA2_API int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const fl
                    const int64_t *pos, float rope_base, float *out_f32, uint16_t *out_bf16,
                    csa2_stream_t stream);
 
-/* ---- a4: lightning-indexer scores over every visible entry ---------------
+/* ---- lightning-indexer scores over every visible entry -------------------
  * score(p) = sum_h w[h] * ReLU(qi[h] . k_p), k_p = e4m3(code_p) * scale_p,
  * for every entry p visible to each query; block_max[b8] = max over the
  * visible positions of block b8 (positions 8*b8 .. 8*b8+7).
@@ -344,7 +345,7 @@ CSA2_API int csa2_index_scores_pool(const csa2_cache *cache, const csa2_batch *b
  * sections); 0 for an invalid batch or ld. */
 CSA2_API size_t csa2_index_scores_pool_workspace_size(const csa2_batch *batch, int64_t ld);
 
-/* ---- a5/a6: Top-K selection ---------------------------------------------
+/* ---- Top-K selection ---------------------------------------------------
  * For each of `rows` rows: the k slots i < len[r] with the largest scores
  * (ties -> lower slot), reported as positions (cand[r][i] when cand is
  * non-NULL, else i) in ascending order, the rest of out[r][0..k) set to -1.
@@ -368,7 +369,7 @@ CSA2_API int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const i
                      int32_t rows, int32_t pmax, int32_t *pool, int32_t *pool_len,
                      csa2_stream_t stream);
 
-/* ---- a9: sparse MQA + SWA attention --------------------------------------
+/* ---- sparse MQA + SWA attention ------------------------------------------
  * For each query (b, i) at token t: key set = the selected entries
  * idx[r][0..k) != -1 (MXFP4 main KV, dequantised exactly) followed by the
  * window rows of tokens [max(s, t-127), t] (FP8, times the row scale); each
@@ -408,9 +409,7 @@ CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch 
  * dequantised. */
 CSA2_API size_t csa2_layer_kv_tiles_size(const csa2_batch *batch);
 
-/* The most workspace a csa2_layer call of this mode needs (a REINDEX call whose
- * io->pool_codes is NULL copies the pool's keys into its workspace; with the
- * carried copy it needs B*Q*16384*132 bytes less); 0 for invalid arguments. */
+/* The workspace a csa2_layer call of this mode needs; 0 for invalid arguments. */
 CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch);
 
 /* ---- allocation-free layer call --------------------------------------------
@@ -423,10 +422,9 @@ CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
  * every GPU that loads the library until the process exits.
  * - Returns CSA2_ERR_WORKSPACE, before any device work, when the scratch this
  *   call needs exceeds CSA2_NOALLOC_SCRATCH_BYTES (for example a Full layer
- *   over 8 x 1M entries, or a Reindex layer of 8 or more query rows whose
- *   io->pool_codes is NULL); use csa2_layer there.  A Reindex layer given the
- *   Full layer's copy of the pool's keys needs only its scores and attention
- *   scratch (about 5.8 MB at 8 rows).
+ *   over 8 x 1M entries); use csa2_layer there.  A Reuse layer needs only the
+ *   attention's scratch (about 5.3 MB at 8 query rows), a Reindex layer that
+ *   plus 64 KB per query row for its rescored pool (about 5.8 MB).
  * - The first call on a device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress); make that first call before any
  *   stream capture.  `stream` must belong to the current device.  The cached

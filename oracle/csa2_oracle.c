@@ -112,7 +112,7 @@ uint8_t or_e4m3_encode(float x)
 }
 
 /* ------------------------------------------------------------------------ */
-/* a2: MXFP4 quantisation of main-KV entries                                */
+/* MXFP4 quantisation of main-KV entries                                    */
 /* ------------------------------------------------------------------------ */
 
 /* OCP MX shared scale of one 32-element block: X = floor(log2(amax)) - 2,
@@ -224,7 +224,7 @@ void or_dequant_fp4_e4m3(const uint8_t *codes, const uint8_t *scales, int64_t n,
 }
 
 /* ------------------------------------------------------------------------ */
-/* a3: FP8 quantisation with a per-row fp32 scale (SWA KV, indexer keys)    */
+/* FP8 quantisation with a per-row fp32 scale (SWA KV, indexer keys)        */
 /* ------------------------------------------------------------------------ */
 
 /* s = amax / 448 (one fp32 IEEE division; amax == 0 gives s = 1), then each
@@ -258,7 +258,7 @@ void or_dequant_fp8(const uint8_t *codes, const float *scales, int64_t n, int di
 }
 
 /* ------------------------------------------------------------------------ */
-/* a1: CSA compressor                                                        */
+/* CSA compressor                                                            */
 /* ------------------------------------------------------------------------ */
 
 /* e_j[d] = sum_i softmax_i(Z_{jm+i}[d] + B_i[d]) * C_{jm+i}[d], i < m.
@@ -289,7 +289,7 @@ void or_compress(const uint16_t *C, const uint16_t *Z, const float *bias, int m,
 }
 
 /* ------------------------------------------------------------------------ */
-/* a4: lightning-indexer score                                               */
+/* lightning-indexer score                                                   */
 /* ------------------------------------------------------------------------ */
 
 /* score = sum_h w_h * ReLU(q_h . k), k = e4m3(code) * scale, 32 heads x 128.
@@ -323,7 +323,7 @@ void or_index_scores(const uint16_t *qi, const float *w, const uint8_t *codes,
 }
 
 /* ------------------------------------------------------------------------ */
-/* a5/a6: selection                                                          */
+/* selection                                                                 */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
@@ -398,7 +398,7 @@ int64_t or_block_pool(const double *score, int64_t n, int blk, int pmax, int32_t
 }
 
 /* ------------------------------------------------------------------------ */
-/* a9: sparse MQA attention over selected entries plus the SWA window        */
+/* sparse MQA attention over selected entries plus the SWA window            */
 /* ------------------------------------------------------------------------ */
 
 /* One query: 64 heads x 512 dims against nk keys shared by all heads, each

@@ -127,7 +127,7 @@ def mx_exponent(amax: float) -> int:
     return lib().or_mx_exponent(amax)
 
 
-# ------------------------------------------------------------------ a1-a3
+# ------------------------------------------------------------------ compressor, quantisers
 def compress(C_bits: np.ndarray, Z_bits: np.ndarray, bias: np.ndarray, m: int) -> np.ndarray:
     """C, Z: [n_tok, 512] bf16 patterns (uint16); bias [m, 512] fp32 -> [n_tok//m, 512] fp32."""
     C = _c(C_bits, np.uint16)
@@ -195,7 +195,7 @@ def dequant_fp8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return out
 
 
-# ------------------------------------------------------------------ a4
+# ------------------------------------------------------------------ indexer score
 def index_scores(qi_bits, w, ik_codes, ik_scales, positions=None) -> np.ndarray:
     """Scores (float64) of the entries at ``positions`` (default: all rows)."""
     qi = _c(qi_bits, np.uint16).reshape(32, 128)
@@ -214,7 +214,7 @@ def index_scores(qi_bits, w, ik_codes, ik_scales, positions=None) -> np.ndarray:
     return out
 
 
-# ------------------------------------------------------------------ a5/a6
+# ------------------------------------------------------------------ selection
 def topk(scores: np.ndarray, positions=None, k: int = TOPK) -> np.ndarray:
     """k best (score desc, position asc) positions, returned ascending, -1 padded."""
     s = _c(scores, np.float64)
@@ -236,7 +236,7 @@ def block_pool(scores: np.ndarray, n_visible: int, blk: int = BLOCK,
     return pool[:npool].copy()
 
 
-# ------------------------------------------------------------------ a9
+# ------------------------------------------------------------------ attention
 def swa_window(i: int, s: int = 0, W: int = SWA_W):
     """SWAKeys(i) = [max(s, i - W + 1), i] ([P2] §5, bounded-replay window)."""
     return max(int(s), int(i) - W + 1), int(i)

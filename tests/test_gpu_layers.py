@@ -255,24 +255,6 @@ def test_carried_kv_tiles_bit_identical():
         _check_sequence(a, bb)
 
 
-def test_reindex_with_and_without_the_carried_pool_keys():
-    """Reindex layers reading the Full layer's copy of the pool keys give the
-    same indices and outputs, bit for bit, as Reindex layers that copy them
-    into their own workspace."""
-    wl = W.Workload("pool_keys", 73, 3, [20000, 3000, 70000], 1,
-                    ["full", "reuse", "reindex", "reuse", "reindex"], planted_blocks=4)
-    a = DeviceWorkload(wl)                         # carried copy
-    b = DeviceWorkload(wl, carry_pool_keys=False)  # workspace copies
-    assert a.pool_keys is not None and b.pool_keys is None
-    _run_recording(a)
-    _run_recording(b)
-    for l in range(len(wl.layers)):
-        assert np.array_equal(a.hist_idx[l], b.hist_idx[l]), l
-        assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
-    for bb in range(wl.batch):
-        _check_sequence(a, bb)
-
-
 def test_layers_with_fp4_e4m3_main_kv():
     """The main KV in the 16-element / E4M3-scale FP4 format (csa2_cache.kv_format
     = CSA2_KV_FP4_E4M3): selection and attention against the oracle, which

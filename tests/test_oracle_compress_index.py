@@ -1,4 +1,4 @@
-"""Pins of the oracle's compressor (a1) and lightning-indexer score (a4).
+"""Pins of the oracle's compressor and lightning-indexer score.
 
 Anchors: closed forms (m = 1 identity, m = 2 sigmoid form, equal scores give
 the mean), special inputs that isolate each term of the score (one head, one

@@ -1,4 +1,4 @@
-"""Pins of the oracle's selection (a5/a6/a7/a8) and attention (a9).
+"""Pins of the oracle's selection (Full, Reindex and Reuse layers) and attention.
 
 Anchors: numpy's lexsort (an independent sort) for Top-K order and ties, a
 brute-force block pool, the pool-versus-global equivalence that holds for
