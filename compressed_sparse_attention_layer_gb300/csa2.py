@@ -54,6 +54,7 @@ EXPORTS = {
     "csa2_quant_mxfp4": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_quant_fp8": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _vp, _i64, _vp, _vp]),
     "csa2_quant_fp4_e4m3": (ctypes.c_int, [_vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp]),
+    "csa2_append_entries": (ctypes.c_int, [ctypes.POINTER(Cache), _vp, _vp, _vp, _i32, _i64, _vp, _vp, _vp, _vp]),
     "csa2_norm_rope": (ctypes.c_int, [_vp, _i64, _i32, _vp, _f32, _vp, _f32, _vp, _vp, _vp]),
     "csa2_index_scores": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _vp, _vp, _vp,
                                          _vp, _i64, _vp]),
@@ -207,6 +208,17 @@ def csa2_quant_fp8(x, codes, scales, slots=None, status=None, stream=None):
         _ptr(x, torch.float32, "x"), x.shape[0], x.shape[1], _ptr(slots, torch.int64, "slots"),
         _ptr(codes, torch.uint8), _ptr(scales, torch.float32), codes.shape[0], _ptr(status, torch.int32),
         _stream(stream)))
+
+
+def csa2_append_entries(cache, C, Z, bias, m: int, ik, slots=None, entries=None, stream=None):
+    """A step's new entries: compress C/Z (bf16 [n_tok][512]) into n_tok // m
+    entries, quantise them into cache's main KV and ik (fp32 [n_ent][128])
+    into its indexer keys, at slots (int64 [n_ent]); entries: optional fp32
+    [n_ent][512] copy of the compressed entries.  cache: a csa2.Cache struct."""
+    _check("csa2_append_entries", load().csa2_append_entries(
+        ctypes.byref(cache), _ptr(C, torch.bfloat16, "C"), _ptr(Z, torch.bfloat16, "Z"),
+        _ptr(bias, torch.float32, "bias"), m, C.shape[0], _ptr(ik, torch.float32, "ik"),
+        _ptr(slots, torch.int64, "slots"), _ptr(entries, torch.float32, "entries"), _stream(stream)))
 
 
 def csa2_norm_rope(x, out, gamma=None, eps: float = 1e-6, pos=None, rope_base: float = 0.0, stream=None):

@@ -78,6 +78,8 @@ int launch_quant_fp8(const float *, int64_t, int, const int64_t *, uint8_t *, fl
                      cudaStream_t);
 int launch_quant_fp4_e4m3(const float *, int64_t, const int64_t *, uint8_t *, uint8_t *, int64_t, int32_t *,
                           cudaStream_t);
+int launch_append_entries(const uint16_t *, const uint16_t *, const float *, int, int64_t, const float *,
+                          const int64_t *, const csa2_cache &, float *, cudaStream_t);
 int launch_norm_rope(const float *, int64_t, int, const float *, float, const int64_t *, float, float *, uint16_t *,
                      cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
@@ -265,6 +267,21 @@ int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots,
     if (!slots && n > num_slots) return CSA2_ERR_RANGE;
     if (!aligned(x, 16) || !aligned(codes, 4)) return CSA2_ERR_ALIGN;
     return launch_quant_fp8(x, n, dim, slots, codes, scales, num_slots, status, (cudaStream_t)stream);
+}
+
+int csa2_append_entries(const csa2_cache *cache, const uint16_t *C, const uint16_t *Z, const float *bias, int32_t m,
+                        int64_t n_tok, const float *ik, const int64_t *slots, float *entries, csa2_stream_t stream)
+{
+    if (m < 1 || m > 16 || n_tok < 0) return CSA2_ERR_SHAPE;
+    const int64_t n_ent = n_tok / m;
+    if (n_ent > INT32_MAX) return CSA2_ERR_SHAPE;
+    if (n_ent == 0) return CSA2_OK;
+    int s = check_cache(cache, true, true);
+    if (s) return s;
+    if (!C || !Z || !bias || !ik) return CSA2_ERR_NULL;
+    if (!slots && n_ent > cache->num_slots) return CSA2_ERR_RANGE;
+    if (!aligned(ik, 16) || (entries && !aligned(entries, 4))) return CSA2_ERR_ALIGN;
+    return launch_append_entries(C, Z, bias, m, n_tok, ik, slots, *cache, entries, (cudaStream_t)stream);
 }
 
 int csa2_norm_rope(const float *x, int64_t rows, int32_t vecs, const float *gamma, float eps, const int64_t *pos,

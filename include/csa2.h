@@ -282,6 +282,24 @@ CSA2_API int csa2_quant_fp4_e4m3(const float *x, int64_t n, const int64_t *slots
 CSA2_API int csa2_quant_fp8(const float *x, int64_t n, int32_t dim, const int64_t *slots, uint8_t *codes,
                    float *scales, int64_t num_slots, int32_t *status, csa2_stream_t stream);
 
+/* ---- a step's new entries into the cache, in one launch ------------------
+ * The compressor, the main-KV quantiser of cache->kv_format and the FP8
+ * quantiser of the indexer keys for the n_tok / m entries that n_tok new
+ * tokens make ([P3] §3.1, [P2] §3.2 and §4): the same results, bit for bit,
+ * as csa2_compress, then csa2_quant_mxfp4 (or csa2_quant_fp4_e4m3) of its
+ * output and csa2_quant_fp8 (dim 128) of ik, each at the entry's slot.
+ *   cache    kv_codes, kv_scales, ik_codes, ik_scales, num_slots, kv_format
+ *            and status as for csa2_layer (block_table unused but checked)
+ *   C, Z     bf16 [n_tok][512];  bias fp32 [m][512];  1 <= m <= 16
+ *   ik       fp32 [n_tok / m][128], 16-byte aligned: each entry's indexer key
+ *   slots    int64 [n_tok / m]: a negative slot skips the entry; a slot >=
+ *            num_slots is skipped and flagged CSA2_DEV_BAD_SLOT; NULL: entry
+ *            i -> slot i (CSA2_ERR_RANGE if that overruns the cache)
+ *   entries  fp32 [n_tok / m][512] copy of the compressed entries, or NULL */
+CSA2_API int csa2_append_entries(const csa2_cache *cache, const uint16_t *C, const uint16_t *Z,
+                                 const float *bias, int32_t m, int64_t n_tok, const float *ik,
+                                 const int64_t *slots, float *entries, csa2_stream_t stream);
+
 /* ---- RMSNorm and forward partial RoPE of the attention inputs ------------
  * [P3] §4.3: queries and compressed KV are RMS-normalised before the core
  * attention, and RoPE acts on the last 64 of the 512 dims only (the output is

@@ -119,6 +119,25 @@ def test_workspace_sizes(lib):
     assert lib.csa2_layer_workspace_size(5, ctypes.byref(b)) == 0
 
 
+def test_append_entries_validated_on_the_host(lib):
+    """csa2_append_entries refuses a missing cache or input, a bad group size,
+    an unmapped overrun of the cache and a misaligned key array before any
+    launch, and does nothing for fewer tokens than one group (fake pointers,
+    never dereferenced)."""
+    from compressed_sparse_attention_layer_gb300 import csa2
+    P = ctypes.c_void_p(1 << 12)
+    cache = ctypes.byref(csa2.Cache(P, P, P, P, 64, P, 1, 0, None))
+    f = lib.csa2_append_entries
+    assert f(None, P, P, P, 1, 8, P, None, None, None) == -1               # no cache
+    assert f(cache, P, P, P, 0, 8, P, None, None, None) == -2              # m = 0
+    assert f(cache, P, P, P, 17, 40, P, None, None, None) == -2            # m > 16
+    assert f(cache, P, P, P, 4, 3, P, None, None, None) == 0               # no whole group: nothing to do
+    assert f(cache, None, P, P, 1, 8, P, None, None, None) == -1           # no C
+    assert f(cache, P, P, P, 1, 8, None, None, None, None) == -1           # no indexer keys
+    assert f(cache, P, P, P, 1, 65, P, None, None, None) == -4             # 65 entries, 64 slots, no slot map
+    assert f(cache, P, P, P, 1, 8, ctypes.c_void_p((1 << 12) + 4), None, None, None) == -8
+
+
 def test_norm_rope_validated_on_the_host(lib):
     """csa2_norm_rope refuses bad shapes, missing or doubled outputs and
     misaligned pointers before any launch (fake pointers, never dereferenced)."""

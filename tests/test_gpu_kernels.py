@@ -132,6 +132,57 @@ def test_compress_matches_oracle(m):
     assert np.allclose(got, want, rtol=2e-7, atol=0)
 
 
+@pytest.mark.parametrize("kv_format,m", [(0, 1), (0, 4), (1, 2)])
+def test_append_entries_matches_the_separate_calls(kv_format, m):
+    """csa2_append_entries: the compressor, the main-KV quantiser of the cache's
+    format and the indexer key's FP8 quantiser in one launch, bit for bit the
+    results of csa2_compress + csa2_quant_mxfp4 / _fp4_e4m3 + csa2_quant_fp8 at
+    scattered slots (one skipped, one past the cache and flagged), and the
+    quantised codes equal to the oracle's of the entries it returns."""
+    n_ent = 300
+    n_tok = n_ent * m + (m - 1)                    # a trailing partial group is not compressed
+    C = synth.normal_bf16(synth.stream_id(51, 1, m), 0, n_tok * 512).reshape(n_tok, 512)
+    Z = synth.normal_bf16(synth.stream_id(51, 2, m), 0, n_tok * 512).reshape(n_tok, 512)
+    bias = synth.normal_f32(synth.stream_id(51, 3, m), 0, m * 512, sigma=0.1).reshape(m, 512)
+    ik = _special_rows(n_ent, 128, 9 + m)
+    bt = torch.zeros((1, 8), dtype=torch.int32)
+    caches = [csa2.PagedCache(8, bt, "cuda", kv_format=kv_format) for _ in range(2)]
+    S = caches[0].num_slots
+    slots = np.random.default_rng(12 + m).permutation(S)[:n_ent].astype(np.int64)
+    slots[5] = -1
+    slots[6] = S + 3
+    t = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+    Cd, Zd, bd, ikd = t(C), t(Z), torch.from_numpy(bias).cuda(), torch.from_numpy(ik).cuda()
+    sd = torch.from_numpy(slots).cuda()
+    entries = torch.full((n_ent, 512), float("nan"), dtype=torch.float32, device="cuda")
+    csa2.csa2_append_entries(caches[0].struct(), Cd, Zd, bd, m, ikd, slots=sd, entries=entries)
+    ref = caches[1]
+    e = torch.empty((n_ent, 512), dtype=torch.float32, device="cuda")
+    csa2.csa2_compress(Cd, Zd, bd, m, e)
+    quant = csa2.csa2_quant_fp4_e4m3 if kv_format == csa2.KV_FP4_E4M3 else csa2.csa2_quant_mxfp4
+    quant(e, ref.kv_codes, ref.kv_scales, slots=sd, status=ref.status)
+    csa2.csa2_quant_fp8(ikd, ref.ik_codes, ref.ik_scales, slots=sd, status=ref.status)
+    torch.cuda.synchronize()
+    got, want = caches[0], ref
+    assert np.array_equal(entries.cpu().numpy().view(np.uint32), e.cpu().numpy().view(np.uint32))
+    for name in ("kv_codes", "kv_scales", "ik_codes"):
+        assert torch.equal(getattr(got, name), getattr(want, name)), name
+    assert torch.equal(got.ik_scales.view(torch.int32), want.ik_scales.view(torch.int32))
+    assert int(got.status[0]) == csa2.DEV_BAD_SLOT == int(want.status[0])
+    # against the oracle: the codes at the written slots
+    keep = (slots >= 0) & (slots < S)
+    oq = oracle.quant_fp4_e4m3 if kv_format == csa2.KV_FP4_E4M3 else oracle.quant_mxfp4
+    codes, scales = oq(entries.cpu().numpy())
+    assert np.array_equal(got.kv_codes.cpu().numpy()[slots[keep]], codes[keep])
+    assert np.array_equal(got.kv_scales.cpu().numpy()[slots[keep]], scales[keep])
+    icodes, iscales = oracle.quant_fp8(ik)
+    assert np.array_equal(got.ik_codes.cpu().numpy()[slots[keep]], icodes[keep])
+    assert np.array_equal(got.ik_scales.cpu().numpy()[slots[keep]].view(np.uint32), iscales[keep].view(np.uint32))
+    # untouched slots keep their contents
+    untouched = np.setdiff1d(np.arange(S), slots[keep])
+    assert not got.kv_codes.cpu().numpy()[untouched].any()
+
+
 def _dw(wl, **kw):
     return DeviceWorkload(wl, **kw)
 
