@@ -185,7 +185,7 @@ class DecodeStep:
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 1 + sum({"full": 4, "reindex": 3, "reuse": 1}[m] for m in wl.layers) + \
+        self.launches = 1 + sum({"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
             (len(wl.layers) if Q > 1 else 0)
         # the step's host-fed inputs (new tokens, every layer's queries and window
         # rows) and its outputs (every layer's o and lse) in two device buffers

@@ -46,7 +46,7 @@ class Swa(ctypes.Structure):
 class LayerIO(ctypes.Structure):
     _fields_ = [("q", _vp), ("qi", _vp), ("w", _vp), ("swa", Swa), ("sm_scale", _f32), ("flags", _i32),
                 ("idx", _vp), ("pool", _vp), ("pool_len", _vp), ("o", _vp), ("lse", _vp),
-                ("prof_begin", _vp), ("prof_end", _vp), ("kv_tiles", _vp)]
+                ("prof_begin", _vp), ("prof_end", _vp)]
 
 
 EXPORTS = {
@@ -69,7 +69,6 @@ EXPORTS = {
     "csa2_layer": (ctypes.c_int, [_i32, ctypes.POINTER(Cache), ctypes.POINTER(Batch), ctypes.POINTER(LayerIO),
                                   _vp, _sz, _vp]),
     "csa2_layer_workspace_size": (_sz, [_i32, ctypes.POINTER(Batch)]),
-    "csa2_layer_kv_tiles_size": (_sz, [ctypes.POINTER(Batch)]),
     "csa2_layer_noalloc": (ctypes.c_int, [_i32, ctypes.POINTER(Cache), ctypes.POINTER(Batch),
                                           ctypes.POINTER(LayerIO), _vp]),
     "csa2_debug_set_wait_limit": (ctypes.c_int, [ctypes.c_uint32]),
@@ -169,7 +168,6 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
 ATTN_DEDUP_WINDOW = 1
 LAYER_SCORES_BF16 = 1      # csa2_layer_io.flags: selection on bf16-rounded index scores
 ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
-ATTN_EARLY_TILES = 4       # REUSE layers: carried key tiles copied while the previous layer finishes
 
 
 def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None, sink=None,
@@ -177,7 +175,7 @@ def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=N
     """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
     into the ring by the attention call itself; sink: optional fp32 [64] per-head
     sink logits; rope_base > 0 rotates the output's RoPE dims back by the query
-    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS | ATTN_EARLY_TILES."""
+    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
                int(flags), _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"),
                _ptr(sink, torch.float32, "sink"), float(rope_base), 0)
@@ -289,21 +287,14 @@ def csa2_layer_workspace_size(mode: int, batch: Batch) -> int:
     return int(load().csa2_layer_workspace_size(mode, ctypes.byref(batch)))
 
 
-def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None,
-             flags: int = 0, kv_tiles=None) -> LayerIO:
+def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None, flags: int = 0) -> LayerIO:
     """prof: optional (begin, end) pair of recorded torch.cuda.Event(enable_timing=True).
-    flags: LAYER_SCORES_BF16 or 0.
-    kv_tiles: optional uint8 buffer of csa2_layer_kv_tiles_size bytes: the selection's
-    dequantised entries, written by Full / Reindex layers and read by the Reuse layers after them."""
+    flags: LAYER_SCORES_BF16 or 0."""
     pb, pe = (prof[0].cuda_event, prof[1].cuda_event) if prof else (None, None)
     return LayerIO(_ptr(q, torch.bfloat16, "q"), _ptr(qi, torch.bfloat16, "qi"), _ptr(w, torch.float32, "w"),
                    swa, float(sm_scale), int(flags), _ptr(idx, torch.int32, "idx"), _ptr(pool, torch.int32, "pool"),
                    _ptr(pool_len, torch.int32, "pool_len"), _ptr(o, torch.float32, "o"),
-                   _ptr(lse, torch.float32, "lse"), pb, pe, _ptr(kv_tiles, torch.uint8, "kv tiles"))
-
-
-def csa2_layer_kv_tiles_size(batch: Batch) -> int:
-    return int(load().csa2_layer_kv_tiles_size(ctypes.byref(batch)))
+                   _ptr(lse, torch.float32, "lse"), pb, pe)
 
 
 def csa2_layer(mode: int, cache: Cache, batch: Batch, io: LayerIO, workspace, stream=None):

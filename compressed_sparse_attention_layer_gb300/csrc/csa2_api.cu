@@ -98,9 +98,8 @@ int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
-                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool, uint8_t *, int);
+                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
 size_t attn_workspace_bytes(int64_t rows);
-size_t attn_tile_bytes(int64_t rows);
 int topk_max_k();
 int64_t topk_max_len();
 
@@ -134,7 +133,7 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
-    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS | CSA2_ATTN_EARLY_TILES)) return CSA2_ERR_UNSUPPORTED;
+    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS)) return CSA2_ERR_UNSUPPORTED;
     if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
     if (s->new_rows) {
         // the window of a query in a multi-token chunk holds other new tokens, which
@@ -385,13 +384,7 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
     if (!aligned(q, 16) || !aligned(o, 16)) return CSA2_ERR_ALIGN;
     return launch_attn(*cache, *batch, q, sm_scale, idx, k, *swa, o, lse, workspace, workspace_bytes,
-                       (cudaStream_t)stream, false, nullptr, 0);
-}
-
-size_t csa2_layer_kv_tiles_size(const csa2_batch *batch)
-{
-    if (!batch || batch->batch < 1 || batch->nq < 1) return 0;
-    return attn_tile_bytes((int64_t)batch->batch * batch->nq);
+                       (cudaStream_t)stream, false);
 }
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
@@ -412,7 +405,6 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
     if (io->flags & ~CSA2_LAYER_SCORES_BF16) return CSA2_ERR_UNSUPPORTED;
     const bool bf16 = (io->flags & CSA2_LAYER_SCORES_BF16) != 0;
-    if (io->kv_tiles && !aligned(io->kv_tiles, 16)) return CSA2_ERR_ALIGN;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (mode != CSA2_MODE_REUSE && !aligned(io->pool, 16)) return CSA2_ERR_ALIGN;
     if (!aligned(io->q, 16) || !aligned(io->o, 16)) return CSA2_ERR_ALIGN;
@@ -461,15 +453,10 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
             return s;
         if ((s = prof(io->prof_end))) return s;
     }
-    // REUSE keeps io->idx as it is; the attention for every mode
-    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call;
-    // carried key tiles are written by the selecting modes and read by REUSE (before the dependency
-    // wait with CSA2_ATTN_EARLY_TILES)
-    const bool reuse = mode == CSA2_MODE_REUSE;
-    const int tile_mode = !io->kv_tiles ? 0 : !reuse ? 1 : (io->swa.flags & CSA2_ATTN_EARLY_TILES) ? 3 : 2;
+    // REUSE keeps io->idx as it is; the attention for every mode.
+    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call
     return launch_attn(*cache, *batch, io->q, io->sm_scale, io->idx, CSA2_TOPK, io->swa, io->o, io->lse,
-                       ws.attn, ws.attn_bytes, st, reuse && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS), io->kv_tiles,
-                       tile_mode);
+                       ws.attn, ws.attn_bytes, st, mode == CSA2_MODE_REUSE && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS));
 }
 
 }  // extern "C"

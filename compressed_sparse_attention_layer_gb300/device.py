@@ -23,10 +23,7 @@ def _dev_normal_bf16(stream, start, count, dev, sigma=1.0):
 
 
 class DeviceWorkload:
-    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None, carry_kv_tiles=True):
-        """carry_kv_tiles: give the layers the carried dequantised entries of the selection
-        (written by Full / Reindex layers, read by the Reuse layers after them)."""
-        self.carry_kv_tiles = carry_kv_tiles
+    def __init__(self, wl: Workload, device="cuda", build_cache=True, layers=None):
         self.wl = wl
         self.dev = torch.device(device)
         self.rows = wl.batch * wl.nq
@@ -103,11 +100,6 @@ class DeviceWorkload:
         # Reuse layers load their keys while the previous layer finishes
         # (csa2.ATTN_EARLY_INPUTS): the layers are called one after the other
         self.early_inputs = True
-        # the selection's dequantised entries, carried from each Full / Reindex layer to
-        # the Reuse layers after it (528 KB per query row: decode-sized batches only)
-        self.kv_tiles = None
-        if self.carry_kv_tiles and "reuse" in wl.layers and R <= 256:
-            self.kv_tiles = torch.empty(csa2.csa2_layer_kv_tiles_size(self.batch), dtype=torch.uint8, device=dev)
         self.o = {l: torch.empty((R, 64, 512), dtype=torch.float32, device=dev) for l in self.layers}
         self.lse = {l: torch.empty((R, 64), dtype=torch.float32, device=dev) for l in self.layers}
         ws = max(csa2.csa2_layer_workspace_size(m, self.batch) for m in (0, 1, 2))
@@ -145,18 +137,11 @@ class DeviceWorkload:
         self.swa_codes[l] = codes
         self.swa_scales[l] = scales
 
-    def tiles_early(self, l) -> bool:
-        """Reuse layer l's carried tiles were written before the previous layer call
-        (the selecting layer is at least two layers back)."""
-        return self.wl.layers[l] == "reuse" and l >= 2 and self.wl.layers[l - 1] == "reuse"
-
     def swa(self, l, new_rows=None) -> csa2.Swa:
         opts = dict(self.attn_options)
         if self.early_inputs and self.wl.layers[l] == "reuse":
             # every layer call follows the previous one on the stream (run / run_layer in order)
             opts["flags"] = opts.get("flags", 0) | csa2.ATTN_EARLY_INPUTS
-            if self.kv_tiles is not None and self.tiles_early(l):
-                opts["flags"] |= csa2.ATTN_EARLY_TILES
         return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows, **opts)
 
     def swa_new_rows(self, l) -> torch.Tensor:
@@ -170,8 +155,7 @@ class DeviceWorkload:
         qi = self.qi.get(l, self.dummy_qi)
         w = self.w.get(l, self.dummy_w)
         return csa2.layer_io(self.q[l], qi, w, self.swa(l, new_rows), 1.0, self.idx, self.pool, self.pool_len,
-                             self.o[l], self.lse[l], prof=prof, flags=self.layer_flags,
-                             kv_tiles=self.kv_tiles)
+                             self.o[l], self.lse[l], prof=prof, flags=self.layer_flags)
 
     def run_layer(self, l, stream=None, prof=None, new_rows=None):
         """new_rows: optional window rows of the decode tokens, quantised into the

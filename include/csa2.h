@@ -178,12 +178,6 @@ typedef struct csa2_swa {
  * completed).  A decode stack that calls csa2_layer layer after layer, with
  * the window rows of its own tokens passed as new_rows, satisfies it. */
 #define CSA2_ATTN_EARLY_INPUTS 2
-/* csa2_swa.flags, honoured by csa2_layer in REUSE mode with io->kv_tiles: the
- * caller guarantees that the carried key tiles were written before the
- * previous call into this library on the stream (by an earlier FULL or REINDEX
- * call, not by the call just before this one), so they are bulk-copied while
- * the previous layer's last kernel is still running. */
-#define CSA2_ATTN_EARLY_TILES  4
 
 /* csa2_layer_io.flags: FULL and REINDEX layers keep the index scores in bf16
  * (each fp32 score rounded to nearest even) and select on them: the block
@@ -221,20 +215,6 @@ typedef struct csa2_layer_io {
                                     as an external node when captured; NULL
                                     for none                                   */
     void           *prof_end;    /* optional cudaEvent_t recorded just after it */
-    uint8_t        *kv_tiles;    /* optional carried state of
-                                    csa2_layer_kv_tiles_size(batch) bytes,
-                                    16-byte aligned: the dequantised (bf16)
-                                    main-KV entries of the selection and their
-                                    validity, in the attention kernel's own
-                                    layout.  FULL and REINDEX write them for the
-                                    indices they select; REUSE reads them in
-                                    place of the cache, so a REUSE call given
-                                    kv_tiles must follow (on the same stream)
-                                    the FULL or REINDEX call that selected
-                                    io->idx with the same batch and cache, with
-                                    no other selecting call in between.  NULL:
-                                    every call gathers and dequantises the
-                                    entries itself.  Contents are opaque.       */
 } csa2_layer_io;
 
 /* ---- compressor ----------------------------------------------------------
@@ -419,13 +399,6 @@ CSA2_API size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq);
 CSA2_API int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch,
                const csa2_layer_io *io, void *workspace, size_t workspace_bytes,
                csa2_stream_t stream);
-
-/* Bytes of csa2_layer_io.kv_tiles for this batch: 528,384 per query row (the
- * 512 selected entries as bf16 dims plus their validity); 0 for an invalid
- * batch.  The Reuse layers of a decoder group attend to the same entries as
- * the layer that selected them ([P2] §3 mode table), so they can take them
- * dequantised. */
-CSA2_API size_t csa2_layer_kv_tiles_size(const csa2_batch *batch);
 
 /* The workspace a csa2_layer call of this mode needs; 0 for invalid arguments. */
 CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch);

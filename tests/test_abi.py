@@ -94,13 +94,13 @@ def test_layer_option_flags_validated_on_the_host(lib):
     batch = csa2.Batch(1, 1, 1, 0, 1000, P, P)
     def io(layer_flags=0, swa_flags=0):
         s = csa2.Swa(P, P, 128, swa_flags, None, None, None, 0.0, 0)
-        return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None, None)
-    for bad in (io(layer_flags=2), io(layer_flags=1 << 30), io(swa_flags=8)):
+        return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None)
+    for bad in (io(layer_flags=2), io(layer_flags=1 << 30), io(swa_flags=4)):
         assert lib.csa2_layer(csa2.MODES["full"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(bad),
                               P, 1 << 30, None) == -3
     # a negative RoPE base is a shape error
     s = csa2.Swa(P, P, 128, 0, None, None, None, -1.0, 0)
-    neg = csa2.LayerIO(P, P, P, s, 1.0, 0, P, P, P, P, P, None, None, None)
+    neg = csa2.LayerIO(P, P, P, s, 1.0, 0, P, P, P, P, P, None, None)
     assert lib.csa2_layer(csa2.MODES["reuse"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(neg),
                           P, 1 << 30, None) == -2
 

@@ -231,30 +231,6 @@ def test_window_row_quantised_inside_the_attention_call():
         assert torch.equal(fused.lse[l].view(torch.int32), ref.lse[l].view(torch.int32)), l
 
 
-def test_carried_kv_tiles_bit_identical():
-    """Reuse layers that take the selection's dequantised entries from the
-    carried tiles (csa2_layer_io.kv_tiles, written by the Full / Reindex layer
-    before them; copied before the dependency wait from the second Reuse layer
-    of a group on) give the same indices, o and lse, bit for bit, as layers
-    that gather and dequantise the entries themselves, and stay at parity."""
-    wl = W.Workload("kv_tiles", 79, 3, [20000, 3000, 70000], 1,
-                    ["full", "reuse", "reuse", "reuse", "reindex", "reuse", "reuse"], planted_blocks=4)
-    a = DeviceWorkload(wl)                         # carried tiles
-    b = DeviceWorkload(wl, carry_kv_tiles=False)
-    assert a.kv_tiles is not None and b.kv_tiles is None
-    for dw in (a, b):
-        for l in dw.layers:
-            dw.run_layer(l, new_rows=dw.swa_new_rows(l))
-        torch.cuda.synchronize()
-        assert int(dw.cache.status[0]) == 0
-    for l in range(len(wl.layers)):
-        assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
-        assert torch.equal(a.lse[l].view(torch.int32), b.lse[l].view(torch.int32)), l
-    _run_recording(a)
-    for bb in range(wl.batch):
-        _check_sequence(a, bb)
-
-
 def test_layers_with_fp4_e4m3_main_kv():
     """The main KV in the 16-element / E4M3-scale FP4 format (csa2_cache.kv_format
     = CSA2_KV_FP4_E4M3): selection and attention against the oracle, which
