@@ -562,7 +562,7 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-KERNEL_VERSION = "f8-cpasync-scan-v5"
+KERNEL_VERSION = "f8-cpasync-scan-v6"
 NORM_ROPE_VERSION = "norm-rope-int-turns-v1"   # the prologue kernel whose ncu traffic profiles/ records
 
 

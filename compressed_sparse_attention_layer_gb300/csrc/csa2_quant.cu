@@ -20,6 +20,9 @@ __device__ __forceinline__ float compress_channel(const uint16_t *__restrict__ C
                                                   const float *__restrict__ bias, int m, int64_t j, int d)
 {
     const int64_t base = j * m * CSA2_HEAD_DIM + d;
+    // one token: its weight is exp(0) / exp(0) = 1 exactly, so the entry is C
+    // (the general path below gives the same bits, through FP64 exp)
+    if (m == 1) return bf16_to_f32(C[base]);
     double zmax = -INFINITY;
     for (int k = 0; k < m; k++) {
         double z = (double)bf16_to_f32(Z[base + (int64_t)k * CSA2_HEAD_DIM]) + (double)bias[k * CSA2_HEAD_DIM + d];
