@@ -188,12 +188,13 @@ class DecodeStep:
         self.launches = 1 + sum({"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
             (len(wl.layers) if Q > 1 else 0)
         # the step's host-fed inputs (new tokens, every layer's queries and window
-        # rows) and its outputs (every layer's o and lse) in two device buffers
-        # each -- the first layer's inputs / the rest, the first half of the
-        # layers' outputs / the rest -- so that the end-to-end leg copies in
-        # while the first layer runs and copies out while the second half runs
+        # rows) in two device buffers -- the first layer's / the rest -- and its
+        # outputs (every layer's o and lse) in one buffer per group of
+        # OUT_GROUP layers, so that the end-to-end leg copies the inputs in while
+        # the first layer runs and each group's outputs out while the later
+        # layers run
         layers = list(dw.layers)
-        self.half = max(1, len(layers) // 2)
+        self.out_groups = [list(range(g, min(g + OUT_GROUP, len(layers)))) for g in range(0, len(layers), OUT_GROUP)]
         ins0 = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
         ins1 = []
         for i, l in enumerate(layers):
@@ -201,8 +202,7 @@ class DecodeStep:
             (ins0 if i == 0 else ins1).extend(refs)
         self.in_dev = [self._gather(ins0)] + ([self._gather(ins1)] if ins1 else [])
         outs = [[(dw.o, l), (dw.lse, l)] for l in layers]
-        self.out_dev = [self._gather(sum(outs[:self.half], []))] + \
-            ([self._gather(sum(outs[self.half:], []))] if len(layers) > self.half else [])
+        self.out_dev = [self._gather(sum([outs[i] for i in g], [])) for g in self.out_groups]
 
     def _gather(self, refs):
         """One device byte buffer holding the tensors refs name (container, key),
@@ -229,11 +229,12 @@ class DecodeStep:
     def enqueue_e2e(self, host_in, host_out, s2, s3):
         """The step with its copies, for capture on the current stream: the first
         layer's inputs first, the other layers' on s2 while the first layer runs;
-        the first half of the outputs on s3 while the second half of the layers
-        runs, the rest at the end."""
-        torch, dw, csa2, cache = self.torch, self.dw, self.csa2, self.dw.cache
+        each group of layers' outputs on s3 once its last layer has run, the last
+        group's at the end."""
+        torch, dw, csa2 = self.torch, self.dw, self.csa2
         s = torch.cuda.current_stream()
-        ev_in, ev_mid = torch.cuda.Event(), torch.cuda.Event()
+        ev_in = torch.cuda.Event()
+        ev_out = [torch.cuda.Event() for _ in self.out_groups]
         if len(self.in_dev) > 1:
             s2.wait_stream(s)
             with torch.cuda.stream(s2):
@@ -243,15 +244,17 @@ class DecodeStep:
         csa2.csa2_append_entries(self.dw.cstruct, self.C_new, self.Z_new, self.bias, self.wl.m, self.ik_new,
                                  slots=self.new_slots)
         layers = list(dw.layers)
+        last = {g[-1]: gi for gi, g in enumerate(self.out_groups)}
         for i, l in enumerate(layers):
             if i == 1:
                 s.wait_event(ev_in)
             self.enqueue_layers([l])
-            if i == self.half - 1 and len(self.out_dev) > 1:
-                ev_mid.record(s)
-                s3.wait_event(ev_mid)
+            gi = last.get(i)
+            if gi is not None and gi < len(self.out_groups) - 1:
+                ev_out[gi].record(s)
+                s3.wait_event(ev_out[gi])
                 with torch.cuda.stream(s3):
-                    host_out[0].copy_(self.out_dev[0], non_blocking=True)
+                    host_out[gi].copy_(self.out_dev[gi], non_blocking=True)
         host_out[-1].copy_(self.out_dev[-1], non_blocking=True)
         if len(self.in_dev) > 1:
             s.wait_stream(s2)
@@ -283,6 +286,7 @@ class DecodeStep:
 
 # ---------------------------------------------------------------- algorithmic work
 KV_SCALE_BYTES = {0: 16, 1: 32}     # main-KV block-scale bytes per entry: MXFP4, FP4 with E4M3 per 16
+OUT_GROUP = 2                       # e2e: layers whose outputs go back to the host in one copy
 POOL_MAX = 16384                    # candidate pool: 2,048 blocks of 8
 
 

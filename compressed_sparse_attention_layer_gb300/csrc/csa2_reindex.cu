@@ -72,6 +72,11 @@ struct RsSmem {
     int warp_sums[RX_SEL_THREADS / 32];
     uint32_t digit;
     int above;
+    int bincnt;                                    // candidates in the crossing bin
+    int ncand;                                     // of them gathered into cand (at most 32)
+    uint32_t cand[32];
+    uint32_t tval;                                 // the k-th largest offset, once ranked by one warp
+    int tneed;
 };
 
 // Scales copied for the entries of a block that is not read: they score -inf
@@ -410,6 +415,8 @@ __global__ void __launch_bounds__(RX_SEL_THREADS, 1)
                 if (acc + (int)cb[j] >= kk) {
                     S.digit = (uint32_t)(RX_BINS - 1 - (BPT * tid + j));
                     S.above = acc;
+                    S.bincnt = (int)cb[j];
+                    S.ncand = 0;
                     break;
                 }
                 acc += (int)cb[j];
@@ -421,6 +428,33 @@ __global__ void __launch_bounds__(RX_SEL_THREADS, 1)
         kk -= S.above;
         top = shift;
         cur ^= 1;
+        if (top > 0 && S.bincnt <= 32) {
+            // a crossing bin of at most 32 keys: one warp ranks them instead of
+            // further rounds (the kk-th largest of the bin, and how many equal
+            // to it are taken)
+#pragma unroll
+            for (int j = 0; j < RX_KPT; j++)
+                if (((valid >> j) & 1u) && (rk[j] & mask) == prefix) S.cand[atomicAdd(&S.ncand, 1)] = rk[j];
+            __syncthreads();
+            if (warp == 0) {
+                const int nc = S.ncand;
+                const uint32_t v = lane < nc ? S.cand[lane] : 0u;
+                int gt = 0, eq = 0;
+                for (int u = 0; u < nc; u++) {
+                    const uint32_t w2 = __shfl_sync(0xffffffffu, v, u);
+                    gt += w2 > v;
+                    eq += w2 == v;
+                }
+                if (lane < nc && gt < kk && gt + eq >= kk) {   // lanes holding the same value agree
+                    S.tval = v;
+                    S.tneed = kk - gt;
+                }
+            }
+            __syncthreads();
+            prefix = S.tval;
+            kk = S.tneed;
+            break;
+        }
     }
     const uint32_t T = prefix;                     // the k-th largest offset
     const int need_eq = kk;                        // of the offsets equal to T, the first need_eq
