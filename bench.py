@@ -48,6 +48,8 @@ def parse():
                         "norm_rope times the input prologue alone (RMSNorm + RoPE of a prefill chunk's queries)")
     p.add_argument("--bf16-scores", action="store_true",
                    help="Full and Reindex layers select on bf16-rounded index scores (csa2.LAYER_SCORES_BF16)")
+    p.add_argument("--e4m3-query", action="store_true",
+                   help="the Full layer's scan with one e4m3 query part per head (csa2.LAYER_INDEX_E4M3_QUERY)")
     p.add_argument("--queries", type=int, default=1,
                    help="query tokens per sequence per step (>1: a multi-token decode step, e.g. draft "
                         "tokens verified together; the Full layer's scan serves them from one read)")
@@ -343,7 +345,9 @@ def run_native(args):
                       workload=args.workload)
     B, N, Q = step.wl.batch, step.wl.tokens[0], step.queries
     if args.bf16_scores:
-        step.dw.layer_flags = csa2.LAYER_SCORES_BF16
+        step.dw.layer_flags |= csa2.LAYER_SCORES_BF16
+    if args.e4m3_query:
+        step.dw.layer_flags |= csa2.LAYER_INDEX_E4M3_QUERY
 
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
@@ -539,9 +543,9 @@ def run_native(args):
                  f"m={wl.m}, {len(wl.layers)} layers {'/'.join(sorted(set(wl.layers)))}, Top-512, SWA 128")
     inputs_bytes = sum(wl.entries(b) for b in range(B)) * 132
 
-    metric = METRIC if args.workload == "decode_1m" and Q == 1 and not args.bf16_scores else \
-        f"CSA2 query-tokens/s, {args.workload}" + (f", {Q} query tokens per sequence" if Q > 1 else "") + \
-        (", bf16 index scores" if args.bf16_scores else "")
+    metric = METRIC if args.workload == "decode_1m" and Q == 1 and not args.bf16_scores and not args.e4m3_query \
+        else f"CSA2 query-tokens/s, {args.workload}" + (f", {Q} query tokens per sequence" if Q > 1 else "") + \
+        (", bf16 index scores" if args.bf16_scores else "") + (", one-part e4m3 index query" if args.e4m3_query else "")
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -557,7 +561,8 @@ def run_native(args):
                          (f"L2 flushed (512 MB write) before every timed step; the step's indexer keys are "
                           f"{inputs_bytes / 1e6:.1f} MB"),
                    "graph": "one CUDA graph per step",
-                   "index_scores": "bf16 (selection on rounded scores)" if args.bf16_scores else "fp32"},
+                   "index_scores": "bf16 (selection on rounded scores)" if args.bf16_scores else "fp32",
+                   "index_query": "one e4m3 part per head" if args.e4m3_query else "two e4m3 parts (hi + lo)"},
         "roofline": roofline, "per_layer_mode": per_mode, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
         "cpu_baseline": cpu,
     }

@@ -167,6 +167,7 @@ def batch_struct(n_entries: torch.Tensor, q_pos: torch.Tensor, nq: int, m: int, 
 
 ATTN_DEDUP_WINDOW = 1
 LAYER_SCORES_BF16 = 1      # csa2_layer_io.flags: selection on bf16-rounded index scores
+LAYER_INDEX_E4M3_QUERY = 2  # csa2_layer_io.flags: the Full scan's query as one e4m3 part per head
 ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
 
 
@@ -289,7 +290,7 @@ def csa2_layer_workspace_size(mode: int, batch: Batch) -> int:
 
 def layer_io(q, qi, w, swa: Swa, sm_scale, idx, pool, pool_len, o, lse, prof=None, flags: int = 0) -> LayerIO:
     """prof: optional (begin, end) pair of recorded torch.cuda.Event(enable_timing=True).
-    flags: LAYER_SCORES_BF16 or 0."""
+    flags: LAYER_SCORES_BF16 | LAYER_INDEX_E4M3_QUERY or 0."""
     pb, pe = (prof[0].cuda_event, prof[1].cuda_event) if prof else (None, None)
     return LayerIO(_ptr(q, torch.bfloat16, "q"), _ptr(qi, torch.bfloat16, "qi"), _ptr(w, torch.float32, "w"),
                    swa, float(sm_scale), int(flags), _ptr(idx, torch.int32, "idx"), _ptr(pool, torch.int32, "pool"),

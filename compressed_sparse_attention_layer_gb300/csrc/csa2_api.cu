@@ -83,7 +83,8 @@ int launch_append_entries(const uint16_t *, const uint16_t *, const float *, int
 int launch_norm_rope(const float *, int64_t, int, const float *, float, const int64_t *, float, float *, uint16_t *,
                      cudaStream_t);
 int launch_index_scan(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, float *,
-                      float *, int32_t *, int64_t, cudaStream_t, bool bf16_scores = false);
+                      float *, int32_t *, int64_t, cudaStream_t, bool bf16_scores = false,
+                      bool one_part_query = false);
 int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, const int32_t *, int64_t, uint8_t *,
                        float *, cudaStream_t);
 int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const uint16_t *, const float *,
@@ -403,7 +404,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
     if ((s = check_swa(&io->swa, batch))) return s;
     if (!io->q || !io->idx || !io->o || !io->lse) return CSA2_ERR_NULL;
     if (mode != CSA2_MODE_REUSE && (!io->qi || !io->w || !io->pool || !io->pool_len)) return CSA2_ERR_NULL;
-    if (io->flags & ~CSA2_LAYER_SCORES_BF16) return CSA2_ERR_UNSUPPORTED;
+    if (io->flags & ~(CSA2_LAYER_SCORES_BF16 | CSA2_LAYER_INDEX_E4M3_QUERY)) return CSA2_ERR_UNSUPPORTED;
     const bool bf16 = (io->flags & CSA2_LAYER_SCORES_BF16) != 0;
     if (mode == CSA2_MODE_FULL && score_ld(batch) / 8 > topk_max_len()) return CSA2_ERR_SHAPE;
     if (mode != CSA2_MODE_REUSE && !aligned(io->pool, 16)) return CSA2_ERR_ALIGN;
@@ -433,7 +434,7 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
         // scores of every visible entry and the per-block maxima
         if ((s = prof(io->prof_begin))) return s;
         if ((s = launch_index_scan(*cache, *batch, io->qi, io->w, ws.scores, ws.block_max, ws.n_visible, ld, st,
-                                   bf16)))
+                                   bf16, (io->flags & CSA2_LAYER_INDEX_E4M3_QUERY) != 0)))
             return s;
         if ((s = prof(io->prof_end))) return s;
         // the best 2,048 blocks of 8 -> candidate pool

@@ -60,28 +60,33 @@ constexpr int F8_THREADS = 448;
 constexpr int F8_PERSIST_ROWS = 256;       // query groups of the persistent grid
 constexpr uint32_t F8_TMEM_COLS = 512;
 
-template <int QG>
+// QP: parts of each query operand -- 2: hi and lo (the query to about 8
+// significant bits, the parity path); 1: hi only (4 significant bits, the
+// CSA2_LAYER_INDEX_E4M3_QUERY option: one column per head, half the MMA
+// work of the accumulated case).
+template <int QG, int QP = 2>
 struct F8Cfg {
     static constexpr int STAGES = QG == 1 ? 6 : (QG == 2 ? 5 : 4);    // 32 KB of codes per stage
     // hi and lo query parts: stacked along N (one MMA per K step, the epilogue
     // adds the two columns; the fewest MMA instructions) while two tile slots of
     // 2 x 64 QG columns fit in tensor memory, else accumulated into the same
     // columns by two MMAs per K step (half the epilogue's reads)
-    static constexpr bool STACKED = QG <= 2;
+    static constexpr bool STACKED = QP == 2 && QG <= 2;
     static constexpr int N = (STACKED ? 64 : 32) * QG;                // MMA N
-    static constexpr int PARTS = STACKED ? 1 : 2;                     // MMAs per K step and half
+    static constexpr int PARTS = STACKED ? 1 : QP;                    // MMAs per K step and half
     static constexpr int SLOT_COLS = 2 * N;                           // accumulator of a tile (two halves)
     static constexpr int SLOTS = (int)F8_TMEM_COLS / SLOT_COLS;       // 4, 2, 2: even, so that each slot
     static constexpr int ISSUERS = 2;                                 // belongs to one issuer (tile parity)
     static constexpr int WRITERS = QG >= 2 ? 2 : 1;                   // query-operand warps
     static constexpr uint32_t IDESC = tc::idesc_e4m3(128, N);
     static_assert(QG == 1 || QG == 2 || QG == 4, "1, 2 or 4 queries per group");
+    static_assert(QP == 1 || QP == 2, "one or two query parts");
     static_assert(SLOTS >= 2 && SLOTS % 2 == 0, "an even number of tile slots");
 };
 
-template <int QG>
+template <int QG, int QP>
 struct F8Smem {
-    static constexpr int ST = F8Cfg<QG>::STAGES, SL = F8Cfg<QG>::SLOTS;
+    static constexpr int ST = F8Cfg<QG, QP>::STAGES, SL = F8Cfg<QG, QP>::SLOTS;
     uint8_t a[ST][F8_TILE * 128];          // e4m3 keys, 128-byte swizzle (cp.async); rows 128 h .. of half h
     uint8_t b[2][QG * 64 * 128];           // per segment parity: the hi and lo rows of every query
     float sc[ST][F8_TILE];                 // fp32 scales of the stage's entries (cp.async)
@@ -144,7 +149,7 @@ __device__ __forceinline__ int64_t f8_group(const csa2_batch &bt, const int32_t 
 // `polls` bounds each pipeline wait: when one runs out the CTA sets its abort
 // flag and CSA2_DEV_TIMEOUT, every role leaves its loop, and the teardown
 // awaits the CTA's own copies and last MMA commit before freeing memory.
-template <bool PERSIST, bool DENSE, int QG>
+template <bool PERSIST, bool DENSE, int QG, int QP>
 __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_batch bt,
                                                             const uint16_t *__restrict__ qi,
                                                             const float *__restrict__ w,
@@ -154,11 +159,12 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                                                             int32_t *__restrict__ n_visible, int64_t ld,
                                                             int bf16_scores, uint32_t polls)
 {
-    using Cfg = F8Cfg<QG>;
+    using Cfg = F8Cfg<QG, QP>;
     constexpr int ST = Cfg::STAGES, SL = Cfg::SLOTS, N = Cfg::N;
     static_assert(!DENSE || QG == 1, "a dense pool copy has one query per row");
     extern __shared__ uint8_t smem_raw[];
-    F8Smem<QG> &S = *reinterpret_cast<F8Smem<QG> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    F8Smem<QG, QP> &S = *reinterpret_cast<F8Smem<QG, QP> *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    static_assert(F8Smem<QG, QP>::SL == SL && F8Smem<QG, QP>::ST == ST, "the barriers match the pipeline");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rows = bt.batch * bt.nq;
     const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
@@ -438,9 +444,19 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
                         }
                         res[q] = (part[0] + part[1]) + (part[2] + part[3]);
                     }
+                } else if constexpr (QG == 1) {
+                    // one column per head (one query part)
+                    uint32_t d0[32];
+                    tc::tmem_ld32(ta, d0);
+                    tc::tmem_ld_wait();
+                    const float *w0 = S.wq[seg & 1][0];
+                    float p0[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int j = 0; j < 32; j++) p0[j & 3] = fmaf(w0[j], fmaxf(__uint_as_float(d0[j]), 0.0f), p0[j & 3]);
+                    res[0] = (p0[0] + p0[1]) + (p0[2] + p0[3]);
                 } else {
-                    // one column per head (hi . k + lo . k); two queries' columns in
-                    // flight per tensor-memory wait
+                    // one column per head (hi . k + lo . k, or hi . k alone); two queries'
+                    // columns in flight per tensor-memory wait
 #pragma unroll
                     for (int q = 0; q < QG; q += 2) {
                         uint32_t d0[32], d1[32];
@@ -508,17 +524,17 @@ __global__ void __launch_bounds__(F8_THREADS, 1) k_index_f8(csa2_cache c, csa2_b
 }
 
 // ---------------------------------------------------------------- host side
-template <bool DENSE, int QG>
+template <bool DENSE, int QG, int QP>
 static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                        const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
                        cudaStream_t st, bool bf16, int sms)
 {
     const int groups = bt.batch * ((bt.nq + QG - 1) / QG);
-    const size_t smem = sizeof(F8Smem<QG>) + 1024;
+    const size_t smem = sizeof(F8Smem<QG, QP>) + 1024;
     int s = CSA2_OK;
     if constexpr (QG == 1)
-        s = kernel_smem_limit((const void *)k_index_f8<true, DENSE, QG>, smem);
-    if (s || (s = kernel_smem_limit((const void *)k_index_f8<false, DENSE, QG>, smem))) return s;
+        s = kernel_smem_limit((const void *)k_index_f8<true, DENSE, QG, QP>, smem);
+    if (s || (s = kernel_smem_limit((const void *)k_index_f8<false, DENSE, QG, QP>, smem))) return s;
     const int64_t per_row = DENSE ? ld : bt.max_entries;
     const int64_t tiles_row = std::max<int64_t>(1, (per_row + F8_TILE - 1) / F8_TILE);
     // the persistent grid (ragged single-query batches) for QG = 1; query groups
@@ -526,19 +542,19 @@ static int launch_f8_q(const csa2_cache &c, const csa2_batch &bt, const uint16_t
     if constexpr (QG == 1) {
         if (groups <= F8_PERSIST_ROWS) {
             const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)groups * tiles_row, sms));
-            return launch_pdl(k_index_f8<true, DENSE, QG>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
+            return launch_pdl(k_index_f8<true, DENSE, QG, QP>, dim3(grid), dim3(F8_THREADS), smem, st, c, bt, qi, w,
                               pool_len, scores, block_max, n_visible, ld, (int)bf16, wait_polls());
         }
     }
     if (groups > 65535) return CSA2_ERR_SHAPE;   // groups run along the grid's y dimension
     const int x = (int)std::max<int64_t>(1, std::min<int64_t>(tiles_row, ((int64_t)sms + groups - 1) / groups));
-    return launch_pdl(k_index_f8<false, DENSE, QG>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
+    return launch_pdl(k_index_f8<false, DENSE, QG, QP>, dim3(x, groups), dim3(F8_THREADS), smem, st, c, bt, qi, w,
                       pool_len, scores, block_max, n_visible, ld, (int)bf16, wait_polls());
 }
 
 // Queries per group: the largest of 4, 2, 1 that the per-sequence query count
 // fills (a dense pool copy holds one query's keys per row).
-template <bool DENSE>
+template <bool DENSE, int QP>
 static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                      const int32_t *pool_len, float *scores, float *block_max, int32_t *n_visible, int64_t ld,
                      cudaStream_t st, bool bf16)
@@ -546,17 +562,19 @@ static int launch_f8(const csa2_cache &c, const csa2_batch &bt, const uint16_t *
     const int sms = device_sms();
     if (sms <= 0) return CSA2_ERR_CUDA;
     if (DENSE || bt.nq < 2)
-        return launch_f8_q<DENSE, 1>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
+        return launch_f8_q<DENSE, 1, QP>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
     if (bt.nq < 4)
-        return launch_f8_q<false, 2>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
-    return launch_f8_q<false, 4>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
+        return launch_f8_q<false, 2, QP>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
+    return launch_f8_q<false, 4, QP>(c, bt, qi, w, pool_len, scores, block_max, n_visible, ld, st, bf16, sms);
 }
 
 int launch_index_scan(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi, const float *w,
                       float *scores, float *block_max, int32_t *n_visible, int64_t ld, cudaStream_t st,
-                      bool bf16_scores)
+                      bool bf16_scores, bool one_part_query)
 {
-    return launch_f8<false>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st, bf16_scores);
+    if (one_part_query)
+        return launch_f8<false, 1>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st, bf16_scores);
+    return launch_f8<false, 2>(c, bt, qi, w, nullptr, scores, block_max, n_visible, ld, st, bf16_scores);
 }
 
 // Dense copy of the indexer keys of each row's candidate pool: slot e of row r
@@ -618,7 +636,7 @@ int launch_index_dense(const uint8_t *codes, const float *scales, const csa2_bat
     d.ik_codes = const_cast<uint8_t *>(codes);
     d.ik_scales = const_cast<float *>(scales);
     d.num_slots = (int64_t)bt.batch * bt.nq * ld;
-    return launch_f8<true>(d, bt, qi, w, pool_len, scores, nullptr, nullptr, ld, st, bf16_scores);
+    return launch_f8<true, 2>(d, bt, qi, w, pool_len, scores, nullptr, nullptr, ld, st, bf16_scores);
 }
 
 }  // namespace csa2

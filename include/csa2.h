@@ -187,6 +187,17 @@ typedef struct csa2_swa {
  * §10.2); this is that trade, outside the fp32 parity rule: near-ties at the
  * threshold may resolve differently from fp32 scores. */
 #define CSA2_LAYER_SCORES_BF16 1
+/* csa2_layer_io.flags: a FULL layer's scan takes each indexer query as one
+ * e4m3 operand per head (q_h scaled by the power of two that puts its largest
+ * element in [128, 256), rounded to e4m3: 4 significant bits) instead of two
+ * (hi + lo, about 8, the precision of the bf16 query).  Fewer products per
+ * key tile and one tensor-memory column per head to read; a trade outside the
+ * fp32 parity rule, the counterpart for the index scan of the FP8 indexer
+ * the pages describe ("DeepSeek-V4 report explainer" §3.2, §10.2): each score
+ * then carries the query's e4m3 rounding (a relative error of order 2^-5 per
+ * element), so near-ties at the Top-K threshold may resolve differently.
+ * REINDEX layers and csa2_index_scores keep the two-part query. */
+#define CSA2_LAYER_INDEX_E4M3_QUERY 2
 
 /* Per-layer inputs, outputs and carried selection state for csa2_layer. */
 typedef struct csa2_layer_io {

@@ -95,7 +95,7 @@ def test_layer_option_flags_validated_on_the_host(lib):
     def io(layer_flags=0, swa_flags=0):
         s = csa2.Swa(P, P, 128, swa_flags, None, None, None, 0.0, 0)
         return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None)
-    for bad in (io(layer_flags=2), io(layer_flags=1 << 30), io(swa_flags=4)):
+    for bad in (io(layer_flags=4), io(layer_flags=1 << 30), io(swa_flags=4)):
         assert lib.csa2_layer(csa2.MODES["full"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(bad),
                               P, 1 << 30, None) == -3
     # a negative RoPE base is a shape error
