@@ -398,7 +398,7 @@ def test_layers_with_bf16_index_scores():
             ok, info = attn_close(dw.o[l][b].cpu().numpy(), dw.lse[l][b].cpu().numpy(), o_ref, lse_ref)
             assert ok, (b, l, info)
     print("bf16-score selection recall per (row, Full/Reindex layer):", [round(x, 4) for x in recalls])
-    assert min(recalls) >= 0.94, recalls
+    assert min(recalls) >= 0.95, recalls
 
 
 @pytest.mark.parametrize("nq", [1, 4])
