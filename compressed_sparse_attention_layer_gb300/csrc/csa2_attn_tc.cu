@@ -322,6 +322,16 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     bool stored = false;
     uint32_t ring_word = 0;                        // the new token's window row, stored at the end
     int64_t ring_idx = -1, ring_scale_idx = -1;
+    // this CTA's slice of the queries (64 heads x AC_DIMS dims: one 128-byte line
+    // per thread) and the decode token's new window row into L2 while the previous
+    // kernel finishes: a prefetch carries no data into this CTA, so it may run
+    // before the wait
+    if (tid < CSA2_HEADS * AC_DIMS * 2 / 128) {
+        constexpr int LPH = AC_DIMS * 2 / 128;     // lines per head
+        prefetch_l2(q + (r * CSA2_HEADS + tid / LPH) * CSA2_HEAD_DIM + AC_DIMS * dq + 64 * (tid % LPH));
+    } else if (window && swa.new_rows && tid - CSA2_HEADS * AC_DIMS * 2 / 128 < CSA2_HEAD_DIM * 4 / 128) {
+        prefetch_l2(swa.new_rows + r * CSA2_HEAD_DIM + 32 * (tid - CSA2_HEADS * AC_DIMS * 2 / 128));
+    }
     if (early) {
         if (window) load_window_row();
         else load_selected();
