@@ -138,6 +138,49 @@ def test_all_equal_scores_tie_to_the_lower_positions():
             assert np.array_equal(got, np.arange(512)), (b, l, got[:10])
 
 
+def test_reindex_pool_not_written_by_a_full_layer():
+    """A Reindex pool that is not what a Full layer writes: a block whose
+    positions are not 8 consecutive visible positions from a multiple of 8
+    (reordered, shifted, past the context, negative) scores -inf and is
+    flagged CSA2_DEV_BAD_INDEX ("DeepSeek-V4.1-Flash 架构详解" §3.2: the pool is
+    whole blocks of 8); the selection is the Top-512 of the remaining blocks
+    (checked against the oracle on them) and the attention over it is at
+    parity."""
+    wl = W.Workload("badpool", 93, 2, [50000, 30000], 1, ["full", "reindex"], planted_blocks=2)
+    dw = DeviceWorkload(wl)
+    dw.run_layer(0)
+    torch.cuda.synchronize()
+    assert int(dw.cache.status[0]) == 0
+    p = dw.pool.cpu().numpy().copy()
+    lens = dw.pool_len.cpu().numpy()
+    bad = {0: [3, 10], 1: [5, 7]}                  # blocks of each row's pool
+    p[0, 24:32] = p[0, 24:32][::-1].copy()        # reordered
+    p[0, 80:88] += 1                              # not from a multiple of 8
+    p[1, 40:48] = (wl.entries(1) // 8 + 10) * 8 + np.arange(8)   # past the context
+    p[1, 56:64] = -1                              # no position
+    dw.pool.copy_(torch.from_numpy(p))
+    dw.run_layer(1)
+    torch.cuda.synchronize()
+    status = int(dw.cache.status[0])
+    assert status & csa2.DEV_BAD_INDEX and not status & csa2.DEV_BAD_PAGE, status
+    idx = dw.idx.cpu().numpy()
+    for b in range(wl.batch):
+        so = SeqOracle(wl, b)
+        keep = np.ones(int(lens[b]), bool)
+        for k in bad[b]:
+            keep[8 * k: 8 * k + 8] = False
+        good = p[b, :lens[b]][keep]
+        idx_ref, ps = so.reindex(1, 0, good)
+        kth = np.sort(ps)[::-1][min(511, ps.size - 1)]
+        got = idx[b]
+        assert not np.isin(got, p[b, :lens[b]][~keep]).any(), b
+        ok, info = topk_valid(got, lambda s: so.scores(1, 0, s), kth, idx_ref)
+        assert ok, (b, info)
+        o_ref, lse_ref = so.attention(1, 0, got)
+        ok, info = attn_close(dw.o[1][b].cpu().numpy(), dw.lse[1][b].cpu().numpy(), o_ref, lse_ref)
+        assert ok, (b, info)
+
+
 def test_layer_decode_group_full_size():
     """64 x 32,768 tokens, random page permutation, 16 planted blocks each;
     Full + 3 Reuse, Reindex + 3 Reuse.  Four sequences checked end to end,
