@@ -50,6 +50,9 @@ def parse():
                    help="Full and Reindex layers select on bf16-rounded index scores (csa2.LAYER_SCORES_BF16)")
     p.add_argument("--e4m3-query", action="store_true",
                    help="the Full layer's scan with one e4m3 query part per head (csa2.LAYER_INDEX_E4M3_QUERY)")
+    p.add_argument("--attn-schedule", default="auto", choices=["auto", "chunks", "rows"],
+                   help="attention schedule (csa2.ATTN_SCHEDULE_*): one cluster per (row, key chunk) and a "
+                        "merge, or persistent clusters over whole rows; auto picks by the number of rows")
     p.add_argument("--queries", type=int, default=1,
                    help="query tokens per sequence per step (>1: a multi-token decode step, e.g. draft "
                         "tokens verified together; the Full layer's scan serves them from one read)")
@@ -187,8 +190,7 @@ class DecodeStep:
         self.scan_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
         for e in self.scan_ev:
             e.record()                       # materialise the CUDA events
-        self.launches = 1 + sum({"full": 5, "reindex": 4, "reuse": 2}[m] for m in wl.layers) + \
-            (len(wl.layers) if Q > 1 else 0)
+        self.set_schedule()
         # the step's host-fed inputs (new tokens, every layer's queries and window
         # rows) in two device buffers -- the first layer's / the rest -- and its
         # outputs (every layer's o and lse) in one buffer per group of
@@ -205,6 +207,20 @@ class DecodeStep:
         self.in_dev = [self._gather(ins0)] + ([self._gather(ins1)] if ins1 else [])
         outs = [[(dw.o, l), (dw.lse, l)] for l in layers]
         self.out_dev = [self._gather(sum([outs[i] for i in g], [])) for g in self.out_groups]
+
+    def set_schedule(self):
+        """The attention schedule the library takes for this step, and the step's
+        kernel launches: Full (scan, block Top-2,048, pool Top-512) and Reindex
+        (rescoring, select) ahead of the attention, which is one launch in the
+        row schedule and two (attention, merge) in the chunk schedule; the new
+        entries' launch; with several new tokens, their window rows per layer."""
+        csa2, dw, wl = self.csa2, self.dw, self.wl
+        l0 = dw.layers[0]
+        self.schedule = csa2.csa2_sparse_attn_schedule(
+            dw.batch, dw.swa(l0, new_rows=self.swa_new[l0] if self.queries == 1 else None))
+        attn = 1 if self.schedule == csa2.ATTN_SCHEDULE_ROWS else 2
+        self.launches = 1 + sum({"full": 3, "reindex": 2, "reuse": 0}[m] + attn for m in wl.layers) + \
+            (len(wl.layers) if self.queries > 1 else 0)
 
     def _gather(self, refs):
         """One device byte buffer holding the tensors refs name (container, key),
@@ -348,6 +364,10 @@ def run_native(args):
         step.dw.layer_flags |= csa2.LAYER_SCORES_BF16
     if args.e4m3_query:
         step.dw.layer_flags |= csa2.LAYER_INDEX_E4M3_QUERY
+    if args.attn_schedule != "auto":
+        sch = {"chunks": csa2.ATTN_SCHEDULE_CHUNKS, "rows": csa2.ATTN_SCHEDULE_ROWS}[args.attn_schedule]
+        step.dw.attn_options["flags"] = step.dw.attn_options.get("flags", 0) | sch
+        step.set_schedule()
 
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
@@ -562,7 +582,9 @@ def run_native(args):
                           f"{inputs_bytes / 1e6:.1f} MB"),
                    "graph": "one CUDA graph per step",
                    "index_scores": "bf16 (selection on rounded scores)" if args.bf16_scores else "fp32",
-                   "index_query": "one e4m3 part per head" if args.e4m3_query else "two e4m3 parts (hi + lo)"},
+                   "index_query": "one e4m3 part per head" if args.e4m3_query else "two e4m3 parts (hi + lo)",
+                   "attention": "persistent clusters over whole rows" if step.schedule == csa2.ATTN_SCHEDULE_ROWS
+                   else "one cluster per (row, 128-key chunk) and a merge"},
         "roofline": roofline, "per_layer_mode": per_mode, "clocks": clk, "e2e": e2e, "gpu_launches": step.launches * args.steps,
         "cpu_baseline": cpu,
     }

@@ -66,6 +66,7 @@ EXPORTS = {
     "csa2_sparse_attn": (ctypes.c_int, [ctypes.POINTER(Cache), ctypes.POINTER(Batch), _vp, _f32, _vp, _i32,
                                         ctypes.POINTER(Swa), _vp, _vp, _vp, _sz, _vp]),
     "csa2_sparse_attn_workspace_size": (_sz, [_i32, _i32]),
+    "csa2_sparse_attn_schedule": (ctypes.c_int, [ctypes.POINTER(Batch), ctypes.POINTER(Swa)]),
     "csa2_layer": (ctypes.c_int, [_i32, ctypes.POINTER(Cache), ctypes.POINTER(Batch), ctypes.POINTER(LayerIO),
                                   _vp, _sz, _vp]),
     "csa2_layer_workspace_size": (_sz, [_i32, ctypes.POINTER(Batch)]),
@@ -169,6 +170,8 @@ ATTN_DEDUP_WINDOW = 1
 LAYER_SCORES_BF16 = 1      # csa2_layer_io.flags: selection on bf16-rounded index scores
 LAYER_INDEX_E4M3_QUERY = 2  # csa2_layer_io.flags: the Full scan's query as one e4m3 part per head
 ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
+ATTN_SCHEDULE_CHUNKS = 4   # attention: one cluster per (row, key chunk) and a merge kernel
+ATTN_SCHEDULE_ROWS = 8     # attention: persistent clusters over whole rows (many rows; no new_rows)
 
 
 def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=None, sink=None,
@@ -176,7 +179,8 @@ def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=N
     """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
     into the ring by the attention call itself; sink: optional fp32 [64] per-head
     sink logits; rope_base > 0 rotates the output's RoPE dims back by the query
-    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS."""
+    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS | ATTN_SCHEDULE_CHUNKS or
+    ATTN_SCHEDULE_ROWS."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
                int(flags), _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"),
                _ptr(sink, torch.float32, "sink"), float(rope_base), 0)
@@ -273,6 +277,13 @@ def csa2_topk_blocks(block_max, n_visible, pmax: int, pool, pool_len, stream=Non
 
 def csa2_sparse_attn_workspace_size(batch: int, nq: int) -> int:
     return int(load().csa2_sparse_attn_workspace_size(batch, nq))
+
+
+def csa2_sparse_attn_schedule(batch: Batch, swa: Swa) -> int:
+    """ATTN_SCHEDULE_CHUNKS or ATTN_SCHEDULE_ROWS: the schedule the attention takes."""
+    r = int(load().csa2_sparse_attn_schedule(ctypes.byref(batch), ctypes.byref(swa)))
+    _check("csa2_sparse_attn_schedule", min(r, 0))
+    return r
 
 
 def csa2_sparse_attn(cache: Cache, batch: Batch, q, sm_scale: float, idx, swa: Swa, o, lse, workspace=None,

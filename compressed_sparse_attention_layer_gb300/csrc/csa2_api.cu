@@ -101,6 +101,7 @@ int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
                 const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
 size_t attn_workspace_bytes(int64_t rows);
+bool attn_by_rows(int64_t rows, const csa2_swa &swa);
 int topk_max_k();
 int64_t topk_max_len();
 
@@ -134,7 +135,10 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (!s || !s->codes || !s->scales) return CSA2_ERR_NULL;
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
-    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS)) return CSA2_ERR_UNSUPPORTED;
+    if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS | CSA2_ATTN_SCHEDULE_CHUNKS |
+                     CSA2_ATTN_SCHEDULE_ROWS))
+        return CSA2_ERR_UNSUPPORTED;
+    if ((s->flags & CSA2_ATTN_SCHEDULE_CHUNKS) && (s->flags & CSA2_ATTN_SCHEDULE_ROWS)) return CSA2_ERR_UNSUPPORTED;
     if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
     if (s->new_rows) {
         // the window of a query in a multi-token chunk holds other new tokens, which
@@ -362,6 +366,14 @@ int csa2_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n
     if (ld_blocks > topk_max_len()) return CSA2_ERR_SHAPE;
     return launch_topk_blocks(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len,
                               (cudaStream_t)stream);
+}
+
+int csa2_sparse_attn_schedule(const csa2_batch *batch, const csa2_swa *swa)
+{
+    if (!batch || !swa) return CSA2_ERR_NULL;
+    if (batch->batch < 1 || batch->nq < 1) return CSA2_ERR_SHAPE;
+    if (const int s = check_swa(swa, batch)) return s;
+    return attn_by_rows((int64_t)batch->batch * batch->nq, *swa) ? CSA2_ATTN_SCHEDULE_ROWS : CSA2_ATTN_SCHEDULE_CHUNKS;
 }
 
 size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq)

@@ -178,6 +178,16 @@ typedef struct csa2_swa {
  * completed).  A decode stack that calls csa2_layer layer after layer, with
  * the window rows of its own tokens passed as new_rows, satisfies it. */
 #define CSA2_ATTN_EARLY_INPUTS 2
+/* csa2_swa.flags: the schedule of the attention kernels (the same arithmetic
+ * either way up to the order of the softmax rescaling; no counterpart in the
+ * pages).  CHUNKS: one two-CTA cluster per (query row, 128-key chunk) and a
+ * merge kernel -- the shortest latency for a few rows.  ROWS: persistent
+ * two-CTA clusters, each taking whole rows with an online softmax over the
+ * row's chunks and writing o and lse directly -- for many rows (prefill,
+ * several query tokens per sequence, large decode batches).  Neither bit:
+ * CHUNKS below 40 query rows, ROWS from 40.  Both bits: CSA2_ERR_UNSUPPORTED. */
+#define CSA2_ATTN_SCHEDULE_CHUNKS 4
+#define CSA2_ATTN_SCHEDULE_ROWS 8
 
 /* csa2_layer_io.flags: FULL and REINDEX layers keep the index scores in bf16
  * (each fp32 score rounded to nearest even) and select on them: the block
@@ -395,6 +405,13 @@ CSA2_API int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, 
                      csa2_stream_t stream);
 
 CSA2_API size_t csa2_sparse_attn_workspace_size(int32_t batch, int32_t nq);
+
+/* The schedule csa2_sparse_attn and csa2_layer take for these arguments
+ * (CSA2_ATTN_SCHEDULE_CHUNKS: two launches, the attention and its merge;
+ * CSA2_ATTN_SCHEDULE_ROWS: one), or a negative CSA2_ERR_* for arguments the
+ * calls would refuse (swa->codes and swa->scales must be non-NULL; nothing is
+ * dereferenced on the device).  Host only. */
+CSA2_API int csa2_sparse_attn_schedule(const csa2_batch *batch, const csa2_swa *swa);
 
 /* ---- a10: one CSA2 layer ---------------------------------------------------
  * mode CSA2_MODE_FULL    : index every visible entry, pool of the best 2,048

@@ -92,10 +92,11 @@ def test_layer_option_flags_validated_on_the_host(lib):
     P = ctypes.c_void_p(1 << 12)
     cache = csa2.Cache(P, P, P, P, 1 << 12, P, 64, 0, None)
     batch = csa2.Batch(1, 1, 1, 0, 1000, P, P)
-    def io(layer_flags=0, swa_flags=0):
-        s = csa2.Swa(P, P, 128, swa_flags, None, None, None, 0.0, 0)
+    def io(layer_flags=0, swa_flags=0, new_rows=None):
+        s = csa2.Swa(P, P, 128, swa_flags, None, new_rows, None, 0.0, 0)
         return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None)
-    for bad in (io(layer_flags=4), io(layer_flags=1 << 30), io(swa_flags=4)):
+    both = csa2.ATTN_SCHEDULE_CHUNKS | csa2.ATTN_SCHEDULE_ROWS
+    for bad in (io(layer_flags=4), io(layer_flags=1 << 30), io(swa_flags=16), io(swa_flags=both)):
         assert lib.csa2_layer(csa2.MODES["full"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(bad),
                               P, 1 << 30, None) == -3
     # a negative RoPE base is a shape error
@@ -103,6 +104,26 @@ def test_layer_option_flags_validated_on_the_host(lib):
     neg = csa2.LayerIO(P, P, P, s, 1.0, 0, P, P, P, P, P, None, None)
     assert lib.csa2_layer(csa2.MODES["reuse"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(neg),
                           P, 1 << 30, None) == -2
+
+
+def test_attention_schedule_choice(lib):
+    """csa2_sparse_attn_schedule: fewer than 40 query rows -> one cluster per
+    key chunk and a merge; 40 or more -> persistent clusters over whole rows;
+    the flags force either; refusals as the attention call itself (host only,
+    fake pointers)."""
+    from compressed_sparse_attention_layer_gb300 import csa2
+    P = ctypes.c_void_p(1 << 12)
+    def sched(batch, nq, flags=0, new_rows=None):
+        b = csa2.Batch(batch, nq, 1, 0, 1000, P, P)
+        s = csa2.Swa(P, P, 256, flags, None, new_rows, None, 0.0, 0)
+        return lib.csa2_sparse_attn_schedule(ctypes.byref(b), ctypes.byref(s))
+    C, R = csa2.ATTN_SCHEDULE_CHUNKS, csa2.ATTN_SCHEDULE_ROWS
+    assert sched(8, 1) == C and sched(39, 1) == C and sched(8, 1, new_rows=P) == C and sched(8, 4) == C
+    assert sched(40, 1) == R and sched(10, 4) == R and sched(1, 8192) == R and sched(64, 1, new_rows=P) == R
+    assert sched(64, 1, flags=C) == C and sched(1, 1, flags=R) == R and sched(1, 1, flags=R, new_rows=P) == R
+    assert sched(8, 1, flags=C | R) == -3 and sched(8, 4, new_rows=P) == -3
+    assert sched(0, 1) == -2
+    assert lib.csa2_sparse_attn_schedule(None, None) == -1
 
 
 def test_workspace_sizes(lib):

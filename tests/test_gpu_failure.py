@@ -51,3 +51,31 @@ def test_waits_time_out_and_the_context_stays_usable():
     for b in range(wl.batch):
         _check_sequence(fresh, b)
     assert int(fresh.cache.status[0]) == 0
+
+
+def test_row_schedule_waits_time_out_and_the_context_stays_usable():
+    """The persistent row schedule of the attention under a one-poll limit:
+    every wait of its item loop runs out first (flagged), then waits for the
+    same phase once more with the long limit, so the two CTAs of a cluster
+    keep the same sequence of exchanges and the call completes."""
+    wl = W.Workload("timeout_rows", 82, 2, [5000, 30000], 1, ["full", "reuse"], planted_blocks=2,
+                    nq=3, prefill_new=3, swa_rows=W.W + 3)
+    dw = DeviceWorkload(wl)
+    dw.attn_options = dict(flags=csa2.ATTN_SCHEDULE_ROWS)
+    csa2.csa2_debug_set_wait_limit(1)
+    try:
+        for l in dw.layers:
+            dw.run_layer(l)
+        torch.cuda.synchronize()
+    finally:
+        csa2.csa2_debug_set_wait_limit(0)
+    status = int(dw.cache.status[0])
+    assert status & csa2.DEV_TIMEOUT, status
+    assert not (status & (csa2.DEV_BAD_PAGE | csa2.DEV_BAD_SLOT)), status
+    fresh = DeviceWorkload(wl)
+    fresh.attn_options = dict(flags=csa2.ATTN_SCHEDULE_ROWS)
+    _run_recording(fresh)
+    for b in range(wl.batch):
+        for i in range(wl.nq):
+            _check_sequence(fresh, b, i)
+    assert int(fresh.cache.status[0]) == 0

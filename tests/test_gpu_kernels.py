@@ -312,9 +312,15 @@ def test_topk_blocks_single_stage_bit_exact():
         assert gl[r] == want.size and np.array_equal(got[r, :gl[r]], want), r
 
 
-def test_sparse_attn_given_oracle_indices():
+@pytest.mark.parametrize("schedule", [csa2.ATTN_SCHEDULE_CHUNKS, csa2.ATTN_SCHEDULE_ROWS])
+def test_sparse_attn_given_oracle_indices(schedule):
+    """Both attention schedules (one cluster per key chunk and a merge; one
+    persistent cluster per row with an online softmax) on the oracle's
+    selection, a padded one, the window alone, and selections of k = 200 and
+    k = 1 (a partial chunk, one chunk plus the window)."""
     wl = W.decode_small()
     dw = _dw(wl)
+    dw.attn_options = dict(flags=schedule)
     so = SeqOracle(wl, 0)
     idx, pool, _ = so.full(0, 0)
     o_ref, lse_ref = so.attention(0, 0, idx)
@@ -326,6 +332,14 @@ def test_sparse_attn_given_oracle_indices():
                           o, lse, workspace=ws)
     ok, info = attn_close(o[0].cpu().numpy(), lse[0].cpu().numpy(), o_ref, lse_ref)
     assert ok, info
+    for kk in (200, 1):
+        sub = np.ascontiguousarray(idx[:kk])
+        o_ref_k, lse_ref_k = so.attention(0, 0, sub)
+        csa2.csa2_sparse_attn(dw.cstruct, dw.batch, dw.q[0], 1.0, torch.from_numpy(sub[None]).cuda(), dw.swa(0),
+                              o, lse, workspace=ws)
+        ok, info = attn_close(o[0].cpu().numpy(), lse[0].cpu().numpy(), o_ref_k, lse_ref_k)
+        assert ok, (kk, info)
+    assert int(dw.cache.status[0]) == 0
     # a shorter, padded selection (-1 slots) and the window alone
     idx2 = idx.copy()
     idx2[100:] = -1

@@ -273,14 +273,19 @@ def test_decode_step_deterministic():
     torch.cuda.empty_cache()
 
 
-def test_window_row_quantised_inside_the_attention_call():
+@pytest.mark.parametrize("schedule", [0, csa2.ATTN_SCHEDULE_ROWS])
+def test_window_row_quantised_inside_the_attention_call(schedule):
     """csa2_swa.new_rows: the decode token's window row quantised by the layer
     call itself gives the same ring bytes and the same o / lse, bit for bit, as
-    csa2_quant_fp8 followed by the layer."""
+    csa2_quant_fp8 followed by the layer -- in the chunk schedule, where the
+    attention quantises it in place, and in the row schedule, where each
+    cluster quantises its rows' new rows first."""
     wl = W.Workload("fused_swa", 71, 3, [5000, 300, 77], 1, ["full", "reuse"])
     ref = DeviceWorkload(wl)                      # its rings already hold the decode tokens' rows
+    ref.attn_options = dict(flags=schedule)
     ref.run()
     fused = DeviceWorkload(wl)
+    fused.attn_options = dict(flags=schedule)
     R = wl.swa_rows
     for l in fused.layers:
         for b in range(wl.batch):
@@ -335,6 +340,46 @@ def test_attention_options_sink_rotation_dedup(tokens):
     _run_recording(plain)
     for l in range(len(wl.layers)):
         assert np.array_equal(plain.hist_idx[l], dw.hist_idx[l]), l
+
+
+@pytest.mark.parametrize("schedule", [csa2.ATTN_SCHEDULE_ROWS, csa2.ATTN_SCHEDULE_CHUNKS])
+def test_attention_schedules_many_rows_with_options(schedule):
+    """120 query rows (3 sequences x 40 query tokens, more rows than the row
+    schedule has clusters, so clusters take two rows and some one) through
+    Full / Reuse / Reindex layers with the sink, the output rotation and the
+    window de-duplication, under each attention schedule forced: sampled rows
+    against the oracle, and the two schedules' outputs within the attention
+    tolerance of each other on every row (their softmax rescaling order
+    differs; the selections are identical)."""
+    wl = W.Workload("sched", 79, 3, [3000, 700, 9000], 1, ["full", "reuse", "reindex"], planted_blocks=2,
+                    nq=40, prefill_new=40, swa_rows=W.W + 40)
+    g = np.random.default_rng(79)
+    sink = g.normal(2.0, 3.0, 64).astype(np.float32)
+    sink[:3] = [-np.inf, 40.0, -40.0]
+    runs = {}
+    for sch in (schedule, csa2.ATTN_SCHEDULE_CHUNKS if schedule == csa2.ATTN_SCHEDULE_ROWS else csa2.ATTN_SCHEDULE_ROWS):
+        dw = DeviceWorkload(wl)
+        dw.attn_options = dict(sink=torch.from_numpy(sink).to(dw.dev), rope_base=10000.0,
+                               flags=csa2.ATTN_DEDUP_WINDOW | sch)
+        _run_recording(dw)
+        runs[sch] = dw
+    dw = runs[schedule]
+    for b in range(wl.batch):
+        so = SeqOracle(wl, b)
+        for i in (0, 13, 39):
+            r = b * wl.nq + i
+            for l in range(len(wl.layers)):
+                o_ref, lse_ref = so.attention(l, i, dw.hist_idx[l][r], sink=sink, rope_base=10000.0, dedup=True)
+                ok, info = attn_close(dw.o[l][r].cpu().numpy(), dw.lse[l][r].cpu().numpy(), o_ref, lse_ref)
+                assert ok, (b, i, l, info)
+    other = [v for k, v in runs.items() if k != schedule][0]
+    for l in range(len(wl.layers)):
+        assert np.array_equal(other.hist_idx[l], dw.hist_idx[l]), l
+        for r in range(dw.rows):
+            ok, info = attn_close(dw.o[l][r].cpu().numpy(), dw.lse[l][r].cpu().numpy(),
+                                  other.o[l][r].cpu().numpy().astype(np.float64),
+                                  other.lse[l][r].cpu().numpy().astype(np.float64))
+            assert ok, (l, r, info)
 
 
 def test_normed_rotated_queries_feed_the_layers():
