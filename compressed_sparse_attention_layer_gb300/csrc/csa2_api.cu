@@ -90,13 +90,13 @@ int launch_gather_pool(const csa2_cache &, const csa2_batch &, const int32_t *, 
 int launch_index_dense(const uint8_t *, const float *, const csa2_batch &, const uint16_t *, const float *,
                        const int32_t *, int64_t, float *, cudaStream_t, bool bf16_scores = false);
 int launch_topk(const float *, int64_t, const int32_t *, int32_t, const int32_t *, int32_t, int32_t *,
-                cudaStream_t, bool bf16_scores = false);
+                cudaStream_t);
 int launch_reindex(const csa2_cache &, const csa2_batch &, const uint16_t *, const float *, const int32_t *,
                    const int32_t *, int, int32_t *, bool, void *, cudaStream_t);
 size_t reindex_workspace_bytes(int64_t rows);
-int launch_topk_pool(const float *, int64_t, const int32_t *, int64_t, const int32_t *, int32_t, int32_t,
-                     int32_t *, cudaStream_t, bool bf16_scores = false);
 int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t, int32_t *, int32_t *,
+                       cudaStream_t, const PoolKeys * = nullptr, int * = nullptr);
+int launch_pool_select(const int32_t *, const int32_t *, const uint32_t *, const uint2 *, int, int, int32_t *, int64_t,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
                 const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
@@ -158,7 +158,7 @@ static inline int64_t score_ld(const csa2_batch *b)
 }
 
 // FULL workspace:    scores [rows][ld] | block_max [rows][ld/8] | n_visible [rows]
-//                    | attention workspace
+//                    | the pool's keys [rows][16384] and bounds | attention workspace
 // REINDEX workspace: the pool's rescored keys [rows][16384] and group minima
 //                    | attention workspace
 // REUSE workspace:   attention workspace
@@ -187,7 +187,7 @@ static LayerWs layer_ws(int32_t mode, const csa2_batch *b, void *base)
         w.block_max = (float *)take((size_t)rows * (ld / 8) * 4);
         w.n_visible = (int32_t *)take((size_t)rows * 4);
     }
-    if (mode == CSA2_MODE_REINDEX) w.rx = take(reindex_workspace_bytes(rows));
+    if (mode != CSA2_MODE_REUSE) w.rx = take(reindex_workspace_bytes(rows));
     w.attn_bytes = attn_workspace_bytes(rows);
     w.attn = take(w.attn_bytes);
     w.total = off;
@@ -449,13 +449,22 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
                                    bf16, (io->flags & CSA2_LAYER_INDEX_E4M3_QUERY) != 0)))
             return s;
         if ((s = prof(io->prof_end))) return s;
-        // the best 2,048 blocks of 8 -> candidate pool
+        // the best 2,048 blocks of 8 -> candidate pool, with the pool's scores as
+        // order keys and a lower bound of its 512th largest
+        PoolKeys pk;
+        pk.scores = ws.scores;
+        pk.ld_scores = ld;
+        pk.bf16 = bf16;
+        pk.k = CSA2_TOPK;
+        pk.keys = static_cast<uint32_t *>(ws.rx);
+        pk.bound = reinterpret_cast<uint2 *>(pk.keys + (int64_t)rows * CSA2_POOL_MAX);
+        pk.bound_ld = 32;
+        int P = 0;
         if ((s = launch_topk_blocks(ws.block_max, ld / 8, ws.n_visible, rows, CSA2_POOL_BLOCKS, io->pool,
-                                    io->pool_len, st)))
+                                    io->pool_len, st, &pk, &P)))
             return s;
-        // Top-512 of the pool, its scores read from the scan's score rows
-        if ((s = launch_topk_pool(ws.scores, ld, io->pool, CSA2_POOL_MAX, io->pool_len, rows, CSA2_TOPK, io->idx, st,
-                                  bf16)))
+        // Top-512 of the pool (the Reindex layer's select)
+        if ((s = launch_pool_select(io->pool, io->pool_len, pk.keys, pk.bound, P, CSA2_TOPK, io->idx, rows, st)))
             return s;
     } else if (mode == CSA2_MODE_REINDEX) {
         // rescore the pool (its blocks' keys read from the cache) with this

@@ -71,6 +71,18 @@ size_t layer_workspace_need(int32_t mode, const csa2_batch *b, const csa2_layer_
 
 inline bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// The pool's own selection input, written by the block-level Top-K as it
+// writes the pool (host-side launch argument; all pointers NULL: not wanted).
+struct PoolKeys {
+    const void *scores = nullptr;  // the scan's score rows the pool indexes (fp32, or bf16 with bf16)
+    int64_t ld_scores = 0;         // their row length, a multiple of 8
+    bool bf16 = false;
+    int k = 0;                     // the pool select's k: the bound holds only over >= k selected blocks
+    uint32_t *keys = nullptr;      // [rows][pool slots] order keys of the pool's scores
+    uint2 *bound = nullptr;        // [rows][bound_ld]: per cluster CTA, (lower bound, largest key)
+    int bound_ld = 0;
+};
+
 // ---------------------------------------------------------------- device side
 // Programmatic dependent launch: let the next kernel on the stream be
 // scheduled now (it still waits for this grid before reading its results) /

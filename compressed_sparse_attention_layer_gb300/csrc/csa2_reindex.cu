@@ -541,4 +541,17 @@ int launch_reindex(const csa2_cache &c, const csa2_batch &bt, const uint16_t *qi
     return launch_status();
 }
 
+// The Full layer's pool Top-k with the select above: keys and per-CTA bounds as
+// the block-level Top-K wrote them (P bounds per row, at most RX_PMAX), out
+// [rows][k] ascending, -1 after.
+int launch_pool_select(const int32_t *pool, const int32_t *pool_len, const uint32_t *keys, const uint2 *bound,
+                       int P, int k, int32_t *out, int64_t rows, cudaStream_t st)
+{
+    if (rows == 0) return CSA2_OK;
+    if (k < 1 || k > CSA2_POOL_MAX / 32 || P < 1 || P > RX_PMAX) return CSA2_ERR_SHAPE;
+    if (!aligned(keys, 16)) return CSA2_ERR_ALIGN;
+    return launch_pdl(k_rx_select, dim3((unsigned)rows), dim3(RX_SEL_THREADS), 0, st, pool, pool_len, keys, bound,
+                      P, k, out);
+}
+
 }  // namespace csa2

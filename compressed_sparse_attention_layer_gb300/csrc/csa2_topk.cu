@@ -87,11 +87,21 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(const float *__restrict__ s
 }
 
 // Block level of the hierarchy: the pmax best blocks -> their visible positions.
+// With pkeys, also the pool's own selection input: the order keys of its slots'
+// scores (pkeys[r][8 j + t] for block rank j; scores rows of ld_scores, fp32 or
+// bf16) and, per CTA q of the cluster, (the smallest, the largest) block maximum
+// it selected in pbound[r * bound_ld + q].  Every selected block holds a key
+// equal to its maximum (the scan's block maximum is one of its scores), so with
+// at least kbound selected blocks the smallest of those is a lower bound of the
+// pool's kbound-th largest key; with fewer, the bound is 0 (none).
 template <int CL>
 __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restrict__ block_max, int64_t ld_blocks,
                                                             const int32_t *__restrict__ n_visible, int pmax,
                                                             int32_t *__restrict__ pool,
-                                                            int32_t *__restrict__ pool_len)
+                                                            int32_t *__restrict__ pool_len,
+                                                            const void *__restrict__ scores, int64_t ld_scores,
+                                                            int bf16, int kbound, uint32_t *__restrict__ pkeys,
+                                                            uint2 *__restrict__ pbound, int bound_ld)
 {
     extern __shared__ uint32_t keys[];
     __shared__ TkShared sh;
@@ -110,6 +120,7 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
     __syncthreads();
     int32_t *pr = pool + r * (int64_t)pmax * 8;
     const int nsel = (int)(nb < pmax ? nb : pmax);
+    uint32_t bmin = 0xFFFFFFFFu, bmax = 0u;          // this thread's selected block maxima
     cluster_select<CL>(cluster, keys, keys + slice_cap(ld_blocks, CL), lo, m, nb, pmax, sh, [&](int j, int64_t blk) {
         if (j >= pmax) return;
 #pragma unroll
@@ -121,8 +132,50 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk_blocks(const float *__restr
             const int64_t tail = nv - blk * 8 < 8 ? nv - blk * 8 : 8;
             pool_len[r] = (nsel - 1) * 8 + (int)tail;
         }
+        if (pkeys) {
+            uint32_t kv[8];
+            if (bf16) {
+                const uint4 h = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(scores) +
+                                                                       r * ld_scores + blk * 8));
+                const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int t = 0; t < 8; t++) kv[t] = order_key(__uint_as_float((hw[t >> 1] >> (16 * (t & 1))) << 16));
+            } else {
+                const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(scores) +
+                                                                     r * ld_scores + blk * 8);
+                const float4 a = __ldcg(src), b = __ldcg(src + 1);
+                const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int t = 0; t < 8; t++) kv[t] = order_key(f[t]);
+            }
+#pragma unroll
+            for (int t = 0; t < 8; t++)
+                if (blk * 8 + t >= nv) kv[t] = 0u;   // past the visible entries (outside the pool)
+            uint4 *dst = reinterpret_cast<uint4 *>(pkeys + (r * pmax + j) * 8);
+            dst[0] = make_uint4(kv[0], kv[1], kv[2], kv[3]);
+            dst[1] = make_uint4(kv[4], kv[5], kv[6], kv[7]);
+            const uint32_t bk = keys[blk - lo];      // the block's maximum, as staged
+            bmin = min(bmin, bk);
+            bmax = max(bmax, bk);
+        }
     });
     if (nsel == 0 && q == 0 && threadIdx.x == 0) pool_len[r] = 0;
+    if (pkeys) {
+        bmin = __reduce_min_sync(0xffffffffu, bmin);
+        bmax = __reduce_max_sync(0xffffffffu, bmax);
+        __syncthreads();                             // the select's shared state is no longer read
+        if (threadIdx.x == 0) {
+            sh.kmin = 0xFFFFFFFFu;
+            sh.kmax = 0u;
+        }
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) {
+            atomicMin(&sh.kmin, bmin);
+            atomicMax(&sh.kmax, bmax);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) pbound[r * bound_ld + q] = make_uint2(nsel >= kbound ? sh.kmin : 0u, sh.kmax);
+    }
 }
 
 // ---------------------------------------------------------------- one CTA per row, keys in registers
@@ -325,74 +378,40 @@ __device__ int rs_select(const uint32_t (&key)[RS_PER], uint32_t valid, int n, i
     return k;
 }
 
-// Slots 16 t .. 16 t + 15 of a row of n keys as order keys: direct
-// (row[i]) when ind is NULL, else gathered (src[ind[i]]; an index outside
-// [0, src_len) reads as -inf).  Returns the valid mask (slots < n).
-__device__ __forceinline__ uint32_t rs_load(const float *__restrict__ row, const int32_t *__restrict__ ind,
-                                            int64_t src_len, int n, uint32_t (&key)[RS_PER], bool bf16)
+// Slots 16 t .. 16 t + 15 of a row of n scores as order keys.  Returns the
+// valid mask (slots < n).
+__device__ __forceinline__ uint32_t rs_load(const float *__restrict__ row, int n, uint32_t (&key)[RS_PER])
 {
     const int s0 = RS_PER * threadIdx.x;
+    if (s0 + RS_PER <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+#pragma unroll
+        for (int q = 0; q < RS_PER / 4; q++) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(row + s0) + q);
+            key[4 * q] = order_key(v.x);
+            key[4 * q + 1] = order_key(v.y);
+            key[4 * q + 2] = order_key(v.z);
+            key[4 * q + 3] = order_key(v.w);
+        }
+        return 0xFFFFu;
+    }
     uint32_t valid = 0;
-    if (bf16) {                                    // bf16 score rows (same slots, two bytes each)
-        const uint16_t *row16 = reinterpret_cast<const uint16_t *>(row);
-        int32_t p[RS_PER];
-#pragma unroll
-        for (int j = 0; j < RS_PER; j++) p[j] = s0 + j < n ? (ind ? __ldg(ind + s0 + j) : s0 + j) : -1;
-#pragma unroll
-        for (int j = 0; j < RS_PER; j++) {
-            key[j] = 0u;
-            if (s0 + j < n) {
-                const bool ok = p[j] >= 0 && (!ind || p[j] < src_len);
-                key[j] = order_key(ok ? bf16_to_f32(__ldg(row16 + p[j])) : -INFINITY);
-                valid |= 1u << j;
-            }
-        }
-        return valid;
-    }
-    if (!ind) {
-        if (s0 + RS_PER <= n && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-#pragma unroll
-            for (int q = 0; q < RS_PER / 4; q++) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(row + s0) + q);
-                key[4 * q] = order_key(v.x);
-                key[4 * q + 1] = order_key(v.y);
-                key[4 * q + 2] = order_key(v.z);
-                key[4 * q + 3] = order_key(v.w);
-            }
-            return 0xFFFFu;
-        }
-#pragma unroll
-        for (int j = 0; j < RS_PER; j++) {
-            key[j] = 0u;
-            if (s0 + j < n) {
-                key[j] = order_key(__ldg(row + s0 + j));
-                valid |= 1u << j;
-            }
-        }
-        return valid;
-    }
-    int32_t p[RS_PER];
-#pragma unroll
-    for (int j = 0; j < RS_PER; j++) p[j] = s0 + j < n ? __ldg(ind + s0 + j) : -1;
 #pragma unroll
     for (int j = 0; j < RS_PER; j++) {
         key[j] = 0u;
         if (s0 + j < n) {
-            key[j] = order_key(p[j] >= 0 && p[j] < src_len ? __ldg(row + p[j]) : -INFINITY);
+            key[j] = order_key(__ldg(row + s0 + j));
             valid |= 1u << j;
         }
     }
     return valid;
 }
 
-// Top k of each row (one CTA per row, len[r] <= RS_MAX slots): keys direct
-// (scores[r][i]) or gathered through ind (scores[r][ind[r][i]], scores rows of
-// src_len), reported as cand[r][i] (or i) ascending, -1 after.
-__global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__restrict__ scores, int64_t src_len,
-                                                              const int32_t *__restrict__ ind, int64_t ld,
+// Top k of each row (one CTA per row, len[r] <= RS_MAX slots of scores[r]),
+// reported as cand[r][i] (or i) ascending, -1 after.
+__global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__restrict__ scores, int64_t ld,
                                                               const int32_t *__restrict__ len,
                                                               const int32_t *__restrict__ cand, int k,
-                                                              int32_t *__restrict__ out, int bf16)
+                                                              int32_t *__restrict__ out)
 {
     __shared__ RsShared sh;
     pdl_launch_dependents();
@@ -402,12 +421,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) k_topk_rows(const float *__rest
     n64 = n64 < 0 ? 0 : (n64 > ld ? ld : n64);
     const int n = (int)n64;
     uint32_t key[RS_PER];
-    // row offsets in elements of the score type (fp32, or bf16 with bf16 != 0)
-    const float *srow = bf16 ? reinterpret_cast<const float *>(reinterpret_cast<const uint16_t *>(scores) +
-                                                               r * (ind ? src_len : ld))
-                             : scores + r * (ind ? src_len : ld);
-    const uint32_t valid = ind ? rs_load(srow, ind + r * ld, src_len, n, key, bf16 != 0)
-                               : rs_load(srow, nullptr, 0, n, key, bf16 != 0);
+    const uint32_t valid = rs_load(scores + r * ld, n, key);
     int32_t *o = out + r * k;
     const int32_t *cr = cand ? cand + r * ld : nullptr;
     const int s0 = RS_PER * threadIdx.x;
@@ -459,22 +473,20 @@ static int topk_cl(const float *scores, int64_t ld, const int32_t *len, int32_t 
 
 template <int CL>
 static int blocks_cl(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
-                     int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
+                     int32_t pmax, int32_t *pool, int32_t *pool_len, const PoolKeys &pk, cudaStream_t st)
 {
     if (const int s = kernel_smem_limit((const void *)k_topk_blocks<CL>, 2 * TK_SLICE * 4)) return s;
     return launch_cluster(k_topk_blocks<CL>, CL, ld_blocks, rows, st, block_max, ld_blocks, n_visible, (int)pmax,
-                          pool, pool_len);
+                          pool, pool_len, pk.scores, pk.ld_scores, (int)pk.bf16, pk.k, pk.keys, pk.bound, pk.bound_ld);
 }
 
 int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t rows, const int32_t *cand,
-                int32_t k, int32_t *out, cudaStream_t st, bool bf16_scores)
+                int32_t k, int32_t *out, cudaStream_t st)
 {
     if (rows == 0) return CSA2_OK;
-    if (ld <= RS_MAX) {
-        return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, (int64_t)0,
-                          (const int32_t *)nullptr, ld, len, cand, (int)k, out, (int)bf16_scores);
-    }
-    if (bf16_scores) return CSA2_ERR_UNSUPPORTED;      // bf16 rows: the one-CTA select only
+    if (ld <= RS_MAX)
+        return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, ld, len, cand, (int)k,
+                          out);
     switch (topk_cluster_for(ld)) {
     case 1: return topk_cl<1>(scores, ld, len, rows, cand, k, out, st);
     case 2: return topk_cl<2>(scores, ld, len, rows, cand, k, out, st);
@@ -483,27 +495,22 @@ int launch_topk(const float *scores, int64_t ld, const int32_t *len, int32_t row
     }
 }
 
-// Top-k of the pool positions pool[r][0 .. pool_len[r]) by their scores in a
-// full score row (scores[r][pool[r][i]], rows of ld_scores), reported as
-// positions, ascending.
-int launch_topk_pool(const float *scores, int64_t ld_scores, const int32_t *pool, int64_t ld_pool,
-                     const int32_t *pool_len, int32_t rows, int32_t k, int32_t *out, cudaStream_t st, bool bf16_scores)
-{
-    if (rows == 0) return CSA2_OK;
-    if (ld_pool > RS_MAX) return CSA2_ERR_SHAPE;
-    return launch_pdl(k_topk_rows, dim3((unsigned)rows), dim3(RS_THREADS), 0, st, scores, ld_scores, pool, ld_pool,
-                      pool_len, pool, (int)k, out, (int)bf16_scores);
-}
-
 int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t *n_visible, int32_t rows,
-                       int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st)
+                       int32_t pmax, int32_t *pool, int32_t *pool_len, cudaStream_t st, const PoolKeys *pool_keys,
+                       int *bounds_per_row)
 {
     if (rows == 0) return CSA2_OK;
-    switch (topk_cluster_for(ld_blocks)) {
-    case 1: return blocks_cl<1>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
-    case 2: return blocks_cl<2>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
-    case 4: return blocks_cl<4>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
-    default: return blocks_cl<8>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, st);
+    const PoolKeys pk = pool_keys ? *pool_keys : PoolKeys{};
+    const int cl = topk_cluster_for(ld_blocks);
+    if (bounds_per_row) *bounds_per_row = cl;
+    if (pk.keys && (cl > pk.bound_ld || !aligned(pk.scores, 16) || !aligned(pk.keys, 16) ||
+                    (pk.ld_scores & 7) != 0))
+        return CSA2_ERR_ALIGN;
+    switch (cl) {
+    case 1: return blocks_cl<1>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, pk, st);
+    case 2: return blocks_cl<2>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, pk, st);
+    case 4: return blocks_cl<4>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, pk, st);
+    default: return blocks_cl<8>(block_max, ld_blocks, n_visible, rows, pmax, pool, pool_len, pk, st);
     }
 }
 
