@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--attn-schedule", default="auto", choices=["auto", "chunks", "rows"],
                    help="attention schedule (csa2.ATTN_SCHEDULE_*): one cluster per (row, key chunk) and a "
                         "merge, or persistent clusters over whole rows; auto picks by the number of rows")
+    p.add_argument("--no-early-all", action="store_true",
+                   help="Reuse layers wait for the previous layer before their attention's products "
+                        "(csa2.ATTN_EARLY_INPUTS only, instead of csa2.ATTN_EARLY_ALL)")
     p.add_argument("--queries", type=int, default=1,
                    help="query tokens per sequence per step (>1: a multi-token decode step, e.g. draft "
                         "tokens verified together; the Full layer's scan serves them from one read)")
@@ -142,7 +145,7 @@ class ClockSampler:
 class DecodeStep:
     """Device state and the launch sequence of one decode step."""
 
-    def __init__(self, batch, tokens, seed, device, kv_format=0, queries=1, workload="decode_1m"):
+    def __init__(self, batch, tokens, seed, device, kv_format=0, queries=1, workload="decode_1m", early_all=True):
         import numpy as np
         import torch
         from compressed_sparse_attention_layer_gb300 import csa2, synth
@@ -170,6 +173,10 @@ class DecodeStep:
         # several new tokens: their window rows are written by the FP8 quantiser
         # right before each layer call, so keys may not be read ahead of it
         dw.early_inputs = T == 1
+        # one new token: every layer's q and window row are in place before the
+        # step, so a Reuse layer's whole attention may run ahead of its dependency
+        # wait (csa2.ATTN_EARLY_ALL; Reuse layers alternate between two workspaces)
+        dw.early_all = T == 1 and early_all
         dev = dw.dev
         Ns = [wl.tokens[b] for b in range(B)]
         N = Ns[0]
@@ -358,7 +365,7 @@ def run_native(args):
     dev = torch.device("cuda", local)
     seed = rank_seed(rank) if args.workload == "decode_1m" else None
     step = DecodeStep(args.batch, args.tokens, seed, dev, kv_format=args.kv_format, queries=args.queries,
-                      workload=args.workload)
+                      workload=args.workload, early_all=not args.no_early_all)
     B, N, Q = step.wl.batch, step.wl.tokens[0], step.queries
     if args.bf16_scores:
         step.dw.layer_flags |= csa2.LAYER_SCORES_BF16

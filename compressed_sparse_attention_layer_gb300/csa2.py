@@ -170,6 +170,7 @@ ATTN_DEDUP_WINDOW = 1
 LAYER_SCORES_BF16 = 1      # csa2_layer_io.flags: selection on bf16-rounded index scores
 LAYER_INDEX_E4M3_QUERY = 2  # csa2_layer_io.flags: the Full scan's query as one e4m3 part per head
 ATTN_EARLY_INPUTS = 2      # REUSE layers: keys loaded while the previous layer finishes (see the header)
+ATTN_EARLY_ALL = 16        # REUSE layers: the whole attention before the dependency wait (see the header)
 ATTN_SCHEDULE_CHUNKS = 4   # attention: one cluster per (row, key chunk) and a merge kernel
 ATTN_SCHEDULE_ROWS = 8     # attention: persistent clusters over whole rows (many rows; no new_rows)
 
@@ -179,8 +180,8 @@ def swa_struct(codes: torch.Tensor, scales: torch.Tensor, start=None, new_rows=N
     """new_rows: optional fp32 [B][512] window rows of the decode tokens, quantised
     into the ring by the attention call itself; sink: optional fp32 [64] per-head
     sink logits; rope_base > 0 rotates the output's RoPE dims back by the query
-    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS | ATTN_SCHEDULE_CHUNKS or
-    ATTN_SCHEDULE_ROWS."""
+    position; flags: ATTN_DEDUP_WINDOW | ATTN_EARLY_INPUTS | ATTN_EARLY_ALL |
+    ATTN_SCHEDULE_CHUNKS or ATTN_SCHEDULE_ROWS."""
     return Swa(_ptr(codes, torch.uint8, "swa codes"), _ptr(scales, torch.float32, "swa scales"), codes.shape[1],
                int(flags), _ptr(start, torch.int64, "swa start"), _ptr(new_rows, torch.float32, "swa new rows"),
                _ptr(sink, torch.float32, "sink"), float(rope_base), 0)

@@ -99,7 +99,7 @@ int launch_topk_blocks(const float *, int64_t, const int32_t *, int32_t, int32_t
 int launch_pool_select(const int32_t *, const int32_t *, const uint32_t *, const uint2 *, int, int, int32_t *, int64_t,
                        cudaStream_t);
 int launch_attn(const csa2_cache &, const csa2_batch &, const uint16_t *, float, const int32_t *, int,
-                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, bool);
+                const csa2_swa &, float *, float *, void *, size_t, cudaStream_t, int);
 size_t attn_workspace_bytes(int64_t rows);
 bool attn_by_rows(int64_t rows, const csa2_swa &swa);
 int topk_max_k();
@@ -136,7 +136,7 @@ static int check_swa(const csa2_swa *s, const csa2_batch *b)
     if (s->rows < CSA2_SWA_WINDOW) return CSA2_ERR_SHAPE;
     if (!aligned(s->codes, 16)) return CSA2_ERR_ALIGN;
     if (s->flags & ~(CSA2_ATTN_DEDUP_WINDOW | CSA2_ATTN_EARLY_INPUTS | CSA2_ATTN_SCHEDULE_CHUNKS |
-                     CSA2_ATTN_SCHEDULE_ROWS))
+                     CSA2_ATTN_SCHEDULE_ROWS | CSA2_ATTN_EARLY_ALL))
         return CSA2_ERR_UNSUPPORTED;
     if ((s->flags & CSA2_ATTN_SCHEDULE_CHUNKS) && (s->flags & CSA2_ATTN_SCHEDULE_ROWS)) return CSA2_ERR_UNSUPPORTED;
     if (!(s->rope_base >= 0.0f)) return CSA2_ERR_SHAPE;           // negative or NaN
@@ -397,7 +397,7 @@ int csa2_sparse_attn(const csa2_cache *cache, const csa2_batch *batch, const uin
     if (workspace && !aligned(workspace, 256)) return CSA2_ERR_ALIGN;
     if (!aligned(q, 16) || !aligned(o, 16)) return CSA2_ERR_ALIGN;
     return launch_attn(*cache, *batch, q, sm_scale, idx, k, *swa, o, lse, workspace, workspace_bytes,
-                       (cudaStream_t)stream, false);
+                       (cudaStream_t)stream, 0);
 }
 
 size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
@@ -476,9 +476,12 @@ int csa2_layer(int32_t mode, const csa2_cache *cache, const csa2_batch *batch, c
         if ((s = prof(io->prof_end))) return s;
     }
     // REUSE keeps io->idx as it is; the attention for every mode.
-    // CSA2_ATTN_EARLY_INPUTS is honoured in REUSE mode, where the indices come from an earlier layer call
+    // CSA2_ATTN_EARLY_INPUTS / _ALL are honoured in REUSE mode, where the indices come from an earlier layer call
+    const int early = mode != CSA2_MODE_REUSE ? 0
+                      : (io->swa.flags & CSA2_ATTN_EARLY_ALL) ? 2
+                      : (io->swa.flags & CSA2_ATTN_EARLY_INPUTS) ? 1 : 0;
     return launch_attn(*cache, *batch, io->q, io->sm_scale, io->idx, CSA2_TOPK, io->swa, io->o, io->lse,
-                       ws.attn, ws.attn_bytes, st, mode == CSA2_MODE_REUSE && (io->swa.flags & CSA2_ATTN_EARLY_INPUTS));
+                       ws.attn, ws.attn_bytes, st, early);
 }
 
 }  // extern "C"

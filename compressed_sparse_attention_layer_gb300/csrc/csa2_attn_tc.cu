@@ -53,6 +53,8 @@ struct AcSmem {
     uint32_t e2m1_pair[256][32];                   // byte -> bf16x2 of its two E2M1 codes, one
                                                    // copy per lane (bank = lane: no conflicts)  32 KB
     float kscale[AC_KEYS];                         // window row scale (1 for entries), -1: no key
+    float2 mlv[AC_OWN];                            // (m_c, l_c) of the owned heads, held until the
+                                                   // workspace may be written (early = 2)
     uint64_t mbar;                                 // the products' commits
     uint64_t sbar;                                 // the other CTAs' partial logits have landed
     uint64_t pbar;                                 // the other CTAs' probability rows have landed
@@ -177,7 +179,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
     // `early`, where the caller has guaranteed that the index array, the selected
     // entries and the window rows other than the query's own token were written
     // before that kernel's predecessors (a Reuse layer after another layer call):
-    // those keys are then loaded and dequantised while that kernel finishes.
+    // those keys are then loaded and dequantised while that kernel finishes.  With
+    // early = 2 the caller has also written q and new_rows before then and given
+    // this call a workspace of its own: the whole computation runs before the
+    // wait, which comes only before the workspace is written (the previous merge
+    // may still be reading its own).
     bool stored = false;
     uint32_t ring_word = 0;                        // the new token's window row, stored at the end
     int64_t ring_idx = -1, ring_scale_idx = -1;
@@ -200,7 +206,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
             stored = true;
         }
     }
-    pdl_wait();
+    if (early < 2) pdl_wait();
 
     // ---- this CTA's dims of the 64 queries (coalesced 16-byte loads)
     constexpr int QCH = AC_DIMS / 8;               // 16-byte chunks per head
@@ -392,8 +398,12 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
         *reinterpret_cast<uint4 *>(S.p + off_hi) = make_uint4(hi2[0], hi2[1], hi2[2], hi2[3]);
         *reinterpret_cast<uint4 *>(S.p + off_lo) = make_uint4(lo2[0], lo2[1], lo2[2], lo2[3]);
         if (part == 0 && !fail && !s_fail) {
-            part_ml[(base + h) * 2] = mx;
-            part_ml[(base + h) * 2 + 1] = l;
+            if (early == 2) {
+                S.mlv[hl] = make_float2(mx, l);
+            } else {
+                part_ml[(base + h) * 2] = mx;
+                part_ml[(base + h) * 2 + 1] = l;
+            }
         }
     }
     // this CTA's rows of P, written through the generic proxy, are read by the
@@ -439,6 +449,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, AC_C
             }
         }
         tc::mma_commit(&S.mbar);
+    }
+    if (early == 2) {
+        pdl_wait();                                // the previous merge is done with its workspace
+        if (tid < AC_OWN && !fail && !s_fail)
+            *reinterpret_cast<float2 *>(part_ml + (base + AC_OWN * (int64_t)dq + tid) * 2) = S.mlv[tid];
     }
     if (p_fail && tid == 0) flag(c.status, CSA2_DEV_TIMEOUT);
     bool fail2 = false;
@@ -590,7 +605,7 @@ int launch_attn_rows(const csa2_cache &c, const csa2_batch &bt, const uint16_t *
 
 int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, float sm_scale, const int32_t *idx,
                 int k, const csa2_swa &swa, float *o, float *lse, void *ws, size_t ws_bytes, cudaStream_t st,
-                bool early)
+                int early)
 {
     const int64_t rows = (int64_t)bt.batch * bt.nq;
     if (rows == 0) return CSA2_OK;
@@ -615,7 +630,7 @@ int launch_attn(const csa2_cache &c, const csa2_batch &bt, const uint16_t *q, fl
         ac.attrs = pdl;
         ac.numAttrs = 1;
         const cudaError_t e = cudaLaunchKernelEx(&ac, k_attn_tc, c, bt, q, sm_scale, idx, k, swa, part_o, part_ml,
-                                                 nchunks, (int)early, wait_polls());
+                                                 nchunks, early, wait_polls());
         if (e != cudaSuccess) {
             set_cuda_error(e);
             return CSA2_ERR_CUDA;

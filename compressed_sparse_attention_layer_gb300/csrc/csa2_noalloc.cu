@@ -25,9 +25,9 @@ extern "C" int csa2_layer_noalloc(int32_t mode, const csa2_cache *cache, const c
                                   const csa2_layer_io *io, csa2_stream_t stream)
 {
     if (!batch) return CSA2_ERR_NULL;
-    // reject work whose scratch does not fit before touching the device (a
-    // Reindex layer given the Full layer's copy of the pool's keys needs no room
-    // for them)
+    // every call shares the one array, so no call can have a workspace of its own
+    if (io && (io->swa.flags & CSA2_ATTN_EARLY_ALL)) return CSA2_ERR_UNSUPPORTED;
+    // reject work whose scratch does not fit before touching the device
     const size_t need = csa2::layer_workspace_need(mode, batch, io);
     if (need > (size_t)CSA2_NOALLOC_SCRATCH_BYTES) return CSA2_ERR_WORKSPACE;
 

@@ -100,6 +100,12 @@ class DeviceWorkload:
         # Reuse layers load their keys while the previous layer finishes
         # (csa2.ATTN_EARLY_INPUTS): the layers are called one after the other
         self.early_inputs = True
+        # ... and with early_all their whole attention (csa2.ATTN_EARLY_ALL): q and
+        # the window rows are in place before the layers run, and a Reuse layer
+        # takes the workspace the previous call did not use
+        self.early_all = False
+        self.workspace_alt = None
+        self._last_ws = None
         self.o = {l: torch.empty((R, 64, 512), dtype=torch.float32, device=dev) for l in self.layers}
         self.lse = {l: torch.empty((R, 64), dtype=torch.float32, device=dev) for l in self.layers}
         ws = max(csa2.csa2_layer_workspace_size(m, self.batch) for m in (0, 1, 2))
@@ -142,6 +148,8 @@ class DeviceWorkload:
         if self.early_inputs and self.wl.layers[l] == "reuse":
             # every layer call follows the previous one on the stream (run / run_layer in order)
             opts["flags"] = opts.get("flags", 0) | csa2.ATTN_EARLY_INPUTS
+            if self.early_all:
+                opts["flags"] |= csa2.ATTN_EARLY_ALL
         return csa2.swa_struct(self.swa_codes[l], self.swa_scales[l], new_rows=new_rows, **opts)
 
     def swa_new_rows(self, l) -> torch.Tensor:
@@ -161,7 +169,15 @@ class DeviceWorkload:
         """new_rows: optional window rows of the decode tokens, quantised into the
         ring by the layer call itself (see csa2_swa.new_rows)."""
         mode = csa2.MODES[self.wl.layers[l]]
-        csa2.csa2_layer(mode, self.cstruct, self.batch, self.io(l, prof, new_rows), self.workspace, stream=stream)
+        ws = self.workspace
+        if self.early_inputs and self.early_all and self.wl.layers[l] == "reuse":
+            if self.workspace_alt is None:
+                n = csa2.csa2_layer_workspace_size(csa2.MODES["reuse"], self.batch)
+                self.workspace_alt = torch.empty((n + 255) // 256 * 256, dtype=torch.uint8, device=self.dev)
+            if self._last_ws is self.workspace:
+                ws = self.workspace_alt
+        self._last_ws = ws
+        csa2.csa2_layer(mode, self.cstruct, self.batch, self.io(l, prof, new_rows), ws, stream=stream)
 
     def run(self, stream=None, on_layer=None):
         for l in self.layers:

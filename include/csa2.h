@@ -178,6 +178,20 @@ typedef struct csa2_swa {
  * completed).  A decode stack that calls csa2_layer layer after layer, with
  * the window rows of its own tokens passed as new_rows, satisfies it. */
 #define CSA2_ATTN_EARLY_INPUTS 2
+/* csa2_swa.flags, honoured by csa2_layer in REUSE mode (ignored elsewhere;
+ * refused by csa2_layer_noalloc, whose calls share one scratch array): all of
+ * CSA2_ATTN_EARLY_INPUTS's guarantees, and further that q and new_rows are in
+ * place before this call's kernels can start (written before the previous
+ * call into this library on the stream, or ordered before this call by a
+ * stream or event dependency), and that this call's workspace does not overlap
+ * the previous call's.  The
+ * attention then runs its whole computation while the previous layer's last
+ * kernel is still running and waits for it only before writing its workspace
+ * (which the previous layer's merge may still be reading from its own).  A
+ * decode stack whose inputs are in place before the step and whose layer
+ * calls alternate between two workspaces satisfies it.  No counterpart in the
+ * pages. */
+#define CSA2_ATTN_EARLY_ALL 16
 /* csa2_swa.flags: the schedule of the attention kernels (the same arithmetic
  * either way up to the order of the softmax rescaling; no counterpart in the
  * pages).  CHUNKS: one two-CTA cluster per (query row, 128-key chunk) and a

@@ -96,7 +96,7 @@ def test_layer_option_flags_validated_on_the_host(lib):
         s = csa2.Swa(P, P, 128, swa_flags, None, new_rows, None, 0.0, 0)
         return csa2.LayerIO(P, P, P, s, 1.0, layer_flags, P, P, P, P, P, None, None)
     both = csa2.ATTN_SCHEDULE_CHUNKS | csa2.ATTN_SCHEDULE_ROWS
-    for bad in (io(layer_flags=4), io(layer_flags=1 << 30), io(swa_flags=16), io(swa_flags=both)):
+    for bad in (io(layer_flags=4), io(layer_flags=1 << 30), io(swa_flags=32), io(swa_flags=both)):
         assert lib.csa2_layer(csa2.MODES["full"], ctypes.byref(cache), ctypes.byref(batch), ctypes.byref(bad),
                               P, 1 << 30, None) == -3
     # a negative RoPE base is a shape error

@@ -413,25 +413,31 @@ def test_normed_rotated_queries_feed_the_layers():
 
 def test_reuse_keys_loaded_early_bit_identical():
     """Reuse layers that load and dequantise their keys while the previous
-    layer's merge is still running (csa2.ATTN_EARLY_INPUTS) give the same o and
-    lse, bit for bit, as Reuse layers that load them after it; the window rows
-    of the decode tokens are quantised inside the calls in both."""
+    layer's merge is still running (csa2.ATTN_EARLY_INPUTS), and Reuse layers
+    that run their whole attention before waiting for it (csa2.ATTN_EARLY_ALL,
+    alternating workspaces), give the same o and lse, bit for bit, as Reuse
+    layers that wait first; the window rows of the decode tokens are quantised
+    inside the calls in all three."""
     wl = W.Workload("early", 76, 3, [6000, 700, 90000], 1,
-                    ["full", "reuse", "reuse", "reindex", "reuse"], planted_blocks=4)
+                    ["full", "reuse", "reuse", "reindex", "reuse", "reuse", "reuse"], planted_blocks=4)
     runs = []
-    for early in (False, True):
+    for early, early_all in ((False, False), (True, False), (True, True)):
         dw = DeviceWorkload(wl)
         dw.early_inputs = early
+        dw.early_all = early_all
         for l in dw.layers:
             dw.run_layer(l, new_rows=dw.swa_new_rows(l))
         torch.cuda.synchronize()
         assert int(dw.cache.status[0]) == 0
         runs.append(dw)
-    a, b = runs
-    for l in a.layers:
-        assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
-        assert torch.equal(a.lse[l].view(torch.int32), b.lse[l].view(torch.int32)), l
-        assert torch.equal(a.swa_codes[l], b.swa_codes[l]), l
+    a = runs[0]
+    for b in runs[1:]:
+        for l in a.layers:
+            assert torch.equal(a.o[l].view(torch.int32), b.o[l].view(torch.int32)), l
+            assert torch.equal(a.lse[l].view(torch.int32), b.lse[l].view(torch.int32)), l
+            assert torch.equal(a.swa_codes[l], b.swa_codes[l]), l
+    # the early-all run did alternate its Reuse layers' workspaces
+    assert runs[2].workspace_alt is not None
 
 
 @pytest.mark.parametrize("q", [2, 3, 5])

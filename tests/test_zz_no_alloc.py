@@ -82,6 +82,17 @@ def test_noalloc_layer_matches_layer_twice():
     assert int(dw.cache.status[0]) == 0 and int(other.cache.status[0]) == 0
 
 
+def test_noalloc_refuses_early_all():
+    """csa2_layer_noalloc cannot give a call a workspace of its own, so it
+    refuses csa2.ATTN_EARLY_ALL before touching the device."""
+    lib = csa2.load()
+    P = ctypes.c_void_p(1 << 12)
+    b = csa2.Batch(8, 1, 1, 0, 4096, P, P)
+    s = csa2.Swa(P, P, 128, csa2.ATTN_EARLY_INPUTS | csa2.ATTN_EARLY_ALL, None, None, None, 0.0, 0)
+    io = csa2.LayerIO(P, P, P, s, 1.0, 0, P, P, P, P, P, None, None)
+    assert lib.csa2_layer_noalloc(2, None, ctypes.byref(b), ctypes.byref(io), None) == -3
+
+
 def test_noalloc_refuses_work_beyond_its_scratch():
     lib = csa2.load()
     big = csa2.Batch(8, 1, 1, 0, 1 << 20, None, None)           # a Full layer over 8 x 1M entries
