@@ -27,10 +27,10 @@
 //   - after the last chunk: o = acc x mult, mult = f / L with the sink folded
 //     in (the same arithmetic as the merge kernel), the RoPE dims rotated
 //     back, lse = M + log L.
-// The next chunk's keys are fetched while the current one is processed: the
-// index is loaded after the first product is issued, the page after its
-// read-out, the codes after the softmax, so by the next chunk they are in
-// registers.
+// The keys are fetched ahead: while a chunk's first product is issued, the
+// next chunk's codes (its page already known) and the index of the chunk
+// after it are loaded, and that index's page after the product's read-out,
+// so the codes have a whole chunk to arrive.
 // 512 threads: four per key (64 dims each) for the loads and dequantisation,
 // sixteen per owned head for the softmax, one tensor-memory lane each in the
 // read-outs.
@@ -177,43 +177,33 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
     }
     __syncthreads();
 
-    // ---- the keys of the next chunk, in three steps (registers only)
-    int32_t nx_p = -1, nx_page = -1;
-    bool nx_ok = false;
+    // ---- a chunk's keys in three steps (registers only): its index, the index's
+    //      page, the codes.  The loop keeps the index and page two chunks ahead and
+    //      the codes one chunk ahead.
     uint4 kc[4];
     uint32_t ksc = 0;
     float kscale = 1.0f;
     bool valid = false;
-    auto fetch_index = [&](int64_t i, int ch) {    // step 1: the index
-        nx_p = -1;
-        if (ch != nchunks - 1) {
-            const int j = ch * AC_KEYS + key;
-            if (j < k) nx_p = __ldg(idx + row_of(i) * k + j);
-        }
+    auto load_index = [&](int64_t i, int ch) -> int32_t {
+        const int j = ch * AC_KEYS + key;
+        return ch != nchunks - 1 && j < k ? __ldg(idx + row_of(i) * k + j) : -1;
     };
-    auto fetch_page = [&](int64_t i, int ch) {     // step 2: its page
-        nx_ok = false;
-        if (ch != nchunks - 1) {
-            const RowInfo &R = S.ri[i & 1];
-            const int32_t p = nx_p;
-            if (p >= 0 && !(p >= R.dlo && p <= R.dhi)) {
-                if (p >= R.vis) {
-                    if (hf == 0 && dq == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
-                } else {
-                    nx_page = __ldg(c.block_table + (int64_t)R.b * c.max_pages + (p >> 6));
-                    nx_ok = true;
-                }
-            }
+    auto load_page = [&](int ch, const RowInfo &R, int32_t p, int32_t &page) -> bool {
+        if (ch == nchunks - 1 || p < 0 || (p >= R.dlo && p <= R.dhi)) return false;
+        if (p >= R.vis) {
+            if (hf == 0 && dq == 0) flag(c.status, CSA2_DEV_BAD_INDEX);
+            return false;
         }
+        page = __ldg(c.block_table + (int64_t)R.b * c.max_pages + (p >> 6));
+        return true;
     };
-    auto fetch_codes = [&](int64_t i, int ch) {    // step 3: the codes
-        const RowInfo &R = S.ri[i & 1];
+    auto load_codes = [&](int ch, const RowInfo &R, int32_t p, int32_t page, bool ok) {
         valid = false;
         kscale = 1.0f;
         if (ch != nchunks - 1) {
-            if (nx_ok) {
-                const int64_t slot = (int64_t)nx_page * CSA2_PAGE + (nx_p & 63);
-                if (nx_page < 0 || slot >= c.num_slots) {
+            if (ok) {
+                const int64_t slot = (int64_t)page * CSA2_PAGE + (p & 63);
+                if (page < 0 || slot >= c.num_slots) {
                     flag(c.status, CSA2_DEV_BAD_PAGE);
                 } else {
                     const uint4 *src =
@@ -235,10 +225,18 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
             valid = true;
         }
     };
+    // the chunk after the current one (index, page) and the one after that
+    int32_t p1 = -1, page1 = -1, p2 = -1, page2 = -1;
+    bool ok1 = false, ok2 = false;
     if (n_items > 0) {
-        fetch_index(0, 0);
-        fetch_page(0, 0);
-        fetch_codes(0, 0);
+        // chunk 0 now; chunk 1 (same row: every row has at least two chunks) to step 2
+        int32_t p0 = load_index(0, 0), page0 = -1;
+        const bool ok0 = load_page(0, S.ri[0], p0, page0);
+        load_codes(0, S.ri[0], p0, page0, ok0);
+        if (n_items > 1) {
+            p1 = load_index(0, 1);
+            ok1 = load_page(1, S.ri[0], p1, page1);
+        }
     }
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // the other CTA's mbarriers exist
     const uint32_t tmem = S.tmem;
@@ -313,6 +311,8 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
         // the next item
         const int64_t ni = window ? i + 1 : i;
         const int nch = window ? 0 : ch + 1;
+        const int64_t ni2 = nch == nchunks - 1 ? ni + 1 : ni;   // the chunk after that
+        const int nch2 = nch == nchunks - 1 ? 0 : nch + 1;
         // ---- A: the previous chunk's product has finished: this chunk's keys into
         //      the key tile (and the row's query slice), then the previous chunk's
         //      output share
@@ -366,7 +366,11 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
             }
             tc::mma_commit(&S.mbar);
         }
-        if (it + 1 < n_items) fetch_index(ni, nch);
+        // while the products run: the next chunk's codes (its page is known) and the
+        // index of the chunk after it; the row after this one's scalars
+        if (it + 1 < n_items) load_codes(nch, S.ri[ni & 1], p1, page1, ok1);
+        if (it + 2 < n_items) p2 = load_index(ni2, nch2);
+        if (ch == 0 && tid == 32 && i + 1 < my_rows) row_info(S.ri[(i + 1) & 1], row_of(i + 1));
 
         // ---- D: read the partials out; the other CTA's heads go to it
         hard = __syncthreads_or(!wait_phase(&S.mbar, 0, polls, c.status));
@@ -381,8 +385,7 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; j++) S.pout[col + j][kr] = __uint_as_float(a16[j]);
         }
-        if (ch == 0 && tid == 0 && i + 1 < my_rows) row_info(S.ri[(i + 1) & 1], row_of(i + 1));
-        if (it + 1 < n_items) fetch_page(ni, nch);
+        if (it + 2 < n_items) ok2 = load_page(nch2, S.ri[ni2 & 1], p2, page2);
         tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncthreads();
@@ -484,7 +487,6 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
             bulk_to_peer(cluster_map(xs, peer), xs, AR_XS_BYTES, pb);
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
-        if (it + 1 < n_items) fetch_codes(ni, nch);
 
         // ---- F: [O_hi | O_lo]^T = V_d^T [P_hi | P_lo]^T (M-tiles of 128 dims, K = 128
         //      keys, N = 128); the read-out adds the halves
@@ -507,6 +509,9 @@ __global__ void __cluster_dims__(AC_CL, 1, 1) __launch_bounds__(AC_THREADS, 1)
             }
             tc::mma_commit(&S.mbar);
         }
+        p1 = p2;                                   // the chunk after next becomes the next
+        page1 = page2;
+        ok1 = ok2;
     }
     if (!hard && n_items > 0) {
         hard = __syncthreads_or(!wait_phase(&S.mbar, 1, polls, c.status));
