@@ -199,18 +199,21 @@ class DecodeStep:
             e.record()                       # materialise the CUDA events
         self.set_schedule()
         # the step's host-fed inputs (new tokens, every layer's queries and window
-        # rows) in two device buffers -- the first layer's / the rest -- and its
-        # outputs (every layer's o and lse) in one buffer per group of
-        # OUT_GROUP layers, so that the end-to-end leg copies the inputs in while
-        # the first layer runs and each group's outputs out while the later
-        # layers run
+        # rows) in two device buffers -- the first IN_EARLY layers' / the rest --
+        # and its outputs (every layer's o and lse) in one buffer per group of
+        # OUT_GROUP layers, so that the end-to-end leg copies the later layers'
+        # inputs in once the first layer's HBM-bound scan is over (a copy beside
+        # the scan slows it by about the copy's own time) while the next layers
+        # run, and each group's outputs out while the later layers run
         layers = list(dw.layers)
         self.out_groups = [list(range(g, min(g + OUT_GROUP, len(layers)))) for g in range(0, len(layers), OUT_GROUP)]
+        if len(self.out_groups[-1]) > 1:           # the copy after the last kernel: one layer's outputs
+            self.out_groups[-1:] = [self.out_groups[-1][:-1], self.out_groups[-1][-1:]]
         ins0 = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
         ins1 = []
         for i, l in enumerate(layers):
             refs = [(dw.q, l), (self.swa_new, l)] + ([(dw.qi, l), (dw.w, l)] if l in dw.qi else [])
-            (ins0 if i == 0 else ins1).extend(refs)
+            (ins0 if i < IN_EARLY else ins1).extend(refs)
         self.in_dev = [self._gather(ins0)] + ([self._gather(ins1)] if ins1 else [])
         outs = [[(dw.o, l), (dw.lse, l)] for l in layers]
         self.out_dev = [self._gather(sum([outs[i] for i in g], [])) for g in self.out_groups]
@@ -253,27 +256,27 @@ class DecodeStep:
 
     def enqueue_e2e(self, host_in, host_out, s2, s3):
         """The step with its copies, for capture on the current stream: the first
-        layer's inputs first, the other layers' on s2 while the first layer runs;
-        each group of layers' outputs on s3 once its last layer has run, the last
-        group's at the end."""
+        IN_EARLY layers' inputs first; the other layers' on s2 once the first
+        layer has run, while the next ones run; each group of layers' outputs on
+        s3 once its last layer has run, the last group's at the end."""
         torch, dw, csa2 = self.torch, self.dw, self.csa2
         s = torch.cuda.current_stream()
         ev_in = torch.cuda.Event()
         ev_out = [torch.cuda.Event() for _ in self.out_groups]
-        if len(self.in_dev) > 1:
-            s2.wait_stream(s)
-            with torch.cuda.stream(s2):
-                self.in_dev[1].copy_(host_in[1], non_blocking=True)
-                ev_in.record(s2)
         self.in_dev[0].copy_(host_in[0], non_blocking=True)
         csa2.csa2_append_entries(self.dw.cstruct, self.C_new, self.Z_new, self.bias, self.wl.m, self.ik_new,
                                  slots=self.new_slots)
         layers = list(dw.layers)
         last = {g[-1]: gi for gi, g in enumerate(self.out_groups)}
         for i, l in enumerate(layers):
-            if i == 1:
+            if i == IN_EARLY:
                 s.wait_event(ev_in)
             self.enqueue_layers([l])
+            if i == 0 and len(self.in_dev) > 1:
+                s2.wait_stream(s)
+                with torch.cuda.stream(s2):
+                    self.in_dev[1].copy_(host_in[1], non_blocking=True)
+                    ev_in.record(s2)
             gi = last.get(i)
             if gi is not None and gi < len(self.out_groups) - 1:
                 ev_out[gi].record(s)
@@ -312,6 +315,7 @@ class DecodeStep:
 # ---------------------------------------------------------------- algorithmic work
 KV_SCALE_BYTES = {0: 16, 1: 32}     # main-KV block-scale bytes per entry: MXFP4, FP4 with E4M3 per 16
 OUT_GROUP = 2                       # e2e: layers whose outputs go back to the host in one copy
+IN_EARLY = 5                        # e2e: layers whose inputs are copied in before the step's kernels
 POOL_MAX = 16384                    # candidate pool: 2,048 blocks of 8
 
 
