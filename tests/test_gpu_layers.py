@@ -301,13 +301,16 @@ def test_window_row_quantised_inside_the_attention_call(schedule):
         assert torch.equal(fused.lse[l].view(torch.int32), ref.lse[l].view(torch.int32)), l
 
 
-def test_layers_with_fp4_e4m3_main_kv():
+@pytest.mark.parametrize("schedule", [0, csa2.ATTN_SCHEDULE_ROWS])
+def test_layers_with_fp4_e4m3_main_kv(schedule):
     """The main KV in the 16-element / E4M3-scale FP4 format (csa2_cache.kv_format
     = CSA2_KV_FP4_E4M3): selection and attention against the oracle, which
-    dequantises the same format, in every layer mode."""
+    dequantises the same format, in every layer mode, under the attention's
+    automatic schedule (chunks at 3 rows) and the row schedule forced."""
     wl = W.Workload("fp4_e4m3", 74, 3, [5000, 300, 20000], 1, ["full", "reuse", "reindex", "reuse"],
                     planted_blocks=4, kv_format=1)
     dw = DeviceWorkload(wl)
+    dw.attn_options = dict(flags=schedule)
     assert dw.cache.kv_scales.shape[1] == 32
     _run_recording(dw)
     for b in range(wl.batch):
