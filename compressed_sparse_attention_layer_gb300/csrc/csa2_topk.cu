@@ -3,9 +3,11 @@
 // blocks of 8 form the candidate pool, then the pool's own Top-512; the
 // research note §3.2).
 //
-// Rows of up to 16,384 keys (the pool Top-512) run on one CTA per row with the
-// keys in registers (k_topk_rows; description below).  The block level and
-// generic rows longer than 16,384 keys use one thread-block cluster per row:
+// Rows of up to 16,384 keys (csa2_topk) run on one CTA per row with the keys in
+// registers (k_topk_rows; description below); the layers' pool Top-512 runs the
+// Reindex select (csa2_reindex.cu) on keys the block level writes here.  The
+// block level and generic rows longer than 16,384 keys use one thread-block
+// cluster per row:
 // the CL CTAs each stage one contiguous 1/CL of
 // the row in shared memory as order-preserving 32-bit keys, read once from
 // global memory.  A radix select
