@@ -503,7 +503,12 @@ int launch_topk_blocks(const float *block_max, int64_t ld_blocks, const int32_t 
 {
     if (rows == 0) return CSA2_OK;
     const PoolKeys pk = pool_keys ? *pool_keys : PoolKeys{};
-    const int cl = topk_cluster_for(ld_blocks);
+    int cl = topk_cluster_for(ld_blocks);
+    // many rows fill the GPU by themselves: fewer CTAs per row (fewer cluster
+    // rounds per row), as long as one CTA's slice still fits its shared memory
+    const int sms = device_sms();
+    while (cl > 1 && (int64_t)rows * cl > 2 * (int64_t)(sms > 0 ? sms : 1) && slice_cap(ld_blocks, cl / 2) <= TK_SLICE)
+        cl /= 2;
     if (bounds_per_row) *bounds_per_row = cl;
     if (pk.keys && (cl > pk.bound_ld || !aligned(pk.scores, 16) || !aligned(pk.keys, 16) ||
                     (pk.ld_scores & 7) != 0))
