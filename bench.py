@@ -206,14 +206,12 @@ class DecodeStep:
         # the scan slows it by about the copy's own time) while the next layers
         # run, and each group's outputs out while the later layers run
         layers = list(dw.layers)
-        self.out_groups = [list(range(g, min(g + OUT_GROUP, len(layers)))) for g in range(0, len(layers), OUT_GROUP)]
-        if len(self.out_groups[-1]) > 1:           # the copy after the last kernel: one layer's outputs
-            self.out_groups[-1:] = [self.out_groups[-1][:-1], self.out_groups[-1][-1:]]
+        early, _, self.out_groups = e2e_groups(len(layers))
         ins0 = [(self.__dict__, "C_new"), (self.__dict__, "ik_new")]
         ins1 = []
         for i, l in enumerate(layers):
             refs = [(dw.q, l), (self.swa_new, l)] + ([(dw.qi, l), (dw.w, l)] if l in dw.qi else [])
-            (ins0 if i < IN_EARLY else ins1).extend(refs)
+            (ins0 if i in early else ins1).extend(refs)
         self.in_dev = [self._gather(ins0)] + ([self._gather(ins1)] if ins1 else [])
         outs = [[(dw.o, l), (dw.lse, l)] for l in layers]
         self.out_dev = [self._gather(sum([outs[i] for i in g], [])) for g in self.out_groups]
@@ -316,6 +314,19 @@ class DecodeStep:
 KV_SCALE_BYTES = {0: 16, 1: 32}     # main-KV block-scale bytes per entry: MXFP4, FP4 with E4M3 per 16
 OUT_GROUP = 2                       # e2e: layers whose outputs go back to the host in one copy
 IN_EARLY = 5                        # e2e: layers whose inputs are copied in before the step's kernels
+
+
+def e2e_groups(n_layers):
+    """The end-to-end leg's copies by layer position: the layers whose inputs
+    go in before the step's kernels, those whose inputs go in once the first
+    layer has run, and the groups of layers whose outputs go out together
+    (pairs, the last layer alone: the copy after the last kernel is short)."""
+    early = list(range(min(IN_EARLY, n_layers)))
+    late = list(range(len(early), n_layers))
+    out = [list(range(g, min(g + OUT_GROUP, n_layers))) for g in range(0, n_layers, OUT_GROUP)]
+    if out and len(out[-1]) > 1:
+        out[-1:] = [out[-1][:-1], out[-1][-1:]]
+    return early, late, out
 POOL_MAX = 16384                    # candidate pool: 2,048 blocks of 8
 
 

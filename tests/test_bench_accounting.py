@@ -41,3 +41,18 @@ def test_scan_work_units():
     bound, flops = bench.scan_work(W.prefill())
     assert bound == "tensor"
     assert flops == sum((65537 + i) // 2 for i in range(8192)) * 32 * 128 * 2
+
+
+def test_e2e_copy_groups():
+    """Every layer's inputs are copied in exactly once, the first IN_EARLY
+    layers' before the step's kernels; every layer's outputs go out exactly
+    once, in order, in pairs with the last layer alone."""
+    for n in (1, 2, 3, 4, 5, 6, 8, 20):
+        early, late, out = bench.e2e_groups(n)
+        assert early + late == list(range(n))
+        assert early == list(range(min(bench.IN_EARLY, n)))
+        assert sum(out, []) == list(range(n))
+        assert all(1 <= len(g) <= bench.OUT_GROUP for g in out)
+        assert len(out[-1]) == 1
+    early, late, out = bench.e2e_groups(20)
+    assert early == [0, 1, 2, 3, 4] and len(out) == 11 and out[-2:] == [[18], [19]]
