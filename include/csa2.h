@@ -458,6 +458,9 @@ CSA2_API size_t csa2_layer_workspace_size(int32_t mode, const csa2_batch *batch)
  *   over 8 x 1M entries); use csa2_layer there.  A Reuse layer needs only the
  *   attention's scratch (about 5.3 MB at 8 query rows), a Reindex layer that
  *   plus 64 KB per query row for its rescored pool (about 5.8 MB).
+ * - Returns CSA2_ERR_UNSUPPORTED, before any device work, for
+ *   CSA2_ATTN_EARLY_ALL in io->swa.flags: that option needs a workspace that
+ *   differs from the previous call's, and every call here shares one. 
  * - The first call on a device looks up the array's device address with that
  *   device current (cudaGetSymbolAddress); make that first call before any
  *   stream capture.  `stream` must belong to the current device.  The cached
