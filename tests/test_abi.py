@@ -37,6 +37,22 @@ def test_library_exports_every_declared_symbol(lib):
         assert n in csa2.EXPORTS, n
 
 
+def test_binding_constants_match_the_header():
+    """Every integer constant the header defines and the binding mirrors under
+    the same name (without the CSA2_ prefix) has the same value there."""
+    from compressed_sparse_attention_layer_gb300 import csa2
+    with open(HEADER) as f:
+        src = f.read()
+    defs = {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"#define\s+CSA2_(\w+)\s+\(?\s*(-?\d+)u?\s*\)?", src)}
+    mirrored = [n for n in defs if hasattr(csa2, n)]
+    for n in mirrored:
+        assert getattr(csa2, n) == defs[n], (n, getattr(csa2, n), defs[n])
+    for n in ("ATTN_DEDUP_WINDOW", "ATTN_EARLY_INPUTS", "ATTN_EARLY_ALL", "ATTN_SCHEDULE_CHUNKS",
+              "ATTN_SCHEDULE_ROWS", "LAYER_SCORES_BF16", "LAYER_INDEX_E4M3_QUERY"):
+        assert n in mirrored, n
+
+
 def test_status_strings(lib):
     for s in range(-8, 1):
         assert lib.csa2_status_string(s)
